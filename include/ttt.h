@@ -1,0 +1,152 @@
+/*
+ * ttt.h — C ABI of the B300 chunked test-time-training (TTT) scan library.
+ *
+ * The TTT layer keeps, per (batch row, head), a state that is the weights of a
+ * small model and, for each chunk of b tokens, takes one gradient step on the
+ * key -> value reconstruction loss, with every gradient of the chunk taken at
+ * the chunk-start weights; it reads out z_t = f(q_t; W_t) with the weights
+ * after token t's own gradient.
+ *   - "5 · TestingTime 训练与长上下文" (PaperTrace), section 1.1: the layer's
+ *     three parts (initial state W0, update rule, output rule); chunks of
+ *     b = 16 whose gradients are taken at the chunk-start weights; the dual
+ *     form that turns the chunk's outer products into matrix products.
+ *   - same page, section 2.3: f_W(k) = W k, loss 1/2 ||W k - v||^2,
+ *     gradient (W k - v) k^T (the delta rule); section 2.1: read-out
+ *     y_t = f(q_t; W_t); section 2.4: state reset per sequence.
+ *   - "Test-Time Training (TTT) guide" (diosapp), section 3: TTT-Linear and
+ *     TTT-MLP (two layers, hidden width 4x the input, GELU), mini-batch TTT
+ *     and the dual form.
+ *
+ * Conventions for every call
+ *   Row vectors: z = q W, W[i][j] with i the input and j the output index
+ *   (the pages' W k is k W^T here). Dual form of one chunk c, Wa = state at
+ *   its start:  E = K_c Wa - V_c;  Z_c = Q_c Wa - eta tril(Q_c K_c^T) E
+ *   (diagonal included: update, then read);  W = Wa - eta K_c^T E.
+ *   Gradients of a chunk are summed (an averaged step equals eta / b).
+ *   A final chunk shorter than b follows the same rule.
+ *
+ *   Memory: every pointer is device memory owned by the caller, contiguous
+ *   row-major, 16-byte aligned. The library allocates nothing; the caller
+ *   passes a workspace of ttt_workspace_bytes() bytes.
+ *
+ *   Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *   legacy default stream) and the call returns without waiting. Argument
+ *   errors are returned before anything is enqueued. Errors a kernel detects
+ *   (a wait that ran out of time) are written to a status word inside the
+ *   workspace; ttt_last_device_status() reads it.
+ *
+ *   Inputs are never modified. Outputs may not alias inputs.
+ */
+#ifndef TTT_B300_H
+#define TTT_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TTT_API __attribute__((visibility("default")))
+#else
+#define TTT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TTT_OK = 0,
+  TTT_ERR_ARG = -1,          /* bad pointer, size, alignment or workspace */
+  TTT_ERR_UNSUPPORTED = -2,  /* valid request this build does not serve (e.g. d > 64) */
+  TTT_ERR_CUDA = -3,         /* a CUDA runtime call failed (launch, copy, no device) */
+  TTT_ERR_TIMEOUT = -4,      /* a kernel's bounded wait ran out (reported via the workspace) */
+  TTT_ERR_DEVICE_CHECK = -5  /* a kernel's own consistency check failed */
+} ttt_status;
+
+typedef enum {
+  TTT_F32 = 0,   /* Q, K, V, Z are float32 */
+  TTT_BF16 = 1   /* Q, K, V, Z are bfloat16 (state and arithmetic stay fp32-accumulated) */
+} ttt_dtype;
+
+typedef enum { TTT_VARIANT_LINEAR = 0, TTT_VARIANT_MLP = 1 } ttt_variant;
+
+/* Options for the *_ex calls. Zero-initialise, then set fields. */
+typedef struct {
+  uint64_t wait_timeout_ns; /* limit for every wait inside a kernel; 0 = 2 s */
+  int32_t inject_stall;     /* test hook: 1 = the load pipeline never fills, so the
+                               consumers' bounded wait must run out (TTT_ERR_TIMEOUT) */
+  int32_t force_path;       /* 0 = automatic; 1 = general fp32 SIMT kernel;
+                               2 = tensor-core kernel (TTT_ERR_UNSUPPORTED if it cannot serve) */
+} ttt_options;
+
+/* Bytes of workspace a call with these sizes needs (>= 256; a status word
+ * lives at its start). variant: TTT_VARIANT_LINEAR or TTT_VARIANT_MLP.
+ * Returns 0 for invalid sizes. */
+TTT_API size_t ttt_workspace_bytes(int B, int H, int T, int d, int b, int variant);
+
+/*
+ * TTT-Linear forward over whole sequences.
+ *   Q, K, V  [B][H][T][d], dtype dt.  eta [H] float32 (per-head inner learning rate).
+ *   W0       [H][d][d] float32: initial state per head, shared by the batch
+ *            (an outer-loop parameter); every batch row restarts from it.
+ *   Z        [B][H][T][d], dtype dt: z_t = q_t W_t.
+ *   W_out    [B][H][d][d] float32: state after the last token (resume point
+ *            when T % b == 0).
+ *   Sizes: B >= 1, H >= 1, T >= 0, 1 <= d <= 64, b >= 1.
+ * Returns TTT_ERR_ARG for null/misaligned pointers, bad sizes or a short
+ * workspace; TTT_ERR_CUDA if a launch fails.
+ */
+TTT_API ttt_status ttt_linear_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                          const float* eta, const float* W0, int B, int H, int T, int d, int b,
+                          void* Z, float* W_out, void* workspace, size_t ws_bytes, void* stream);
+
+TTT_API ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                             const float* eta, const float* W0, int B, int H, int T, int d, int b,
+                             void* Z, float* W_out, void* workspace, size_t ws_bytes, void* stream,
+                             const ttt_options* opt);
+
+/*
+ * TTT-MLP forward: f(x) = gelu(x W1) W2 with tanh-GELU (Hendrycks and Gimpel
+ * 2016), hidden width m = 4 d ("Test-Time Training (TTT) guide", section 3).
+ *   W1_0 [H][d][4d], W2_0 [H][4d][d] float32, shared by the batch.
+ *   W1_out [B][H][d][4d], W2_out [B][H][4d][d] float32.
+ *   Other arguments as ttt_linear_fwd.
+ */
+TTT_API ttt_status ttt_mlp_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                       const float* eta, const float* W1_0, const float* W2_0, int B, int H, int T,
+                       int d, int b, void* Z, float* W1_out, float* W2_out, void* workspace,
+                       size_t ws_bytes, void* stream);
+
+TTT_API ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                          const float* eta, const float* W1_0, const float* W2_0, int B, int H,
+                          int T, int d, int b, void* Z, float* W1_out, float* W2_out,
+                          void* workspace, size_t ws_bytes, void* stream, const ttt_options* opt);
+
+/*
+ * One TTT-Linear decode token per (batch row, head), in O(d^2) per head.
+ *   q, k, v, z [B][H][d], dtype dt.  eta [H].
+ *   W_anchor [B][H][d][d] float32 in/out: state at the start of the current chunk.
+ *   W_run    [B][H][d][d] float32 in/out: state after the tokens seen so far.
+ *   pos = tokens already seen; this token is number pos.
+ *   e = k W_anchor - v;  W_run -= eta k^T e;  z = q W_run;
+ *   if (pos + 1) % b == 0 then W_anchor = W_run (the chunk is complete).
+ * After ttt_linear_fwd over T tokens with T % b == 0, W_anchor = W_run =
+ * W_out and pos = T continue the sequence exactly.
+ */
+TTT_API ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, ttt_dtype dt,
+                                  const float* eta, float* W_anchor, float* W_run, int B, int H,
+                                  int d, int pos, int b, void* z, void* stream);
+
+/* Waits for `stream`, then reads and clears the status word of `workspace`.
+ * Every *_fwd call clears that word when it is enqueued, so this reports the
+ * kernels of the latest *_fwd call that used this workspace: TTT_OK, or the
+ * first error one of them recorded (TTT_ERR_TIMEOUT, TTT_ERR_DEVICE_CHECK). */
+TTT_API ttt_status ttt_last_device_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+TTT_API const char* ttt_status_str(ttt_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTT_B300_H */

@@ -1,0 +1,205 @@
+"""Python binding of the B300 chunked TTT scan library (libttt_b300.so).
+
+Argument marshalling only: every step of the scan runs in the library's CUDA
+kernels. torch provides device memory and the current stream; the functions
+take torch CUDA tensors, pass their data pointers to the C ABI of
+include/ttt.h and raise on a non-OK status. There is no CPU fallback: if the
+library is missing or no GPU is present the calls fail loudly.
+
+Names match the C entry points: ttt_workspace_bytes, ttt_linear_fwd,
+ttt_mlp_fwd, ttt_linear_decode_step, ttt_last_device_status, ttt_status_str.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libttt_b300.so")
+
+TTT_OK, TTT_ERR_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT, TTT_ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
+TTT_F32, TTT_BF16 = 0, 1
+TTT_VARIANT_LINEAR, TTT_VARIANT_MLP = 0, 1
+PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
+
+# Every entry point include/ttt.h declares.
+EXPORTS = ("ttt_workspace_bytes", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
+           "ttt_linear_decode_step", "ttt_last_device_status", "ttt_status_str")
+
+
+class TTTError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({ttt_status_str(status)})")
+
+
+class ttt_options(ctypes.Structure):
+    _fields_ = [("wait_timeout_ns", ctypes.c_uint64), ("inject_stall", ctypes.c_int32),
+                ("force_path", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libttt_b300.so (raises if it has not been built) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.ttt_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.ttt_workspace_bytes.restype = sz
+    lin = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, sz, vp]
+    lib.ttt_linear_fwd.argtypes = lin
+    lib.ttt_linear_fwd_ex.argtypes = lin + [ctypes.POINTER(ttt_options)]
+    mlp = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+    lib.ttt_mlp_fwd.argtypes = mlp
+    lib.ttt_mlp_fwd_ex.argtypes = mlp + [ctypes.POINTER(ttt_options)]
+    lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp]
+    lib.ttt_last_device_status.argtypes = [vp, vp]
+    lib.ttt_status_str.argtypes = [i]
+    lib.ttt_status_str.restype = ctypes.c_char_p
+    for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
+              "ttt_linear_decode_step", "ttt_last_device_status"):
+        getattr(lib, f).restype = i
+    _lib = lib
+    return lib
+
+
+def ttt_status_str(status: int) -> str:
+    return load_library().ttt_status_str(int(status)).decode()
+
+
+def ttt_workspace_bytes(B: int, H: int, T: int, d: int, b: int, variant: int = TTT_VARIANT_LINEAR) -> int:
+    return int(load_library().ttt_workspace_bytes(B, H, T, d, b, variant))
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return TTT_BF16
+    if t.dtype == torch.float32:
+        return TTT_F32
+    raise TypeError(f"Q/K/V must be bfloat16 or float32, got {t.dtype}")
+
+
+def _check(t, name, dtype=None, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _stream_ptr(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _opts(options):
+    if options is None:
+        return None
+    if isinstance(options, ttt_options):
+        return ctypes.byref(options)
+    o = ttt_options()
+    for k, v in dict(options).items():
+        setattr(o, k, v)
+    return ctypes.byref(o)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def ttt_linear_fwd(Q, K, V, eta, W0, b: int, Z=None, W_out=None, workspace=None, stream=None, options=None):
+    """TTT-Linear over [B, H, T, d] sequences; returns (Z, W_out). Asynchronous on `stream`."""
+    import torch
+    lib = load_library()
+    B, H, T, d = Q.shape
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _check(t, n, Q.dtype, (B, H, T, d))
+    _check(eta, "eta", torch.float32, (H,))
+    _check(W0, "W0", torch.float32, (H, d, d))
+    if Z is None:
+        Z = torch.empty_like(Q)
+    if W_out is None:
+        W_out = torch.empty((B, H, d, d), dtype=torch.float32, device=Q.device)
+    _check(Z, "Z", Q.dtype, (B, H, T, d))
+    _check(W_out, "W_out", torch.float32, (B, H, d, d))
+    need = ttt_workspace_bytes(B, H, T, d, b, TTT_VARIANT_LINEAR)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), B, H, T, d, int(b), _p(Z), _p(W_out),
+            _p(workspace), workspace.numel(), _stream_ptr(stream))
+    if options is None:
+        st = lib.ttt_linear_fwd(*args)
+    else:
+        st = lib.ttt_linear_fwd_ex(*args, _opts(options))
+    if st != TTT_OK:
+        raise TTTError("ttt_linear_fwd", st)
+    return Z, W_out
+
+
+def ttt_mlp_fwd(Q, K, V, eta, W1_0, W2_0, b: int, Z=None, W1_out=None, W2_out=None, workspace=None,
+                stream=None, options=None):
+    """TTT-MLP (hidden 4d, tanh-GELU) over [B, H, T, d]; returns (Z, W1_out, W2_out)."""
+    import torch
+    lib = load_library()
+    B, H, T, d = Q.shape
+    m = 4 * d
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _check(t, n, Q.dtype, (B, H, T, d))
+    _check(eta, "eta", torch.float32, (H,))
+    _check(W1_0, "W1_0", torch.float32, (H, d, m))
+    _check(W2_0, "W2_0", torch.float32, (H, m, d))
+    if Z is None:
+        Z = torch.empty_like(Q)
+    if W1_out is None:
+        W1_out = torch.empty((B, H, d, m), dtype=torch.float32, device=Q.device)
+    if W2_out is None:
+        W2_out = torch.empty((B, H, m, d), dtype=torch.float32, device=Q.device)
+    need = ttt_workspace_bytes(B, H, T, d, b, TTT_VARIANT_MLP)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W1_0), _p(W2_0), B, H, T, d, int(b), _p(Z),
+            _p(W1_out), _p(W2_out), _p(workspace), workspace.numel(), _stream_ptr(stream))
+    if options is None:
+        st = lib.ttt_mlp_fwd(*args)
+    else:
+        st = lib.ttt_mlp_fwd_ex(*args, _opts(options))
+    if st != TTT_OK:
+        raise TTTError("ttt_mlp_fwd", st)
+    return Z, W1_out, W2_out
+
+
+def ttt_linear_decode_step(q, k, v, eta, W_anchor, W_run, pos: int, b: int, z=None, stream=None):
+    """One decode token per (batch row, head); q, k, v [B, H, d]. Updates W_anchor/W_run in place; returns z."""
+    import torch
+    lib = load_library()
+    B, H, d = q.shape
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, n, q.dtype, (B, H, d))
+    _check(eta, "eta", torch.float32, (H,))
+    _check(W_anchor, "W_anchor", torch.float32, (B, H, d, d))
+    _check(W_run, "W_run", torch.float32, (B, H, d, d))
+    if z is None:
+        z = torch.empty_like(q)
+    st = lib.ttt_linear_decode_step(_p(q), _p(k), _p(v), _dtype_code(q), _p(eta), _p(W_anchor), _p(W_run),
+                                    B, H, d, int(pos), int(b), _p(z), _stream_ptr(stream))
+    if st != TTT_OK:
+        raise TTTError("ttt_linear_decode_step", st)
+    return z
+
+
+def ttt_last_device_status(workspace, stream=None) -> int:
+    """Wait for the stream, then read and clear the workspace's device status word."""
+    return int(load_library().ttt_last_device_status(_p(workspace), _stream_ptr(stream)))

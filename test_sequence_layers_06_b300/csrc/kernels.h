@@ -1,0 +1,76 @@
+// Launch interface between the C ABI (ttt_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ttt {
+
+struct StatusBlock;
+
+struct LinearParams {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* Z;
+  const float* eta;    // [H]
+  const float* W0;     // [H][d][d]
+  float* W_out;        // [B][H][d][d]
+  int B, H, T, d, b;
+  int units;           // B * H
+  bool bf16;           // Q, K, V, Z are bf16 (else fp32)
+  StatusBlock* status;
+  uint64_t timeout_ns;
+  int inject_stall;
+};
+
+struct MlpParams {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* Z;
+  const float* eta;
+  const float* W1_0;   // [H][d][m]
+  const float* W2_0;   // [H][m][d]
+  float* W1_out;       // [B][H][d][m]  (running state while the kernel works)
+  float* W2_out;       // [B][H][m][d]
+  float* snap;         // workspace: per unit d*m + m*d floats (chunk-start snapshot)
+  int B, H, T, d, m, b;
+  int units;
+  bool bf16;
+  StatusBlock* status;
+  uint64_t timeout_ns;
+  int inject_stall;
+};
+
+struct DecodeParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* z;
+  const float* eta;
+  float* W_anchor;
+  float* W_run;
+  int B, H, d, pos, b;
+  int units;
+  bool bf16;
+};
+
+// Tensor-core TTT-Linear (bf16, d = 64, b % 16 == 0).
+bool linear_mma_supported(const LinearParams& p);
+int linear_mma_tile_rows();
+cudaError_t launch_linear_mma(const LinearParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                              const CUtensorMap& mv, const CUtensorMap& mz, cudaStream_t stream);
+
+// General fp32-arithmetic TTT-Linear (any dtype, d <= 64, any b).
+cudaError_t launch_linear_simt(const LinearParams& p, cudaStream_t stream);
+
+// General fp32-arithmetic TTT-MLP.
+size_t mlp_simt_snapshot_bytes(int units, int d, int m);
+cudaError_t launch_mlp_simt(const MlpParams& p, cudaStream_t stream);
+
+// Decode token.
+cudaError_t launch_linear_decode(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace ttt

@@ -1,0 +1,242 @@
+// C ABI of the chunked TTT scan: argument checks, workspace layout, TMA
+// descriptors and kernel dispatch. Declarations and contracts: include/ttt.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/ttt.h"
+#include "kernels.h"
+#include "ttt_device.cuh"
+
+namespace {
+
+using ttt::kStatusBytes;
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+constexpr int kMaxD = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool sizes_ok(int B, int H, int T, int d, int b) {
+  if (B < 1 || H < 1 || T < 0 || d < 1 || b < 1) return false;
+  // Every flat index of [B][H][T][d] must fit a signed 64-bit offset and every
+  // TMA coordinate a signed 32-bit one.
+  const long double n = static_cast<long double>(B) * H * T * d;
+  return n < 9.0e18L && static_cast<long double>(B) * H < 2147483647.0L;
+}
+
+size_t mlp_hidden(int d) { return static_cast<size_t>(4) * d; }
+
+// Workspace: [status block 256 B][variant scratch].
+size_t workspace_bytes_impl(int B, int H, int T, int d, int b, int variant) {
+  if (!sizes_ok(B, H, T, d, b)) return 0;
+  size_t bytes = kStatusBytes;
+  if (variant == TTT_VARIANT_MLP)
+    bytes += round_up(ttt::mlp_simt_snapshot_bytes(B * H, d, static_cast<int>(mlp_hidden(d))), 256);
+  else if (variant != TTT_VARIANT_LINEAR)
+    return 0;
+  return bytes;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D map over a [units][T][d] bf16 tensor, box [1][box_t][box_d].
+bool encode_3d(CUtensorMap* map, const void* base, int units, int T, int d, int box_t, int box_d,
+               CUtensorMapSwizzle swz) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T > 0 ? T : 1),
+                              static_cast<cuuint64_t>(units)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(T > 0 ? T : 1) * d * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_d), static_cast<cuuint32_t>(box_t), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+ttt_options defaults(const ttt_options* opt) {
+  ttt_options o;
+  std::memset(&o, 0, sizeof(o));
+  if (opt) o = *opt;
+  if (o.wait_timeout_ns == 0) o.wait_timeout_ns = kDefaultTimeoutNs;
+  return o;
+}
+
+ttt_status reset_status(void* ws, cudaStream_t s) {
+  return cudaMemsetAsync(ws, 0, sizeof(ttt::StatusBlock), s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ttt_workspace_bytes(int B, int H, int T, int d, int b, int variant) {
+  return workspace_bytes_impl(B, H, T, d, b, variant);
+}
+
+const char* ttt_status_str(ttt_status s) {
+  switch (s) {
+    case TTT_OK: return "ok";
+    case TTT_ERR_ARG: return "invalid argument";
+    case TTT_ERR_UNSUPPORTED: return "unsupported request";
+    case TTT_ERR_CUDA: return "CUDA runtime error";
+    case TTT_ERR_TIMEOUT: return "a kernel wait ran out of time";
+    case TTT_ERR_DEVICE_CHECK: return "a kernel consistency check failed";
+  }
+  return "unknown status";
+}
+
+ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                             const float* W0, int B, int H, int T, int d, int b, void* Z, float* W_out,
+                             void* workspace, size_t ws_bytes, void* stream, const ttt_options* opt) {
+  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
+  if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
+  if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
+  if (!eta || !W0 || !W_out || !workspace) return TTT_ERR_ARG;
+  if (T > 0 && (!Q || !K || !V || !Z)) return TTT_ERR_ARG;
+  for (const void* p : {static_cast<const void*>(Q), static_cast<const void*>(K), static_cast<const void*>(V),
+                        static_cast<const void*>(Z), static_cast<const void*>(eta), static_cast<const void*>(W0),
+                        static_cast<const void*>(W_out), static_cast<const void*>(workspace)})
+    if (p && !aligned16(p)) return TTT_ERR_ARG;
+  if (ws_bytes < workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_LINEAR)) return TTT_ERR_ARG;
+  const ttt_options o = defaults(opt);
+  if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  ttt::LinearParams p;
+  p.Q = Q; p.K = K; p.V = V; p.Z = Z;
+  p.eta = eta; p.W0 = W0; p.W_out = W_out;
+  p.B = B; p.H = H; p.T = T; p.d = d; p.b = b;
+  p.units = B * H;
+  p.bf16 = (dt == TTT_BF16);
+  p.status = static_cast<ttt::StatusBlock*>(workspace);
+  p.timeout_ns = o.wait_timeout_ns;
+  p.inject_stall = o.inject_stall;
+
+  const bool mma_ok = ttt::linear_mma_supported(p);
+  if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
+  const bool use_mma = mma_ok && o.force_path != 1 && T > 0;
+
+  ttt_status st = reset_status(workspace, s);
+  if (st != TTT_OK) return st;
+  cudaError_t err;
+  if (use_mma) {
+    CUtensorMap mq, mk, mv, mz;
+    const int rows = ttt::linear_mma_tile_rows();
+    if (!encode_3d(&mq, Q, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mk, K, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mz, Z, p.units, T, d, rows, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return TTT_ERR_CUDA;
+    err = ttt::launch_linear_mma(p, mq, mk, mv, mz, s);
+  } else {
+    err = ttt::launch_linear_simt(p, s);
+  }
+  return err == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_linear_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                          const float* W0, int B, int H, int T, int d, int b, void* Z, float* W_out,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  return ttt_linear_fwd_ex(Q, K, V, dt, eta, W0, B, H, T, d, b, Z, W_out, workspace, ws_bytes, stream,
+                           nullptr);
+}
+
+ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                          const float* W1_0, const float* W2_0, int B, int H, int T, int d, int b, void* Z,
+                          float* W1_out, float* W2_out, void* workspace, size_t ws_bytes, void* stream,
+                          const ttt_options* opt) {
+  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
+  if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
+  if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
+  if (!eta || !W1_0 || !W2_0 || !W1_out || !W2_out || !workspace) return TTT_ERR_ARG;
+  if (T > 0 && (!Q || !K || !V || !Z)) return TTT_ERR_ARG;
+  for (const void* p : {static_cast<const void*>(Q), static_cast<const void*>(K), static_cast<const void*>(V),
+                        static_cast<const void*>(Z), static_cast<const void*>(eta), static_cast<const void*>(W1_0),
+                        static_cast<const void*>(W2_0), static_cast<const void*>(W1_out),
+                        static_cast<const void*>(W2_out), static_cast<const void*>(workspace)})
+    if (p && !aligned16(p)) return TTT_ERR_ARG;
+  if (ws_bytes < workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP)) return TTT_ERR_ARG;
+  const ttt_options o = defaults(opt);
+  if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
+  if (o.force_path == 2) return TTT_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  ttt::MlpParams p;
+  p.Q = Q; p.K = K; p.V = V; p.Z = Z;
+  p.eta = eta; p.W1_0 = W1_0; p.W2_0 = W2_0; p.W1_out = W1_out; p.W2_out = W2_out;
+  p.snap = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+  p.B = B; p.H = H; p.T = T; p.d = d; p.m = static_cast<int>(mlp_hidden(d)); p.b = b;
+  p.units = B * H;
+  p.bf16 = (dt == TTT_BF16);
+  p.status = static_cast<ttt::StatusBlock*>(workspace);
+  p.timeout_ns = o.wait_timeout_ns;
+  p.inject_stall = o.inject_stall;
+
+  ttt_status st = reset_status(workspace, s);
+  if (st != TTT_OK) return st;
+  return ttt::launch_mlp_simt(p, s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_mlp_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                       const float* W1_0, const float* W2_0, int B, int H, int T, int d, int b, void* Z,
+                       float* W1_out, float* W2_out, void* workspace, size_t ws_bytes, void* stream) {
+  return ttt_mlp_fwd_ex(Q, K, V, dt, eta, W1_0, W2_0, B, H, T, d, b, Z, W1_out, W2_out, workspace, ws_bytes,
+                        stream, nullptr);
+}
+
+ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, ttt_dtype dt, const float* eta,
+                                  float* W_anchor, float* W_run, int B, int H, int d, int pos, int b, void* z,
+                                  void* stream) {
+  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
+  if (B < 1 || H < 1 || d < 1 || b < 1 || pos < 0) return TTT_ERR_ARG;
+  if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !z || !eta || !W_anchor || !W_run) return TTT_ERR_ARG;
+  if (W_anchor == W_run) return TTT_ERR_ARG;
+  for (const void* p : {q, k, v, static_cast<const void*>(z), static_cast<const void*>(eta),
+                        static_cast<const void*>(W_anchor), static_cast<const void*>(W_run)})
+    if (!aligned16(p)) return TTT_ERR_ARG;
+  ttt::DecodeParams p;
+  p.q = q; p.k = k; p.v = v; p.z = z; p.eta = eta;
+  p.W_anchor = W_anchor; p.W_run = W_run;
+  p.B = B; p.H = H; p.d = d; p.pos = pos; p.b = b;
+  p.units = B * H;
+  p.bf16 = (dt == TTT_BF16);
+  return ttt::launch_linear_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TTT_OK
+                                                                                           : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_last_device_status(void* workspace, void* stream) {
+  if (!workspace || !aligned16(workspace)) return TTT_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ttt::StatusBlock host;
+  if (cudaMemcpyAsync(&host, workspace, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return TTT_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return TTT_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(host), s) != cudaSuccess) return TTT_ERR_CUDA;
+  if (host.code == 0) return TTT_OK;
+  return static_cast<ttt_status>(host.code);
+}
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, sizes its workspace and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import test_sequence_layers_06_b300 as ttt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from test_sequence_layers_06_b300 import build
+    build.build()
+    return ttt.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ttt.h")).read()
+    return sorted(set(re.findall(r"TTT_API\s+[\w\s\*]+?\b(ttt_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) == 8
+    assert set(names) == set(ttt.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert ttt.ttt_status_str(0) == "ok"
+    assert "argument" in ttt.ttt_status_str(-1)
+    assert "time" in ttt.ttt_status_str(-4)
+
+
+def test_workspace_bytes(lib):
+    assert ttt.ttt_workspace_bytes(1, 32, 131072, 64, 16, 0) >= 256
+    mlp = ttt.ttt_workspace_bytes(4, 12, 8192, 64, 16, 1)
+    assert mlp >= 256 + 4 * 12 * 2 * 64 * 256 * 4
+    assert ttt.ttt_workspace_bytes(0, 1, 1, 64, 16, 0) == 0
+    assert ttt.ttt_workspace_bytes(1, 1, 1, 64, 0, 0) == 0
+    assert ttt.ttt_workspace_bytes(1, 1, 1, 64, 16, 7) == 0
+
+
+def _lin(lib, **kw):
+    a = dict(Q=4096, K=4096, V=4096, dt=1, eta=4096, W0=4096, B=1, H=1, T=16, d=64, b=16, Z=4096, W=4096,
+             ws=4096, wsb=1 << 20, s=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.ttt_linear_fwd(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W0"]), a["B"],
+                              a["H"], a["T"], a["d"], a["b"], vp(a["Z"]), vp(a["W"]), vp(a["ws"]), a["wsb"],
+                              vp(a["s"]))
+
+
+@pytest.mark.parametrize("kw", [dict(Q=0), dict(K=4100), dict(eta=0), dict(W0=8), dict(ws=0), dict(wsb=16),
+                                dict(B=0), dict(H=-1), dict(T=-1), dict(b=0), dict(d=0), dict(dt=5),
+                                dict(Z=0)])
+def test_linear_rejects_bad_arguments(lib, kw):
+    assert _lin(lib, **kw) == ttt.TTT_ERR_ARG
+
+
+def test_linear_rejects_unsupported_width(lib):
+    assert _lin(lib, d=65) == ttt.TTT_ERR_UNSUPPORTED
+
+
+def test_forced_tensor_path_rejects_shapes_it_cannot_serve(lib):
+    vp = ctypes.c_void_p
+    o = ttt.ttt_options(0, 0, ttt.PATH_TENSOR)
+    for kw in (dict(d=32), dict(b=8), dict(dt=0)):
+        a = dict(dt=1, d=64, b=16)
+        a.update(kw)
+        st = lib.ttt_linear_fwd_ex(vp(4096), vp(4096), vp(4096), a["dt"], vp(4096), vp(4096), 1, 1, 16, a["d"],
+                                   a["b"], vp(4096), vp(4096), vp(4096), 1 << 20, vp(0), ctypes.byref(o))
+        assert st == ttt.TTT_ERR_UNSUPPORTED, kw
+
+
+def test_mlp_and_decode_reject_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    st = lib.ttt_mlp_fwd(vp(4096), vp(4096), vp(4096), 1, vp(4096), vp(4096), vp(4096), 1, 1, 16, 64, 16,
+                         vp(4096), vp(4096), vp(4096), vp(4096), 256, vp(0))
+    assert st == ttt.TTT_ERR_ARG  # workspace too small for the snapshot
+    st = lib.ttt_linear_decode_step(vp(4096), vp(4096), vp(4096), 1, vp(4096), vp(4096), vp(4096), 1, 1, 64, 0,
+                                    16, vp(4096), vp(0))
+    assert st == ttt.TTT_ERR_ARG  # W_anchor and W_run alias
+    st = lib.ttt_linear_decode_step(vp(4096), vp(4096), vp(4096), 1, vp(4096), vp(4096), vp(8192), 1, 1, 64, -1,
+                                    16, vp(4096), vp(0))
+    assert st == ttt.TTT_ERR_ARG
+    assert lib.ttt_last_device_status(vp(0), vp(0)) == ttt.TTT_ERR_ARG
+
+
+def test_no_cpu_fallback_without_a_gpu(lib):
+    """With valid arguments and no GPU the call fails loudly instead of computing on the host."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; this checks the CPU-only failure mode")
+    assert _lin(lib) == ttt.TTT_ERR_CUDA

@@ -1,0 +1,184 @@
+"""TTT-Linear on the GPU (through the C ABI) against the fp64 oracle.
+
+Small cases run the oracle over every unit; the full-size workloads run the
+GPU on everything and the oracle on sampled (batch row, head) units, which the
+counter-based generator can draw on their own. Bars: rel-L2 <= 1e-4 with fp32
+operands, <= 2e-2 with bf16 operands (fp32 state and accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import test_sequence_layers_06_b300 as ttt
+from ttt_testlib import oracle_linear, rel_l2, to64, tolerance, torch_inputs, worst_unit_rel
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+
+def run_linear(inp, b, path=ttt.PATH_AUTO):
+    t = torch_inputs(inp)
+    opts = None if path == ttt.PATH_AUTO else {"force_path": path}
+    Z, Wo = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], b, options=opts)
+    torch.cuda.synchronize()
+    return to64(Z), to64(Wo)
+
+
+def check(inp, b, path=ttt.PATH_AUTO, tol=None):
+    tol = tolerance(inp.w) if tol is None else tol
+    Z, Wo = run_linear(inp, b, path)
+    Zr, Wr = oracle_linear(inp, b)
+    ez, ew = rel_l2(Z, Zr), rel_l2(Wo, Wr)
+    assert np.all(np.isfinite(Z)) and np.all(np.isfinite(Wo))
+    assert ez <= tol and ew <= tol, (ez, ew, worst_unit_rel(Z, Zr))
+    return ez, ew
+
+
+def test_tiny_fp32_workload():
+    """B1 H1 T64 d16 b16, fp32 operands: the 1e-4 bar."""
+    inp = synth.make_inputs(W["linear_tiny_f32"])
+    ez, ew = check(inp, 16)
+    assert ez < 1e-5 and ew < 1e-5
+
+
+def test_small_bf16_workload_tensor_path():
+    """B2 H4 T2048 d64 b16, bf16: the tensor-core kernel."""
+    inp = synth.make_inputs(W["linear_small"])
+    check(inp, 16, ttt.PATH_TENSOR)
+
+
+def test_small_bf16_workload_simt_path():
+    inp = synth.make_inputs(W["linear_small"])
+    check(inp, 16, ttt.PATH_SIMT)
+
+
+@pytest.mark.parametrize("T,b", [(1, 16), (15, 16), (17, 16), (50, 16), (100, 32), (130, 64), (300, 256),
+                                 (64, 48), (0, 16)])
+def test_tensor_path_ragged_and_chunk_sizes(T, b):
+    """Several 16-token tiles with a ragged tail; chunks of 1, 2, 3 and 16 tiles."""
+    w = W["linear_small"].with_(B=1, H=3, T=T, seed=100 + T)
+    inp = synth.make_inputs(w)
+    if T == 0:
+        Z, Wo = run_linear(inp, b, ttt.PATH_TENSOR)
+        assert Z.size == 0 and np.array_equal(Wo[0], inp.W0.astype(np.float64))
+        return
+    check(inp, b, ttt.PATH_TENSOR)
+
+
+@pytest.mark.parametrize("d,T,b,dtype", [(16, 40, 16, "f32"), (32, 37, 5, "f32"), (64, 33, 1, "f32"),
+                                         (16, 64, 16, "bf16"), (32, 70, 7, "bf16"), (64, 19, 3, "bf16"),
+                                         (8, 23, 4, "f32")])
+def test_simt_path_shapes(d, T, b, dtype):
+    w = W["linear_small"].with_(B=2, H=2, T=T, d=d, dtype=dtype, seed=200 + d + T)
+    check(synth.make_inputs(w), b)
+
+
+def test_fp32_bigger_workload_meets_1e4():
+    w = W["linear_tiny_f32"].with_(B=2, H=3, T=512, d=64, w_std=0.02, q_mode="normalized")
+    check(synth.make_inputs(w), 16)
+
+
+@pytest.mark.parametrize("name,units", [("linear_125m", [(0, 0), (3, 7), (7, 11)])])
+def test_full_size_125m_sampled(name, units):
+    """B8 H12 T8192: GPU over all 96 units, oracle on sampled ones; per-head eta differs."""
+    w = W[name]
+    full = synth.make_inputs(w, want_exact=False)
+    t = torch_inputs(full)
+    Z, Wo = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], w.b)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(Z.float()).all()) and bool(torch.isfinite(Wo).all())
+    sub = synth.make_inputs(w, units=units)
+    Zr, Wr = oracle_linear(sub, w.b)
+    for k, (n, h) in enumerate(units):
+        assert rel_l2(to64(Z[n, h]), Zr[0, k]) <= tolerance(w)
+        assert rel_l2(to64(Wo[n, h]), Wr[0, k]) <= tolerance(w)
+
+
+@pytest.mark.parametrize("b", [16, 64, 256])
+def test_full_size_long_context_sampled(b):
+    """B1 H32 T131072 at b in {16, 64, 256}: oracle on two sampled heads."""
+    w = W["linear_long"].with_(b=b)
+    full = synth.make_inputs(w, want_exact=False)
+    t = torch_inputs(full)
+    Z, Wo = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], b)
+    torch.cuda.synchronize()
+    units = [(0, 5), (0, 31)]
+    sub = synth.make_inputs(w, units=units)
+    Zr, Wr = oracle_linear(sub, b)
+    for k, (n, h) in enumerate(units):
+        ez = rel_l2(to64(Z[n, h]), Zr[0, k])
+        ew = rel_l2(to64(Wo[n, h]), Wr[0, k])
+        assert ez <= tolerance(w) and ew <= tolerance(w), (h, ez, ew)
+    # every head: finite and bounded (the state update contracts for these eta)
+    assert bool(torch.isfinite(Z.float()).all()) and float(Wo.abs().max()) < 10.0
+
+
+def test_chain_two_calls_equal_one():
+    w = W["linear_small"].with_(B=1, H=2, T=96, seed=9)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    Z, Wo = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16)
+    Za, Wa = ttt.ttt_linear_fwd(t["Q"][:, :, :48].contiguous(), t["K"][:, :, :48].contiguous(),
+                                t["V"][:, :, :48].contiguous(), t["eta"], t["W0"], 16)
+    Zb, Wb = ttt.ttt_linear_fwd(t["Q"][:, :, 48:].contiguous(), t["K"][:, :, 48:].contiguous(),
+                                t["V"][:, :, 48:].contiguous(), t["eta"], Wa[0].contiguous(), 16)
+    torch.cuda.synchronize()
+    assert rel_l2(to64(torch.cat([Za, Zb], 2)), to64(Z)) < 1e-2
+    assert rel_l2(to64(Wb), to64(Wo)) < 1e-3
+
+
+def test_decode_continues_forward():
+    """Prefill T1 (b | T1), then decode N tokens one by one: equals the oracle over T1 + N."""
+    T1, N = 32, 20
+    w = W["linear_small"].with_(B=2, H=3, T=T1 + N, seed=77)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    _, Wp = ttt.ttt_linear_fwd(t["Q"][:, :, :T1].contiguous(), t["K"][:, :, :T1].contiguous(),
+                               t["V"][:, :, :T1].contiguous(), t["eta"], t["W0"], 16)
+    Wa, Wr = Wp.clone(), Wp.clone()
+    zs = []
+    for s in range(N):
+        tt = T1 + s
+        zs.append(ttt.ttt_linear_decode_step(t["Q"][:, :, tt].contiguous(), t["K"][:, :, tt].contiguous(),
+                                             t["V"][:, :, tt].contiguous(), t["eta"], Wa, Wr, tt, 16))
+    torch.cuda.synchronize()
+    Zr, Wref = oracle_linear(inp, 16)
+    assert rel_l2(to64(torch.stack(zs, 2)), Zr[:, :, T1:]) <= 2e-2
+    assert rel_l2(to64(Wr), Wref) <= 2e-2
+
+
+def test_decode_fp32_single_token_matches_oracle():
+    g = np.random.default_rng(3)
+    B, H, d = 2, 4, 64
+    q, k, v = (g.standard_normal((B, H, d)).astype(np.float32) for _ in range(3))
+    eta = g.uniform(0.05, 0.5, H).astype(np.float32)
+    Wa = (0.05 * g.standard_normal((B, H, d, d))).astype(np.float32)
+    Wr = (0.05 * g.standard_normal((B, H, d, d))).astype(np.float32)
+    for pos, b in ((5, 16), (15, 16)):
+        z, Wa2, Wr2 = oracle.linear_decode_step(q, k, v, eta, Wa, Wr, pos, b)
+        tq = [torch.from_numpy(x).cuda() for x in (q, k, v, eta)]
+        ta, tr = torch.from_numpy(Wa).cuda(), torch.from_numpy(Wr).cuda()
+        zz = ttt.ttt_linear_decode_step(*tq[:3], tq[3], ta, tr, pos, b)
+        torch.cuda.synchronize()
+        assert rel_l2(to64(zz), z) < 1e-5
+        assert rel_l2(to64(tr), Wr2) < 1e-6 and rel_l2(to64(ta), Wa2) < 1e-6
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The load pipeline is told never to fill: the consumers' wait runs out
+    after 1 ms, the kernel returns, the status says TTT_ERR_TIMEOUT, and the
+    next call on the same context works."""
+    w = W["linear_small"].with_(B=1, H=2, T=64)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16, workspace=ws,
+                       options={"inject_stall": 1, "wait_timeout_ns": 1_000_000, "force_path": ttt.PATH_TENSOR})
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_ERR_TIMEOUT
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK  # reading clears it
+    check(inp, 16, ttt.PATH_TENSOR)
+    ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16, workspace=ws)
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK

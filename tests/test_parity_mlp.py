@@ -1,0 +1,48 @@
+"""TTT-MLP on the GPU (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import test_sequence_layers_06_b300 as ttt
+from ttt_testlib import oracle_mlp, rel_l2, to64, tolerance, torch_inputs
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+
+
+def run_mlp(inp, b):
+    t = torch_inputs(inp)
+    Z, W1, W2 = ttt.ttt_mlp_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W1"], t["W2"], b)
+    torch.cuda.synchronize()
+    return to64(Z), to64(W1), to64(W2)
+
+
+@pytest.mark.parametrize("T,b,dtype,d", [(64, 16, "bf16", 64), (37, 16, "bf16", 64), (20, 5, "f32", 16),
+                                         (48, 16, "f32", 64), (1, 16, "bf16", 32)])
+def test_mlp_small(T, b, dtype, d):
+    w = W["mlp_125m"].with_(B=2, H=2, T=T, d=d, hidden=4 * d, dtype=dtype, seed=300 + T)
+    inp = synth.make_inputs(w)
+    Z, W1, W2 = run_mlp(inp, b)
+    Zr, W1r, W2r = oracle_mlp(inp, b)
+    tol = 1e-4 if dtype == "f32" else tolerance(w)
+    for x, r in ((Z, Zr), (W1, W1r), (W2, W2r)):
+        assert rel_l2(x, r) <= tol, rel_l2(x, r)
+
+
+def test_mlp_full_size_sampled():
+    """B4 H12 T8192 d64 hidden 256: GPU over all units, oracle on two sampled ones."""
+    w = W["mlp_125m"]
+    full = synth.make_inputs(w, want_exact=False)
+    t = torch_inputs(full)
+    Z, W1, W2 = ttt.ttt_mlp_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W1"], t["W2"], w.b)
+    torch.cuda.synchronize()
+    units = [(0, 0), (3, 11)]
+    sub = synth.make_inputs(w, units=units)
+    Zr, W1r, W2r = oracle_mlp(sub, w.b)
+    for k, (n, h) in enumerate(units):
+        assert rel_l2(to64(Z[n, h]), Zr[0, k]) <= tolerance(w)
+        assert rel_l2(to64(W1[n, h]), W1r[0, k]) <= tolerance(w)
+        assert rel_l2(to64(W2[n, h]), W2r[0, k]) <= tolerance(w)
+    assert bool(torch.isfinite(Z.float()).all())
