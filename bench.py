@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Throughput of the chunked TTT-Linear scan on B300, one JSON line.
+
+A step is one ttt_linear_fwd over the whole long-context workload
+(B1 H32 T131072 d64, chunk b = 16, bf16 Q/K/V, fp32 state): every stage of the
+hot path (chunk loads, error at the chunk start, intra-chunk scores, read-out,
+state update, write-back of Z and W_out). Metric: token·heads per second, and
+the dominant kernel's fraction of the HBM roofline (algorithmic bytes: Q, K, V
+read and Z written, plus the state read and written once).
+
+Arms
+  default            our CUDA library through its C ABI (device-resident inputs),
+                     plus an end-to-end figure through host buffers and the
+                     oracle timed on the host cores as a CPU baseline.
+  --impl reference   the fp64 CPU oracle on the host cores (a bounded sample of
+                     the same workload per step): the baseline arm.
+
+Multi-GPU: the (batch row, head) units are independent, so N GPUs run N
+replicas of the workload (weak scaling, no collective); value = all ranks'
+token·heads over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "TTT-Linear scan tokens·heads/sec and % of binding roofline (1×B300)"
+UNIT = "token·heads/s"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_HBM_GBS = 6400.0
+KERNEL_SOURCES = ("test_sequence_layers_06_b300/csrc/linear_mma.cu",)
+PROFILE_SUMMARY = "profiles/linear_mma_long_b16.md"
+BAD_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="linear_long")
+    ap.add_argument("--b", type=int, default=16)
+    ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+def algorithmic_bytes(w: synth.Workload) -> int:
+    """Bytes one pass must move: Q, K, V read and Z written once, W0 read once, W_out written once."""
+    es = 2 if w.dtype == "bf16" else 4
+    return w.token_heads * 4 * w.d * es + w.H * w.d * w.d * 4 + w.units * w.d * w.d * 4
+
+
+def algorithmic_flops(w: synth.Workload, b: int) -> int:
+    """Per chunk of b tokens: E, Q W and K^T E (2 b d^2 each) plus Q K^T and S E (2 b^2 d each)."""
+    return w.token_heads * (6 * w.d * w.d + 4 * b * w.d)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, 1800.0, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch from the committed ncu summary, if it was taken on today's kernel source."""
+    path = os.path.join(ROOT, PROFILE_SUMMARY)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha")):
+                k, v = line.strip().split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha") != source_digest():
+        return None
+    try:
+        return int(float(vals["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+
+    NAMES = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+             0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+             0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index: int, period_s: float = 0.01):
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        self.period = period_s
+        self.index = index
+        self.mode = None
+        self.error = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok, self.mode = True, "nvml"
+        except Exception as e:  # no NVML: sample nvidia-smi instead
+            self.error = repr(e)
+            self.max_mhz = None
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.ok, self.mode = True, "nvidia-smi"
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                self.reasons |= self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+            except Exception as e:
+                self.error = repr(e)
+            time.sleep(self.period)
+
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active")
+
+    def __enter__(self):
+        if self.mode == "nvml":
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        elif self.mode == "nvidia-smi":
+            import subprocess
+            self._p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}",
+                                        "--format=csv,noheader,nounits", "-lms", "50"],
+                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        return self
+
+    def __exit__(self, *a):
+        if self.mode == "nvml":
+            self._stop.set()
+            self._t.join()
+        elif self.mode == "nvidia-smi":
+            self._p.terminate()
+            out, _ = self._p.communicate()
+            for line in out.splitlines():
+                try:
+                    sm, mx, reasons = [x.strip() for x in line.split(",")]
+                    self.samples.append(float(sm))
+                    self.max_mhz = float(mx)
+                    self.reasons |= int(reasons, 16)
+                except ValueError:
+                    continue
+
+    def report(self):
+        reasons = sorted(n for bit, n in self.NAMES.items() if self.reasons & bit and n != "gpu_idle")
+        med = statistics.median(self.samples) if self.samples else None
+        r = {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+             "source": self.mode}
+        if not self.samples and self.error:
+            r["error"] = self.error
+        return r
+
+    def rejected(self) -> bool:
+        r = self.report()
+        if set(r["reasons"]) & BAD_REASONS:
+            return True
+        if r["sm_mhz"] and r["sm_max_mhz"] and not r["reasons"] and r["sm_mhz"] < 0.7 * r["sm_max_mhz"]:
+            return True
+        return False
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_rate(w: synth.Workload, b: int, target_s: float):
+    """The oracle (as it stands) on a bounded sample: every head of batch row 0, the first Ts tokens.
+    Returns (token·heads/s, threads, sample description, seconds)."""
+    import oracle
+    threads = oracle.max_threads()
+
+    def prepare(Ts):
+        inp = synth.make_inputs(w.with_(B=1, T=Ts))
+        if w.variant == "mlp":
+            return lambda: oracle.mlp_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W1_64, inp.W2_64, b)
+        return lambda: oracle.linear_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, b)
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    probe = max(b, 1024)
+    dt = timed(prepare(probe))
+    Ts = int(min(w.T, max(probe, probe * target_s / max(dt, 1e-6))))
+    Ts = max(b, Ts // b * b)
+    fn = prepare(Ts)
+    reps, total = 0, 0.0
+    while True:  # one pass over the sample, repeated until about target_s of work
+        total += timed(fn)
+        reps += 1
+        if total >= 0.8 * target_s or reps >= 20:
+            break
+    sample = (f"{w.name}: batch row 0, all {w.H} heads, first {Ts} of {w.T} tokens, {reps} pass(es) "
+              f"(fp64 primal oracle)")
+    return reps * w.H * Ts / total, threads, sample, total
+
+
+# --------------------------------------------------------------------------- our arm
+def bench_ours(args, world, rank, local):
+    import torch
+    import test_sequence_layers_06_b300 as ttt
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = synth.WORKLOADS[args.workload].with_(b=args.b)
+    inp = synth.make_inputs(w, want_exact=False)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    Q, K, V = to_dev(inp.q), to_dev(inp.k), to_dev(inp.v)
+    eta, W0 = torch.from_numpy(inp.eta).to(dev), torch.from_numpy(inp.W0).to(dev)
+    Z = torch.empty_like(Q)
+    Wo = torch.empty((w.B, w.H, w.d, w.d), dtype=torch.float32, device=dev)
+    ws = torch.zeros(ttt.ttt_workspace_bytes(w.B, w.H, w.T, w.d, args.b), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1  # ttt_linear_fwd enqueues one kernel (plus a 16-byte status memset)
+
+    def step():
+        ttt.ttt_linear_fwd(Q, K, V, eta, W0, args.b, Z=Z, W_out=Wo, workspace=ws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if ttt.ttt_last_device_status(ws, stream) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    def timed():
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(local)
+        with sampler:
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for i in range(args.steps):
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            t1.record(stream)
+            torch.cuda.synchronize()
+        barrier()
+        total_ms = t0.elapsed_time(t1)
+        per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return total_ms, per, sampler
+
+    total_ms, per, sampler = timed()
+    if sampler.rejected():  # throttled or stuck clocks: measure once more
+        total_ms, per, sampler = timed()
+    if ttt.ttt_last_device_status(ws, stream) != 0:
+        raise RuntimeError("device status not OK after the timed region")
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.token_heads / (ms_per_step * 1e-3)
+
+    # roofline of the dominant (only) kernel
+    hbm_gbs, _, peak_kind = measured_peaks()
+    kernel_ms = float(np.mean(per))
+    alg_bytes = algorithmic_bytes(w)
+    achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(achieved / hbm_gbs, 4), "traffic": profiled_traffic(),
+                "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.4 TB/s",
+                "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": round(kernel_ms, 4),
+                "flops_per_launch": algorithmic_flops(w, args.b)}
+
+    # end to end: pinned host buffers in, Z and W_out back out, through the public call
+    e2e = None
+    if args.e2e_steps > 0:
+        hq = torch.from_numpy(inp.q.view(np.int16)).pin_memory() if inp.q.dtype == np.uint16 else \
+            torch.from_numpy(inp.q).pin_memory()
+        hk = torch.from_numpy(inp.k.view(np.int16)).pin_memory() if inp.k.dtype == np.uint16 else \
+            torch.from_numpy(inp.k).pin_memory()
+        hv = torch.from_numpy(inp.v.view(np.int16)).pin_memory() if inp.v.dtype == np.uint16 else \
+            torch.from_numpy(inp.v).pin_memory()
+        hz = torch.empty(hq.shape, dtype=hq.dtype).pin_memory()
+        hw = torch.empty(tuple(Wo.shape), dtype=torch.float32).pin_memory()
+        Qi = Q.view(torch.int16) if Q.dtype == torch.bfloat16 else Q
+        Ki = K.view(torch.int16) if K.dtype == torch.bfloat16 else K
+        Vi = V.view(torch.int16) if V.dtype == torch.bfloat16 else V
+        Zi = Z.view(torch.int16) if Z.dtype == torch.bfloat16 else Z
+
+        def e2e_step():
+            Qi.copy_(hq, non_blocking=True)
+            Ki.copy_(hk, non_blocking=True)
+            Vi.copy_(hv, non_blocking=True)
+            step()
+            hz.copy_(Zi, non_blocking=True)
+            hw.copy_(Wo, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, bq = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        bq.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(bq) / args.e2e_steps
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = hq.numel() * hq.element_size() * 3
+        d2h = hz.numel() * hz.element_size() + hw.numel() * 4
+        e2e = {"value": world * w.token_heads / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": round(e2e_ms, 3),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        extras = bench_extras(ttt, dev, stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, sample, secs = oracle_rate(w, args.b, target_s=10.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+               "seconds": round(secs, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "b": args.b,
+                       "inputs": f"Q/K/V {w.dtype} {w.note}", "state": "fp32",
+                       "l2": "inputs larger than L2 (%.2f GB vs 126 MB)" % (3 * w.token_heads * w.d * 2 / 1e9),
+                       "parallelism": f"replicas x{world} (independent units, no collective)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": sampler.report(),
+            "extras": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def bench_extras(ttt, dev, stream):
+    """Secondary workloads, a few steps each (device-resident inputs)."""
+    import torch
+    hbm_gbs, tflops, _ = measured_peaks()
+    out = {}
+
+    def t_ms(fn, n):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    def dev_inputs(w):
+        inp = synth.make_inputs(w, want_exact=False)
+        cv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev))
+        return inp, cv(inp.q), cv(inp.k), cv(inp.v), torch.from_numpy(inp.eta).to(dev)
+
+    for name, b in (("linear_125m", 16), ("linear_small", 16), ("linear_long", 64), ("linear_long", 256)):
+        w = synth.WORKLOADS[name].with_(b=b)
+        inp, Q, K, V, eta = dev_inputs(w)
+        W0 = torch.from_numpy(inp.W0).to(dev)
+        Z = torch.empty_like(Q)
+        Wo = torch.empty((w.B, w.H, w.d, w.d), dtype=torch.float32, device=dev)
+        ws = torch.zeros(ttt.ttt_workspace_bytes(w.B, w.H, w.T, w.d, b), dtype=torch.uint8, device=dev)
+        ms = t_ms(lambda: ttt.ttt_linear_fwd(Q, K, V, eta, W0, b, Z=Z, W_out=Wo, workspace=ws, stream=stream),
+                  10 if w.T < 100000 else 5)
+        gbs = algorithmic_bytes(w) / (ms * 1e-3) / 1e9
+        out[f"{name}_b{b}"] = {"ms": round(ms, 4), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                               "hbm_frac": round(gbs / hbm_gbs, 4)}
+        del Q, K, V, Z
+    # TTT-MLP
+    w = synth.WORKLOADS["mlp_125m"]
+    inp, Q, K, V, eta = dev_inputs(w)
+    W1, W2 = torch.from_numpy(inp.W1).to(dev), torch.from_numpy(inp.W2).to(dev)
+    ms = t_ms(lambda: ttt.ttt_mlp_fwd(Q, K, V, eta, W1, W2, 16, stream=stream), 2)
+    m = w.hidden
+    flops = w.token_heads * (16 * w.d * m + 4 * 16 * (w.d + m))
+    out["mlp_125m_b16"] = {"ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                           "tensor_frac": round(flops / (ms * 1e-3) / (tflops * 1e12), 5)}
+    # decode: one token for B1 H32 from a state
+    q = torch.randn(1, 32, 64, device=dev).to(torch.bfloat16)
+    Wa = torch.zeros(1, 32, 64, 64, device=dev)
+    Wr = torch.zeros(1, 32, 64, 64, device=dev)
+    e32 = torch.full((32,), 0.1, device=dev)
+    ms = t_ms(lambda: ttt.ttt_linear_decode_step(q, q, q, e32, Wa, Wr, 5, 16, stream=stream), 200)
+    out["decode_long_1tok"] = {"us_per_step": round(ms * 1e3, 2)}
+    return out
+
+
+# --------------------------------------------------------------------------- reference arm
+def bench_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    w = synth.WORKLOADS[args.workload].with_(b=args.b)
+    # bounded sample per step: batch row 0, all heads, the first Ts tokens, sized so that the
+    # whole run stays within a few minutes
+    steps = args.steps
+    warm = max(3, args.warmup)
+    budget_s = 120.0
+    threads = oracle.max_threads()
+    probe = synth.make_inputs(w.with_(B=1, T=256))
+    t0 = time.perf_counter()
+    oracle.linear_primal(probe.q64, probe.k64, probe.v64, probe.eta64, probe.W0_64, args.b)
+    per_tok = (time.perf_counter() - t0) / 256
+    Ts = int(max(args.b, min(w.T, budget_s / (steps + warm) / max(per_tok, 1e-9))))
+    Ts = max(args.b, Ts // args.b * args.b)
+    inp = synth.make_inputs(w.with_(B=1, T=Ts))
+    run = lambda: oracle.linear_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, args.b)
+    for _ in range(warm):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run()
+    dt = (time.perf_counter() - t0) / steps
+    value = w.H * Ts / dt
+    sample = f"{w.name}: batch row 0, all {w.H} heads, first {Ts} of {w.T} tokens per step (fp64 primal oracle)"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "b": args.b,
+                       "inputs": f"Q/K/V {w.dtype} (exact fp64 values) {w.note}"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        bench_reference(args, world, rank)
+    else:
+        bench_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()
