@@ -122,6 +122,25 @@ TTT_API ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, t
                           void* workspace, size_t ws_bytes, void* stream, const ttt_options* opt);
 
 /*
+ * TTT-MLP forward that allocates nothing and takes no workspace. (No
+ * counterpart on the pages: it exists for callers that cannot allocate
+ * device memory.) The workspace ttt_mlp_fwd needs (a status word and a
+ * chunk-start copy of W1, W2 per unit) comes from a fixed 8 MiB array inside
+ * the library instead, so at d = 64 at most 64 (batch row, head) units fit;
+ * larger requests return TTT_ERR_UNSUPPORTED before anything is enqueued.
+ *   - Every GPU that loads the library holds that array until the process exits.
+ *   - All calls on a device share it: calls whose kernels overlap on the GPU
+ *     race and give wrong results, so order them (one stream, or events).
+ *   - The first call on a device looks up the array's address with that
+ *     device current; make that first call before any stream capture.
+ * Arguments and results as ttt_mlp_fwd; TTT_ERR_CUDA if the lookup fails.
+ */
+TTT_API ttt_status ttt_mlp_fwd_noalloc(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                       const float* eta, const float* W1_0, const float* W2_0, int B,
+                                       int H, int T, int d, int b, void* Z, float* W1_out,
+                                       float* W2_out, void* stream);
+
+/*
  * One TTT-Linear decode token per (batch row, head), in O(d^2) per head.
  *   q, k, v, z [B][H][d], dtype dt.  eta [H].
  *   W_anchor [B][H][d][d] float32 in/out: state at the start of the current chunk.

@@ -7,7 +7,8 @@ include/ttt.h and raise on a non-OK status. There is no CPU fallback: if the
 library is missing or no GPU is present the calls fail loudly.
 
 Names match the C entry points: ttt_workspace_bytes, ttt_linear_fwd,
-ttt_mlp_fwd, ttt_linear_decode_step, ttt_last_device_status, ttt_status_str.
+ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_linear_decode_step,
+ttt_last_device_status, ttt_status_str.
 """
 from __future__ import annotations
 
@@ -24,7 +25,7 @@ PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
 
 # Every entry point include/ttt.h declares.
 EXPORTS = ("ttt_workspace_bytes", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
-           "ttt_linear_decode_step", "ttt_last_device_status", "ttt_status_str")
+           "ttt_mlp_fwd_noalloc", "ttt_linear_decode_step", "ttt_last_device_status", "ttt_status_str")
 
 
 class TTTError(RuntimeError):
@@ -59,11 +60,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     mlp = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
     lib.ttt_mlp_fwd.argtypes = mlp
     lib.ttt_mlp_fwd_ex.argtypes = mlp + [ctypes.POINTER(ttt_options)]
+    lib.ttt_mlp_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
     lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp]
     lib.ttt_last_device_status.argtypes = [vp, vp]
     lib.ttt_status_str.argtypes = [i]
     lib.ttt_status_str.restype = ctypes.c_char_p
-    for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
+    for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex", "ttt_mlp_fwd_noalloc",
               "ttt_linear_decode_step", "ttt_last_device_status"):
         getattr(lib, f).restype = i
     _lib = lib
@@ -178,6 +180,28 @@ def ttt_mlp_fwd(Q, K, V, eta, W1_0, W2_0, b: int, Z=None, W1_out=None, W2_out=No
         st = lib.ttt_mlp_fwd_ex(*args, _opts(options))
     if st != TTT_OK:
         raise TTTError("ttt_mlp_fwd", st)
+    return Z, W1_out, W2_out
+
+
+def ttt_mlp_fwd_noalloc(Q, K, V, eta, W1_0, W2_0, b: int, Z=None, W1_out=None, W2_out=None, stream=None):
+    """TTT-MLP without a workspace (the library's fixed 8 MiB scratch array; at d = 64 up to 64 units).
+    For callers that cannot allocate device memory; calls that overlap on the GPU race."""
+    import torch
+    lib = load_library()
+    B, H, T, d = Q.shape
+    m = 4 * d
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _check(t, n, Q.dtype, (B, H, T, d))
+    _check(eta, "eta", torch.float32, (H,))
+    _check(W1_0, "W1_0", torch.float32, (H, d, m))
+    _check(W2_0, "W2_0", torch.float32, (H, m, d))
+    Z = torch.empty_like(Q) if Z is None else Z
+    W1_out = torch.empty((B, H, d, m), dtype=torch.float32, device=Q.device) if W1_out is None else W1_out
+    W2_out = torch.empty((B, H, m, d), dtype=torch.float32, device=Q.device) if W2_out is None else W2_out
+    st = lib.ttt_mlp_fwd_noalloc(_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W1_0), _p(W2_0), B, H, T, d,
+                                 int(b), _p(Z), _p(W1_out), _p(W2_out), _stream_ptr(stream))
+    if st != TTT_OK:
+        raise TTTError("ttt_mlp_fwd_noalloc", st)
     return Z, W1_out, W2_out
 
 
