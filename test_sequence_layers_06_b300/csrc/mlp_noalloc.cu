@@ -30,7 +30,7 @@
 
 #include <mutex>
 
-#include "../../include/ttt.h"
+#include "ttt.h"
 
 namespace {
 

@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <cstring>
 
-#include "../../include/ttt.h"
+#include "ttt.h"
 #include "kernels.h"
 #include "ttt_device.cuh"
 

@@ -8,7 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/ttt.h"
+#include "ttt.h"
 
 namespace ttt {
 
