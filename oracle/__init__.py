@@ -8,8 +8,9 @@ marshals numpy arrays.
 
 What it computes, and the passages it follows, is in the C file's header. In
 short: TTT-Linear and TTT-MLP, per-token primal form (the reference) and a
-separate per-chunk dual form (kept to pin primal == dual), plus one decode
-token with an (anchor, running) weight pair.
+separate per-chunk dual form (kept to pin primal == dual), the affine map of
+each segment of chunks (the segment-parallel form), plus one decode token with
+an (anchor, running) weight pair.
 
 Parity pins live in tests/test_oracle_pins.py (b = 1 delta rule; causal linear
 attention; finite differences and autograd; eta = 0; chaining; b = T closed
@@ -55,6 +56,8 @@ def _load():
             f = getattr(lib, name)
             f.argtypes = args
             f.restype = ci
+        lib.oracle_linear_segment_maps.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, i64, dp, dp, ci]
+        lib.oracle_linear_segment_maps.restype = ci
         lib.oracle_gelu_array.argtypes = [dp, i64, dp, dp]
         lib.oracle_gelu_array.restype = None
         lib.oracle_max_threads.argtypes = []
@@ -98,6 +101,23 @@ def linear_primal(Q, K, V, eta, W0, b, nthreads: int = 0):
 def linear_dual(Q, K, V, eta, W0, b, nthreads: int = 0):
     """TTT-Linear, per-chunk dual form (same results as linear_primal up to rounding)."""
     return _linear(_load().oracle_linear_dual, Q, K, V, eta, W0, b, nthreads)
+
+
+def linear_segment_maps(K, V, eta, b, L, nthreads: int = 0):
+    """Affine map of every L-token segment of TTT-Linear (L a multiple of b):
+    the segment takes its start state W to A_s W + B_s. K, V [B,H,T,d]; eta [H].
+    Returns (A [B,H,S,d,d], B [B,H,S,d,d]) in fp64, S = ceil(T / L)."""
+    K, V, eta = map(_f64, (K, V, eta))
+    B, H, T, d = K.shape
+    assert V.shape == K.shape and eta.shape == (H,)
+    S = (T + L - 1) // L
+    A = np.empty((B, H, S, d, d))
+    Bm = np.empty((B, H, S, d, d))
+    rc = _load().oracle_linear_segment_maps(_p(K), _p(V), _p(eta), B, H, T, d, int(b), int(L), _p(A), _p(Bm),
+                                             int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle returned {rc}")
+    return A, Bm
 
 
 def _mlp(fn, Q, K, V, eta, W1, W2, b, nthreads):

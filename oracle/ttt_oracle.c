@@ -39,7 +39,10 @@
  * Parity pins: b = 1 equals the delta rule; W0 = 0 with one chunk equals
  * causal linear attention; primal equals dual; gradients equal finite
  * differences and autograd; eta = 0 is the plain forward; chaining two calls
- * equals one call; b = T equals the single closed form. The tests hold them.
+ * equals one call; b = T equals the single closed form; the segment affine
+ * maps, applied in turn from W0, give the primal scan's state at every
+ * segment end, and a one-token chunk's map is I - eta k^T k, eta k^T v.
+ * The tests hold them.
  */
 #include <math.h>
 #include <stdint.h>
@@ -239,6 +242,91 @@ int oracle_linear_decode_step(const double* q, const double* k, const double* v,
   }
   free(e);
   return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * TTT-Linear as a chain of affine maps (the segment-parallel form).
+ * One chunk's gradient step, W <- W - eta K_c^T (K_c W - V_c), is affine in W:
+ *   W <- A_c W + B_c,   A_c = I - eta K_c^T K_c,   B_c = eta K_c^T V_c.
+ * Two maps applied in turn compose as (A2, B2) o (A1, B1) = (A2 A1, A2 B1 + B2).
+ * For every segment of L tokens (the last may be shorter) this returns the
+ * composition of its chunks' maps, so that the state at the segment's end is
+ * A_s W_start + B_s. The pages write the chunk update ([ch5] section 4,
+ * [guide] section 3) but not this rearrangement; it is exact algebra on it.
+ * L must be a multiple of b, so that no chunk straddles two segments.
+ * Outputs A_out, B_out [B][H][S][d][d], S = ceil(T / L).
+ * ------------------------------------------------------------------------- */
+static void linear_segment_maps_unit(const double* K, const double* V, double eta, int64_t T,
+                                     int64_t d, int64_t b, int64_t L, double* A_out, double* B_out,
+                                     double* Ac, double* Bc, double* tmp) {
+  int64_t s = 0;
+  for (int64_t s0 = 0; s0 < T; s0 += L, ++s) {
+    const int64_t s1 = (s0 + L < T) ? s0 + L : T;
+    double* A = A_out + s * d * d;
+    double* Bm = B_out + s * d * d;
+    for (int64_t i = 0; i < d; ++i)
+      for (int64_t j = 0; j < d; ++j) {
+        A[i * d + j] = (i == j) ? 1.0 : 0.0;
+        Bm[i * d + j] = 0.0;
+      }
+    for (int64_t c0 = s0; c0 < s1; c0 += b) {
+      const int64_t c1 = (c0 + b < s1) ? c0 + b : s1;
+      /* the chunk's own map */
+      for (int64_t i = 0; i < d; ++i)
+        for (int64_t j = 0; j < d; ++j) {
+          double kk = 0.0, kv = 0.0;
+          for (int64_t t = c0; t < c1; ++t) {
+            kk += K[t * d + i] * K[t * d + j];
+            kv += K[t * d + i] * V[t * d + j];
+          }
+          Ac[i * d + j] = ((i == j) ? 1.0 : 0.0) - eta * kk;
+          Bc[i * d + j] = eta * kv;
+        }
+      /* (A, B) <- (Ac A, Ac B + Bc) */
+      for (int64_t i = 0; i < d; ++i)
+        for (int64_t j = 0; j < d; ++j) {
+          double sa = 0.0, sb = 0.0;
+          for (int64_t k = 0; k < d; ++k) {
+            sa += Ac[i * d + k] * A[k * d + j];
+            sb += Ac[i * d + k] * Bm[k * d + j];
+          }
+          tmp[i * d + j] = sa;
+          tmp[d * d + i * d + j] = sb + Bc[i * d + j];
+        }
+      memcpy(A, tmp, sizeof(double) * d * d);
+      memcpy(Bm, tmp + d * d, sizeof(double) * d * d);
+    }
+  }
+}
+
+int oracle_linear_segment_maps(const double* K, const double* V, const double* eta, int64_t B,
+                               int64_t H, int64_t T, int64_t d, int64_t b, int64_t L,
+                               double* A_out, double* B_out, int nthreads) {
+  if (B < 0 || H < 1 || T < 0 || d < 1 || b < 1 || L < 1 || L % b != 0) return -1;
+  set_threads(nthreads);
+  const int64_t S = (T + L - 1) / L;
+  int bad = 0;
+#pragma omp parallel
+  {
+    double* Ac = (double*)malloc(sizeof(double) * d * d);
+    double* Bc = (double*)malloc(sizeof(double) * d * d);
+    double* tmp = (double*)malloc(sizeof(double) * 2 * d * d);
+    if (!Ac || !Bc || !tmp) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t u = 0; u < B * H; ++u) {
+      if (!Ac || !Bc || !tmp) continue;
+      const int64_t h = u % H;
+      linear_segment_maps_unit(K + u * T * d, V + u * T * d, eta[h], T, d, b, L,
+                               A_out + u * S * d * d, B_out + u * S * d * d, Ac, Bc, tmp);
+    }
+    free(Ac);
+    free(Bc);
+    free(tmp);
+  }
+  return bad ? -2 : 0;
 }
 
 /* ---------------------------------------------------------------------------

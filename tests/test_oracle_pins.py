@@ -6,7 +6,9 @@ Each pin checks the oracle against something other than itself:
   - finite differences and torch autograd (with torch's own tanh-GELU) for the
     gradient of 1/2 ||f(k) - v||^2 taken at the chunk-start weights;
   - the single closed form of one chunk, the eta = 0 forward, chaining,
-    batch-row independence, and hand-worked examples in tests/golden/.
+    batch-row independence, and hand-worked examples in tests/golden/;
+  - the segment affine maps against the per-token scan at every segment end,
+    and a one-token map by hand in exact rationals.
 A plausible slip (a dropped 1/2, a wrong sign, read-before-write, a gradient at
 the running instead of the chunk-start weights, a transposed W) fails at least
 one of them: test_planted_mistakes_are_caught plants each in a copy of the
@@ -131,6 +133,49 @@ def test_one_chunk_closed_form_with_w0():
         E = k @ w - v
         assert rel(Z[0, h], q @ w - eta[h] * np.tril(q @ k.T) @ E) < 1e-13
         assert rel(W[0, h], w - eta[h] * k.T @ E) < 1e-13
+
+
+# ------------------------------------------- P7: segment affine maps (a6 form)
+@pytest.mark.parametrize("T,b,L", [(96, 16, 32), (100, 16, 48), (64, 8, 64), (45, 5, 15), (30, 3, 30)])
+def test_segment_maps_compose_to_the_scan(T, b, L):
+    """Each chunk's step is W -> (I - eta K^T K) W + eta K^T V; a segment's map
+    is their composition. Applied in turn from W0 they must give the per-token
+    scan's state at every segment end (the scan itself is pinned above)."""
+    Q, K, V, eta, W0 = rand_linear(2, 3, T, 8, seed=T + b + L)
+    A, Bm = oracle.linear_segment_maps(K, V, eta, b, L)
+    S = -(-T // L)
+    assert A.shape == (2, 3, S, 8, 8)
+    for n in range(2):
+        for h in range(3):
+            W = W0[h].copy()
+            for s in range(S):
+                W = A[n, h, s] @ W + Bm[n, h, s]
+                end = min(T, (s + 1) * L)
+                _, Wref = oracle.linear_primal(Q[n:n + 1, :, :end], K[n:n + 1, :, :end], V[n:n + 1, :, :end],
+                                               eta, W0, b)
+                assert rel(W, Wref[0, h]) < 1e-12
+
+
+def test_segment_map_of_one_token_is_exact():
+    """One token, b = 1: the map is (I - eta k^T k, eta k^T v), by hand in exact rationals."""
+    k = [[0.5, -1.0, 0.25]]
+    v = [[2.0, 0.0, -3.0]]
+    eta = Fraction(1, 4)
+    d = 3
+    A, Bm = oracle.linear_segment_maps(np.array(k)[None, None], np.array(v)[None, None], [0.25], 1, 1)
+    Ax = [[(1 if i == j else 0) - eta * Fraction(k[0][i]) * Fraction(k[0][j]) for j in range(d)] for i in range(d)]
+    Bx = [[eta * Fraction(k[0][i]) * Fraction(v[0][j]) for j in range(d)] for i in range(d)]
+    assert np.array_equal(A[0, 0, 0], np.array(Ax, dtype=float))
+    assert np.array_equal(Bm[0, 0, 0], np.array(Bx, dtype=float))
+
+
+def test_segment_maps_of_long_segments_contract():
+    """With unit keys and 0 < eta < 2, every chunk map shrinks the span of its
+    keys, so a long segment's linear part is far below the identity."""
+    _, K, V, eta, _ = rand_linear(1, 2, 512, 8, seed=3)
+    A, _ = oracle.linear_segment_maps(K, V, eta, 16, 512)
+    for h in range(2):
+        assert np.linalg.norm(A[0, h, 0], 2) < 0.5
 
 
 # ------------------------------------------------------------ P3: primal == dual
