@@ -75,16 +75,40 @@ typedef struct {
   int32_t inject_stall;     /* test hook: 1 = the load pipeline never fills, so the
                                consumers' bounded wait must run out (TTT_ERR_TIMEOUT) */
   int32_t force_path;       /* 0 = automatic; 1 = general fp32 SIMT kernel;
-                               2 = tensor-core kernel (TTT_ERR_UNSUPPORTED if it cannot serve) */
+                               2 = tensor-core kernel, one pass per sequence;
+                               3 = tensor-core kernels, segment-parallel form.
+                               2 and 3 return TTT_ERR_UNSUPPORTED where they cannot
+                               serve (they need bf16, d = 64, b % 16 == 0). */
+  int32_t seg_len;          /* segment-parallel form only: tokens per segment, a
+                               multiple of b and of 16; 0 = chosen automatically */
 } ttt_options;
 
-/* Bytes of workspace a call with these sizes needs (>= 256; a status word
- * lives at its start). variant: TTT_VARIANT_LINEAR or TTT_VARIANT_MLP.
- * Returns 0 for invalid sizes. */
+/* Bytes of workspace a call with these sizes needs on the current device
+ * (>= 256; a status word lives at its start). variant: TTT_VARIANT_LINEAR or
+ * TTT_VARIANT_MLP. TTT-Linear with bf16 operands may run in the
+ * segment-parallel form, whose per-segment affine maps and start states live
+ * in the workspace (3 d^2 floats per segment boundary); the size covers that
+ * whatever the dtype. Returns 0 for invalid sizes. */
 TTT_API size_t ttt_workspace_bytes(int B, int H, int T, int d, int b, int variant);
+
+/* As ttt_workspace_bytes, for a call made with these options (a forced path
+ * or segment length may need more, or less). opt may be NULL. */
+TTT_API size_t ttt_workspace_bytes_ex(int B, int H, int T, int d, int b, int variant,
+                                      const ttt_options* opt);
 
 /*
  * TTT-Linear forward over whole sequences.
+ *
+ * How it runs. With bf16 operands, d = 64 and b % 16 == 0 the tensor-core
+ * kernels serve the call. When there are too few (batch row, head) units to
+ * fill the GPU, the sequence is cut into segments of whole chunks and run in
+ * the segment-parallel form: one chunk's step W <- W - eta K_c^T (K_c W - V_c)
+ * is the affine map W <- A_c W + B_c (A_c = I - eta K_c^T K_c,
+ * B_c = eta K_c^T V_c), so each segment's composed map is computed on its own,
+ * the maps are chained from W0 to give every segment's start state, and the
+ * segments are then read out side by side. Exact algebra on the chunk update
+ * ("5 · TestingTime 训练与长上下文", section 4); results agree with the one-pass
+ * form within bf16 rounding. Three kernels are enqueued; otherwise one.
  *   Q, K, V  [B][H][T][d], dtype dt.  eta [H] float32 (per-head inner learning rate).
  *   W0       [H][d][d] float32: initial state per head, shared by the batch
  *            (an outer-loop parameter); every batch row restarts from it.

@@ -6,7 +6,7 @@ take torch CUDA tensors, pass their data pointers to the C ABI of
 include/ttt.h and raise on a non-OK status. There is no CPU fallback: if the
 library is missing or no GPU is present the calls fail loudly.
 
-Names match the C entry points: ttt_workspace_bytes, ttt_linear_fwd,
+Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_fwd,
 ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_linear_decode_step,
 ttt_last_device_status, ttt_status_str.
 """
@@ -21,10 +21,10 @@ LIB_PATH = os.path.join(HERE, "libttt_b300.so")
 TTT_OK, TTT_ERR_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT, TTT_ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
 TTT_F32, TTT_BF16 = 0, 1
 TTT_VARIANT_LINEAR, TTT_VARIANT_MLP = 0, 1
-PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
+PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_SEGMENTED = 0, 1, 2, 3
 
 # Every entry point include/ttt.h declares.
-EXPORTS = ("ttt_workspace_bytes", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
+EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
            "ttt_mlp_fwd_noalloc", "ttt_linear_decode_step", "ttt_last_device_status", "ttt_status_str")
 
 
@@ -36,7 +36,7 @@ class TTTError(RuntimeError):
 
 class ttt_options(ctypes.Structure):
     _fields_ = [("wait_timeout_ns", ctypes.c_uint64), ("inject_stall", ctypes.c_int32),
-                ("force_path", ctypes.c_int32)]
+                ("force_path", ctypes.c_int32), ("seg_len", ctypes.c_int32)]
 
 
 _lib = None
@@ -54,6 +54,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.ttt_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.ttt_workspace_bytes.restype = sz
+    lib.ttt_workspace_bytes_ex.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ttt_options)]
+    lib.ttt_workspace_bytes_ex.restype = sz
     lin = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, sz, vp]
     lib.ttt_linear_fwd.argtypes = lin
     lib.ttt_linear_fwd_ex.argtypes = lin + [ctypes.POINTER(ttt_options)]
@@ -76,8 +78,12 @@ def ttt_status_str(status: int) -> str:
     return load_library().ttt_status_str(int(status)).decode()
 
 
-def ttt_workspace_bytes(B: int, H: int, T: int, d: int, b: int, variant: int = TTT_VARIANT_LINEAR) -> int:
-    return int(load_library().ttt_workspace_bytes(B, H, T, d, b, variant))
+def ttt_workspace_bytes(B: int, H: int, T: int, d: int, b: int, variant: int = TTT_VARIANT_LINEAR,
+                        options=None) -> int:
+    lib = load_library()
+    if options is None:
+        return int(lib.ttt_workspace_bytes(B, H, T, d, b, variant))
+    return int(lib.ttt_workspace_bytes_ex(B, H, T, d, b, variant, _opts(options)))
 
 
 def _dtype_code(t):
@@ -137,7 +143,7 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b: int, Z=None, W_out=None, workspace=None,
         W_out = torch.empty((B, H, d, d), dtype=torch.float32, device=Q.device)
     _check(Z, "Z", Q.dtype, (B, H, T, d))
     _check(W_out, "W_out", torch.float32, (B, H, d, d))
-    need = ttt_workspace_bytes(B, H, T, d, b, TTT_VARIANT_LINEAR)
+    need = ttt_workspace_bytes(B, H, T, d, b, TTT_VARIANT_LINEAR, options)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
     args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), B, H, T, d, int(b), _p(Z), _p(W_out),

@@ -23,6 +23,14 @@ struct LinearParams {
   StatusBlock* status;
   uint64_t timeout_ns;
   int inject_stall;
+  // Segment-parallel form (tensor-core path only). seg_count == 1: one pass
+  // over the whole sequence. Otherwise the sequence is cut into seg_count
+  // segments of seg_len tokens (a multiple of b and of 16; the last may be
+  // shorter) that run side by side from start states the combine step computes.
+  int seg_len;
+  int seg_count;
+  float* seg_maps;     // workspace [units][seg_count-1][2][d][d]: (A_s, B_s)
+  float* seg_starts;   // workspace [units][seg_count-1][d][d]: start state of segment s+1
 };
 
 struct MlpParams {
@@ -62,6 +70,13 @@ bool linear_mma_supported(const LinearParams& p);
 int linear_mma_tile_rows();
 cudaError_t launch_linear_mma(const LinearParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& mv, const CUtensorMap& mz, cudaStream_t stream);
+
+// Segment-parallel TTT-Linear (bf16, d = 64, b % 16 == 0): per-segment affine
+// maps, then the combine over segments; linear_mma then runs every segment.
+bool linear_seg_supported(const LinearParams& p);
+cudaError_t launch_linear_seg_affine(const LinearParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
+                                     cudaStream_t stream);
+cudaError_t launch_linear_seg_combine(const LinearParams& p, cudaStream_t stream);
 
 // General fp32-arithmetic TTT-Linear (any dtype, d <= 64, any b).
 cudaError_t launch_linear_simt(const LinearParams& p, cudaStream_t stream);

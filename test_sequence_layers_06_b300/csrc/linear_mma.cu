@@ -28,6 +28,10 @@
 // 2 KB each) with TMA into a 4-stage ring (128-byte swizzle, so ldmatrix is
 // conflict-free); Z leaves through a small shared staging tile per warp and a
 // TMA store. Every wait is bounded in wall-clock time.
+//
+// Segments: with p.seg_count > 1 a CTA serves one segment of one unit, starting
+// from the state the combine step of linear_seg.cu computed for it (W0 for the
+// first segment); only the last segment writes the final state.
 #include "ttt_device.cuh"
 #include "kernels.h"
 
@@ -49,7 +53,7 @@ constexpr int kSmemBytes = kAbortOff + 16 + 1024;  // + slack to align the base 
 
 enum : int { kWhereProducer = 1, kWhereConsumer = 2 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 3)
     linear_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                       const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mz,
                       LinearParams p) {
@@ -59,11 +63,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
 
-  const int unit = blockIdx.x;
+  const int unit = blockIdx.x / p.seg_count;
+  const int seg = blockIdx.x % p.seg_count;
   const int h = unit % p.H;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = (p.T + kTile - 1) / kTile;
+  const int t0 = seg * p.seg_len;  // a multiple of b: segments start on a chunk boundary
+  const int t1 = min(p.T, t0 + p.seg_len);
+  const int num_tiles = (t1 - t0 + kTile - 1) / kTile;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -92,9 +99,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*abort_flag || p.inject_stall) break;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
         uint8_t* st = smem + s * kStageBytes;
-        tma_load_3d(st, &mq, &full[s], 0, u * kTile, unit);
-        tma_load_3d(st + kTileBytes, &mk, &full[s], 0, u * kTile, unit);
-        tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, u * kTile, unit);
+        tma_load_3d(st, &mq, &full[s], 0, t0 + u * kTile, unit);
+        tma_load_3d(st + kTileBytes, &mk, &full[s], 0, t0 + u * kTile, unit);
+        tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, t0 + u * kTile, unit);
         ++issued;
       }
       // Loads still in flight must land before the CTA may exit.
@@ -115,7 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // W^T fragments: Wt[q] covers input columns i in [8q, 8q+8) of rows j = jw+g, jw+g+8.
   float Wt[8][4];
   {
-    const float* W0 = p.W0 + static_cast<size_t>(h) * kD * kD;
+    const float* W0 = seg == 0 ? p.W0 + static_cast<size_t>(h) * kD * kD
+                               : p.seg_starts + (static_cast<size_t>(unit) * (p.seg_count - 1) + seg - 1) * kD * kD;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int i = 8 * q + 2 * tg;
@@ -273,11 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_3d(&mz, zbuf, jw, u * kTile, unit);
+      tma_store_3d(&mz, zbuf, jw, t0 + u * kTile, unit);
       bulk_commit();
     }
   }
   if (lane == 0) bulk_wait<0>();
+  if (seg != p.seg_count - 1) return;
 
   // Final state, W_out[unit][i][j].
   float* Wo = p.W_out + static_cast<size_t>(unit) * kD * kD;
@@ -298,7 +307,7 @@ bool linear_mma_supported(const LinearParams& p) { return p.d == kD && p.b % kTi
 cudaError_t launch_linear_mma(const LinearParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& mv, const CUtensorMap& mz, cudaStream_t stream) {
   if (p.units == 0) return cudaSuccess;
-  linear_mma_kernel<<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mz, p);
+  linear_mma_kernel<<<p.units * p.seg_count, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mz, p);
   return cudaGetLastError();
 }
 

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 
 #include "ttt.h"
@@ -32,14 +33,93 @@ bool sizes_ok(int B, int H, int T, int d, int b) {
 
 size_t mlp_hidden(int d) { return static_cast<size_t>(4) * d; }
 
+ttt_options defaults(const ttt_options* opt) {
+  ttt_options o;
+  std::memset(&o, 0, sizeof(o));
+  if (opt) o = *opt;
+  if (o.wait_timeout_ns == 0) o.wait_timeout_ns = kDefaultTimeoutNs;
+  return o;
+}
+
+// Streaming multiprocessors of the current device (148 on a B300 if the query fails).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// How TTT-Linear runs: which kernel, and for the segment-parallel form how the
+// sequence is cut. A plan with seg_count == 1 is one pass over every sequence.
+struct LinearPlan {
+  bool mma;       // tensor-core kernels (bf16, d = 64, b % 16 == 0); else fp32 SIMT
+  int seg_len;    // tokens per segment (a multiple of b)
+  int seg_count;  // segments per (batch row, head)
+};
+
+constexpr int kSegMinTokens = 256;  // shortest segment the automatic plan makes
+constexpr int kSegWavesTarget = 2;  // read-out work items per resident CTA slot (at most)
+constexpr int kMmaCtasPerSm = 3;    // linear_mma_kernel's occupancy (its launch bounds)
+
+ttt_status plan_linear(int B, int H, int T, int d, int b, bool bf16, const ttt_options& o, LinearPlan* out) {
+  LinearPlan pl{false, T > 0 ? T : 1, 1};
+  const bool mma_ok = d == 64 && b % 16 == 0 && bf16;
+  if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
+  if (o.force_path == 3 && !mma_ok) return TTT_ERR_UNSUPPORTED;
+  if (o.seg_len < 0) return TTT_ERR_ARG;
+  if (o.seg_len > 0 && (o.seg_len % b != 0 || o.seg_len % 16 != 0)) return TTT_ERR_ARG;
+  pl.mma = mma_ok && o.force_path != 1 && T > 0;
+  if (!pl.mma) {
+    *out = pl;
+    return TTT_OK;
+  }
+  const int units = B * H;
+  const int slots = kMmaCtasPerSm * sm_count();  // resident read-out CTAs
+  bool seg = false;
+  if (o.force_path == 3) seg = true;
+  if (o.force_path == 0 && units < slots && T >= 2 * kSegMinTokens) seg = true;
+  if (seg) {
+    long long len = o.seg_len;
+    if (len == 0) {
+      // Whole waves of read-out CTAs: units * S <= kSegWavesTarget * slots.
+      const long long S = std::max(1LL, static_cast<long long>(kSegWavesTarget) * slots / units);
+      len = (T + S - 1) / S;
+      const long long min_len = ((kSegMinTokens + b - 1) / b) * b;
+      len = ((len + b - 1) / b) * b;
+      if (len < min_len) len = min_len;
+    }
+    const long long count = (T + len - 1) / len;
+    if (count >= 2) {
+      pl.seg_len = static_cast<int>(len);
+      pl.seg_count = static_cast<int>(count);
+    }
+  }
+  *out = pl;
+  return TTT_OK;
+}
+
+// Bytes of segment scratch: affine maps (A_s, B_s) and start states, both for
+// every segment but one, fp32.
+size_t seg_scratch_bytes(const LinearPlan& pl, int units, int d) {
+  if (pl.seg_count < 2) return 0;
+  const size_t per = static_cast<size_t>(units) * (pl.seg_count - 1) * d * d * sizeof(float);
+  return 3 * per;
+}
+
 // Workspace: [status block 256 B][variant scratch].
-size_t workspace_bytes_impl(int B, int H, int T, int d, int b, int variant) {
+size_t workspace_bytes_impl(int B, int H, int T, int d, int b, int variant, const ttt_options* opt) {
   if (!sizes_ok(B, H, T, d, b)) return 0;
   size_t bytes = kStatusBytes;
-  if (variant == TTT_VARIANT_MLP)
+  if (variant == TTT_VARIANT_MLP) {
     bytes += round_up(ttt::mlp_simt_snapshot_bytes(B * H, d, static_cast<int>(mlp_hidden(d))), 256);
-  else if (variant != TTT_VARIANT_LINEAR)
+  } else if (variant == TTT_VARIANT_LINEAR) {
+    // Sized for bf16 operands, the only dtype whose plan may use segments.
+    LinearPlan pl;
+    if (plan_linear(B, H, T, d, b, true, defaults(opt), &pl) == TTT_OK) bytes += seg_scratch_bytes(pl, B * H, d);
+  } else {
     return 0;
+  }
   return bytes;
 }
 
@@ -75,14 +155,6 @@ bool encode_3d(CUtensorMap* map, const void* base, int units, int T, int d, int 
   return r == CUDA_SUCCESS;
 }
 
-ttt_options defaults(const ttt_options* opt) {
-  ttt_options o;
-  std::memset(&o, 0, sizeof(o));
-  if (opt) o = *opt;
-  if (o.wait_timeout_ns == 0) o.wait_timeout_ns = kDefaultTimeoutNs;
-  return o;
-}
-
 ttt_status reset_status(void* ws, cudaStream_t s) {
   return cudaMemsetAsync(ws, 0, sizeof(ttt::StatusBlock), s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
@@ -92,7 +164,11 @@ ttt_status reset_status(void* ws, cudaStream_t s) {
 extern "C" {
 
 size_t ttt_workspace_bytes(int B, int H, int T, int d, int b, int variant) {
-  return workspace_bytes_impl(B, H, T, d, b, variant);
+  return workspace_bytes_impl(B, H, T, d, b, variant, nullptr);
+}
+
+size_t ttt_workspace_bytes_ex(int B, int H, int T, int d, int b, int variant, const ttt_options* opt) {
+  return workspace_bytes_impl(B, H, T, d, b, variant, opt);
 }
 
 const char* ttt_status_str(ttt_status s) {
@@ -119,9 +195,12 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
                         static_cast<const void*>(Z), static_cast<const void*>(eta), static_cast<const void*>(W0),
                         static_cast<const void*>(W_out), static_cast<const void*>(workspace)})
     if (p && !aligned16(p)) return TTT_ERR_ARG;
-  if (ws_bytes < workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_LINEAR)) return TTT_ERR_ARG;
   const ttt_options o = defaults(opt);
-  if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
+  if (o.force_path < 0 || o.force_path > 3) return TTT_ERR_ARG;
+  LinearPlan pl;
+  const ttt_status pst = plan_linear(B, H, T, d, b, dt == TTT_BF16, o, &pl);
+  if (pst != TTT_OK) return pst;
+  if (ws_bytes < kStatusBytes + seg_scratch_bytes(pl, B * H, d)) return TTT_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   ttt::LinearParams p;
@@ -133,15 +212,20 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
   p.status = static_cast<ttt::StatusBlock*>(workspace);
   p.timeout_ns = o.wait_timeout_ns;
   p.inject_stall = o.inject_stall;
-
-  const bool mma_ok = ttt::linear_mma_supported(p);
-  if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
-  const bool use_mma = mma_ok && o.force_path != 1 && T > 0;
+  p.seg_len = pl.seg_len;
+  p.seg_count = pl.seg_count;
+  p.seg_maps = nullptr;
+  p.seg_starts = nullptr;
+  if (pl.seg_count > 1) {
+    const size_t per = static_cast<size_t>(p.units) * (pl.seg_count - 1) * d * d;
+    p.seg_maps = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+    p.seg_starts = p.seg_maps + 2 * per;
+  }
 
   ttt_status st = reset_status(workspace, s);
   if (st != TTT_OK) return st;
   cudaError_t err;
-  if (use_mma) {
+  if (pl.mma) {
     CUtensorMap mq, mk, mv, mz;
     const int rows = ttt::linear_mma_tile_rows();
     if (!encode_3d(&mq, Q, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -149,7 +233,12 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
         !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_3d(&mz, Z, p.units, T, d, rows, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
       return TTT_ERR_CUDA;
-    err = ttt::launch_linear_mma(p, mq, mk, mv, mz, s);
+    err = cudaSuccess;
+    if (pl.seg_count > 1) {
+      err = ttt::launch_linear_seg_affine(p, mk, mv, s);
+      if (err == cudaSuccess) err = ttt::launch_linear_seg_combine(p, s);
+    }
+    if (err == cudaSuccess) err = ttt::launch_linear_mma(p, mq, mk, mv, mz, s);
   } else {
     err = ttt::launch_linear_simt(p, s);
   }
@@ -177,7 +266,7 @@ ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype
                         static_cast<const void*>(W2_0), static_cast<const void*>(W1_out),
                         static_cast<const void*>(W2_out), static_cast<const void*>(workspace)})
     if (p && !aligned16(p)) return TTT_ERR_ARG;
-  if (ws_bytes < workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP)) return TTT_ERR_ARG;
+  if (ws_bytes < workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP, nullptr)) return TTT_ERR_ARG;
   const ttt_options o = defaults(opt);
   if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
   if (o.force_path == 2) return TTT_ERR_UNSUPPORTED;

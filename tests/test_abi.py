@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 9
+    assert len(names) == 10
     assert set(names) == set(ttt.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -44,6 +44,19 @@ def test_workspace_bytes(lib):
     assert ttt.ttt_workspace_bytes(0, 1, 1, 64, 16, 0) == 0
     assert ttt.ttt_workspace_bytes(1, 1, 1, 64, 0, 0) == 0
     assert ttt.ttt_workspace_bytes(1, 1, 1, 64, 16, 7) == 0
+
+
+def test_workspace_bytes_for_the_segment_parallel_form(lib):
+    """bf16 TTT-Linear with few units is cut into segments whose affine maps and
+    start states live in the workspace: 3 d^2 floats per segment boundary."""
+    base = ttt.ttt_workspace_bytes(1, 32, 131072, 64, 16, 0)
+    assert base > 256 and (base - 256) % (3 * 32 * 64 * 64 * 4) == 0
+    # a forced one-pass run needs only the status block; a forced segment length sets the count
+    assert ttt.ttt_workspace_bytes(1, 32, 131072, 64, 16, 0, {"force_path": ttt.PATH_TENSOR}) == 256
+    seg = ttt.ttt_workspace_bytes(2, 3, 1000, 64, 16, 0, {"force_path": ttt.PATH_SEGMENTED, "seg_len": 256})
+    assert seg == 256 + 3 * (2 * 3) * 3 * 64 * 64 * 4  # ceil(1000 / 256) = 4 segments, 3 boundaries
+    # plenty of units: one pass
+    assert ttt.ttt_workspace_bytes(64, 64, 8192, 64, 16, 0) == 256
 
 
 def _lin(lib, **kw):
@@ -76,6 +89,20 @@ def test_forced_tensor_path_rejects_shapes_it_cannot_serve(lib):
         st = lib.ttt_linear_fwd_ex(vp(4096), vp(4096), vp(4096), a["dt"], vp(4096), vp(4096), 1, 1, 16, a["d"],
                                    a["b"], vp(4096), vp(4096), vp(4096), 1 << 20, vp(0), ctypes.byref(o))
         assert st == ttt.TTT_ERR_UNSUPPORTED, kw
+
+
+def test_segment_options_are_checked(lib):
+    vp = ctypes.c_void_p
+
+    def call(o, b=16, dt=1):
+        return lib.ttt_linear_fwd_ex(vp(4096), vp(4096), vp(4096), dt, vp(4096), vp(4096), 1, 1, 1024, 64, b,
+                                     vp(4096), vp(4096), vp(4096), 1 << 20, vp(0), ctypes.byref(o))
+    assert call(ttt.ttt_options(0, 0, ttt.PATH_SEGMENTED, 40)) == ttt.TTT_ERR_ARG   # not a multiple of 16
+    assert call(ttt.ttt_options(0, 0, ttt.PATH_SEGMENTED, 48), b=32) == ttt.TTT_ERR_ARG  # not a multiple of b
+    assert call(ttt.ttt_options(0, 0, ttt.PATH_SEGMENTED, -16)) == ttt.TTT_ERR_ARG
+    assert call(ttt.ttt_options(0, 0, 4, 0)) == ttt.TTT_ERR_ARG
+    assert call(ttt.ttt_options(0, 0, ttt.PATH_SEGMENTED, 0), dt=0) == ttt.TTT_ERR_UNSUPPORTED
+    assert call(ttt.ttt_options(0, 0, ttt.PATH_SEGMENTED, 0), b=8) == ttt.TTT_ERR_UNSUPPORTED
 
 
 def test_mlp_and_decode_reject_bad_arguments(lib):

@@ -68,6 +68,50 @@ def test_tensor_path_ragged_and_chunk_sizes(T, b):
     check(inp, b, ttt.PATH_TENSOR)
 
 
+@pytest.mark.parametrize("T,b,seg", [(1024, 16, 256), (1000, 16, 256), (64, 16, 32), (777, 16, 16),
+                                     (2048, 64, 512), (2560, 256, 512), (1300, 32, 64), (4096, 16, 1024)])
+def test_segment_parallel_path(T, b, seg):
+    """Segment-parallel form: per-segment affine maps, the combine, and a read-out
+    per segment from its start state. Full, ragged and one-tile segments; chunks
+    of 1, 2, 4 and 16 tiles; per-head eta."""
+    w = W["linear_125m"].with_(B=2, H=3, T=T, seed=300 + T + b + seg)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    opts = {"force_path": ttt.PATH_SEGMENTED, "seg_len": seg}
+    Z, Wo = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], b, options=opts)
+    torch.cuda.synchronize()
+    Zr, Wr = oracle_linear(inp, b)
+    ez, ew = rel_l2(to64(Z), Zr), rel_l2(to64(Wo), Wr)
+    assert ez <= tolerance(w) and ew <= tolerance(w), (ez, ew, worst_unit_rel(to64(Z), Zr))
+
+
+def test_segment_parallel_equals_one_pass():
+    """The two tensor-core forms agree with each other within bf16 rounding."""
+    w = W["linear_small"].with_(B=2, H=4, T=2048, seed=41)
+    t = torch_inputs(synth.make_inputs(w, want_exact=False))
+    Z1, W1 = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16,
+                                options={"force_path": ttt.PATH_TENSOR})
+    Z2, W2 = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16,
+                                options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 256})
+    torch.cuda.synchronize()
+    assert rel_l2(to64(Z2), to64(Z1)) < 1e-2 and rel_l2(to64(W2), to64(W1)) < 1e-2
+
+
+def test_segment_parallel_bounded_wait_reports_timeout():
+    w = W["linear_small"].with_(B=1, H=2, T=512)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    opts = {"force_path": ttt.PATH_SEGMENTED, "seg_len": 128}
+    ws = torch.zeros(ttt.ttt_workspace_bytes(1, 2, 512, 64, 16, 0, opts), dtype=torch.uint8, device="cuda")
+    ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16, workspace=ws,
+                       options=dict(opts, inject_stall=1, wait_timeout_ns=1_000_000))
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_ERR_TIMEOUT
+    Z, Wo = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16, workspace=ws, options=opts)
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    Zr, Wr = oracle_linear(inp, 16)
+    assert rel_l2(to64(Z), Zr) <= 2e-2 and rel_l2(to64(Wo), Wr) <= 2e-2
+
+
 @pytest.mark.parametrize("d,T,b,dtype", [(16, 40, 16, "f32"), (32, 37, 5, "f32"), (64, 33, 1, "f32"),
                                          (16, 64, 16, "bf16"), (32, 70, 7, "bf16"), (64, 19, 3, "bf16"),
                                          (8, 23, 4, "f32")])
@@ -99,7 +143,8 @@ def test_full_size_125m_sampled(name, units):
 
 @pytest.mark.parametrize("b", [16, 64, 256])
 def test_full_size_long_context_sampled(b):
-    """B1 H32 T131072 at b in {16, 64, 256}: oracle on two sampled heads."""
+    """B1 H32 T131072 at b in {16, 64, 256} (the automatic plan runs the
+    segment-parallel form here, as the benchmark does): oracle on two sampled heads."""
     w = W["linear_long"].with_(b=b)
     full = synth.make_inputs(w, want_exact=False)
     t = torch_inputs(full)
