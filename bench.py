@@ -4,9 +4,12 @@
 A step is one ttt_linear_fwd over the whole long-context workload
 (B1 H32 T131072 d64, chunk b = 16, bf16 Q/K/V, fp32 state): every stage of the
 hot path (chunk loads, error at the chunk start, intra-chunk scores, read-out,
-state update, write-back of Z and W_out). Metric: token·heads per second, and
-the dominant kernel's fraction of the HBM roofline (algorithmic bytes: Q, K, V
-read and Z written, plus the state read and written once).
+state update, write-back of Z and W_out). With 32 heads the library runs the
+segment-parallel form: an affine-map kernel, a combine kernel and the read-out
+kernel. Metric: token·heads per second, and the dominant kernel's fraction of
+the HBM roofline (its algorithmic bytes over its own event-timed duration; for
+the read-out kernel: Q, K, V read and Z written, plus the states), with every
+kernel's share and the whole step's fraction beside it.
 
 Arms
   default            our CUDA library through its C ABI (device-resident inputs),
@@ -22,6 +25,7 @@ token·heads over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -41,15 +45,21 @@ METRIC = "TTT-Linear scan tokens·heads/sec and % of binding roofline (1×B300)"
 UNIT = "token·heads/s"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
-KERNEL_SOURCES = ("test_sequence_layers_06_b300/csrc/linear_mma.cu",)
-PROFILE_SUMMARY = "profiles/linear_mma_long_b16.md"
+# kernel -> (source files whose digest a committed ncu summary must match, summary file)
+KERNEL_PROFILES = {
+    "linear_mma_kernel": (("test_sequence_layers_06_b300/csrc/linear_mma.cu",), "profiles/linear_mma_long_b16.md"),
+    "linear_seg_affine_kernel": (("test_sequence_layers_06_b300/csrc/linear_seg.cu",),
+                                 "profiles/linear_seg_affine_long_b16.md"),
+    "linear_seg_combine_kernel": (("test_sequence_layers_06_b300/csrc/linear_seg.cu",),
+                                  "profiles/linear_seg_combine_long_b16.md"),
+}
 BAD_REASONS = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="linear_long")
@@ -67,6 +77,21 @@ def algorithmic_bytes(w: synth.Workload) -> int:
     return w.token_heads * 4 * w.d * es + w.H * w.d * w.d * 4 + w.units * w.d * w.d * 4
 
 
+def kernel_bytes(w: synth.Workload, plan) -> tuple:
+    """Algorithmic bytes of each kernel of one step: (affine maps, combine, read-out).
+    Affine maps: K, V of every segment that has a map read once, the maps written.
+    Combine: the maps read, the start states written (and W0). Read-out: Q, K, V
+    read and Z written once, W0 and the start states read, W_out written."""
+    es = 2 if w.dtype == "bf16" else 4
+    state = w.d * w.d * 4
+    bounds = w.units * (plan["seg_count"] - 1)
+    if bounds == 0:
+        return 0, 0, algorithmic_bytes(w)
+    affine = bounds * plan["seg_len"] * 2 * w.d * es + bounds * 2 * state
+    combine = bounds * 3 * state + w.units * state
+    return affine, combine, algorithmic_bytes(w) + bounds * state
+
+
 def algorithmic_flops(w: synth.Workload, b: int) -> int:
     """Per chunk of b tokens: E, Q W and K^T E (2 b d^2 each) plus Q K^T and S E (2 b^2 d each)."""
     return w.token_heads * (6 * w.d * w.d + 4 * b * w.d)
@@ -81,26 +106,28 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, 1800.0, "fallback"
 
 
-def source_digest() -> str:
+def source_digest(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_PROFILES[kernel][0]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """dram bytes per launch from the committed ncu summary, if it was taken on today's kernel source."""
-    path = os.path.join(ROOT, PROFILE_SUMMARY)
+def profiled_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary of `kernel`, if it was taken on today's
+    kernel source and on this workload."""
+    path = os.path.join(ROOT, KERNEL_PROFILES[kernel][1])
     if not os.path.exists(path):
         return None
     vals = {}
     with open(path) as f:
         for line in f:
-            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha")):
+            if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha",
+                                                        "workload")):
                 k, v = line.strip().split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha") != source_digest():
+    if vals.get("kernel_source_sha") != source_digest(kernel) or vals.get("workload") != workload:
         return None
     try:
         return int(float(vals["traffic_bytes_per_launch"]))
@@ -148,33 +175,44 @@ class ClockSampler:
 
     SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active")
 
+    def _smi_reader(self):
+        for line in self._p.stdout:
+            if self._stop.is_set():
+                continue  # drain without recording
+            try:
+                sm, mx, reasons = [x.strip() for x in line.split(",")]
+                self.samples.append(float(sm))
+                self.max_mhz = float(mx)
+                self.reasons |= int(reasons, 16)
+                self._first.set()
+            except ValueError:
+                continue
+
     def __enter__(self):
+        self._stop = threading.Event()
         if self.mode == "nvml":
-            self._stop = threading.Event()
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
         elif self.mode == "nvidia-smi":
             import subprocess
+            self._first = threading.Event()
             self._p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}",
-                                        "--format=csv,noheader,nounits", "-lms", "50"],
+                                        "--format=csv,noheader,nounits", "-lms", "20"],
                                        stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._smi_reader, daemon=True)
+            self._t.start()
+            self._first.wait(5.0)  # the timed region starts once sampling runs
+            self.samples.clear()
+            self.reasons = 0
         return self
 
     def __exit__(self, *a):
+        self._stop.set()
         if self.mode == "nvml":
-            self._stop.set()
             self._t.join()
         elif self.mode == "nvidia-smi":
             self._p.terminate()
-            out, _ = self._p.communicate()
-            for line in out.splitlines():
-                try:
-                    sm, mx, reasons = [x.strip() for x in line.split(",")]
-                    self.samples.append(float(sm))
-                    self.max_mhz = float(mx)
-                    self.reasons |= int(reasons, 16)
-                except ValueError:
-                    continue
+            self._t.join(2.0)
 
     def report(self):
         reasons = sorted(n for bit, n in self.NAMES.items() if self.reasons & bit and n != "gpu_idle")
@@ -260,10 +298,21 @@ def bench_ours(args, world, rank, local):
     Wo = torch.empty((w.B, w.H, w.d, w.d), dtype=torch.float32, device=dev)
     ws = torch.zeros(ttt.ttt_workspace_bytes(w.B, w.H, w.T, w.d, args.b), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 1  # ttt_linear_fwd enqueues one kernel (plus a 16-byte status memset)
+    plan = ttt.ttt_linear_plan(w.B, w.H, w.T, w.d, args.b, ttt.TTT_BF16 if w.dtype == "bf16" else ttt.TTT_F32)
+    launches_per_step = plan["kernels"]  # plus a 16-byte status memset per call
 
-    def step():
-        ttt.ttt_linear_fwd(Q, K, V, eta, W0, args.b, Z=Z, W_out=Wo, workspace=ws, stream=stream)
+    # Per-step phase events, recorded by the library on its stream around each kernel:
+    # [start, after affine maps, after combine, after read-out].
+    phase = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for evs in phase:  # create the CUDA events (torch makes them on first record)
+        for e in evs:
+            e.record(stream)
+    phase_handles = [(ctypes.c_void_p * 4)(*[e.cuda_event for e in evs]) for evs in phase]
+    phase_opts = [ttt.ttt_options(0, 0, 0, 0, ctypes.cast(h, ctypes.c_void_p)) for h in phase_handles]
+
+    def step(i=None):
+        ttt.ttt_linear_fwd(Q, K, V, eta, W0, args.b, Z=Z, W_out=Wo, workspace=ws, stream=stream,
+                           options=None if i is None else phase_opts[i])
 
     def barrier():
         if world > 1:
@@ -277,8 +326,6 @@ def bench_ours(args, world, rank, local):
         raise RuntimeError("device status not OK after warm-up")
 
     def timed():
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         barrier()
         torch.cuda.synchronize()
         sampler = ClockSampler(local)
@@ -287,14 +334,12 @@ def bench_ours(args, world, rank, local):
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
             for i in range(args.steps):
-                starts[i].record(stream)
-                step()
-                ends[i].record(stream)
+                step(i)
             t1.record(stream)
             torch.cuda.synchronize()
         barrier()
         total_ms = t0.elapsed_time(t1)
-        per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        per = [[evs[k].elapsed_time(evs[k + 1]) for k in range(3)] for evs in phase]
         return total_ms, per, sampler
 
     total_ms, per, sampler = timed()
@@ -311,17 +356,30 @@ def bench_ours(args, world, rank, local):
     ms_per_step = total_ms / args.steps
     value = world * w.token_heads / (ms_per_step * 1e-3)
 
-    # roofline of the dominant (only) kernel
+    # roofline: every kernel's algorithmic bytes over its own mean event-timed duration
     hbm_gbs, _, peak_kind = measured_peaks()
-    kernel_ms = float(np.mean(per))
+    kernel_ms = [float(np.mean([p[k] for p in per])) for k in range(3)]
+    kbytes = kernel_bytes(w, plan)
+    names = ("linear_seg_affine_kernel", "linear_seg_combine_kernel", "linear_mma_kernel")
+    kernels = {}
+    for k, name in enumerate(names):
+        if kbytes[k] == 0:
+            continue
+        gbs = kbytes[k] / (kernel_ms[k] * 1e-3) / 1e9
+        kernels[name] = {"ms": round(kernel_ms[k], 4), "share": round(kernel_ms[k] / ms_per_step, 4),
+                         "algorithmic_bytes": kbytes[k], "achieved_gbs": round(gbs, 1),
+                         "frac": round(gbs / hbm_gbs, 4)}
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
     alg_bytes = algorithmic_bytes(w)
-    achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
-                "frac": round(achieved / hbm_gbs, 4), "traffic": profiled_traffic(),
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": hbm_gbs,
+                "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": profiled_traffic(dom, w.name),
                 "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.4 TB/s",
-                "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": round(kernel_ms, 4),
-                "flops_per_launch": algorithmic_flops(w, args.b)}
+                "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes"], "kernel_ms": kernels[dom]["ms"],
+                "kernels": kernels,
+                "step": {"algorithmic_bytes": alg_bytes, "ms": round(ms_per_step, 4),
+                         "frac": round(alg_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_gbs, 4)},
+                "flops_per_step": algorithmic_flops(w, args.b)}
 
     # end to end: pinned host buffers in, Z and W_out back out, through the public call
     e2e = None
@@ -385,6 +443,8 @@ def bench_ours(args, world, rank, local):
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "b": args.b,
                        "inputs": f"Q/K/V {w.dtype} {w.note}", "state": "fp32",
+                       "path": {1: "fp32 SIMT", 2: "tensor-core one pass", 3: "segment-parallel"}[plan["path"]],
+                       "seg_len": plan["seg_len"], "seg_count": plan["seg_count"],
                        "l2": "inputs larger than L2 (%.2f GB vs 126 MB)" % (3 * w.token_heads * w.d * 2 / 1e9),
                        "parallelism": f"replicas x{world} (independent units, no collective)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
