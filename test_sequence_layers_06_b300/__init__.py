@@ -6,7 +6,7 @@ take torch CUDA tensors, pass their data pointers to the C ABI of
 include/ttt.h and raise on a non-OK status. There is no CPU fallback: if the
 library is missing or no GPU is present the calls fail loudly.
 
-Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_fwd,
+Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_plan, ttt_linear_fwd,
 ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_linear_decode_step,
 ttt_last_device_status, ttt_status_str.
 """
@@ -24,7 +24,7 @@ TTT_VARIANT_LINEAR, TTT_VARIANT_MLP = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_SEGMENTED = 0, 1, 2, 3
 
 # Every entry point include/ttt.h declares.
-EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
+EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_plan", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
            "ttt_mlp_fwd_noalloc", "ttt_linear_decode_step", "ttt_last_device_status", "ttt_status_str")
 
 
@@ -36,7 +36,13 @@ class TTTError(RuntimeError):
 
 class ttt_options(ctypes.Structure):
     _fields_ = [("wait_timeout_ns", ctypes.c_uint64), ("inject_stall", ctypes.c_int32),
-                ("force_path", ctypes.c_int32), ("seg_len", ctypes.c_int32)]
+                ("force_path", ctypes.c_int32), ("seg_len", ctypes.c_int32),
+                ("phase_events", ctypes.c_void_p)]
+
+
+class ttt_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("seg_len", ctypes.c_int32), ("seg_count", ctypes.c_int32),
+                ("kernels", ctypes.c_int32)]
 
 
 _lib = None
@@ -56,6 +62,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_workspace_bytes.restype = sz
     lib.ttt_workspace_bytes_ex.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ttt_options)]
     lib.ttt_workspace_bytes_ex.restype = sz
+    lib.ttt_linear_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ttt_options), ctypes.POINTER(ttt_plan)]
+    lib.ttt_linear_plan.restype = i
     lin = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, sz, vp]
     lib.ttt_linear_fwd.argtypes = lin
     lib.ttt_linear_fwd_ex.argtypes = lin + [ctypes.POINTER(ttt_options)]
@@ -84,6 +92,15 @@ def ttt_workspace_bytes(B: int, H: int, T: int, d: int, b: int, variant: int = T
     if options is None:
         return int(lib.ttt_workspace_bytes(B, H, T, d, b, variant))
     return int(lib.ttt_workspace_bytes_ex(B, H, T, d, b, variant, _opts(options)))
+
+
+def ttt_linear_plan(B: int, H: int, T: int, d: int, b: int, dtype: int = TTT_BF16, options=None) -> dict:
+    """How ttt_linear_fwd runs for these sizes: {path, seg_len, seg_count, kernels}."""
+    out = ttt_plan()
+    st = load_library().ttt_linear_plan(B, H, T, d, b, dtype, _opts(options), ctypes.byref(out))
+    if st != TTT_OK:
+        raise TTTError("ttt_linear_plan", st)
+    return {f: int(getattr(out, f)) for f, _ in ttt_plan._fields_}
 
 
 def _dtype_code(t):

@@ -31,6 +31,7 @@ struct LinearParams {
   int seg_count;
   float* seg_maps;     // workspace [units][seg_count-1][2][d][d]: (A_s, B_s)
   float* seg_starts;   // workspace [units][seg_count-1][d][d]: start state of segment s+1
+  int affine_wy;       // affine maps on the tcgen05 kernel (64-token steps); else warp-level MMAs
 };
 
 struct MlpParams {
@@ -77,6 +78,12 @@ bool linear_seg_supported(const LinearParams& p);
 cudaError_t launch_linear_seg_affine(const LinearParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                                      cudaStream_t stream);
 cudaError_t launch_linear_seg_combine(const LinearParams& p, cudaStream_t stream);
+// The affine maps on tcgen05 in 64-token steps (b = 16, 32 or a multiple of 64;
+// seg_len a multiple of 64 and of b). Tensor maps with 64-row boxes.
+bool linear_seg_wy_supported(int b, int seg_len);
+int linear_seg_wy_rows();
+cudaError_t launch_linear_seg_affine_wy(const LinearParams& p, const CUtensorMap& mk64, const CUtensorMap& mv64,
+                                        cudaStream_t stream);
 
 // General fp32-arithmetic TTT-Linear (any dtype, d <= 64, any b).
 cudaError_t launch_linear_simt(const LinearParams& p, cudaStream_t stream);

@@ -9,7 +9,9 @@
 // write the update this way; it is exact algebra on it, and it lets one head's
 // sequence be cut into S segments that run side by side:
 //
-//   1. linear_seg_affine_kernel: (A_s, B_s) of every segment but the last, all
+//   1. linear_seg_affine_kernel (here, warp-level MMAs) or
+//      linear_seg_affine_wy_kernel (linear_seg_wy.cu, tcgen05 tensor cores, the
+//      default where it applies): (A_s, B_s) of every segment but the last, all
 //      at once. It runs the chunk update on the 64 x 128 state X = [A | B] from
 //      X = [I | 0]; the value rows are 0 for the A half and V_c for the B half,
 //      so the A half follows A <- A_c A and the B half B <- A_c B + B_c.
@@ -24,6 +26,7 @@
 // error at the chunk-start snapshot of X.
 #include "ttt_device.cuh"
 #include "kernels.h"
+
 
 namespace ttt {
 namespace {

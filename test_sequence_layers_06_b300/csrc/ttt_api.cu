@@ -56,6 +56,7 @@ struct LinearPlan {
   bool mma;       // tensor-core kernels (bf16, d = 64, b % 16 == 0); else fp32 SIMT
   int seg_len;    // tokens per segment (a multiple of b)
   int seg_count;  // segments per (batch row, head)
+  bool affine_wy; // affine maps on tcgen05 in 64-token steps (else warp-level MMAs)
 };
 
 constexpr int kSegMinTokens = 256;  // shortest segment the automatic plan makes
@@ -63,7 +64,7 @@ constexpr int kSegWavesTarget = 2;  // read-out work items per resident CTA slot
 constexpr int kMmaCtasPerSm = 3;    // linear_mma_kernel's occupancy (its launch bounds)
 
 ttt_status plan_linear(int B, int H, int T, int d, int b, bool bf16, const ttt_options& o, LinearPlan* out) {
-  LinearPlan pl{false, T > 0 ? T : 1, 1};
+  LinearPlan pl{false, T > 0 ? T : 1, 1, false};
   const bool mma_ok = d == 64 && b % 16 == 0 && bf16;
   if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
   if (o.force_path == 3 && !mma_ok) return TTT_ERR_UNSUPPORTED;
@@ -85,14 +86,18 @@ ttt_status plan_linear(int B, int H, int T, int d, int b, bool bf16, const ttt_o
       // Whole waves of read-out CTAs: units * S <= kSegWavesTarget * slots.
       const long long S = std::max(1LL, static_cast<long long>(kSegWavesTarget) * slots / units);
       len = (T + S - 1) / S;
-      const long long min_len = ((kSegMinTokens + b - 1) / b) * b;
-      len = ((len + b - 1) / b) * b;
+      // Segments hold whole chunks; where the 64-token tensor-core affine kernel
+      // applies (b = 16, 32 or a multiple of 64) they also hold whole 64-token steps.
+      const long long align = (b % 64 == 0 || 64 % b == 0) ? std::max(b, 64) : b;
+      const long long min_len = ((kSegMinTokens + align - 1) / align) * align;
+      len = ((len + align - 1) / align) * align;
       if (len < min_len) len = min_len;
     }
     const long long count = (T + len - 1) / len;
     if (count >= 2) {
       pl.seg_len = static_cast<int>(len);
       pl.seg_count = static_cast<int>(count);
+      pl.affine_wy = ttt::linear_seg_wy_supported(b, pl.seg_len);
     }
   }
   *out = pl;
@@ -183,6 +188,24 @@ const char* ttt_status_str(ttt_status s) {
   return "unknown status";
 }
 
+ttt_status ttt_linear_plan(int B, int H, int T, int d, int b, ttt_dtype dt, const ttt_options* opt,
+                           ttt_plan* out) {
+  if (out == nullptr) return TTT_ERR_ARG;
+  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
+  if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
+  if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
+  const ttt_options o = defaults(opt);
+  if (o.force_path < 0 || o.force_path > 3) return TTT_ERR_ARG;
+  LinearPlan pl;
+  const ttt_status st = plan_linear(B, H, T, d, b, dt == TTT_BF16, o, &pl);
+  if (st != TTT_OK) return st;
+  out->path = !pl.mma ? 1 : (pl.seg_count > 1 ? 3 : 2);
+  out->seg_len = pl.seg_len;
+  out->seg_count = pl.seg_count;
+  out->kernels = T == 0 ? 0 : (pl.seg_count > 1 ? 3 : 1);
+  return TTT_OK;
+}
+
 ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
                              const float* W0, int B, int H, int T, int d, int b, void* Z, float* W_out,
                              void* workspace, size_t ws_bytes, void* stream, const ttt_options* opt) {
@@ -216,6 +239,7 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
   p.seg_count = pl.seg_count;
   p.seg_maps = nullptr;
   p.seg_starts = nullptr;
+  p.affine_wy = pl.affine_wy ? 1 : 0;
   if (pl.seg_count > 1) {
     const size_t per = static_cast<size_t>(p.units) * (pl.seg_count - 1) * d * d;
     p.seg_maps = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
@@ -233,12 +257,25 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
         !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_3d(&mz, Z, p.units, T, d, rows, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
       return TTT_ERR_CUDA;
-    err = cudaSuccess;
-    if (pl.seg_count > 1) {
-      err = ttt::launch_linear_seg_affine(p, mk, mv, s);
-      if (err == cudaSuccess) err = ttt::launch_linear_seg_combine(p, s);
+    cudaEvent_t* ev = static_cast<cudaEvent_t*>(o.phase_events);
+    err = ev ? cudaEventRecord(ev[0], s) : cudaSuccess;
+    if (err == cudaSuccess && pl.seg_count > 1) {
+      if (pl.affine_wy) {
+        CUtensorMap mk64, mv64;
+        const int rows64 = ttt::linear_seg_wy_rows();
+        if (!encode_3d(&mk64, K, p.units, T, d, rows64, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_3d(&mv64, V, p.units, T, d, rows64, d, CU_TENSOR_MAP_SWIZZLE_128B))
+          return TTT_ERR_CUDA;
+        err = ttt::launch_linear_seg_affine_wy(p, mk64, mv64, s);
+      } else {
+        err = ttt::launch_linear_seg_affine(p, mk, mv, s);
+      }
     }
+    if (err == cudaSuccess && ev) err = cudaEventRecord(ev[1], s);
+    if (err == cudaSuccess && pl.seg_count > 1) err = ttt::launch_linear_seg_combine(p, s);
+    if (err == cudaSuccess && ev) err = cudaEventRecord(ev[2], s);
     if (err == cudaSuccess) err = ttt::launch_linear_mma(p, mq, mk, mv, mz, s);
+    if (err == cudaSuccess && ev) err = cudaEventRecord(ev[3], s);
   } else {
     err = ttt::launch_linear_simt(p, s);
   }
