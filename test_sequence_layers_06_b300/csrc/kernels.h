@@ -88,6 +88,12 @@ cudaError_t launch_linear_seg_affine_wy(const LinearParams& p, const CUtensorMap
 // General fp32-arithmetic TTT-Linear (any dtype, d <= 64, any b).
 cudaError_t launch_linear_simt(const LinearParams& p, cudaStream_t stream);
 
+// Tensor-core TTT-MLP (bf16, d = 64, hidden 256, b % 16 == 0), one CTA per unit.
+bool mlp_mma_supported(const MlpParams& p);
+int mlp_mma_tile_rows();
+cudaError_t launch_mlp_mma(const MlpParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           cudaStream_t stream);
+
 // General fp32-arithmetic TTT-MLP.
 size_t mlp_simt_snapshot_bytes(int units, int d, int m);
 cudaError_t launch_mlp_simt(const MlpParams& p, cudaStream_t stream);

@@ -1,0 +1,496 @@
+// TTT-MLP forward on the tensor cores (bf16 inputs, d = 64, hidden m = 256,
+// chunk b a multiple of 16): one CTA of 16 warps per (batch row, head).
+//
+// Method ("Test-Time Training (TTT) guide", section 3: two layers, hidden 4x
+// the input, GELU; "5 · TestingTime 训练与长上下文", section 1.1: gradients at
+// the chunk-start weights, dual form). Per 16-token tile of a chunk, with
+// W1a, W2a the chunk-start weights and W1, W2 the running ones:
+//   U = K W1a,  A = gelu(U),  P = gelu'(U)
+//   G = A W2a - V,  D = (G W2a^T) .* P
+//   Hq = Q W1 - eta tril(Q K^T) D,  Aq = gelu(Hq)
+//   Z = Aq W2 - eta tril(Aq A^T) G
+//   W1 -= eta K^T D,  W2 -= eta A^T G
+// (for b = 16 every tile is a chunk and W1a = W1, W2a = W2). gelu is the tanh
+// form of Hendrycks and Gimpel (2016), evaluated with the tanh.approx.f32
+// instruction.
+//
+// Layout. The fp32 weights live in registers as mma.sync accumulator
+// fragments, split by hidden unit: warp w owns W1[:, 16w:16w+16] and
+// W2[16w:16w+16, :] (64 floats per lane), and updates them with the chunk's
+// rank-16 gradient products. bf16 copies of W1 and W2 sit in shared memory
+// (rewritten after every update, 128-byte XOR swizzle), so every product reads
+// whatever fragment layout it needs with ldmatrix, transposed or not. Q, K, V
+// tiles arrive by TMA, double-buffered. Products over the hidden dimension
+// (G, Z, tril(Aq A^T)) are split across warps and summed through shared memory.
+#include "kernels.h"
+#include "ttt_device.cuh"
+
+namespace ttt {
+namespace {
+
+constexpr int kD = 64;
+constexpr int kM = 256;
+constexpr int kTile = 16;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTileBytes = kTile * kD * 2;          // 2 KB
+constexpr int kRowM = kM * 2;                        // 512-byte rows of [.][256] bf16
+// shared memory map (bytes from a 1024-aligned base)
+constexpr int kQKV = 0;                              // [2 stages][Q, K, V] tiles
+constexpr int kW1b = kQKV + 2 * 3 * kTileBytes;      // W1 running, bf16 [64][256]
+constexpr int kW2b = kW1b + kD * kRowM;              // W2 running, bf16 [256][64]
+constexpr int kAb = kW2b + kM * 128;                 // A, bf16 [16][256]
+constexpr int kDb = kAb + kTile * kRowM;             // D
+constexpr int kAqb = kDb + kTile * kRowM;            // Aq
+constexpr int kGb = kAqb + kTile * kRowM;            // G, bf16 [16][64]
+constexpr int kSb = kGb + kTile * 128;               // tril(Q K^T), bf16 [16][16] in 128-byte rows
+constexpr int kPart = kSb + kTile * 128;             // partial sums, fp32: G or Z [4][16][kPad]
+constexpr int kPad = 68;                             // fp32 row stride of the partial buffers
+constexpr int kSap = kPart + 4 * kTile * kPad * 4;   // tril(Aq A^T) partials [16][16][16] fp32
+constexpr int kGf = kSap + kWarps * kTile * kTile * 4;  // G fp32 [16][kPad]
+constexpr int kSaf = kGf + kTile * kPad * 4;         // tril(Aq A^T) fp32 [16][16]
+constexpr int kBar = kSaf + kTile * kTile * 4;       // 2 mbarriers
+constexpr int kBaseBytes = kBar + 64;
+constexpr int kW1s = kBaseBytes;                     // chunk-start copies (b > 16 only)
+constexpr int kW2s = kW1s + kD * kRowM;
+constexpr int kSnapBytes = kD * kRowM + kM * 128;
+
+enum : int { kWhereMlpLoad = 12 };
+
+// Byte offset of 16-byte chunk `c` of row `r` in a matrix with `rb`-byte rows,
+// XOR-swizzled within each 128-byte group (conflict-free 8-row ldmatrix).
+__device__ __forceinline__ uint32_t swz(int r, int c, int rb) {
+  return static_cast<uint32_t>(r * rb + (((c & ~7) | ((c ^ r) & 7)) << 4));
+}
+
+// Fragment loads (m16n8k16 operands) from a bf16 matrix in shared memory.
+// A operand, 16 x 16, from storage [m][k]: rows r0.., k chunks c0, c0+1.
+__device__ __forceinline__ void ldA(uint32_t* a, uint32_t base, int rb, int r0, int c0, int lane) {
+  const int mi = lane >> 3, mr = lane & 7;
+  ldsm_x4(a, base + swz(r0 + ((mi & 1) << 3) + mr, c0 + (mi >> 1), rb));
+}
+// A operand of the transpose of storage [k][m]: k rows r0.., m chunks c0, c0+1.
+__device__ __forceinline__ void ldAT(uint32_t* a, uint32_t base, int rb, int r0, int c0, int lane) {
+  const int mi = lane >> 3, mr = lane & 7;
+  ldsm_x4_t(a, base + swz(r0 + ((mi >> 1) << 3) + mr, c0 + (mi & 1), rb));
+}
+// B operands of two 8-wide n-tiles, from storage [n][k]: n rows r0.., k chunks c0, c0+1.
+__device__ __forceinline__ void ldB(uint32_t* b, uint32_t base, int rb, int r0, int c0, int lane) {
+  const int mi = lane >> 3, mr = lane & 7;
+  ldsm_x4(b, base + swz(r0 + ((mi >> 1) << 3) + mr, c0 + (mi & 1), rb));
+}
+// B operands of two 8-wide n-tiles, from storage [k][n]: k rows r0.., n chunks c0, c0+1.
+__device__ __forceinline__ void ldBT(uint32_t* b, uint32_t base, int rb, int r0, int c0, int lane) {
+  const int mi = lane >> 3, mr = lane & 7;
+  ldsm_x4_t(b, base + swz(r0 + ((mi & 1) << 3) + mr, c0 + (mi >> 1), rb));
+}
+
+__device__ __forceinline__ void mma2(float (*acc)[4], const uint32_t* a, const uint32_t* b4) {
+  const uint32_t b0[2] = {b4[0], b4[1]}, b1[2] = {b4[2], b4[3]};
+  mma_bf16_16816(acc[0], a, b0);
+  mma_bf16_16816(acc[1], a, b1);
+}
+
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh-GELU and its derivative.
+__device__ __forceinline__ void gelu2(float u, float& g, float& gp) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  const float th = tanh_fast(c * (u + a * u * u * u));
+  g = 0.5f * u * (1.f + th);
+  gp = 0.5f * (1.f + th) + 0.5f * u * (1.f - th * th) * c * (1.f + 3.f * a * u * u);
+}
+__device__ __forceinline__ float gelu1(float u) {
+  const float c = 0.7978845608028654f, a = 0.044715f;
+  return 0.5f * u * (1.f + tanh_fast(c * (u + a * u * u * u)));
+}
+
+// Store a 16 x 16 C tile (rows r0 + g, + 8; columns 16*cb + 2tg, +1 of n-tiles
+// 0 and 1) as bf16 into storage with `rb`-byte rows.
+__device__ __forceinline__ void st_tile(uint8_t* base, int rb, int r0, int cb, const float (*c)[4], int lane) {
+  const int g = lane >> 2, tg = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int ch = 2 * cb + nt;
+    *reinterpret_cast<uint32_t*>(base + swz(r0 + g, ch, rb) + 4 * tg) = pack_bf16(c[nt][0], c[nt][1]);
+    *reinterpret_cast<uint32_t*>(base + swz(r0 + g + 8, ch, rb) + 4 * tg) = pack_bf16(c[nt][2], c[nt][3]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mlp_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, MlpParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kBar);
+  const uint32_t s0 = smem_u32(sm);
+  const bool snap = p.b > kTile;  // separate chunk-start copies
+  uint8_t* W1s = snap ? sm + kW1s : sm + kW1b;
+  uint8_t* W2s = snap ? sm + kW2s : sm + kW2b;
+  float* part = reinterpret_cast<float*>(sm + kPart);
+  float* sap = reinterpret_cast<float*>(sm + kSap);
+  float* gf = reinterpret_cast<float*>(sm + kGf);
+  float* saf = reinterpret_cast<float*>(sm + kSaf);
+
+  const int unit = blockIdx.x;
+  const int h = unit % p.H;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, tg = lane & 3;
+  const float eta = p.eta[h];
+  const int n_tiles = (p.T + kTile - 1) / kTile;
+
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_barrier_init();
+  }
+  // fp32 masters (C fragments): W1[:, 16w:16w+16] as 4 m-tiles (i) x 2 n-tiles (hidden),
+  // W2[16w:16w+16, :] as 8 n-tiles (j).
+  float w1[4][2][4], w2[8][4];
+  {
+    const float* W10 = p.W1_0 + static_cast<size_t>(h) * kD * kM;
+    const float* W20 = p.W2_0 + static_cast<size_t>(h) * kM * kD;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int i = 16 * mt + g, c = 16 * warp + 8 * nt + 2 * tg;
+        w1[mt][nt][0] = W10[i * kM + c];
+        w1[mt][nt][1] = W10[i * kM + c + 1];
+        w1[mt][nt][2] = W10[(i + 8) * kM + c];
+        w1[mt][nt][3] = W10[(i + 8) * kM + c + 1];
+      }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int r = 16 * warp + g, c = 8 * nt + 2 * tg;
+      w2[nt][0] = W20[r * kD + c];
+      w2[nt][1] = W20[r * kD + c + 1];
+      w2[nt][2] = W20[(r + 8) * kD + c];
+      w2[nt][3] = W20[(r + 8) * kD + c + 1];
+    }
+  }
+// bf16 copies of this warp's slices of the running weights.
+#define TTT_STORE_W1(dst)                                                          \
+  do {                                                                              \
+    _Pragma("unroll") for (int mt = 0; mt < 4; ++mt)                               \
+      _Pragma("unroll") for (int nt = 0; nt < 2; ++nt) {                           \
+        const int ch = 2 * warp + nt;                                               \
+        *reinterpret_cast<uint32_t*>((dst) + swz(16 * mt + g, ch, kRowM) + 4 * tg) =  \
+            pack_bf16(w1[mt][nt][0], w1[mt][nt][1]);                                 \
+        *reinterpret_cast<uint32_t*>((dst) + swz(16 * mt + g + 8, ch, kRowM) + 4 * tg) = \
+            pack_bf16(w1[mt][nt][2], w1[mt][nt][3]);                                 \
+      }                                                                             \
+  } while (0)
+#define TTT_STORE_W2(dst)                                                          \
+  do {                                                                              \
+    _Pragma("unroll") for (int nt = 0; nt < 8; ++nt) {                             \
+      *reinterpret_cast<uint32_t*>((dst) + swz(16 * warp + g, nt, 128) + 4 * tg) =  \
+          pack_bf16(w2[nt][0], w2[nt][1]);                                          \
+      *reinterpret_cast<uint32_t*>((dst) + swz(16 * warp + g + 8, nt, 128) + 4 * tg) = \
+          pack_bf16(w2[nt][2], w2[nt][3]);                                          \
+    }                                                                               \
+  } while (0)
+  TTT_STORE_W1(sm + kW1b);
+  TTT_STORE_W2(sm + kW2b);
+  if (snap) {
+    TTT_STORE_W1(W1s);
+    TTT_STORE_W2(W2s);
+  }
+  __syncthreads();
+
+  auto load_tile = [&mq, &mk, &mv, &full, sm, unit](int u) {
+    const int s = u & 1;
+    uint8_t* st = sm + kQKV + s * 3 * kTileBytes;
+    mbar_arrive_expect_tx(&full[s], 3 * kTileBytes);
+    tma_load_3d(st, &mq, &full[s], 0, u * kTile, unit);
+    tma_load_3d(st + kTileBytes, &mk, &full[s], 0, u * kTile, unit);
+    tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, u * kTile, unit);
+  };
+  if (tid == 0 && n_tiles > 0) {
+    prefetch_tmap(&mq);
+    prefetch_tmap(&mk);
+    prefetch_tmap(&mv);
+    load_tile(0);
+  }
+
+  const uint32_t W1b = s0 + kW1b, W2b = s0 + kW2b, W1sa = smem_u32(W1s), W2sa = smem_u32(W2s);
+  const uint32_t Ab = s0 + kAb, Db = s0 + kDb, Aqb = s0 + kAqb, Gb = s0 + kGb, Sb = s0 + kSb;
+  bool ok = true;
+
+  for (int u = 0; u < n_tiles; ++u) {
+    const int s = u & 1;
+    const uint32_t sQ = s0 + kQKV + s * 3 * kTileBytes, sK = sQ + kTileBytes;
+    const uint8_t* sVp = sm + kQKV + s * 3 * kTileBytes + 2 * kTileBytes;
+    // Every thread waits for this tile's data (bounded); the next tile's loads go
+    // into the other stage, whose last readers finished before the previous
+    // tile's final barrier.
+    if (!mbar_wait_bounded(&full[s], (u >> 1) & 1, p.timeout_ns)) {
+      if (lane == 0) report_error(p.status, TTT_ERR_TIMEOUT, kWhereMlpLoad, unit);
+      ok = false;
+    }
+    if (__syncthreads_or(!ok)) {
+      // This tile's load may still be in flight: let it land before the CTA exits.
+      if (tid == 0) (void)mbar_wait_bounded(&full[s], (u >> 1) & 1, p.timeout_ns);
+      break;
+    }
+    if (tid == 0 && u + 1 < n_tiles) load_tile(u + 1);
+    const bool chunk_end = ((u + 1) * kTile) % p.b == 0 || u + 1 == n_tiles;
+
+    // (1) U = K W1a for hidden [16w, 16w+16); A, P.  Warp 0 also forms tril(Q K^T).
+    float cu[2][4] = {}, cp[2][4];
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t a[4], b[4];
+      ldA(a, sK, 128, 0, 2 * ks, lane);
+      ldBT(b, W1sa, kRowM, 16 * ks, 2 * warp, lane);
+      mma2(cu, a, b);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) gelu2(cu[nt][r], cu[nt][r], cp[nt][r]);
+    st_tile(sm + kAb, kRowM, 0, warp, cu, lane);
+    if (warp == 0) {
+      float cs[2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4], b[4];
+        ldA(a, sQ, 128, 0, 2 * ks, lane);
+        ldB(b, sK, 128, 0, 2 * ks, lane);
+        mma2(cs, a, b);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {  // keep column <= row (update, then read)
+        const int c = 8 * nt + 2 * tg;
+        if (c > g) cs[nt][0] = 0.f;
+        if (c + 1 > g) cs[nt][1] = 0.f;
+        if (c > g + 8) cs[nt][2] = 0.f;
+        if (c + 1 > g + 8) cs[nt][3] = 0.f;
+      }
+      st_tile(sm + kSb, 128, 0, 0, cs, lane);
+    }
+    __syncthreads();
+
+    // (2) G partials: warp -> value columns [16(w&3), +16), hidden quarter w>>2.
+    {
+      const int np = warp & 3, kq = warp >> 2;
+      float cg[2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4], b[4];
+        ldA(a, Ab, kRowM, 0, 8 * kq + 2 * ks, lane);
+        ldBT(b, W2sa, 128, 64 * kq + 16 * ks, 2 * np, lane);
+        mma2(cg, a, b);
+      }
+      float* dst = part + kq * kTile * kPad;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 16 * np + 8 * nt + 2 * tg;
+        *reinterpret_cast<float2*>(dst + g * kPad + c) = make_float2(cg[nt][0], cg[nt][1]);
+        *reinterpret_cast<float2*>(dst + (g + 8) * kPad + c) = make_float2(cg[nt][2], cg[nt][3]);
+      }
+    }
+    __syncthreads();
+    // G = sum of the quarters - V, fp32 and bf16.
+    {
+      const int t = tid >> 5, j = (tid & 31) * 2;
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const float2 v = *reinterpret_cast<const float2*>(part + kq * kTile * kPad + t * kPad + j);
+        acc.x += v.x;
+        acc.y += v.y;
+      }
+      const uint32_t vv = *reinterpret_cast<const uint32_t*>(sVp + swz(t, j >> 3, 128) + (j & 7) * 2);
+      acc.x -= bf16_lo(vv);
+      acc.y -= bf16_hi(vv);
+      *reinterpret_cast<float2*>(gf + t * kPad + j) = acc;
+      *reinterpret_cast<uint32_t*>(sm + kGb + swz(t, j >> 3, 128) + (j & 7) * 2) = pack_bf16(acc.x, acc.y);
+    }
+    __syncthreads();
+
+    // (3) D = (G W2a^T) .* P for hidden [16w, +16);  W2 -= eta A^T G (this warp's rows).
+    {
+      float cd[2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4], b[4];
+        ldA(a, Gb, 128, 0, 2 * ks, lane);
+        ldB(b, W2sa, 128, 16 * warp, 2 * ks, lane);
+        mma2(cd, a, b);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) cd[nt][r] *= cp[nt][r];
+      st_tile(sm + kDb, kRowM, 0, warp, cd, lane);
+
+      uint32_t a[4];
+      ldAT(a, Ab, kRowM, 0, 2 * warp, lane);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t b[4];
+        ldBT(b, Gb, 128, 0, 2 * q, lane);
+        float acc[2][4] = {};
+        mma2(acc, a, b);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) w2[2 * q + nt][r] = fmaf(-eta, acc[nt][r], w2[2 * q + nt][r]);
+      }
+    }
+    __syncthreads();
+
+    // (4) Hq = Q W1 - eta tril(Q K^T) D, Aq = gelu(Hq);  W1 -= eta K^T D (this warp's columns).
+    {
+      float ch[2][4] = {}, cs[2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4], b[4];
+        ldA(a, sQ, 128, 0, 2 * ks, lane);
+        ldBT(b, W1b, kRowM, 16 * ks, 2 * warp, lane);
+        mma2(ch, a, b);
+      }
+      uint32_t bd[4];
+      ldBT(bd, Db, kRowM, 0, 2 * warp, lane);
+      {
+        uint32_t a[4];
+        ldA(a, Sb, 128, 0, 0, lane);
+        mma2(cs, a, bd);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) ch[nt][r] = gelu1(fmaf(-eta, cs[nt][r], ch[nt][r]));
+      st_tile(sm + kAqb, kRowM, 0, warp, ch, lane);
+
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        uint32_t a[4];
+        ldAT(a, sK, 128, 0, 2 * mt, lane);
+        float acc[2][4] = {};
+        mma2(acc, a, bd);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) w1[mt][nt][r] = fmaf(-eta, acc[nt][r], w1[mt][nt][r]);
+      }
+    }
+    __syncthreads();  // Aq complete; every read of the running W1 copy is done
+
+    TTT_STORE_W1(sm + kW1b);
+    if (snap && chunk_end) TTT_STORE_W1(W1s);
+    // (5) Z partials (value columns [16(w&3), +16), hidden quarter w>>2) and
+    //     tril(Aq A^T) partials (hidden [16w, +16)).
+    {
+      const int np = warp & 3, kq = warp >> 2;
+      float cz[2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4], b[4];
+        ldA(a, Aqb, kRowM, 0, 8 * kq + 2 * ks, lane);
+        ldBT(b, W2b, 128, 64 * kq + 16 * ks, 2 * np, lane);
+        mma2(cz, a, b);
+      }
+      float* dst = part + kq * kTile * kPad;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 16 * np + 8 * nt + 2 * tg;
+        *reinterpret_cast<float2*>(dst + g * kPad + c) = make_float2(cz[nt][0], cz[nt][1]);
+        *reinterpret_cast<float2*>(dst + (g + 8) * kPad + c) = make_float2(cz[nt][2], cz[nt][3]);
+      }
+      float csa[2][4] = {};
+      uint32_t a[4], b[4];
+      ldA(a, Aqb, kRowM, 0, 2 * warp, lane);
+      ldB(b, Ab, kRowM, 0, 2 * warp, lane);
+      mma2(csa, a, b);
+      float* sd = sap + warp * kTile * kTile;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 8 * nt + 2 * tg;
+        *reinterpret_cast<float2*>(sd + g * kTile + c) = make_float2(csa[nt][0], csa[nt][1]);
+        *reinterpret_cast<float2*>(sd + (g + 8) * kTile + c) = make_float2(csa[nt][2], csa[nt][3]);
+      }
+    }
+    __syncthreads();  // every read of the running W2 copy is done
+
+    TTT_STORE_W2(sm + kW2b);
+    if (snap && chunk_end) TTT_STORE_W2(W2s);
+    if (tid < kTile * kTile) {
+      const int t = tid >> 4, t2 = tid & 15;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += sap[w * kTile * kTile + tid];
+      saf[tid] = t2 <= t ? v : 0.f;
+    }
+    __syncthreads();
+    // Z = sum of the quarters - eta tril(Aq A^T) G, written for the rows inside the sequence.
+    {
+      const int t = tid >> 5, j = (tid & 31) * 2;
+      float2 z = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+        const float2 v = *reinterpret_cast<const float2*>(part + kq * kTile * kPad + t * kPad + j);
+        z.x += v.x;
+        z.y += v.y;
+      }
+      float2 r = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int t2 = 0; t2 < kTile; ++t2) {
+        const float sv = saf[t * kTile + t2];
+        const float2 gv = *reinterpret_cast<const float2*>(gf + t2 * kPad + j);
+        r.x = fmaf(sv, gv.x, r.x);
+        r.y = fmaf(sv, gv.y, r.y);
+      }
+      const int tt = u * kTile + t;
+      if (tt < p.T) {
+        __nv_bfloat16* Z = static_cast<__nv_bfloat16*>(p.Z) + (static_cast<size_t>(unit) * p.T + tt) * kD + j;
+        *reinterpret_cast<uint32_t*>(Z) = pack_bf16(fmaf(-eta, r.x, z.x), fmaf(-eta, r.y, z.y));
+      }
+    }
+    __syncthreads();
+  }
+  // Final state.
+  float* W1o = p.W1_out + static_cast<size_t>(unit) * kD * kM;
+  float* W2o = p.W2_out + static_cast<size_t>(unit) * kM * kD;
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int i = 16 * mt + g, c = 16 * warp + 8 * nt + 2 * tg;
+      *reinterpret_cast<float2*>(W1o + i * kM + c) = make_float2(w1[mt][nt][0], w1[mt][nt][1]);
+      *reinterpret_cast<float2*>(W1o + (i + 8) * kM + c) = make_float2(w1[mt][nt][2], w1[mt][nt][3]);
+    }
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) {
+    const int r = 16 * warp + g, c = 8 * nt + 2 * tg;
+    *reinterpret_cast<float2*>(W2o + r * kD + c) = make_float2(w2[nt][0], w2[nt][1]);
+    *reinterpret_cast<float2*>(W2o + (r + 8) * kD + c) = make_float2(w2[nt][2], w2[nt][3]);
+  }
+}
+
+#undef TTT_STORE_W1
+#undef TTT_STORE_W2
+
+}  // namespace
+
+bool mlp_mma_supported(const MlpParams& p) { return p.bf16 && p.d == kD && p.m == kM && p.b % kTile == 0; }
+
+int mlp_mma_tile_rows() { return kTile; }
+
+cudaError_t launch_mlp_mma(const MlpParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           cudaStream_t stream) {
+  if (p.units == 0) return cudaSuccess;
+  const int smem = kBaseBytes + (p.b > kTile ? kSnapBytes : 0) + 1024;
+  const cudaError_t e = cudaFuncSetAttribute(mlp_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mlp_mma_kernel<<<p.units, kThreads, smem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ttt

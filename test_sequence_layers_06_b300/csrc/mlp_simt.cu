@@ -1,5 +1,6 @@
 // TTT-MLP forward in plain fp32 arithmetic (any dtype, d <= 64, hidden m,
-// any b). f(x) = gelu(x W1) W2 with tanh-GELU ("Test-Time Training (TTT)
+// any b): the path for fp32 operands and for shapes the tensor-core kernel
+// (mlp_mma.cu) does not take. f(x) = gelu(x W1) W2 with tanh-GELU ("Test-Time Training (TTT)
 // guide", section 3: two layers, hidden 4x, GELU; it stores the hidden
 // activations, so it moves more memory than TTT-Linear).
 //

@@ -306,7 +306,6 @@ ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype
   if (ws_bytes < workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP, nullptr)) return TTT_ERR_ARG;
   const ttt_options o = defaults(opt);
   if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
-  if (o.force_path == 2) return TTT_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   ttt::MlpParams p;
@@ -320,9 +319,25 @@ ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype
   p.timeout_ns = o.wait_timeout_ns;
   p.inject_stall = o.inject_stall;
 
+  const bool mma_ok = ttt::mlp_mma_supported(p);
+  if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
+  const bool use_mma = mma_ok && o.force_path != 1 && T > 0;
+
   ttt_status st = reset_status(workspace, s);
   if (st != TTT_OK) return st;
-  return ttt::launch_mlp_simt(p, s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+  cudaError_t err;
+  if (use_mma) {
+    CUtensorMap mq, mk, mv;
+    const int rows = ttt::mlp_mma_tile_rows();
+    if (!encode_3d(&mq, Q, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mk, K, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
+      return TTT_ERR_CUDA;
+    err = ttt::launch_mlp_mma(p, mq, mk, mv, s);
+  } else {
+    err = ttt::launch_mlp_simt(p, s);
+  }
+  return err == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
 ttt_status ttt_mlp_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,

@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 10
+    assert len(names) == 11
     assert set(names) == set(ttt.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -57,6 +57,18 @@ def test_workspace_bytes_for_the_segment_parallel_form(lib):
     assert seg == 256 + 3 * (2 * 3) * 3 * 64 * 64 * 4  # ceil(1000 / 256) = 4 segments, 3 boundaries
     # plenty of units: one pass
     assert ttt.ttt_workspace_bytes(64, 64, 8192, 64, 16, 0) == 256
+
+
+def test_linear_plan(lib):
+    assert ttt.ttt_linear_plan(1, 32, 131072, 64, 16)["path"] == 3
+    p = ttt.ttt_linear_plan(2, 3, 1000, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 256})
+    assert p == {"path": 3, "seg_len": 256, "seg_count": 4, "kernels": 3}
+    assert ttt.ttt_linear_plan(1, 1, 100, 64, 16)["path"] == 2       # too short to cut
+    assert ttt.ttt_linear_plan(1, 1, 100, 32, 16)["path"] == 1       # width the tensor kernels do not take
+    assert ttt.ttt_linear_plan(1, 1, 100, 64, 16, ttt.TTT_F32)["path"] == 1
+    assert ttt.ttt_linear_plan(1, 1, 0, 64, 16)["kernels"] == 0
+    with pytest.raises(ttt.TTTError):
+        ttt.ttt_linear_plan(1, 1, 100, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 24})
 
 
 def _lin(lib, **kw):

@@ -1,4 +1,5 @@
-"""TTT-MLP on the GPU (through the C ABI) against the fp64 oracle."""
+"""TTT-MLP on the GPU (through the C ABI) against the fp64 oracle: the
+tensor-core kernel (bf16, d = 64, b % 16 == 0) and the fp32 SIMT kernel."""
 import numpy as np
 import pytest
 import torch
@@ -29,6 +30,35 @@ def test_mlp_small(T, b, dtype, d):
     tol = 1e-4 if dtype == "f32" else tolerance(w)
     for x, r in ((Z, Zr), (W1, W1r), (W2, W2r)):
         assert rel_l2(x, r) <= tol, rel_l2(x, r)
+
+
+@pytest.mark.parametrize("T,b", [(96, 32), (80, 48), (130, 64)])
+def test_mlp_tensor_path_chunks_of_several_tiles(T, b):
+    """Chunks of 2-4 tiles: gradients at the chunk-start weights, read-out with
+    the running ones (the tensor-core kernel keeps both bf16 copies)."""
+    w = W["mlp_125m"].with_(B=1, H=3, T=T, seed=400 + T + b)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    Z, W1, W2 = ttt.ttt_mlp_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W1"], t["W2"], b,
+                                options={"force_path": ttt.PATH_TENSOR})
+    torch.cuda.synchronize()
+    Zr, W1r, W2r = oracle_mlp(inp, b)
+    for x, r in ((Z, Zr), (W1, W1r), (W2, W2r)):
+        assert rel_l2(to64(x), r) <= tolerance(w), rel_l2(to64(x), r)
+
+
+def test_mlp_simt_path_bf16_agrees_with_tensor_path():
+    w = W["mlp_125m"].with_(B=2, H=2, T=64, seed=77)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    outs = [ttt.ttt_mlp_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W1"], t["W2"], 16, options={"force_path": fp})
+            for fp in (ttt.PATH_SIMT, ttt.PATH_TENSOR)]
+    torch.cuda.synchronize()
+    Zr, W1r, W2r = oracle_mlp(inp, 16)
+    for (Z, W1, W2) in outs:
+        for x, r in ((Z, Zr), (W1, W1r), (W2, W2r)):
+            assert rel_l2(to64(x), r) <= tolerance(w)
+    assert rel_l2(to64(outs[0][0]), to64(outs[1][0])) < 2e-2
 
 
 def test_mlp_full_size_sampled():
