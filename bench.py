@@ -50,6 +50,8 @@ KERNEL_PROFILES = {
     "linear_mma_kernel": (("test_sequence_layers_06_b300/csrc/linear_mma.cu",), "profiles/linear_mma_long_b16.md"),
     "linear_seg_affine_kernel": (("test_sequence_layers_06_b300/csrc/linear_seg.cu",),
                                  "profiles/linear_seg_affine_long_b16.md"),
+    "linear_seg_affine_wy_kernel": (("test_sequence_layers_06_b300/csrc/linear_seg_wy.cu",),
+                                    "profiles/linear_seg_affine_wy_long_b16.md"),
     "linear_seg_combine_kernel": (("test_sequence_layers_06_b300/csrc/linear_seg.cu",),
                                   "profiles/linear_seg_combine_long_b16.md"),
 }
@@ -64,6 +66,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="linear_long")
     ap.add_argument("--b", type=int, default=16)
+    ap.add_argument("--T", type=int, default=0, help="override the workload's sequence length (profiling cases)")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -360,7 +363,8 @@ def bench_ours(args, world, rank, local):
     hbm_gbs, _, peak_kind = measured_peaks()
     kernel_ms = [float(np.mean([p[k] for p in per])) for k in range(3)]
     kbytes = kernel_bytes(w, plan)
-    names = ("linear_seg_affine_kernel", "linear_seg_combine_kernel", "linear_mma_kernel")
+    names = ("linear_seg_affine_wy_kernel" if plan["affine"] == 2 else "linear_seg_affine_kernel",
+             "linear_seg_combine_kernel", "linear_mma_kernel")
     kernels = {}
     for k, name in enumerate(names):
         if kbytes[k] == 0:
@@ -551,11 +555,54 @@ def bench_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def bench_mlp(args, world, rank, local):
+    """A TTT-MLP workload through ttt_mlp_fwd (secondary; used for profiling the
+    tensor-core TTT-MLP kernel). Reports against the bf16 tensor roofline."""
+    import torch
+    import test_sequence_layers_06_b300 as ttt
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload].with_(b=args.b)
+    if args.T:
+        w = w.with_(T=args.T)
+    inp = synth.make_inputs(w, want_exact=False)
+    cv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev))
+    Q, K, V = cv(inp.q), cv(inp.k), cv(inp.v)
+    eta = torch.from_numpy(inp.eta).to(dev)
+    W1, W2 = torch.from_numpy(inp.W1).to(dev), torch.from_numpy(inp.W2).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: ttt.ttt_mlp_fwd(Q, K, V, eta, W1, W2, args.b, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / args.steps
+    _, tflops, kind = measured_peaks()
+    flops = w.token_heads * (16 * w.d * w.hidden + 4 * args.b * (w.d + w.hidden))
+    achieved = flops / (ms * 1e-3) / 1e12
+    if rank == 0:
+        print(json.dumps({"metric": "TTT-MLP scan tokens·heads/sec", "value": w.token_heads / (ms * 1e-3),
+                          "unit": UNIT, "n_gpus": world, "steps": args.steps, "ms_per_step": round(ms, 4),
+                          "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                          "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "hidden": w.hidden,
+                                     "b": args.b},
+                          "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": tflops,
+                                       "unit": "TFLOP/s", "frac": round(achieved / tflops, 5),
+                                       "peak_kind": f"{kind} bf16 burst"}}), flush=True)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
         bench_reference(args, world, rank)
+    elif synth.WORKLOADS[args.workload].variant == "mlp":
+        bench_mlp(args, world, rank, local)
     else:
         bench_ours(args, world, rank, local)
 

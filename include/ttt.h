@@ -81,7 +81,23 @@ typedef struct {
                                serve (they need bf16, d = 64, b % 16 == 0). */
   int32_t seg_len;          /* segment-parallel form only: tokens per segment, a
                                multiple of b and of 16; 0 = chosen automatically */
+  void* phase_events;       /* optional instrumentation, NULL = none: an array of 4
+                               cudaEvent_t (created by the caller) that TTT-Linear
+                               records on `stream` before its first kernel, after the
+                               affine-map kernel, after the combine kernel and after
+                               the read-out kernel. On the one-pass path the first
+                               three are recorded back to back. */
 } ttt_options;
+
+/* How a TTT-Linear call with these arguments runs (filled by ttt_linear_plan). */
+typedef struct {
+  int32_t path;       /* 1 = fp32 SIMT kernel, 2 = tensor-core one pass, 3 = segment-parallel */
+  int32_t seg_len;    /* tokens per segment (the whole sequence on paths 1 and 2) */
+  int32_t seg_count;  /* segments per (batch row, head) */
+  int32_t kernels;    /* kernels one call enqueues (besides a 16-byte status reset) */
+  int32_t affine;     /* path 3: 1 = affine maps by warp-level MMAs (16-token tiles),
+                         2 = by tcgen05 tensor cores (64-token steps); else 0 */
+} ttt_plan;
 
 /* Bytes of workspace a call with these sizes needs on the current device
  * (>= 256; a status word lives at its start). variant: TTT_VARIANT_LINEAR or
@@ -123,6 +139,11 @@ TTT_API ttt_status ttt_linear_fwd(const void* Q, const void* K, const void* V, t
                           const float* eta, const float* W0, int B, int H, int T, int d, int b,
                           void* Z, float* W_out, void* workspace, size_t ws_bytes, void* stream);
 
+/* The plan ttt_linear_fwd(_ex) follows for these arguments on the current
+ * device; nothing is enqueued. Same argument errors as the forward call. */
+TTT_API ttt_status ttt_linear_plan(int B, int H, int T, int d, int b, ttt_dtype dt, const ttt_options* opt,
+                                   ttt_plan* out);
+
 TTT_API ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt,
                              const float* eta, const float* W0, int B, int H, int T, int d, int b,
                              void* Z, float* W_out, void* workspace, size_t ws_bytes, void* stream,
@@ -131,6 +152,8 @@ TTT_API ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V
 /*
  * TTT-MLP forward: f(x) = gelu(x W1) W2 with tanh-GELU (Hendrycks and Gimpel
  * 2016), hidden width m = 4 d ("Test-Time Training (TTT) guide", section 3).
+ * With bf16 operands, d = 64 and b % 16 == 0 a tensor-core kernel serves the
+ * call (ttt_options.force_path = 2 requires it, 1 forces the fp32 SIMT kernel).
  *   W1_0 [H][d][4d], W2_0 [H][4d][d] float32, shared by the batch.
  *   W1_out [B][H][d][4d], W2_out [B][H][4d][d] float32.
  *   Other arguments as ttt_linear_fwd.

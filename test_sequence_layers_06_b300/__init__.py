@@ -42,7 +42,7 @@ class ttt_options(ctypes.Structure):
 
 class ttt_plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("seg_len", ctypes.c_int32), ("seg_count", ctypes.c_int32),
-                ("kernels", ctypes.c_int32)]
+                ("kernels", ctypes.c_int32), ("affine", ctypes.c_int32)]
 
 
 _lib = None
@@ -95,7 +95,7 @@ def ttt_workspace_bytes(B: int, H: int, T: int, d: int, b: int, variant: int = T
 
 
 def ttt_linear_plan(B: int, H: int, T: int, d: int, b: int, dtype: int = TTT_BF16, options=None) -> dict:
-    """How ttt_linear_fwd runs for these sizes: {path, seg_len, seg_count, kernels}."""
+    """How ttt_linear_fwd runs for these sizes: {path, seg_len, seg_count, kernels, affine}."""
     out = ttt_plan()
     st = load_library().ttt_linear_plan(B, H, T, d, b, dtype, _opts(options), ctypes.byref(out))
     if st != TTT_OK:

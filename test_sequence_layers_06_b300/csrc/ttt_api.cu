@@ -203,6 +203,7 @@ ttt_status ttt_linear_plan(int B, int H, int T, int d, int b, ttt_dtype dt, cons
   out->seg_len = pl.seg_len;
   out->seg_count = pl.seg_count;
   out->kernels = T == 0 ? 0 : (pl.seg_count > 1 ? 3 : 1);
+  out->affine = pl.seg_count > 1 ? (pl.affine_wy ? 2 : 1) : 0;
   return TTT_OK;
 }
 

@@ -62,7 +62,9 @@ def test_workspace_bytes_for_the_segment_parallel_form(lib):
 def test_linear_plan(lib):
     assert ttt.ttt_linear_plan(1, 32, 131072, 64, 16)["path"] == 3
     p = ttt.ttt_linear_plan(2, 3, 1000, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 256})
-    assert p == {"path": 3, "seg_len": 256, "seg_count": 4, "kernels": 3}
+    assert p == {"path": 3, "seg_len": 256, "seg_count": 4, "kernels": 3, "affine": 2}
+    p = ttt.ttt_linear_plan(2, 3, 1000, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 48})
+    assert p["affine"] == 1  # 48-token segments are not whole 64-token steps
     assert ttt.ttt_linear_plan(1, 1, 100, 64, 16)["path"] == 2       # too short to cut
     assert ttt.ttt_linear_plan(1, 1, 100, 32, 16)["path"] == 1       # width the tensor kernels do not take
     assert ttt.ttt_linear_plan(1, 1, 100, 64, 16, ttt.TTT_F32)["path"] == 1
