@@ -1,35 +1,41 @@
-// Segment affine maps of TTT-Linear on the tcgen05 tensor cores, 64 tokens per
-// step (bf16 inputs, d = 64; b = 16, 32 or a multiple of 64).
+// Segment affine maps of TTT-Linear on the tcgen05 tensor cores, one product
+// per 64 tokens on the serial chain (bf16 inputs, d = 64; b = 16, 32 or a
+// multiple of 64).
 //
 // What is computed is the same as linear_seg_affine_kernel (linear_seg.cu): for a
 // segment of whole chunks, the composed affine map X = [A | B] of its chunk
 // updates, run on the 64 x 128 state X from [I | 0] with value rows [0 | V].
 //
-// Super-chunks. Take 64 consecutive tokens holding whole chunks (b = 16 or 32),
-// X0 the state before them. Chunk c's error is taken at its own start state
-// X0 - eta sum_{c' < c} K_c'^T E_c', so
-//   E_c = K_c X0 - [0|V]_c - eta sum_{c' < c} (K_c K_c'^T) E_c',
-// i.e. (I + eta N) E = R with R = K X0 - [0|V] and N the strictly block-lower
-// part (chunk blocks) of K K^T. With T = (I + eta N)^-1:
-//   X_end = X0 - eta K^T T R = X0 - eta Kh^T R,   Kh = T^T K.
-// This is exact algebra on the chunk rule ("5 · TestingTime 训练与长上下文",
-// sections 1.1 and 4); the pages do not write it. Kh depends only on the
-// inputs, so two helper warps compute it ahead of time with warp-level MMAs,
-// in registers: the 16 x 16 blocks of T^T by the short recurrence
-// U_cr = -eta sum_m U_cm G_mr (U = T^T, G = K K^T blocks, U_cc = I), then
-// Kh_c = K_c + sum_{r > c} U_cr K_r. They also store V transposed, so that the
-// thread owning column j of B reads its 64 values with eight 16-byte loads.
-// The chain that depends on X is two tensor-core products per 64 tokens
-// instead of two per chunk:
-//   R^T = X0^T K^T                    (M 128, N 64, K 64)
-//   -eta R^T + eta [0|V]^T            (registers: thread r owns row r of X^T)
-//   X^T += (-eta R^T) Kh              (M 128, N 64, K 64; Kh read MN-major)
-// For b >= 64 every 64-token step lies inside one chunk: T = I, Kh = K, and X0
-// stays the chunk-start state until the chunk ends.
+// Groups. A group is 64 tokens holding whole chunks (b = 16, 32, 64) or one
+// whole chunk (b a multiple of 64). Chunk c's error is taken at its own start
+// state, E_c = K_c X_c - [0|V]_c with X_c = X0 - eta sum_{c' < c} K_c'^T E_c',
+// so (I + eta N) E = K X0 - [0|V] with N the strictly block-lower part (chunk
+// blocks) of K K^T. With T = (I + eta N)^-1 and Kh = T^T K the group's update is
+//   X_end = X0 - eta Kh^T (K X0 - [0|V]) = X0 + M X0 + [0 | Q],
+//   M = -eta Kh^T K,   Q = eta Kh^T V,
+// an affine map that depends on the inputs only (for b >= 64, Kh = K and the
+// sums run over the chunk's 64-token steps). This is exact algebra on the chunk
+// rule ("5 · TestingTime 训练与长上下文", sections 1.1 and 4); the pages do not
+// write it. So the serial chain is one tensor-core product per group,
+//   X^T += X^T M^T                     (M 128, N 64, K 64; A in tensor memory),
+// then the row threads add Q^T to the B rows of X^T (fp32) and round the new
+// X^T to bf16 (the next product's A operand). Everything else runs ahead of it:
+//   - two helper warps form Kh = T^T K with warp-level MMAs, in registers: the
+//     16 x 16 blocks of T^T by U_cr = -eta sum_m U_cm G_mr (G = K K^T blocks,
+//     U_cc = I), then Kh_c = K_c + sum_{r > c} U_cr K_r;
+//   - one M = 128 product [K^T; V^T] Kh = [-M^T / eta; Q^T / eta] per step, two
+//     groups ahead, into one of two tensor-memory buffers;
+//   - while the chain product of the previous group runs, the A-row threads
+//     round the top half to bf16 M^T (the chain's B operand, read MN-major: no
+//     transposition anywhere) and the B-row threads take their row of Q^T
+//     into registers (bf16 pairs, the rounding Q^T would get as an operand).
+// Products complete in issue order and a commit lands only once the products
+// issued after it are done too (measured), so the control lane waits for each
+// chain product before it issues prep products for later groups.
 //
-// Roles (224 threads): warps 0-3 own the 128 rows of X^T (tensor memory <->
-// registers <-> shared memory); warp 4 lane 0 issues the TMA loads and the
-// MMAs; warps 5 and 6 compute Kh and V^T for even and odd steps. Every wait is
+// Roles (224 threads): warps 0-3 own the 128 rows of X^T and of the prep
+// product; warp 4 lane 0 issues the TMA loads and the MMAs; warps 5 and 6
+// compute Kh for even and odd steps, each into its own buffer. Every wait is
 // bounded in time and gives up early when another role has given up.
 #include "ttt_device.cuh"
 #include "tcgen05.cuh"
@@ -39,30 +45,32 @@ namespace ttt {
 namespace {
 
 constexpr int kD = 64;
-constexpr int kStep = 64;                         // tokens per super-chunk
-constexpr int kStages = 3;
+constexpr int kStep = 64;                          // tokens per TMA step
+constexpr int kStages = 3;                         // (a fourth stage measured slower)
 constexpr int kThreads = 224;
-constexpr int kTileBytes = kStep * kD * 2;        // 8 KB: one 64 x 64 bf16 tile
-constexpr int kXOff = 0;                          // X0^T bf16 [128][64] (and -eta E^T when b < 64)
-constexpr int kPOff = 16384;                      // Kh[2] (b < 64) or -eta R^T (b >= 64); then V^T[2]
-constexpr int kStageOff = kPOff + 4 * kTileBytes; // stages: K tile, V tile
-constexpr int kBarOff = kStageOff + kStages * 2 * kTileBytes;
-constexpr int kNumBars = 2 * kStages + 4 + 5;
+constexpr int kTileBytes = kStep * kD * 2;         // 8 KB: one 64 x 64 bf16 tile
+constexpr int kMOff = 0;                           // [2] M^T tiles, bf16 [64][64]
+constexpr int kStageOff = kMOff + 2 * kTileBytes;  // [kStages] x (K tile, V tile)
+constexpr int kKhOff = kStageOff + kStages * 2 * kTileBytes;  // Kh [2] (b < 64)
+constexpr int kBarOff = kKhOff + 2 * kTileBytes;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 3;
+static_assert(kNumBars * 8 + 16 + 1024 + kBarOff <= 113 * 1024 - 512, "two CTAs per SM");
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1024
-constexpr uint32_t kCols = 128;                   // X^T: [0, 64); R^T: [64, 128)
-constexpr uint32_t kIdR = tc::idesc_bf16_f32(128, 64, false, false);
-constexpr uint32_t kIdU = tc::idesc_bf16_f32(128, 64, false, true);
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + slack to align the base to 1024
+// Tensor memory: X^T fp32 [0, 64); prep [2] x 64 at [64, 192); X^T bf16 [192, 224).
+constexpr uint32_t kCols = 256;
+constexpr uint32_t kIdChain = tc::idesc_bf16_f32(128, 64, false, true);  // A from tensor memory
+constexpr uint32_t kIdPrep = tc::idesc_bf16_f32(128, 64, true, true);
 
 enum : int { kWhereControl = 8, kWhereRows = 9, kWherePrep = 10, kWhereDrain = 11 };
 
-// Whether block pair (r, m), m < r, of the step's four 16-token blocks lies in
+// Whether block pair (r, m), m < r, of a step's four 16-token blocks lies in
 // different chunks (chunks of bt tokens): only then does G_rm enter N.
 __device__ __forceinline__ bool needed(int r, int m, int bt) { return m < r && (16 * m) / bt < (16 * r) / bt; }
 
-// Kh = T^T K for one 64-token step (b = 16 or 32), written as rows of tokens
-// (128-byte swizzled), the MN-major B operand of the state update.
-__device__ void prep_khat(uint32_t sK, uint8_t* kh, float neta, int bt, int lane) {
+// The 16 x 16 blocks of U = T^T for one 64-token step (b = 16 or 32), as bf16 A
+// fragments (rows: tokens of block c, k: tokens of block r), and which are nonzero.
+__device__ void prep_u(uint32_t sK, float neta, int bt, int lane, uint32_t (&ua)[4][4][4], bool (&nz)[4][4]) {
   const int g = lane >> 2;
   const int tg = lane & 3;
   const int mi = lane >> 3;
@@ -91,11 +99,8 @@ __device__ void prep_khat(uint32_t sK, uint8_t* kh, float neta, int bt, int lane
         gb[r][m][nr][1] = pack_bf16(acc[1][2 * nr], acc[1][2 * nr + 1]);
       }
     }
-  // U = T^T by blocks, as A fragments (rows: tokens of block c, k: tokens of block r).
   const uint32_t eye = (g == 2 * tg ? 0x00003F80u : 0u) | (g == 2 * tg + 1 ? 0x3F800000u : 0u);
   const uint32_t ident[4] = {eye, 0u, 0u, eye};
-  uint32_t ua[4][4][4];
-  bool nz[4][4];
 #pragma unroll
   for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -121,7 +126,14 @@ __device__ void prep_khat(uint32_t sK, uint8_t* kh, float neta, int bt, int lane
       ua[c][r][2] = pack_bf16(neta * acc[1][0], neta * acc[1][1]);
       ua[c][r][3] = pack_bf16(neta * acc[1][2], neta * acc[1][3]);
     }
-  // Kh_c = K_c + sum_{r > c} U_cr K_r.
+}
+
+// Kh_c = K_c + sum_{r > c} U_cr K_r, written as rows of tokens (128-byte swizzled).
+__device__ void prep_kh(uint32_t sK, uint8_t* kh, int lane, const uint32_t (&ua)[4][4][4], const bool (&nz)[4][4]) {
+  const int g = lane >> 2;
+  const int tg = lane & 3;
+  const int mi = lane >> 3;
+  const int mr = lane & 7;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     float acc[8][4];
@@ -158,36 +170,20 @@ __device__ void prep_khat(uint32_t sK, uint8_t* kh, float neta, int bt, int lane
   }
 }
 
-// V transposed into rows of value columns (128-byte swizzled).
-__device__ void transpose_v(uint32_t sV, uint8_t* vtt, int lane) {
-  const int mi = lane >> 3;
-  const int mr = lane & 7;
-  const uint32_t svt = smem_u32(vtt);
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-      uint32_t a[4];
-      ldsm_x4(a, sV + swz128(16 * r + ((mi & 1) << 3) + mr, 2 * qq + (mi >> 1)));
-      stsm_x4_t(svt + swz128(8 * (2 * qq + (mi >> 1)) + mr, 2 * r + (mi & 1)), a);
-    }
-  __syncwarp();
-}
-
 __global__ void __launch_bounds__(kThreads, 2)
     linear_seg_affine_wy_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                                 LinearParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // [kStages] TMA data landed
-  uint64_t* sfree = full + kStages;                               // [kStages] MMAs done with the stage
-  uint64_t* prepready = sfree + kStages;                          // [2] Kh, V^T written
-  uint64_t* pfree = prepready + 2;                                // [2] MMAs and rows done with Kh, V^T
-  uint64_t* rdone = pfree + 2;
-  uint64_t* eready = rdone + 1;
-  uint64_t* udone = rdone + 2;
-  uint64_t* xready = rdone + 3;
-  uint64_t* drain = rdone + 4;
+  uint64_t* sfree = full + kStages;                               // [kStages] the step's product is done
+  uint64_t* khready = sfree + kStages;                            // [2] Kh of step j written to buffer j & 1
+  uint64_t* pdone = khready + 2;      // [2] the group's prep product is in its tensor-memory buffer
+  uint64_t* mqready = pdone + 2;      // [2] bf16 M^T written to buffer g & 1 (2 warp arrivals)
+  uint64_t* qtaken = pdone + 4;       // [2] Q^T of buffer g & 1 read into registers (2 warp arrivals)
+  uint64_t* xready = pdone + 6;       // X^T refreshed (4 warp arrivals)
+  uint64_t* xdone = pdone + 7;        // the group's chain product is done
+  uint64_t* drain = pdone + 8;        // every MMA issued has completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
 
@@ -196,26 +192,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int seg = blockIdx.x % maps;
   const int h = unit % p.H;
   const int t0 = seg * p.seg_len;
-  const int n = p.seg_len / kStep;
-  const bool wy = p.b < kStep;                   // b = 16 or 32: Kh differs from K
-  const int spc = wy ? 1 : p.b / kStep;          // steps per chunk
+  const int n = p.seg_len / kStep;                // TMA steps
+  const bool wy = p.b < kStep;                    // b = 16 or 32: Kh differs from K
+  const int spc = wy ? 1 : p.b / kStep;           // steps per group
+  const int ng = n / spc;                         // groups
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const float neta = -p.eta[h];
+  const float eta = p.eta[h];
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&sfree[s], 1);
     }
-    for (int q = 0; q < 2; ++q) {
-      mbar_init(&prepready[q], 1);
-      mbar_init(&pfree[q], 1);
-    }
-    mbar_init(rdone, 1);
-    mbar_init(eready, 4);
-    mbar_init(udone, 1);
+    mbar_init(&khready[0], 1);
+    mbar_init(&khready[1], 1);
+    mbar_init(&pdone[0], 1);
+    mbar_init(&pdone[1], 1);
+    mbar_init(&mqready[0], 2);
+    mbar_init(&mqready[1], 2);
+    mbar_init(&qtaken[0], 2);
+    mbar_init(&qtaken[1], 2);
     mbar_init(xready, 4);
+    mbar_init(xdone, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -229,19 +228,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
   const uint32_t tX = tmem;
-  const uint32_t tR = tmem + 64;
-  uint8_t* sXp = smem + kXOff;
-  uint8_t* sEp = wy ? smem + kXOff : smem + kPOff;
+  const uint32_t tP = tmem + 64;  // + 64 * (group & 1)
+  const uint32_t tXb = tmem + 192;
   auto stageK = [&](int s) { return smem + kStageOff + s * 2 * kTileBytes; };
-  auto khp = [&](int q) { return smem + kPOff + q * kTileBytes; };        // Kh
-  auto vtp = [&](int q) { return smem + kPOff + (2 + q) * kTileBytes; };  // V^T
+  auto mtile = [&](int q) { return smem + kMOff + q * kTileBytes; };
+  auto khp = [&](int q) { return smem + kKhOff + q * kTileBytes; };
 
   if (warp == 4) {
     // -------------------------------------------------- control: TMA and MMA issue
     if (lane == 0) {
       prefetch_tmap(&mk);
       prefetch_tmap(&mv);
-      int loaded = 0;
+      int loaded = 0, consumed = 0;
       auto load = [&](int j) {
         const int s = j % kStages;
         mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
@@ -251,41 +249,49 @@ __global__ void __launch_bounds__(kThreads, 2)
       };
       if (!p.inject_stall)
         for (int j = 0; j < min(kStages, n); ++j) load(j);
-      bool ok = true;
-      int consumed = 0;  // steps whose TMA data this thread has seen land
-      for (int j = 0; j < n; ++j) {
-        const int s = j % kStages;
-        const int q = j & 1;
-        ok = mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns, abort_flag);
-        if (ok) consumed = j + 1;
-        if (ok && j % spc == 0) ok = mbar_wait_or_abort(xready, (j / spc) & 1, p.timeout_ns, abort_flag);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint32_t sX = smem_u32(sXp);
-        const uint32_t sB = smem_u32(stageK(s));
+      // [K^T; V^T] Kh of group g, accumulated over its steps into buffer g & 1.
+      auto issue_prep = [&](int g) -> bool {
+        const uint32_t dst = tP + 64 * (g & 1);
+        for (int j = g * spc; j < (g + 1) * spc; ++j) {
+          const int s = j % kStages;
+          if (j >= 1 && j + kStages - 1 < n && !p.inject_stall) {  // refill the stage of step j-1
+            if (!mbar_wait_or_abort(&sfree[(j - 1) % kStages], ((j - 1) / kStages) & 1, p.timeout_ns, abort_flag))
+              return false;
+            load(j + kStages - 1);
+          }
+          if (!mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns, abort_flag)) return false;
+          consumed = j + 1;
+          if (wy && !mbar_wait_or_abort(&khready[j & 1], (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
+          tc::fence_after_sync();
+          const uint32_t sK = smem_u32(stageK(s));
+          const uint32_t sB = wy ? smem_u32(khp(j & 1)) : sK;
+          const bool first = (j % spc) == 0;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tR, tc::sdesc(sX + 32 * kk, 16, 1024, tc::kSw128), tc::sdesc(sB + 32 * kk, 16, 1024, tc::kSw128),
-                       kIdR, kk > 0 ? 1u : 0u);
-        tc::commit(rdone);
-        ok = mbar_wait_or_abort(eready, j & 1, p.timeout_ns, abort_flag);
-        if (ok && wy) ok = mbar_wait_or_abort(&prepready[q], (j >> 1) & 1, p.timeout_ns, abort_flag);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint32_t sE = smem_u32(sEp);
-        const uint32_t sK = smem_u32(wy ? khp(q) : stageK(s));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_bf16(tX, tc::sdesc(sE + 32 * kk, 16, 1024, tc::kSw128),
-                       tc::sdesc(sK + 2048 * kk, 1024, 1024, tc::kSw128), kIdU, 1u);
-        if (j % spc == spc - 1) tc::commit(udone);
-        tc::commit(&pfree[q]);
-        tc::commit(&sfree[s]);
-        if (j + kStages < n && !p.inject_stall) {
-          ok = mbar_wait_or_abort(&sfree[s], (j / kStages) & 1, p.timeout_ns, abort_flag);
-          if (!ok) break;
-          load(j + kStages);
+          for (int kk = 0; kk < 4; ++kk)  // A: K tile then V tile, MN-major, 8 KB apart; B: Kh, MN-major
+            tc::mma_bf16(dst, tc::sdesc(sK + 2048 * kk, kTileBytes, 1024, tc::kSw128),
+                         tc::sdesc(sB + 2048 * kk, 1024, 1024, tc::kSw128), kIdPrep, (!first || kk > 0) ? 1u : 0u);
+          tc::commit(&sfree[s]);
         }
+        tc::commit(&pdone[g & 1]);
+        return true;
+      };
+      bool ok = issue_prep(0);
+      if (ok && ng > 1) ok = issue_prep(1);
+      for (int g = 0; ok && g < ng; ++g) {
+        ok = mbar_wait_or_abort(&mqready[g & 1], (g >> 1) & 1, p.timeout_ns, abort_flag) &&
+             mbar_wait_or_abort(xready, g & 1, p.timeout_ns, abort_flag);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t sM = smem_u32(mtile(g & 1));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16_ta(tX, tXb + 8 * kk, tc::sdesc(sM + 2048 * kk, 1024, 1024, tc::kSw128), kIdChain, 1u);
+        tc::commit(xdone);
+        // Let the chain product land before anything else enters the pipe; the
+        // prep buffer of group g is free once its Q^T rows have been read.
+        ok = mbar_wait_or_abort(xdone, g & 1, p.timeout_ns, abort_flag) &&
+             mbar_wait_or_abort(&qtaken[g & 1], (g >> 1) & 1, p.timeout_ns, abort_flag);
+        if (ok && g + 2 < ng) ok = issue_prep(g + 2);
       }
       if (!ok) {
         if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereControl, unit);
@@ -298,20 +304,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         (void)mbar_wait_bounded(&full[v % kStages], (v / kStages) & 1, p.timeout_ns);
     }
   } else if (warp >= 5) {
-    // -------------------------------------------------- Kh and V^T for every other step
-    {
+    // -------------------------------------------------- Kh for every other step
+    if (wy) {
       bool ok = true;
       for (int j = warp - 5; j < n; j += 2) {
         const int s = j % kStages;
-        const int q = j & 1;
         ok = mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns, abort_flag);
-        if (ok && j >= 2) ok = mbar_wait_or_abort(&pfree[q], ((j - 2) >> 1) & 1, p.timeout_ns, abort_flag);
         if (!ok) break;
-        transpose_v(smem_u32(stageK(s) + kTileBytes), vtp(q), lane);
-        if (wy) prep_khat(smem_u32(stageK(s)), khp(q), neta, p.b, lane);
+        uint32_t ua[4][4][4];
+        bool nz[4][4];
+        prep_u(smem_u32(stageK(s)), -eta, p.b, lane, ua, nz);
+        // The Kh buffer's previous user, step j-2, must have finished its product.
+        if (j >= 2)
+          ok = mbar_wait_or_abort(&sfree[(j - 2) % kStages], ((j - 2) / kStages) & 1, p.timeout_ns, abort_flag);
+        if (!ok) break;
+        prep_kh(smem_u32(stageK(s)), khp(j & 1), lane, ua, nz);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&prepready[q]);
+        if (lane == 0) mbar_arrive(&khready[j & 1]);
       }
       if (!ok && lane == 0) {
         if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWherePrep, unit);
@@ -324,8 +334,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int half = r >> 6;    // 0: a column of A, 1: a column of B
     const int jc = r & 63;
     const uint32_t lanes = static_cast<uint32_t>(32 * warp) << 16;
-    const int rx = (r >> 3) * 1024 + (r & 7) * 128;  // row r in a [128][64] 128-byte-swizzled tile
 
+    // X^T = [I | 0]^T in fp32 and as a bf16 A operand (two bf16 per column, the
+    // even k in the low half).
     {
       float v[16];
 #pragma unroll
@@ -334,88 +345,99 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int i = 0; i < 16; ++i) v[i] = (half == 0 && c + i == jc) ? 1.f : 0.f;
         tc::st16(tX + lanes + c, v);
       }
+      uint32_t xb[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t one = (half == 0 && (jc >> 3) == c) ? ((jc & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
-        const int slot = (jc & 7) >> 1;
-        *reinterpret_cast<uint4*>(sXp + rx + (((c ^ (r & 7)) & 7) << 4)) =
-            make_uint4(slot == 0 ? one : 0u, slot == 1 ? one : 0u, slot == 2 ? one : 0u, slot == 3 ? one : 0u);
-      }
+      for (int c = 0; c < 32; ++c)
+        xb[c] = (half == 0 && (jc >> 1) == c) ? ((jc & 1) ? 0x3F800000u : 0x00003F80u) : 0u;
+      tc::st32(tXb + lanes, xb);
     }
-    fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(xready);
 
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int q = j & 1;
-      if (!mbar_wait_or_abort(rdone, j & 1, p.timeout_ns, abort_flag)) {
-        ok = false;
-        break;
-      }
+    // Group g's prep product: the A rows (warps 0, 1) write bf16 M^T = -eta x
+    // (row r of the top half) for the chain; the B rows (warps 2, 3) keep
+    // Q^T = eta x (row r of the bottom half) as bf16 pairs in qv.
+    uint8_t* mrow = smem + kMOff + ((jc >> 3) * 1024 + (jc & 7) * 128);
+    uint32_t qv[32];
+    auto convert = [&](int g) -> bool {
+      if (!mbar_wait_or_abort(&pdone[g & 1], (g >> 1) & 1, p.timeout_ns, abort_flag)) return false;
       tc::fence_after_sync();
-      float v[64];
-      tc::ld32(tR + lanes, v);
-      tc::ld32(tR + lanes + 32, v + 32);
-      if (half) {
-        // Row jc of V^T, written by a helper warp: wait for it directly.
-        if (!mbar_wait_or_abort(&prepready[q], (j >> 1) & 1, p.timeout_ns, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* vrow = vtp(q) + jc * 128;
+      if (half == 0) {
+        uint8_t* dst = mrow + (g & 1) * kTileBytes;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(vrow + (((c ^ (jc & 7)) & 7) << 4));
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        for (int part = 0; part < 2; ++part) {
+          float v[32];
+          tc::ld32(tP + 64 * (g & 1) + lanes + 32 * part, v);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[8 * c + 2 * e] -= bf16_lo(ww[e]);
-            v[8 * c + 2 * e + 1] -= bf16_hi(ww[e]);
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c = 4 * part + cc;
+            *reinterpret_cast<uint4*>(dst + (((c ^ (jc & 7)) & 7) << 4)) =
+                make_uint4(pack_bf16(-eta * v[8 * cc], -eta * v[8 * cc + 1]),
+                           pack_bf16(-eta * v[8 * cc + 2], -eta * v[8 * cc + 3]),
+                           pack_bf16(-eta * v[8 * cc + 4], -eta * v[8 * cc + 5]),
+                           pack_bf16(-eta * v[8 * cc + 6], -eta * v[8 * cc + 7]));
           }
         }
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(sEp + rx + (((c ^ (r & 7)) & 7) << 4)) =
-            make_uint4(pack_bf16(neta * v[8 * c], neta * v[8 * c + 1]), pack_bf16(neta * v[8 * c + 2], neta * v[8 * c + 3]),
-                       pack_bf16(neta * v[8 * c + 4], neta * v[8 * c + 5]),
-                       pack_bf16(neta * v[8 * c + 6], neta * v[8 * c + 7]));
-      fence_proxy_async_smem();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(eready);
-      if (j % spc == spc - 1 && j + 1 < n) {
-        if (!mbar_wait_or_abort(udone, (j / spc) & 1, p.timeout_ns, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
-        float x[64];
-        tc::ld32(tX + lanes, x);
-        tc::ld32(tX + lanes + 32, x + 32);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(sXp + rx + (((c ^ (r & 7)) & 7) << 4)) =
-              make_uint4(pack_bf16(x[8 * c], x[8 * c + 1]), pack_bf16(x[8 * c + 2], x[8 * c + 3]),
-                         pack_bf16(x[8 * c + 4], x[8 * c + 5]), pack_bf16(x[8 * c + 6], x[8 * c + 7]));
         fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(xready);
+        if (lane == 0) mbar_arrive(&mqready[g & 1]);
+      } else {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          float v[32];
+          tc::ld32(tP + 64 * (g & 1) + lanes + 32 * part, v);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) qv[16 * part + c] = pack_bf16(eta * v[2 * c], eta * v[2 * c + 1]);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qtaken[g & 1]);
       }
-    }
-    if (ok && mbar_wait_or_abort(udone, ((n - 1) / spc) & 1, p.timeout_ns, abort_flag)) {
-      // (A_s or B_s)[i][jc] = X^T[r][i]
+      return true;
+    };
+
+    bool ok = convert(0);
+    for (int g = 0; ok && g < ng; ++g) {
+      if (half == 0 && g + 1 < ng && !(ok = convert(g + 1))) break;
+      if (!(ok = mbar_wait_or_abort(xdone, g & 1, p.timeout_ns, abort_flag))) break;
       tc::fence_after_sync();
-      float* out = p.seg_maps + (static_cast<size_t>(unit) * maps + seg) * 2 * kD * kD + half * kD * kD;
       float x[64];
       tc::ld32(tX + lanes, x);
       tc::ld32(tX + lanes + 32, x + 32);
+      if (half == 1) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) out[i * kD + jc] = x[i];
-    } else {
+        for (int c = 0; c < 32; ++c) {
+          x[2 * c] += bf16_lo(qv[c]);
+          x[2 * c + 1] += bf16_hi(qv[c]);
+        }
+      }
+      if (g + 1 < ng) {
+        uint32_t xb[32];
+        if (half == 1) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) xb[c] = __float_as_uint(x[c]);
+          tc::st32(tX + lanes, xb);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) xb[c] = __float_as_uint(x[32 + c]);
+          tc::st32(tX + lanes + 32, xb);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) xb[c] = pack_bf16(x[2 * c], x[2 * c + 1]);
+        tc::st32(tXb + lanes, xb);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xready);
+        if (half == 1 && !(ok = convert(g + 1))) break;
+      } else {
+        // (A_s or B_s)[i][jc] = X^T[r][i]
+        float* out = p.seg_maps + (static_cast<size_t>(unit) * maps + seg) * 2 * kD * kD + half * kD * kD;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) out[i * kD + jc] = x[i];
+      }
+    }
+    if (!ok) {
       if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereRows, unit);
       *abort_flag = 1;
     }
