@@ -288,6 +288,8 @@ def bench_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = synth.WORKLOADS[args.workload].with_(b=args.b)
+    if args.T:
+        w = w.with_(T=args.T)
     inp = synth.make_inputs(w, want_exact=False)
 
     def to_dev(a):
@@ -366,17 +368,18 @@ def bench_ours(args, world, rank, local):
     names = ("linear_seg_affine_wy_kernel" if plan["affine"] == 2 else "linear_seg_affine_kernel",
              "linear_seg_combine_kernel", "linear_mma_kernel")
     kernels = {}
+    profile_key = f"{w.name} B{w.B} H{w.H} T{w.T} b{args.b}"
     for k, name in enumerate(names):
         if kbytes[k] == 0:
             continue
         gbs = kbytes[k] / (kernel_ms[k] * 1e-3) / 1e9
         kernels[name] = {"ms": round(kernel_ms[k], 4), "share": round(kernel_ms[k] / ms_per_step, 4),
                          "algorithmic_bytes": kbytes[k], "achieved_gbs": round(gbs, 1),
-                         "frac": round(gbs / hbm_gbs, 4)}
+                         "frac": round(gbs / hbm_gbs, 4), "traffic": profiled_traffic(name, profile_key)}
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     alg_bytes = algorithmic_bytes(w)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": hbm_gbs,
-                "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": profiled_traffic(dom, w.name),
+                "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": kernels[dom]["traffic"],
                 "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.4 TB/s",
                 "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes"], "kernel_ms": kernels[dom]["ms"],

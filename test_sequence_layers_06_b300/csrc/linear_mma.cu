@@ -25,7 +25,7 @@
 // to the tile, because Q_u Wa - eta sum_{u'<u} (Q_u K_u'^T) E_u' = Q_u W_run.
 //
 // Data movement: a producer warp streams the Q, K, V tiles (16 x 64 bf16,
-// 2 KB each) with TMA into a 4-stage ring (128-byte swizzle, so ldmatrix is
+// 2 KB each) with TMA into a 6-stage ring (128-byte swizzle, so ldmatrix is
 // conflict-free); Z leaves through a small shared staging tile per warp and a
 // TMA store. Every wait is bounded in wall-clock time.
 //
@@ -40,7 +40,7 @@ namespace {
 
 constexpr int kD = 64;
 constexpr int kTile = 16;
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kWarps = 4;                     // consumer warps; one more produces
 constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kTileBytes = kTile * kD * 2;    // 2048
@@ -50,6 +50,8 @@ constexpr int kZBytes = kTile * 16 * 2;       // 512 per warp and buffer
 constexpr int kBarOff = kZOff + kWarps * 2 * kZBytes;
 constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
 constexpr int kSmemBytes = kAbortOff + 16 + 1024;  // + slack to align the base to 1024
+static_assert(kSmemBytes <= 48 * 1024, "no opt-in to more dynamic shared memory");
+static_assert(3 * kSmemBytes <= 227 * 1024, "three CTAs per SM");
 
 enum : int { kWhereProducer = 1, kWhereConsumer = 2 };
 
