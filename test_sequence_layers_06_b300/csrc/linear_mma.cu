@@ -47,8 +47,10 @@ constexpr int kTileBytes = kTile * kD * 2;    // 2048
 constexpr int kStageBytes = 3 * kTileBytes;   // Q, K, V
 constexpr int kZOff = kStages * kStageBytes;  // 24576
 constexpr int kZBytes = kTile * 16 * 2;       // 512 per warp and buffer
-constexpr int kBarOff = kZOff + kWarps * 2 * kZBytes;
-constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
+constexpr int kSOff = kZOff + kWarps * 2 * kZBytes;  // per stage: S^T B fragments, 16 bytes per lane
+constexpr int kSBytes = 32 * 16;
+constexpr int kBarOff = kSOff + kStages * kSBytes;
+constexpr int kAbortOff = kBarOff + 3 * kStages * 8;
 constexpr int kSmemBytes = kAbortOff + 16 + 1024;  // + slack to align the base to 1024
 static_assert(kSmemBytes <= 48 * 1024, "no opt-in to more dynamic shared memory");
 static_assert(3 * kSmemBytes <= 227 * 1024, "three CTAs per SM");
@@ -63,6 +65,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* empty = full + kStages;
+  uint64_t* sready = empty + kStages;  // the tile's S fragments are written
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
 
   const int unit = blockIdx.x / p.seg_count;
@@ -78,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kWarps);
+      mbar_init(&sready[s], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -86,25 +90,76 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   if (warp == kWarps) {
     // ------------------------------------------------------------ producer
+    // Lane 0 streams the tiles; the whole warp forms each tile's S = tril(Q K^T)
+    // once for the four consumer warps, as the B fragments of S^T they use.
+    const int g = lane >> 2, tg = lane & 3, mi = lane >> 3, mr = lane & 7;
+    int issued = 0;  // lane 0
+    auto load = [&](int u) {
+      const int s = u % kStages;
+      mbar_arrive_expect_tx(&full[s], kStageBytes);
+      uint8_t* st = smem + s * kStageBytes;
+      tma_load_3d(st, &mq, &full[s], 0, t0 + u * kTile, unit);
+      tma_load_3d(st + kTileBytes, &mk, &full[s], 0, t0 + u * kTile, unit);
+      tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, t0 + u * kTile, unit);
+      ++issued;
+    };
     if (lane == 0) {
       prefetch_tmap(&mq);
       prefetch_tmap(&mk);
       prefetch_tmap(&mv);
-      int issued = 0;
-      for (int u = 0; u < num_tiles; ++u) {
-        const int s = u % kStages;
-        if (u >= kStages && !mbar_wait_bounded(&empty[s], ((u / kStages) - 1) & 1, p.timeout_ns)) {
-          report_error(p.status, TTT_ERR_TIMEOUT, kWhereProducer, unit);
-          *abort_flag = 1;
-          break;
+      if (!p.inject_stall)
+        for (int u = 0; u < min(kStages, num_tiles); ++u) load(u);
+    }
+    bool ok = true;
+    for (int u = 0; u < num_tiles; ++u) {
+      const int s = u % kStages;
+      if (!mbar_wait_or_abort(&full[s], (u / kStages) & 1, p.timeout_ns, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sQ = smem_u32(smem + s * kStageBytes);
+      const uint32_t sK = sQ + kTileBytes;
+      float sacc[2][4] = {};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t qa[4], r[4];
+        ldsm_x4(qa, sQ + swz128(((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));  // Q: A (m = t, k = i)
+        ldsm_x4(r, sK + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));   // K: B (k = i, n = t')
+        const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
+        mma_bf16_16816(sacc[0], qa, b0);
+        mma_bf16_16816(sacc[1], qa, b1);
+      }
+      // Element (t, t') with t = g (+8), t' = 8nt + 2tg (+1); keep t' <= t (each token
+      // sees its own gradient).
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 8 * nt + 2 * tg;
+        if (c > g) sacc[nt][0] = 0.f;
+        if (c + 1 > g) sacc[nt][1] = 0.f;
+        if (c > g + 8) sacc[nt][2] = 0.f;
+        if (c + 1 > g + 8) sacc[nt][3] = 0.f;
+      }
+      // S's C fragment (rows t, columns t') is the B fragment (k = t', n = t) of S^T.
+      *reinterpret_cast<uint4*>(smem + kSOff + s * kSBytes + lane * 16) =
+          make_uint4(pack_bf16(sacc[0][0], sacc[0][1]), pack_bf16(sacc[1][0], sacc[1][1]),
+                     pack_bf16(sacc[0][2], sacc[0][3]), pack_bf16(sacc[1][2], sacc[1][3]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sready[s]);
+      // Refill the stage of tile u - 1 once the consumers have released it.
+      const int v = u - 1 + kStages;
+      if (u >= 1 && v < num_tiles && !p.inject_stall) {
+        if (lane == 0) {
+          ok = mbar_wait_or_abort(&empty[(u - 1) % kStages], ((u - 1) / kStages) & 1, p.timeout_ns, abort_flag);
+          if (ok) load(v);
         }
-        if (*abort_flag || p.inject_stall) break;
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        uint8_t* st = smem + s * kStageBytes;
-        tma_load_3d(st, &mq, &full[s], 0, t0 + u * kTile, unit);
-        tma_load_3d(st + kTileBytes, &mk, &full[s], 0, t0 + u * kTile, unit);
-        tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, t0 + u * kTile, unit);
-        ++issued;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+    }
+    if (lane == 0) {
+      if (!ok) {
+        if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereProducer, unit);
+        *abort_flag = 1;
       }
       // Loads still in flight must land before the CTA may exit.
       for (int u = (issued > kStages ? issued - kStages : 0); u < issued; ++u)
@@ -141,12 +196,14 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   for (int u = 0; u < num_tiles; ++u) {
     const int s = u % kStages;
-    if (!mbar_wait_bounded(&full[s], (u / kStages) & 1, p.timeout_ns)) {
-      report_error(p.status, TTT_ERR_TIMEOUT, kWhereConsumer, unit);
+    if (!mbar_wait_or_abort(&sready[s], (u / kStages) & 1, p.timeout_ns, abort_flag) ||
+        !mbar_wait_or_abort(&full[s], (u / kStages) & 1, p.timeout_ns, abort_flag)) {
+      if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereConsumer, unit);
       *abort_flag = 1;
       break;
     }
-    if (*abort_flag) break;
+    // S^T's B fragments for this lane, formed by the producer warp.
+    const uint4 sv = *reinterpret_cast<const uint4*>(smem + kSOff + s * kSBytes + lane * 16);
     const uint32_t sQ = smem_u32(smem + s * kStageBytes);
     const uint32_t sK = sQ + kTileBytes;
     const uint32_t sV = sQ + 2 * kTileBytes;
@@ -214,7 +271,6 @@ __global__ void __launch_bounds__(kThreads, 3)
 
     // Read-out part 1: Z^T = W_run^T Q^T (Q as B operand, like K).
     float z[2][4] = {};
-    uint32_t qa[4][4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       uint32_t r[4];
@@ -222,19 +278,10 @@ __global__ void __launch_bounds__(kThreads, 3)
       uint32_t qb0[2] = {r[0], r[1]}, qb1[2] = {r[2], r[3]};
       mma_bf16_16816(z[0], wr[k], qb0);
       mma_bf16_16816(z[1], wr[k], qb1);
-      // Q as the A operand (m = t, k = i) of S = Q K^T.
-      ldsm_x4(qa[k], sQ + swz128(((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));
     }
     // All reads of this stage are in registers: hand it back to the producer.
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-
-    // S = tril(Q K^T) (diagonal kept: each token sees its own gradient).
-    float sacc[2][4] = {};
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(sacc[nt], qa[k], kb[nt][k]);
 
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -254,18 +301,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
     for (int q = 0; q < 8; ++q) mma_bf16_16816(Wt[q], ea, kbt[q]);
 
-    // Mask S: element (t, t') with t = g (+8), t' = 8nt + 2tg (+1); keep t' <= t.
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int c = 8 * nt + 2 * tg;
-      if (c > g) sacc[nt][0] = 0.f;
-      if (c + 1 > g) sacc[nt][1] = 0.f;
-      if (c > g + 8) sacc[nt][2] = 0.f;
-      if (c + 1 > g + 8) sacc[nt][3] = 0.f;
-    }
-    // S's C fragment (rows t, columns t') is the B fragment (k = t', n = t) of S^T.
-    uint32_t sb0[2] = {pack_bf16(sacc[0][0], sacc[0][1]), pack_bf16(sacc[1][0], sacc[1][1])};
-    uint32_t sb1[2] = {pack_bf16(sacc[0][2], sacc[0][3]), pack_bf16(sacc[1][2], sacc[1][3])};
+    const uint32_t sb0[2] = {sv.x, sv.y}, sb1[2] = {sv.z, sv.w};
     // Read-out part 2: Z^T += (-eta E^T) S^T.
     mma_bf16_16816(z[0], ea, sb0);
     mma_bf16_16816(z[1], ea, sb1);

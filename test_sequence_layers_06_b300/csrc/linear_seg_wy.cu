@@ -33,10 +33,10 @@
 // issued after it are done too (measured), so the control lane waits for each
 // chain product before it issues prep products for later groups.
 //
-// Roles (224 threads): warps 0-3 own the 128 rows of X^T and of the prep
-// product; warp 4 lane 0 issues the TMA loads and the MMAs; warps 5 and 6
-// compute Kh for even and odd steps, each into its own buffer. Every wait is
-// bounded in time and gives up early when another role has given up.
+// Roles (256 threads): warps 0-3 own the 128 rows of X^T and of the prep
+// product; warp 4 lane 0 issues the TMA loads and the MMAs; warps 5-7 compute
+// Kh for every third step, each into its own buffer. Every wait is bounded in
+// time and gives up early when another role has given up.
 #include "ttt_device.cuh"
 #include "tcgen05.cuh"
 #include "kernels.h"
@@ -46,14 +46,15 @@ namespace {
 
 constexpr int kD = 64;
 constexpr int kStep = 64;                          // tokens per TMA step
-constexpr int kStages = 3;                         // (a fourth stage measured slower)
-constexpr int kThreads = 224;
+constexpr int kStages = 4;                         // K, V stages (a split K ring measured slower)
+constexpr int kHelpers = 3;                        // Kh warps (b < 64), one buffer each
+constexpr int kThreads = (5 + kHelpers) * 32;
 constexpr int kTileBytes = kStep * kD * 2;         // 8 KB: one 64 x 64 bf16 tile
 constexpr int kMOff = 0;                           // [2] M^T tiles, bf16 [64][64]
 constexpr int kStageOff = kMOff + 2 * kTileBytes;  // [kStages] x (K tile, V tile)
-constexpr int kKhOff = kStageOff + kStages * 2 * kTileBytes;  // Kh [2] (b < 64)
-constexpr int kBarOff = kKhOff + 2 * kTileBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 3;
+constexpr int kKhOff = kStageOff + kStages * 2 * kTileBytes;  // Kh [kHelpers] (b < 64)
+constexpr int kBarOff = kKhOff + kHelpers * kTileBytes;
+constexpr int kNumBars = 2 * kStages + kHelpers + 2 + 2 + 2 + 3;
 static_assert(kNumBars * 8 + 16 + 1024 + kBarOff <= 113 * 1024 - 512, "two CTAs per SM");
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + slack to align the base to 1024
@@ -177,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // [kStages] TMA data landed
   uint64_t* sfree = full + kStages;                               // [kStages] the step's product is done
-  uint64_t* khready = sfree + kStages;                            // [2] Kh of step j written to buffer j & 1
-  uint64_t* pdone = khready + 2;      // [2] the group's prep product is in its tensor-memory buffer
+  uint64_t* khready = sfree + kStages;                            // [kHelpers] Kh of step j in buffer j % kHelpers
+  uint64_t* pdone = khready + kHelpers;  // [2] the group's prep product is in its tensor-memory buffer
   uint64_t* mqready = pdone + 2;      // [2] bf16 M^T written to buffer g & 1 (2 warp arrivals)
   uint64_t* qtaken = pdone + 4;       // [2] Q^T of buffer g & 1 read into registers (2 warp arrivals)
   uint64_t* xready = pdone + 6;       // X^T refreshed (4 warp arrivals)
@@ -205,8 +206,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&full[s], 1);
       mbar_init(&sfree[s], 1);
     }
-    mbar_init(&khready[0], 1);
-    mbar_init(&khready[1], 1);
+    for (int q = 0; q < kHelpers; ++q) mbar_init(&khready[q], 1);
     mbar_init(&pdone[0], 1);
     mbar_init(&pdone[1], 1);
     mbar_init(&mqready[0], 2);
@@ -261,10 +261,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           if (!mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns, abort_flag)) return false;
           consumed = j + 1;
-          if (wy && !mbar_wait_or_abort(&khready[j & 1], (j >> 1) & 1, p.timeout_ns, abort_flag)) return false;
+          if (wy && !mbar_wait_or_abort(&khready[j % kHelpers], (j / kHelpers) & 1, p.timeout_ns, abort_flag))
+            return false;
           tc::fence_after_sync();
           const uint32_t sK = smem_u32(stageK(s));
-          const uint32_t sB = wy ? smem_u32(khp(j & 1)) : sK;
+          const uint32_t sB = wy ? smem_u32(khp(j % kHelpers)) : sK;
           const bool first = (j % spc) == 0;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // A: K tile then V tile, MN-major, 8 KB apart; B: Kh, MN-major
@@ -304,24 +305,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         (void)mbar_wait_bounded(&full[v % kStages], (v / kStages) & 1, p.timeout_ns);
     }
   } else if (warp >= 5) {
-    // -------------------------------------------------- Kh for every other step
+    // -------------------------------------------------- Kh for every kHelpers-th step
     if (wy) {
       bool ok = true;
-      for (int j = warp - 5; j < n; j += 2) {
+      for (int j = warp - 5; j < n; j += kHelpers) {
         const int s = j % kStages;
         ok = mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns, abort_flag);
         if (!ok) break;
         uint32_t ua[4][4][4];
         bool nz[4][4];
         prep_u(smem_u32(stageK(s)), -eta, p.b, lane, ua, nz);
-        // The Kh buffer's previous user, step j-2, must have finished its product.
-        if (j >= 2)
-          ok = mbar_wait_or_abort(&sfree[(j - 2) % kStages], ((j - 2) / kStages) & 1, p.timeout_ns, abort_flag);
+        // The Kh buffer's previous user, step j - kHelpers, must have finished its product.
+        const int jp = j - kHelpers;
+        if (jp >= 0) ok = mbar_wait_or_abort(&sfree[jp % kStages], (jp / kStages) & 1, p.timeout_ns, abort_flag);
         if (!ok) break;
-        prep_kh(smem_u32(stageK(s)), khp(j & 1), lane, ua, nz);
+        prep_kh(smem_u32(stageK(s)), khp(j % kHelpers), lane, ua, nz);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&khready[j & 1]);
+        if (lane == 0) mbar_arrive(&khready[j % kHelpers]);
       }
       if (!ok && lane == 0) {
         if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWherePrep, unit);
