@@ -70,7 +70,7 @@ struct DecodeParams {
 bool linear_mma_supported(const LinearParams& p);
 int linear_mma_tile_rows();
 cudaError_t launch_linear_mma(const LinearParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                              const CUtensorMap& mv, const CUtensorMap& mz, cudaStream_t stream);
+                              const CUtensorMap& mv, cudaStream_t stream);
 
 // Segment-parallel TTT-Linear (bf16, d = 64, b % 16 == 0): per-segment affine
 // maps, then the combine over segments; linear_mma then runs every segment.

@@ -26,8 +26,10 @@
 //
 // Data movement: a producer warp streams the Q, K, V tiles (16 x 64 bf16,
 // 2 KB each) with TMA into a 6-stage ring (128-byte swizzle, so ldmatrix is
-// conflict-free); Z leaves through a small shared staging tile per warp and a
-// TMA store. Every wait is bounded in wall-clock time.
+// conflict-free) and forms each tile's S = tril(Q K^T) once for the four
+// consumer warps; Z leaves through a transposing stmatrix into a small staging
+// tile per warp and one 16-byte store per lane. Every wait is bounded in
+// wall-clock time.
 //
 // Segments: with p.seg_count > 1 a CTA serves one segment of one unit, starting
 // from the state the combine step of linear_seg.cu computed for it (W0 for the
@@ -59,7 +61,7 @@ enum : int { kWhereProducer = 1, kWhereConsumer = 2 };
 
 __global__ void __launch_bounds__(kThreads, 3)
     linear_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                      const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mz,
+                      const __grid_constant__ CUtensorMap mv,
                       LinearParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -175,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int mi = lane >> 3;  // ldmatrix/stmatrix: which 8x8 matrix this lane addresses
   const int mr = lane & 7;   // ... and which of its rows
   const float neta = -p.eta[h];
+  __nv_bfloat16* Zg = static_cast<__nv_bfloat16*>(p.Z);
 
   // W^T fragments: Wt[q] covers input columns i in [8q, 8q+8) of rows j = jw+g, jw+g+8.
   float Wt[8][4];
@@ -196,8 +199,9 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   for (int u = 0; u < num_tiles; ++u) {
     const int s = u % kStages;
-    if (!mbar_wait_or_abort(&sready[s], (u / kStages) & 1, p.timeout_ns, abort_flag) ||
-        !mbar_wait_or_abort(&full[s], (u / kStages) & 1, p.timeout_ns, abort_flag)) {
+    // The producer raises sready only after it has seen the tile land (full) and
+    // read it, so sready alone orders this warp's reads after the TMA writes.
+    if (!mbar_wait_or_abort(&sready[s], (u / kStages) & 1, p.timeout_ns, abort_flag)) {
       if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereConsumer, unit);
       *abort_flag = 1;
       break;
@@ -306,24 +310,22 @@ __global__ void __launch_bounds__(kThreads, 3)
     mma_bf16_16816(z[0], ea, sb0);
     mma_bf16_16816(z[1], ea, sb1);
 
-    // Z^T (rows j, columns t) -> shared tile Z[t][j] (16 x 16 bf16) by a
-    // transposing stmatrix, then one TMA store of the warp's 16 columns.
+    // Z^T (rows j, columns t) -> Z[t][j] (16 x 16 bf16) in the warp's staging tile
+    // by a transposing stmatrix, then one 16-byte store per lane: rows of 32 bytes.
     uint8_t* zbuf = smem + kZOff + (warp * 2 + (u & 1)) * kZBytes;
-    if (lane == 0) bulk_wait_read<1>();  // the store issued two tiles ago has read this buffer
-    __syncwarp();
     {
       uint32_t zr[4] = {pack_bf16(z[0][0], z[0][1]), pack_bf16(z[0][2], z[0][3]),
                         pack_bf16(z[1][0], z[1][1]), pack_bf16(z[1][2], z[1][3])};
       stsm_x4_t(smem_u32(zbuf) + (((mi >> 1) << 3) + mr) * 32 + (mi & 1) * 16, zr);
     }
-    fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
-      tma_store_3d(&mz, zbuf, jw, t0 + u * kTile, unit);
-      bulk_commit();
+    {
+      const int tok = t0 + u * kTile + (lane >> 1);
+      const uint4 zv = *reinterpret_cast<const uint4*>(zbuf + (lane >> 1) * 32 + (lane & 1) * 16);
+      if (tok < t1)
+        *reinterpret_cast<uint4*>(Zg + (static_cast<size_t>(unit) * p.T + tok) * kD + jw + 8 * (lane & 1)) = zv;
     }
   }
-  if (lane == 0) bulk_wait<0>();
   if (seg != p.seg_count - 1) return;
 
   // Final state, W_out[unit][i][j].
@@ -343,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 3)
 bool linear_mma_supported(const LinearParams& p) { return p.d == kD && p.b % kTile == 0 && p.bf16; }
 
 cudaError_t launch_linear_mma(const LinearParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                              const CUtensorMap& mv, const CUtensorMap& mz, cudaStream_t stream) {
+                              const CUtensorMap& mv, cudaStream_t stream) {
   if (p.units == 0) return cudaSuccess;
-  linear_mma_kernel<<<p.units * p.seg_count, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mz, p);
+  linear_mma_kernel<<<p.units * p.seg_count, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

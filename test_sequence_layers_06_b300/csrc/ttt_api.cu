@@ -251,12 +251,11 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
   if (st != TTT_OK) return st;
   cudaError_t err;
   if (pl.mma) {
-    CUtensorMap mq, mk, mv, mz;
+    CUtensorMap mq, mk, mv;
     const int rows = ttt::linear_mma_tile_rows();
     if (!encode_3d(&mq, Q, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_3d(&mk, K, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&mz, Z, p.units, T, d, rows, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
       return TTT_ERR_CUDA;
     cudaEvent_t* ev = static_cast<cudaEvent_t*>(o.phase_events);
     err = ev ? cudaEventRecord(ev[0], s) : cudaSuccess;
@@ -275,7 +274,7 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
     if (err == cudaSuccess && ev) err = cudaEventRecord(ev[1], s);
     if (err == cudaSuccess && pl.seg_count > 1) err = ttt::launch_linear_seg_combine(p, s);
     if (err == cudaSuccess && ev) err = cudaEventRecord(ev[2], s);
-    if (err == cudaSuccess) err = ttt::launch_linear_mma(p, mq, mk, mv, mz, s);
+    if (err == cudaSuccess) err = ttt::launch_linear_mma(p, mq, mk, mv, s);
     if (err == cudaSuccess && ev) err = cudaEventRecord(ev[3], s);
   } else {
     err = ttt::launch_linear_simt(p, s);
