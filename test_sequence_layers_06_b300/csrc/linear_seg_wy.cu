@@ -77,27 +77,48 @@ __device__ void prep_u(uint32_t sK, float neta, int bt, int lane, uint32_t (&ua)
   const int mi = lane >> 3;
   const int mr = lane & 7;
   // G_rm = K_r K_m^T for r > m, kept as B fragments of G_mr = G_rm^T
-  // (k = tokens of block m, n = tokens of block r; two 8-wide n-tiles).
+  // (k = tokens of block m, n = tokens of block r; two 8-wide n-tiles). Each
+  // k-step loads every block's fragments once and feeds all the pairs.
+  float gacc[4][4][2][4];
+#pragma unroll
+  for (int r = 1; r < 4; ++r)
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) gacc[r][m][nt][e] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t a[4][4], bb[4][4];
+#pragma unroll
+    for (int r = 1; r < 4; ++r)
+      if (needed(r, 0, bt) || needed(r, r - 1, bt))
+        ldsm_x4(a[r], sK + swz128(16 * r + ((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+      if (needed(3, m, bt) || needed(m + 1, m, bt))
+        ldsm_x4(bb[m], sK + swz128(16 * m + ((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
+#pragma unroll
+    for (int r = 1; r < 4; ++r)
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        if (!needed(r, m, bt)) continue;
+        const uint32_t b0[2] = {bb[m][0], bb[m][1]}, b1[2] = {bb[m][2], bb[m][3]};
+        mma_bf16_16816(gacc[r][m][0], a[r], b0);
+        mma_bf16_16816(gacc[r][m][1], a[r], b1);
+      }
+  }
   uint32_t gb[4][4][2][2];
 #pragma unroll
   for (int r = 1; r < 4; ++r)
 #pragma unroll
     for (int m = 0; m < 3; ++m) {
       if (!needed(r, m, bt)) continue;
-      float acc[2][4] = {};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t a[4], bb[4];
-        ldsm_x4(a, sK + swz128(16 * r + ((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));
-        ldsm_x4(bb, sK + swz128(16 * m + ((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
-        const uint32_t b0[2] = {bb[0], bb[1]}, b1[2] = {bb[2], bb[3]};
-        mma_bf16_16816(acc[0], a, b0);
-        mma_bf16_16816(acc[1], a, b1);
-      }
 #pragma unroll
       for (int nr = 0; nr < 2; ++nr) {
-        gb[r][m][nr][0] = pack_bf16(acc[0][2 * nr], acc[0][2 * nr + 1]);
-        gb[r][m][nr][1] = pack_bf16(acc[1][2 * nr], acc[1][2 * nr + 1]);
+        gb[r][m][nr][0] = pack_bf16(gacc[r][m][0][2 * nr], gacc[r][m][0][2 * nr + 1]);
+        gb[r][m][nr][1] = pack_bf16(gacc[r][m][1][2 * nr], gacc[r][m][1][2 * nr + 1]);
       }
     }
   const uint32_t eye = (g == 2 * tg ? 0x00003F80u : 0u) | (g == 2 * tg + 1 ? 0x3F800000u : 0u);
@@ -131,8 +152,6 @@ __device__ void prep_u(uint32_t sK, float neta, int bt, int lane, uint32_t (&ua)
 
 // Kh_c = K_c + sum_{r > c} U_cr K_r, written as rows of tokens (128-byte swizzled).
 __device__ void prep_kh(uint32_t sK, uint8_t* kh, int lane, const uint32_t (&ua)[4][4][4], const bool (&nz)[4][4]) {
-  const int g = lane >> 2;
-  const int tg = lane & 3;
   const int mi = lane >> 3;
   const int mr = lane & 7;
 #pragma unroll
@@ -163,10 +182,14 @@ __device__ void prep_kh(uint32_t sK, uint8_t* kh, int lane, const uint32_t (&ua)
         mma_bf16_16816(acc[2 * qq + 1], ua[c][r], b1);
       }
     }
+    // Rows 16c.., columns 16qq..: the accumulator fragments are stmatrix's
+    // register layout (matrices: rows 0-7 / 8-15 x columns 0-7 / 8-15).
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      *reinterpret_cast<uint32_t*>(kh + swz128(16 * c + g, nt) + 4 * tg) = pack_bf16(acc[nt][0], acc[nt][1]);
-      *reinterpret_cast<uint32_t*>(kh + swz128(16 * c + g + 8, nt) + 4 * tg) = pack_bf16(acc[nt][2], acc[nt][3]);
+    for (int qq = 0; qq < 4; ++qq) {
+      const uint32_t v[4] = {pack_bf16(acc[2 * qq][0], acc[2 * qq][1]), pack_bf16(acc[2 * qq][2], acc[2 * qq][3]),
+                             pack_bf16(acc[2 * qq + 1][0], acc[2 * qq + 1][1]),
+                             pack_bf16(acc[2 * qq + 1][2], acc[2 * qq + 1][3])};
+      stsm_x4(smem_u32(kh) + swz128(16 * c + ((mi & 1) << 3) + mr, 2 * qq + (mi >> 1)), v);
     }
   }
 }

@@ -69,11 +69,12 @@ def test_tensor_path_ragged_and_chunk_sizes(T, b):
 
 
 @pytest.mark.parametrize("T,b,seg", [(1024, 16, 256), (1000, 16, 256), (64, 16, 32), (777, 16, 16),
-                                     (2048, 64, 512), (2560, 256, 512), (1300, 32, 64), (4096, 16, 1024)])
+                                     (2048, 64, 512), (2560, 256, 512), (2048, 128, 512), (1300, 32, 64),
+                                     (4096, 16, 1024)])
 def test_segment_parallel_path(T, b, seg):
     """Segment-parallel form: per-segment affine maps, the combine, and a read-out
     per segment from its start state. Full, ragged and one-tile segments; chunks
-    of 1, 2, 4 and 16 tiles; per-head eta."""
+    of 1, 2, 4, 8 and 16 tiles (one to four 64-token steps per chunk); per-head eta."""
     w = W["linear_125m"].with_(B=2, H=3, T=T, seed=300 + T + b + seg)
     inp = synth.make_inputs(w)
     t = torch_inputs(inp)
