@@ -56,7 +56,7 @@ constexpr int kKhOff = kStageOff + kStages * 2 * kTileBytes;  // Kh [kHelpers] (
 constexpr int kBarOff = kKhOff + kHelpers * kTileBytes;
 constexpr int kNumBars = 2 * kStages + kHelpers + 2 + 2 + 2 + 3;
 static_assert(kNumBars * 8 + 16 + 1024 + kBarOff <= 113 * 1024 - 512, "two CTAs per SM");
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;     // TMEM address, abort flag, steps loaded
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;   // + slack to align the base to 1024
 // Tensor memory: X^T fp32 [0, 64); prep [2] x 64 at [64, 192); X^T bf16 [192, 224).
 constexpr uint32_t kCols = 256;
@@ -210,6 +210,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* drain = pdone + 8;        // every MMA issued has completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+  // Steps whose TMA load the control lane has issued. A stage is reloaded only
+  // after the product of its previous step, so once this passes j the stage
+  // barrier is in step j's phase: the helpers read it before they wait on that
+  // barrier by parity (they run ahead and could otherwise see the phase before).
+  int* n_loaded = reinterpret_cast<int*>(smem + kMiscOff + 8);
 
   const int maps = p.seg_count - 1;
   const int unit = blockIdx.x / maps;
@@ -240,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(xdone, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *n_loaded = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -269,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_load_3d(stageK(s), &mk, &full[s], 0, t0 + j * kStep, unit);
         tma_load_3d(stageK(s) + kTileBytes, &mv, &full[s], 0, t0 + j * kStep, unit);
         loaded = j + 1;
+        st_release(n_loaded, loaded);
       };
       if (!p.inject_stall)
         for (int j = 0; j < min(kStages, n); ++j) load(j);
@@ -282,10 +289,15 @@ __global__ void __launch_bounds__(kThreads, 2)
               return false;
             load(j + kStages - 1);
           }
-          if (!mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns, abort_flag)) return false;
-          consumed = j + 1;
-          if (wy && !mbar_wait_or_abort(&khready[j % kHelpers], (j / kHelpers) & 1, p.timeout_ns, abort_flag))
+          // b < 64: the helper saw step j's tiles land before it raised khready, so
+          // khready alone orders these products after the TMA writes.
+          if (wy) {
+            if (!mbar_wait_or_abort(&khready[j % kHelpers], (j / kHelpers) & 1, p.timeout_ns, abort_flag))
+              return false;
+          } else if (!mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns, abort_flag)) {
             return false;
+          }
+          consumed = j + 1;
           tc::fence_after_sync();
           const uint32_t sK = smem_u32(stageK(s));
           const uint32_t sB = wy ? smem_u32(khp(j % kHelpers)) : sK;
@@ -333,7 +345,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       bool ok = true;
       for (int j = warp - 5; j < n; j += kHelpers) {
         const int s = j % kStages;
-        ok = mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns, abort_flag);
+        ok = __all_sync(0xffffffffu, wait_count_or_abort(n_loaded, j + 1, p.timeout_ns, abort_flag) &&
+                                         mbar_wait_or_abort(&full[s], (j / kStages) & 1, p.timeout_ns,
+                                                            abort_flag));
         if (!ok) break;
         uint32_t ua[4][4][4];
         bool nz[4][4];

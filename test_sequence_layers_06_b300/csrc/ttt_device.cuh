@@ -74,6 +74,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// A counter in shared memory that one thread raises and others wait for: the
+// store releases everything its thread did before; the load acquires it.
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Wait until *p >= target, giving up after timeout_ns or once *abort is set.
+__device__ __forceinline__ bool wait_count_or_abort(const int* p, int target, uint64_t timeout_ns,
+                                                    volatile int* abort) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (ld_acquire(p) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
 // Wait for the phase of `parity` to complete, giving up after timeout_ns of
 // wall-clock time. Returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
