@@ -488,7 +488,8 @@ def bench_extras(ttt, dev, stream):
         cv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev))
         return inp, cv(inp.q), cv(inp.k), cv(inp.v), torch.from_numpy(inp.eta).to(dev)
 
-    for name, b in (("linear_125m", 16), ("linear_small", 16), ("linear_long", 64), ("linear_long", 256)):
+    for name, b in (("linear_125m", 16), ("linear_small", 16), ("linear_long", 64), ("linear_long", 256),
+                    ("linear_long", 2048)):
         w = synth.WORKLOADS[name].with_(b=b)
         inp, Q, K, V, eta = dev_inputs(w)
         W0 = torch.from_numpy(inp.W0).to(dev)

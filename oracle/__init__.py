@@ -10,7 +10,9 @@ What it computes, and the passages it follows, is in the C file's header. In
 short: TTT-Linear and TTT-MLP, per-token primal form (the reference) and a
 separate per-chunk dual form (kept to pin primal == dual), the affine map of
 each segment of chunks (the segment-parallel form), plus one decode token with
-an (anchor, running) weight pair.
+an (anchor, running) weight pair. ``oracle.backward.linear_backward`` (numpy,
+fp64, small cases) is the backward of the TTT-Linear scan: dQ, dK, dV, deta and
+dW0 for upstream dZ and dW_out, pinned in tests/test_oracle_backward.py.
 
 Parity pins live in tests/test_oracle_pins.py (b = 1 delta rule; causal linear
 attention; finite differences and autograd; eta = 0; chaining; b = T closed

@@ -56,7 +56,7 @@ def test_small_bf16_workload_simt_path():
 
 
 @pytest.mark.parametrize("T,b", [(1, 16), (15, 16), (17, 16), (50, 16), (100, 32), (130, 64), (300, 256),
-                                 (64, 48), (0, 16)])
+                                 (64, 48), (0, 16), (1000, 512)])
 def test_tensor_path_ragged_and_chunk_sizes(T, b):
     """Several 16-token tiles with a ragged tail; chunks of 1, 2, 3 and 16 tiles."""
     w = W["linear_small"].with_(B=1, H=3, T=T, seed=100 + T)
@@ -70,7 +70,7 @@ def test_tensor_path_ragged_and_chunk_sizes(T, b):
 
 @pytest.mark.parametrize("T,b,seg", [(1024, 16, 256), (1000, 16, 256), (64, 16, 32), (777, 16, 16),
                                      (2048, 64, 512), (2560, 256, 512), (2048, 128, 512), (1300, 32, 64),
-                                     (4096, 16, 1024)])
+                                     (4096, 16, 1024), (4096, 1024, 2048), (6144, 2048, 2048)])
 def test_segment_parallel_path(T, b, seg):
     """Segment-parallel form: per-segment affine maps, the combine, and a read-out
     per segment from its start state. Full, ragged and one-tile segments; chunks
