@@ -511,6 +511,22 @@ def bench_extras(ttt, dev, stream):
     flops = w.token_heads * (16 * w.d * m + 4 * 16 * (w.d + m))
     out["mlp_125m_b16"] = {"ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
                            "tensor_frac": round(flops / (ms * 1e-3) / (tflops * 1e12), 5)}
+    # backward of TTT-Linear (fp32 operands, the first GPU form: one CTA per unit)
+    try:
+        w = synth.WORKLOADS["linear_small"].with_(dtype="f32")
+        inp = synth.make_inputs(w, want_exact=False)
+        Q, K, V = (torch.from_numpy(a).to(dev) for a in (inp.q, inp.k, inp.v))
+        eta, W0 = torch.from_numpy(inp.eta).to(dev), torch.from_numpy(inp.W0).to(dev)
+        dZ = torch.randn_like(Q)
+        dW = torch.randn(w.B, w.H, w.d, w.d, device=dev)
+        ws = torch.empty(ttt.ttt_linear_bwd_workspace_bytes(w.B, w.H, w.T, w.d, 16), dtype=torch.uint8, device=dev)
+        ms = t_ms(lambda: ttt.ttt_linear_bwd(Q, K, V, eta, W0, 16, dZ, dW, workspace=ws, stream=stream), 3)
+        out["linear_bwd_small_f32_b16"] = {"ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                                           "note": "B2 H4 T2048 d64 fp32; dQ, dK, dV, d eta, dW0 for given dZ, "
+                                                   "dW_out; one CTA per (batch row, head)"}
+        del Q, K, V, dZ
+    except Exception as exc:  # reported in the line, never silently dropped
+        out["linear_bwd_small_f32_b16"] = {"error": f"{type(exc).__name__}: {exc}"}
     # decode: one token for B1 H32 from a state
     q = torch.randn(1, 32, 64, device=dev).to(torch.bfloat16)
     Wa = torch.zeros(1, 32, 64, 64, device=dev)

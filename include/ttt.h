@@ -202,6 +202,30 @@ TTT_API ttt_status ttt_linear_decode_step(const void* q, const void* k, const vo
                                   const float* eta, float* W_anchor, float* W_run, int B, int H,
                                   int d, int pos, int b, void* z, void* stream);
 
+/*
+ * Backward of ttt_linear_fwd: the vector-Jacobian product of (Z, W_out) with
+ * respect to (Q, K, V, eta, W0), for training the outer loop ("5 · TestingTime
+ * 训练与长上下文", section 2.2: W0 and the projections that make Q, K, V are
+ * outer-loop parameters). Per chunk c with start state W:
+ *   E = K_c W - V_c,  S = tril(Q_c K_c^T),  Z_c = Q_c W - eta S E,  W' = W - eta K_c^T E,
+ * reversed from G = dW_out (G: gradient of the next chunk's start state).
+ *   Q, K, V, dZ [B][H][T][d] float32 (dt must be TTT_F32); eta [H]; W0 [H][d][d];
+ *   dW_out [B][H][d][d]. Outputs dQ, dK, dV [B][H][T][d] float32, deta [H] and
+ *   dW0 [H][d][d] (summed over the batch rows, which share eta and W0).
+ *   Supported: d <= 64 and b <= 64, else TTT_ERR_UNSUPPORTED (also for bf16).
+ *   workspace: ttt_linear_bwd_workspace_bytes(B, H, T, d, b) bytes (a status
+ *   word, every chunk-start state, per-unit partial sums), 16-byte aligned.
+ * All pointers are device memory, 16-byte aligned, caller-owned; work is
+ * enqueued on `stream`. Argument errors return before anything is enqueued.
+ */
+TTT_API size_t ttt_linear_bwd_workspace_bytes(int B, int H, int T, int d, int b);
+
+TTT_API ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                  const float* eta, const float* W0, int B, int H, int T, int d, int b,
+                                  const void* dZ, const float* dW_out, void* dQ, void* dK, void* dV,
+                                  float* deta, float* dW0, void* workspace, size_t ws_bytes,
+                                  void* stream);
+
 /* Waits for `stream`, then reads and clears the status word of `workspace`.
  * Every *_fwd call clears that word when it is enqueued, so this reports the
  * kernels of the latest *_fwd call that used this workspace: TTT_OK, or the

@@ -25,7 +25,8 @@ PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_SEGMENTED = 0, 1, 2, 3
 
 # Every entry point include/ttt.h declares.
 EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_plan", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
-           "ttt_mlp_fwd_noalloc", "ttt_linear_decode_step", "ttt_last_device_status", "ttt_status_str")
+           "ttt_mlp_fwd_noalloc", "ttt_linear_decode_step", "ttt_linear_bwd_workspace_bytes", "ttt_linear_bwd",
+           "ttt_last_device_status", "ttt_status_str")
 
 
 class TTTError(RuntimeError):
@@ -73,10 +74,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_mlp_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
     lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp]
     lib.ttt_last_device_status.argtypes = [vp, vp]
+    lib.ttt_linear_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.ttt_linear_bwd_workspace_bytes.restype = sz
+    lib.ttt_linear_bwd.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.ttt_status_str.argtypes = [i]
     lib.ttt_status_str.restype = ctypes.c_char_p
     for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex", "ttt_mlp_fwd_noalloc",
-              "ttt_linear_decode_step", "ttt_last_device_status"):
+              "ttt_linear_decode_step", "ttt_linear_bwd", "ttt_last_device_status"):
         getattr(lib, f).restype = i
     _lib = lib
     return lib
@@ -245,6 +249,35 @@ def ttt_linear_decode_step(q, k, v, eta, W_anchor, W_run, pos: int, b: int, z=No
     if st != TTT_OK:
         raise TTTError("ttt_linear_decode_step", st)
     return z
+
+
+def ttt_linear_bwd_workspace_bytes(B: int, H: int, T: int, d: int, b: int) -> int:
+    return int(load_library().ttt_linear_bwd_workspace_bytes(B, H, T, d, b))
+
+
+def ttt_linear_bwd(Q, K, V, eta, W0, b: int, dZ, dW_out, workspace=None, stream=None):
+    """Backward of ttt_linear_fwd (float32 operands): returns (dQ, dK, dV, deta, dW0) for
+    upstream gradients dZ [B, H, T, d] and dW_out [B, H, d, d]. Asynchronous on `stream`."""
+    import torch
+    lib = load_library()
+    B, H, T, d = Q.shape
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("dZ", dZ)):
+        _check(t, n, torch.float32, (B, H, T, d))
+    _check(eta, "eta", torch.float32, (H,))
+    _check(W0, "W0", torch.float32, (H, d, d))
+    _check(dW_out, "dW_out", torch.float32, (B, H, d, d))
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    deta = torch.empty((H,), dtype=torch.float32, device=Q.device)
+    dW0 = torch.empty((H, d, d), dtype=torch.float32, device=Q.device)
+    need = ttt_linear_bwd_workspace_bytes(B, H, T, d, b)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    st = lib.ttt_linear_bwd(_p(Q), _p(K), _p(V), TTT_F32, _p(eta), _p(W0), B, H, T, d, int(b), _p(dZ), _p(dW_out),
+                            _p(dQ), _p(dK), _p(dV), _p(deta), _p(dW0), _p(workspace), workspace.numel(),
+                            _stream_ptr(stream))
+    if st != TTT_OK:
+        raise TTTError("ttt_linear_bwd", st)
+    return dQ, dK, dV, deta, dW0
 
 
 def ttt_last_device_status(workspace, stream=None) -> int:

@@ -53,6 +53,27 @@ struct MlpParams {
   int inject_stall;
 };
 
+// Backward of TTT-Linear (fp32 operands): upstream dZ, dW_out -> dQ, dK, dV,
+// d eta [H] and dW0 [H][d][d] (summed over batch rows).
+struct LinearBwdParams {
+  const float* Q;
+  const float* K;
+  const float* V;
+  const float* dZ;
+  const float* eta;
+  const float* W0;
+  const float* dW_out;
+  float* dQ;
+  float* dK;
+  float* dV;
+  float* deta;
+  float* dW0;
+  int B, H, T, d, b;
+  int units;
+  float* states;   // workspace [units][ceil(T/b)][d][d]: chunk-start states
+  float* partial;  // workspace [units][d*d + 1]: per-unit dW0, then d eta
+};
+
 struct DecodeParams {
   const void* q;
   const void* k;
@@ -100,5 +121,11 @@ cudaError_t launch_mlp_simt(const MlpParams& p, cudaStream_t stream);
 
 // Decode token.
 cudaError_t launch_linear_decode(const DecodeParams& p, cudaStream_t stream);
+
+// Backward of TTT-Linear, fp32, d <= 64, b <= 64 (linear_bwd.cu).
+bool linear_bwd_supported(int d, int b);
+size_t linear_bwd_smem_bytes(int d, int b);
+size_t linear_bwd_scratch_bytes(int units, int T, int d, int b);  // states + partials, bytes
+cudaError_t launch_linear_bwd(const LinearBwdParams& p, cudaStream_t stream);
 
 }  // namespace ttt

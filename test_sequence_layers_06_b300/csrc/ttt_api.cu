@@ -368,6 +368,50 @@ ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, t
                                                                                            : TTT_ERR_CUDA;
 }
 
+size_t ttt_linear_bwd_workspace_bytes(int B, int H, int T, int d, int b) {
+  if (!sizes_ok(B, H, T, d, b)) return 0;
+  return kStatusBytes + round_up(ttt::linear_bwd_scratch_bytes(B * H, T, d, b), 16);
+}
+
+ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                          const float* W0, int B, int H, int T, int d, int b, const void* dZ, const float* dW_out,
+                          void* dQ, void* dK, void* dV, float* deta, float* dW0, void* workspace, size_t ws_bytes,
+                          void* stream) {
+  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
+  if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
+  if (dt != TTT_F32 || !ttt::linear_bwd_supported(d, b)) return TTT_ERR_UNSUPPORTED;
+  if (!eta || !W0 || !dW_out || !deta || !dW0 || !workspace) return TTT_ERR_ARG;
+  if (T > 0 && (!Q || !K || !V || !dZ || !dQ || !dK || !dV)) return TTT_ERR_ARG;
+  for (const void* p : {Q, K, V, dZ, static_cast<const void*>(dQ), static_cast<const void*>(dK),
+                        static_cast<const void*>(dV), static_cast<const void*>(eta), static_cast<const void*>(W0),
+                        static_cast<const void*>(dW_out), static_cast<const void*>(deta),
+                        static_cast<const void*>(dW0), static_cast<const void*>(workspace)})
+    if (p && !aligned16(p)) return TTT_ERR_ARG;
+  if (ws_bytes < ttt_linear_bwd_workspace_bytes(B, H, T, d, b)) return TTT_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ttt::LinearBwdParams p;
+  p.Q = static_cast<const float*>(Q);
+  p.K = static_cast<const float*>(K);
+  p.V = static_cast<const float*>(V);
+  p.dZ = static_cast<const float*>(dZ);
+  p.eta = eta;
+  p.W0 = W0;
+  p.dW_out = dW_out;
+  p.dQ = static_cast<float*>(dQ);
+  p.dK = static_cast<float*>(dK);
+  p.dV = static_cast<float*>(dV);
+  p.deta = deta;
+  p.dW0 = dW0;
+  p.B = B; p.H = H; p.T = T; p.d = d; p.b = b;
+  p.units = B * H;
+  p.states = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+  const size_t nch = (static_cast<size_t>(T) + b - 1) / b;
+  p.partial = p.states + static_cast<size_t>(p.units) * nch * d * d;
+  const ttt_status st = reset_status(workspace, s);
+  if (st != TTT_OK) return st;
+  return ttt::launch_linear_bwd(p, s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
 ttt_status ttt_last_device_status(void* workspace, void* stream) {
   if (!workspace || !aligned16(workspace)) return TTT_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

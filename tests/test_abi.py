@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 11
+    assert len(names) == 13
     assert set(names) == set(ttt.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -131,6 +131,32 @@ def test_mlp_and_decode_reject_bad_arguments(lib):
                                     16, vp(4096), vp(0))
     assert st == ttt.TTT_ERR_ARG
     assert lib.ttt_last_device_status(vp(0), vp(0)) == ttt.TTT_ERR_ARG
+
+
+def _bwd(lib, **kw):
+    a = dict(Q=4096, K=4096, V=4096, dt=0, eta=4096, W0=4096, B=2, H=3, T=40, d=16, b=8, dZ=4096, dW=4096,
+             dQ=4096, dK=4096, dV=4096, deta=4096, dW0=4096, ws=4096, wsb=1 << 24, s=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.ttt_linear_bwd(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W0"]), a["B"],
+                              a["H"], a["T"], a["d"], a["b"], vp(a["dZ"]), vp(a["dW"]), vp(a["dQ"]), vp(a["dK"]),
+                              vp(a["dV"]), vp(a["deta"]), vp(a["dW0"]), vp(a["ws"]), a["wsb"], vp(a["s"]))
+
+
+def test_backward_workspace_bytes(lib):
+    """A status block, every chunk-start state and a per-unit partial of dW0 and d eta."""
+    assert ttt.ttt_linear_bwd_workspace_bytes(2, 3, 40, 16, 8) == 256 + 6 * 5 * 16 * 16 * 4 + 6 * (16 * 16 + 1) * 4 + 8
+    assert ttt.ttt_linear_bwd_workspace_bytes(1, 1, 0, 16, 8) == 256 + 1 * (16 * 16 + 1) * 4 + 12
+    assert ttt.ttt_linear_bwd_workspace_bytes(0, 1, 8, 16, 8) == 0
+
+
+@pytest.mark.parametrize("kw,want", [(dict(Q=0), ttt.TTT_ERR_ARG), (dict(dZ=0), ttt.TTT_ERR_ARG),
+                                     (dict(deta=0), ttt.TTT_ERR_ARG), (dict(dW0=4100), ttt.TTT_ERR_ARG),
+                                     (dict(wsb=4096), ttt.TTT_ERR_ARG), (dict(b=0), ttt.TTT_ERR_ARG),
+                                     (dict(dt=5), ttt.TTT_ERR_ARG), (dict(dt=1), ttt.TTT_ERR_UNSUPPORTED),
+                                     (dict(d=65), ttt.TTT_ERR_UNSUPPORTED), (dict(b=65), ttt.TTT_ERR_UNSUPPORTED)])
+def test_backward_rejects_bad_arguments(lib, kw, want):
+    assert _bwd(lib, **kw) == want
 
 
 def test_no_cpu_fallback_without_a_gpu(lib):
