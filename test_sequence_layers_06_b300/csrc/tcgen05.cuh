@@ -96,22 +96,8 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
 }
 
 // ---------------------------------------------------------------- TMEM <-> registers
-// Each thread of the warp reads 16 consecutive 32-bit columns of its own lane
-// (lane = the warp's lane quarter + laneid), and waits for the load.
-__device__ __forceinline__ void ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 consecutive columns in one load-and-wait.
+// Each thread of the warp reads 32 consecutive 32-bit columns of its own lane
+// (lane = the warp's lane quarter + laneid) in one load, and waits for it.
 __device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
   asm volatile(
@@ -152,21 +138,6 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
-}
-
-// ---------------------------------------------------------------- shared-memory layouts
-// Byte offset of element (row r, k) of a K-major bf16 operand whose rows are
-// 64 elements (128 bytes) in the 128-byte-swizzled canonical layout: 8-row
-// groups of 1024 bytes, 16-byte chunks XOR-ed with the row within the group.
-// (The layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B for 64-wide bf16 rows.)
-__device__ __forceinline__ uint32_t kmaj_sw128(int r, int k) {
-  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((((k >> 3) ^ (r & 7)) & 7) << 4) + (k & 7) * 2);
-}
-
-// Byte offset of element (row r, k) of a K-major bf16 operand with no swizzle:
-// 8 x 16-byte core matrices, `lbo` bytes apart along K, `sbo` bytes apart along rows.
-__device__ __forceinline__ uint32_t kmaj_none(int r, int k, int lbo, int sbo) {
-  return static_cast<uint32_t>((r >> 3) * sbo + (k >> 3) * lbo + (r & 7) * 16 + (k & 7) * 2);
 }
 
 }  // namespace tc
