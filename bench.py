@@ -242,6 +242,25 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time: every rank runs its own replica of the workload
+    (independent units, no collective on the data path), so the job takes as long
+    as its slowest rank. The process group's backend decides the device (NCCL: the
+    rank's GPU; gloo: the host)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job token·heads/s: all ranks' units over the slowest rank's step time."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def oracle_rate(w: synth.Workload, b: int, target_s: float):
     """The oracle (as it stands) on a bounded sample: every head of batch row 0, the first Ts tokens.
@@ -353,13 +372,9 @@ def bench_ours(args, world, rank, local):
     if ttt.ttt_last_device_status(ws, stream) != 0:
         raise RuntimeError("device status not OK after the timed region")
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.token_heads / (ms_per_step * 1e-3)
+    value = job_throughput(world, w.token_heads, ms_per_step)
 
     # roofline: every kernel's algorithmic bytes over its own mean event-timed duration
     hbm_gbs, _, peak_kind = measured_peaks()
@@ -422,14 +437,10 @@ def bench_ours(args, world, rank, local):
         bq.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a.elapsed_time(bq) / args.e2e_steps
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         h2d = hq.numel() * hq.element_size() * 3
         d2h = hz.numel() * hz.element_size() + hw.numel() * 4
-        e2e = {"value": world * w.token_heads / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": round(e2e_ms, 3),
+        e2e = {"value": job_throughput(world, w.token_heads, e2e_ms), "unit": UNIT, "ms_per_step": round(e2e_ms, 3),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     extras = {}
