@@ -1,0 +1,120 @@
+"""The algebra the fast kernels rely on, checked in fp64 on the host (no GPU).
+
+Each kernel restates the chunk rule ("5 · TestingTime 训练与长上下文", section 1.1:
+the gradients of a chunk are taken at its start weights) in a form that suits
+the hardware. These tests check each restatement against the rule applied
+chunk by chunk, on random inputs:
+  - segment affine maps on tcgen05: several chunks of one 64-token group fold
+    into one affine map, X_end = X0 + M X0 + [0 | Q], M = -eta Kh^T K,
+    Q = eta Kh^T V, with Kh = T^T K and T = (I + eta N)^-1 (N: the strictly
+    block-lower chunk blocks of K K^T);
+  - the read-out kernel walks a chunk in 16-token tiles: each tile's error uses
+    the chunk-start state, its read-out the running state;
+  - the combine: W_start(s+1) = A_s W_start(s) + B_s reproduces the scan.
+"""
+import numpy as np
+import pytest
+
+
+def chunk_rule(K, V, eta, W, b):
+    """State after the chunk rule over all of K, V (chunks of b tokens)."""
+    for c0 in range(0, len(K), b):
+        Kc, Vc = K[c0:c0 + b], V[c0:c0 + b]
+        W = W - eta * Kc.T @ (Kc @ W - Vc)
+    return W
+
+
+@pytest.mark.parametrize("b", [16, 32, 64])
+def test_group_of_chunks_is_one_affine_map(b):
+    """64 tokens = 64/b chunks: the kernel's map, built from K and V alone, equals
+    the chunk-by-chunk update of X = [A | B] from [I | 0] with value rows [0 | V]."""
+    g = np.random.default_rng(b)
+    d, n = 8, 64
+    K = g.standard_normal((n, d))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    V = g.standard_normal((n, d))
+    eta = 0.3
+    # chunk rule on the augmented state: the A half follows A <- A - eta K^T K A,
+    # the B half B <- B - eta K^T (K B - V)
+    X0 = np.hstack([np.eye(d), np.zeros((d, d))])
+    Y = np.hstack([np.zeros((n, d)), V])
+    X = X0.copy()
+    for c0 in range(0, n, b):
+        Kc, Yc = K[c0:c0 + b], Y[c0:c0 + b]
+        X = X - eta * Kc.T @ (Kc @ X - Yc)
+    # the kernel's form
+    G = K @ K.T
+    blk = np.arange(n) // b
+    N = np.where(blk[:, None] > blk[None, :], G, 0.0)  # strictly block-lower chunk blocks
+    T = np.linalg.inv(np.eye(n) + eta * N)
+    Kh = T.T @ K
+    M = -eta * Kh.T @ K
+    Q = eta * Kh.T @ V
+    X_kernel = X0 + M @ X0 + np.hstack([np.zeros((d, d)), Q])
+    assert np.allclose(X_kernel, X, atol=1e-12, rtol=0)
+    # the map also advances any other start state the same way
+    W = g.standard_normal((d, d))
+    assert np.allclose(W + M @ W + Q, chunk_rule(K, V, eta, W, b), atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("bt", [16, 32])
+def test_unit_lower_blocks_of_T_transposed(bt):
+    """The helper warps build T^T in 16-token blocks by U_cr = -eta sum_{c <= m < r} U_cm G_mr
+    (U_cc = I), where G_mr, the (m, r) block of K K^T, enters only if blocks m and r lie in
+    different chunks: that is the inverse of (I + eta N)^T."""
+    g = np.random.default_rng(7 + bt)
+    d = 8
+    K = g.standard_normal((64, d))
+    eta = 0.2
+    G = K @ K.T
+    blocks = 4
+    Gb = lambda m, r: G[16 * m:16 * m + 16, 16 * r:16 * r + 16] * ((16 * m) // bt < (16 * r) // bt)
+    U = {}
+    for c in range(blocks):
+        U[c, c] = np.eye(16)
+        for r in range(c + 1, blocks):
+            U[c, r] = -eta * sum(U[c, m] @ Gb(m, r) for m in range(c, r))
+    Tt = np.block([[U[c, r] if r >= c else np.zeros((16, 16)) for r in range(blocks)] for c in range(blocks)])
+    blk = np.arange(64) // bt
+    N = np.where(blk[:, None] > blk[None, :], G, 0.0)
+    assert np.allclose(Tt, np.linalg.inv(np.eye(64) + eta * N).T, atol=1e-12)
+
+
+@pytest.mark.parametrize("b", [32, 48, 64])
+def test_chunk_walked_in_16_token_tiles(b):
+    """Z of a chunk equals, tile by tile, Q_u W_run - eta tril(Q_u K_u^T) E_u, where
+    E_u = K_u W_a - V_u uses the chunk-start state W_a and W_run has taken the
+    gradients of the chunk's earlier tiles."""
+    g = np.random.default_rng(b)
+    d = 8
+    Q, K, V = (g.standard_normal((b, d)) for _ in range(3))
+    Wa = g.standard_normal((d, d)) * 0.3
+    eta = 0.25
+    E = K @ Wa - V
+    Z_dual = Q @ Wa - eta * np.tril(Q @ K.T) @ E  # the chunk rule in dual form
+    Wrun = Wa.copy()
+    Z_tiles = np.zeros_like(Z_dual)
+    for u0 in range(0, b, 16):
+        Qu, Ku, Eu = Q[u0:u0 + 16], K[u0:u0 + 16], E[u0:u0 + 16]
+        Z_tiles[u0:u0 + 16] = Qu @ Wrun - eta * np.tril(Qu @ Ku.T) @ Eu
+        Wrun = Wrun - eta * Ku.T @ Eu
+    assert np.allclose(Z_tiles, Z_dual, atol=1e-12)
+    assert np.allclose(Wrun, Wa - eta * K.T @ E, atol=1e-12)
+
+
+def test_segment_maps_combine_to_the_scan():
+    """The combine kernel's recurrence over the segment maps gives every segment's
+    start state of the chunk-by-chunk scan."""
+    g = np.random.default_rng(3)
+    d, b, L, S = 6, 4, 12, 5
+    K = g.standard_normal((L * S, d)) * 0.5
+    V = g.standard_normal((L * S, d))
+    eta = 0.3
+    W0 = g.standard_normal((d, d))
+    W = W0
+    for s in range(S - 1):
+        Ks, Vs = K[s * L:(s + 1) * L], V[s * L:(s + 1) * L]
+        A = chunk_rule(Ks, np.zeros_like(Vs), eta, np.eye(d), b)
+        B = chunk_rule(Ks, Vs, eta, np.zeros((d, d)), b)
+        W = A @ W + B
+        assert np.allclose(W, chunk_rule(K[:(s + 1) * L], V[:(s + 1) * L], eta, W0, b), atol=1e-12)
