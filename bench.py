@@ -532,7 +532,10 @@ def bench_extras(ttt, dev, stream):
         dW = torch.randn(w.B, w.H, w.d, w.d, device=dev)
         ws = torch.empty(ttt.ttt_linear_bwd_workspace_bytes(w.B, w.H, w.T, w.d, 16), dtype=torch.uint8, device=dev)
         ms = t_ms(lambda: ttt.ttt_linear_bwd(Q, K, V, eta, W0, 16, dZ, dW, workspace=ws, stream=stream), 3)
+        # algorithmic bytes: Q, K, V, dZ read and dQ, dK, dV written once (fp32), states aside
+        bwd_bytes = w.token_heads * 7 * w.d * 4
         out["linear_bwd_small_f32_b16"] = {"ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                                           "hbm_frac": round(bwd_bytes / (ms * 1e-3) / 1e9 / hbm_gbs, 5),
                                            "note": "B2 H4 T2048 d64 fp32; dQ, dK, dV, d eta, dW0 for given dZ, "
                                                    "dW_out; one CTA per (batch row, head)"}
         del Q, K, V, dZ
