@@ -118,3 +118,50 @@ def test_segment_maps_combine_to_the_scan():
         B = chunk_rule(Ks, Vs, eta, np.zeros((d, d)), b)
         W = A @ W + B
         assert np.allclose(W, chunk_rule(K[:(s + 1) * L], V[:(s + 1) * L], eta, W0, b), atol=1e-12)
+
+
+def test_backward_runs_segment_parallel_on_the_transposed_maps():
+    """The state gradient is affine too: with Z_c = P_c W_c + eta S_c V_c, P_c = Q_c - eta S_c K_c,
+    G_c = A_c^T G_{c+1} + P_c^T dZ_c from G = dW_out at the end. A segment's backward map is
+    therefore (A_s^T, H_s): the transpose of its forward map, and an additive term that depends
+    on the inputs and dZ only. Composed from the last segment back, these maps give the chunk-level
+    gradient at every segment start, and at the first one dW0 of the oracle's backward."""
+    from oracle.backward import linear_backward
+    g = np.random.default_rng(11)
+    d, b, L, S = 5, 4, 12, 4
+    T = L * S
+    Q, K, V, dZ = (g.standard_normal((T, d)) * 0.6 for _ in range(4))
+    W0, dW = g.standard_normal((d, d)) * 0.4, g.standard_normal((d, d))
+    eta = 0.3
+
+    def chunk_terms(c0):
+        Qc, Kc, dZc = Q[c0:c0 + b], K[c0:c0 + b], dZ[c0:c0 + b]
+        A = np.eye(d) - eta * Kc.T @ Kc
+        P = Qc - eta * np.tril(Qc @ Kc.T) @ Kc
+        return A, P.T @ dZc
+
+    # chunk level, last chunk first
+    G = dW.copy()
+    G_at = {}
+    for c0 in reversed(range(0, T, b)):
+        A, H = chunk_terms(c0)
+        G = A.T @ G + H
+        G_at[c0] = G
+    _, _, _, _, dW0 = linear_backward(Q[None, None], K[None, None], V[None, None], np.array([eta]), W0[None], b,
+                                      dZ[None, None], dW[None, None])
+    assert np.allclose(G_at[0], dW0[0], atol=1e-12)
+    # segment level: (A_s^T, H_s) per segment, each from its own chunks only
+    maps = []
+    for s in range(S):
+        As, Hs = np.eye(d), np.zeros((d, d))
+        for c0 in reversed(range(s * L, (s + 1) * L, b)):  # G_start = A_s^T G_end + H_s
+            A, H = chunk_terms(c0)
+            As, Hs = As @ A, A.T @ Hs + H
+        fwd = chunk_rule(K[s * L:(s + 1) * L], np.zeros((L, d)), eta, np.eye(d), b)  # the forward map's A_s
+        assert np.allclose(As, fwd, atol=1e-12)  # the backward map's matrix is the forward one, transposed
+        maps.append((As, Hs))
+    G = dW.copy()
+    for s in reversed(range(S)):
+        As, Hs = maps[s]
+        G = As.T @ G + Hs
+        assert np.allclose(G, G_at[s * L], atol=1e-12)
