@@ -56,7 +56,7 @@ extern "C" {
 typedef enum {
   TTT_OK = 0,
   TTT_ERR_ARG = -1,          /* bad pointer, size, alignment or workspace */
-  TTT_ERR_UNSUPPORTED = -2,  /* valid request this build does not serve (e.g. d > 64) */
+  TTT_ERR_UNSUPPORTED = -2,  /* a valid request the library does not serve (e.g. d > 64) */
   TTT_ERR_CUDA = -3,         /* a CUDA runtime call failed (launch, copy, no device) */
   TTT_ERR_TIMEOUT = -4,      /* a kernel's bounded wait ran out (reported via the workspace) */
   TTT_ERR_DEVICE_CHECK = -5  /* a kernel's own consistency check failed */
