@@ -20,18 +20,19 @@
 //   X^T += X^T M^T                     (M 128, N 64, K 64; A in tensor memory),
 // then the row threads add Q^T to the B rows of X^T (fp32) and round the new
 // X^T to bf16 (the next product's A operand). Everything else runs ahead of it:
-//   - two helper warps form Kh = T^T K with warp-level MMAs, in registers: the
-//     16 x 16 blocks of T^T by U_cr = -eta sum_m U_cm G_mr (G = K K^T blocks,
-//     U_cc = I), then Kh_c = K_c + sum_{r > c} U_cr K_r;
+//   - three helper warps form Kh = T^T K with warp-level MMAs, in registers, each
+//     for every third step: the 16 x 16 blocks of T^T by
+//     U_cr = -eta sum_m U_cm G_mr (G = K K^T blocks, U_cc = I), then
+//     Kh_c = K_c + sum_{r > c} U_cr K_r;
 //   - one M = 128 product [K^T; V^T] Kh = [-M^T / eta; Q^T / eta] per step, two
 //     groups ahead, into one of two tensor-memory buffers;
 //   - while the chain product of the previous group runs, the A-row threads
 //     round the top half to bf16 M^T (the chain's B operand, read MN-major: no
 //     transposition anywhere) and the B-row threads take their row of Q^T
 //     into registers (bf16 pairs, the rounding Q^T would get as an operand).
-// Products complete in issue order and a commit lands only once the products
-// issued after it are done too (measured), so the control lane waits for each
-// chain product before it issues prep products for later groups.
+// Products run in issue order, so the control lane issues a group's prep product
+// only after the previous chain product has landed: it then fills the pipe while
+// the rows refresh X^T, instead of delaying that chain product.
 //
 // Roles (256 threads): warps 0-3 own the 128 rows of X^T and of the prep
 // product; warp 4 lane 0 issues the TMA loads and the MMAs; warps 5-7 compute
