@@ -1,4 +1,4 @@
-"""The oracle's backward of the TTT-Linear scan, pinned (CPU only).
+"""The oracle's backward of the TTT-Linear and TTT-MLP scans, pinned (CPU only).
 
 linear_backward returns the vector-Jacobian product of (Z, W_out) with respect
 to (Q, K, V, eta, W0). It is checked against:
@@ -10,7 +10,9 @@ to (Q, K, V, eta, W0). It is checked against:
     in closed form.
 Every term of the backward feeds some entry of some gradient at random inputs,
 so a dropped term, a wrong sign or a transposed factor fails the finite
-differences by far more than their tolerance.
+differences by far more than their tolerance. mlp_backward is pinned the same
+way: finite differences of the C TTT-MLP forward on every input, and torch
+autograd (torch's own tanh-GELU and its derivatives) through a per-token loop.
 """
 import numpy as np
 import pytest
@@ -113,3 +115,84 @@ def test_backward_eta_zero_closed_form():
     assert np.array_equal(dK, np.zeros_like(dK)) and np.array_equal(dV, np.zeros_like(dV))
     want = np.einsum("nhti,nhtj->hij", Q, dZ) + dW.sum(0)
     assert np.allclose(dW0, want, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------- TTT-MLP
+from oracle.backward import mlp_backward  # noqa: E402
+
+
+def rand_mlp(B, H, T, d, m, seed):
+    g = np.random.default_rng(seed)
+    Q, K, V = (g.standard_normal((B, H, T, d)) * 0.7 for _ in range(3))
+    eta = g.uniform(0.05, 0.4, H)
+    W1 = g.standard_normal((H, d, m)) * 0.4
+    W2 = g.standard_normal((H, m, d)) * 0.4
+    dZ = g.standard_normal((B, H, T, d))
+    dW1 = g.standard_normal((B, H, d, m))
+    dW2 = g.standard_normal((B, H, m, d))
+    return Q, K, V, eta, W1, W2, dZ, dW1, dW2
+
+
+def mlp_loss(Q, K, V, eta, W1, W2, b, dZ, dW1, dW2):
+    Z, A1, A2 = oracle.mlp_primal(Q, K, V, eta, W1, W2, b)
+    return float(np.sum(Z * dZ) + np.sum(A1 * dW1) + np.sum(A2 * dW2))
+
+
+@pytest.mark.parametrize("B,H,T,d,m,b", [(1, 1, 6, 2, 5, 1), (1, 1, 6, 2, 5, 3), (1, 1, 6, 2, 5, 6),
+                                         (2, 1, 5, 2, 3, 2)])
+def test_mlp_backward_equals_finite_differences(B, H, T, d, m, b):
+    args = rand_mlp(B, H, T, d, m, seed=T + b + m)
+    Q, K, V, eta, W1, W2, dZ, dW1, dW2 = args
+    got = mlp_backward(Q, K, V, eta, W1, W2, b, dZ, dW1, dW2)
+    inputs = [Q, K, V, eta, W1, W2]
+    for idx, (name, g) in enumerate(zip(("dQ", "dK", "dV", "deta", "dW1", "dW2"), got)):
+        def f(x, idx=idx):
+            xs = list(inputs)
+            xs[idx] = x
+            return mlp_loss(*xs, b, dZ, dW1, dW2)
+        want = fd(f, inputs[idx])
+        assert rel(g, want) < 1e-6, (name, rel(g, want))
+
+
+def mlp_primal_torch(Q, K, V, eta, W1, W2, b):
+    """Per-token TTT-MLP in torch fp64 with torch's own tanh-GELU: gradients at the
+    chunk-start weights, read-out with the updated weights."""
+    gelu = lambda x: torch.nn.functional.gelu(x, approximate="tanh")
+    B, H, T, d = Q.shape
+    Zs, W1s, W2s = [], [], []
+    for n in range(B):
+        zr, w1r, w2r = [], [], []
+        for h in range(H):
+            P1, P2 = W1[h], W2[h]
+            zs = []
+            for t in range(T):
+                if t % b == 0:
+                    A1, A2 = P1, P2
+                u = K[n, h, t] @ A1
+                a = gelu(u)
+                gr = a @ A2 - V[n, h, t]
+                # s'(u) by autograd, kept differentiable so that the outer gradient sees s''
+                sprime = torch.autograd.functional.jacobian(gelu, u, create_graph=True).diagonal()
+                dl = (gr @ A2.T) * sprime
+                P1 = P1 - eta[h] * torch.outer(K[n, h, t], dl)
+                P2 = P2 - eta[h] * torch.outer(a, gr)
+                zs.append(gelu(Q[n, h, t] @ P1) @ P2)
+            zr.append(torch.stack(zs))
+            w1r.append(P1)
+            w2r.append(P2)
+        Zs.append(torch.stack(zr))
+        W1s.append(torch.stack(w1r))
+        W2s.append(torch.stack(w2r))
+    return torch.stack(Zs), torch.stack(W1s), torch.stack(W2s)
+
+
+def test_mlp_backward_equals_autograd():
+    args = rand_mlp(1, 2, 5, 3, 4, seed=21)
+    Q, K, V, eta, W1, W2, dZ, dW1, dW2 = args
+    ts = [torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (Q, K, V, eta, W1, W2)]
+    Z, A1, A2 = mlp_primal_torch(*ts, 2)
+    L = (Z * torch.tensor(dZ)).sum() + (A1 * torch.tensor(dW1)).sum() + (A2 * torch.tensor(dW2)).sum()
+    grads = torch.autograd.grad(L, ts)
+    mine = mlp_backward(Q, K, V, eta, W1, W2, 2, dZ, dW1, dW2)
+    for name, got, want in zip(("dQ", "dK", "dV", "deta", "dW1", "dW2"), mine, grads):
+        assert rel(got, want.detach().numpy()) < 1e-10, (name, rel(got, want.detach().numpy()))
