@@ -501,13 +501,11 @@ cudaError_t launch_linear_seg_affine_wy(const LinearParams& p, const CUtensorMap
                                         cudaStream_t stream) {
   const int items = p.units * (p.seg_count - 1);
   if (items == 0) return cudaSuccess;
-  static bool attr_set = false;  // idempotent; a race only repeats the call
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(linear_seg_affine_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // The attribute belongs to the current device: set it on every launch, as the
+  // other large-shared-memory launchers do (a process may drive several GPUs).
+  const cudaError_t e =
+      cudaFuncSetAttribute(linear_seg_affine_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
   linear_seg_affine_wy_kernel<<<items, kThreads, kSmemBytes, stream>>>(mk64, mv64, p);
   return cudaGetLastError();
 }
