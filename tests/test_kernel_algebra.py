@@ -165,3 +165,36 @@ def test_backward_runs_segment_parallel_on_the_transposed_maps():
         As, Hs = maps[s]
         G = As.T @ G + Hs
         assert np.allclose(G, G_at[s * L], atol=1e-12)
+
+
+@pytest.mark.parametrize("b", [1, 3, 8])
+def test_bias_is_an_extra_constant_input(b):
+    """TTT-Linear with a bias, f(k) = k W + beta, trained like W (the same chunk rule on the
+    loss 1/2 ||k W + beta - v||^2, read-out q W_t + beta_t), equals plain TTT-Linear on keys
+    and queries extended by a constant 1, with state [W; beta^T]. The state stays square by
+    one more output column (target 0, start 0); the output columns learn independently, so
+    that column never touches the others. So the library serves the bias variant for d <= 63
+    with no new kernel."""
+    import oracle
+    g = np.random.default_rng(b)
+    T, d = 11, 4
+    Q, K, V = (g.standard_normal((T, d)) for _ in range(3))
+    W0, beta0 = g.standard_normal((d, d)) * 0.3, g.standard_normal(d) * 0.3
+    eta = 0.2
+    # the bias variant, token by token: gradients at the chunk-start (W, beta), then read-out
+    W, beta = W0.copy(), beta0.copy()
+    Z = np.zeros((T, d))
+    for t in range(T):
+        if t % b == 0:
+            Wa, ba = W.copy(), beta.copy()
+        e = K[t] @ Wa + ba - V[t]
+        W = W - eta * np.outer(K[t], e)
+        beta = beta - eta * e
+        Z[t] = Q[t] @ W + beta
+    one, zero = np.ones((T, 1)), np.zeros((T, 1))
+    W0x = np.zeros((d + 1, d + 1))
+    W0x[:d, :d], W0x[d, :d] = W0, beta0
+    Zx, Wx = oracle.linear_primal(np.hstack([Q, one])[None, None], np.hstack([K, one])[None, None],
+                                  np.hstack([V, zero])[None, None], np.array([eta]), W0x[None], b)
+    assert np.allclose(Zx[0, 0, :, :d], Z, atol=1e-12)
+    assert np.allclose(Wx[0, 0, :, :d], np.vstack([W, beta]), atol=1e-12)
