@@ -227,9 +227,10 @@ TTT_API ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, t
                                   void* stream);
 
 /* Waits for `stream`, then reads and clears the status word of `workspace`.
- * Every *_fwd call clears that word when it is enqueued, so this reports the
- * kernels of the latest *_fwd call that used this workspace: TTT_OK, or the
- * first error one of them recorded (TTT_ERR_TIMEOUT, TTT_ERR_DEVICE_CHECK). */
+ * Every call that takes a workspace (the *_fwd calls and ttt_linear_bwd)
+ * clears that word when it is enqueued, so this reports the kernels of the
+ * latest such call that used this workspace: TTT_OK, or the first error one
+ * of them recorded (TTT_ERR_TIMEOUT, TTT_ERR_DEVICE_CHECK). */
 TTT_API ttt_status ttt_last_device_status(void* workspace, void* stream);
 
 /* Static description of a status code. */
