@@ -10,7 +10,13 @@ chunk by chunk, on random inputs:
     block-lower chunk blocks of K K^T);
   - the read-out kernel walks a chunk in 16-token tiles: each tile's error uses
     the chunk-start state, its read-out the running state;
-  - the combine: W_start(s+1) = A_s W_start(s) + B_s reproduces the scan.
+  - the combine: W_start(s+1) = A_s W_start(s) + B_s reproduces the scan;
+  - the backward's segment-parallel form (transposed maps);
+  - two restatements for faster kernels: Kh by a finite (nilpotent) series in
+    Horner form, and a read-out that takes a 64-token group of chunks at once;
+  - two inner-model variants that reduce to plain TTT-Linear on changed inputs:
+    a bias in f (a constant extra input) and a per-token learning rate
+    (keys and values scaled by its square root).
 """
 import numpy as np
 import pytest
@@ -198,3 +204,80 @@ def test_bias_is_an_extra_constant_input(b):
                                   np.hstack([V, zero])[None, None], np.array([eta]), W0x[None], b)
     assert np.allclose(Zx[0, 0, :, :d], Z, atol=1e-12)
     assert np.allclose(Wx[0, 0, :, :d], np.vstack([W, beta]), atol=1e-12)
+
+
+@pytest.mark.parametrize("b", [16, 32, 64])
+def test_khat_by_a_nilpotent_series(b):
+    """T = (I + eta N)^-1 needs no inversion: N is strictly block-lower with 64/b chunk blocks, so
+    (eta N)^(64/b) = 0 and T is the finite series sum_p (-eta N)^p. Applied to K in Horner form,
+    Kh = T^T K = K - eta N^T (K - eta N^T (K - eta N^T K)) for four chunks: 64/b - 1 dependent
+    products of the same 64 x 64 by 64 x d shape, a form for tensor cores in place of the block
+    recursion of the helper warps."""
+    g = np.random.default_rng(40 + b)
+    d, n, eta = 8, 64, 0.35
+    K = g.standard_normal((n, d))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    blk = np.arange(n) // b
+    N = np.where(blk[:, None] > blk[None, :], K @ K.T, 0.0)
+    depth = n // b
+    assert np.allclose(np.linalg.matrix_power(eta * N, depth), 0.0, atol=0)
+    Kh = K.copy()
+    for _ in range(depth - 1):
+        Kh = K - eta * N.T @ Kh
+    assert np.allclose(Kh, np.linalg.inv(np.eye(n) + eta * N).T @ K, atol=1e-12)
+
+
+@pytest.mark.parametrize("b", [16, 32])
+def test_readout_of_a_64_token_group(b):
+    """A read-out can take a 64-token group of several chunks in one pass. With P = K W0 - V the
+    errors at the chunk starts follow E_c = P_c - eta sum_{c' < c} (K_c K_c'^T) E_c' (a short
+    recursion over the group's chunks, or E = T P); then Z = Q W0 - eta tril(Q K^T) E over the whole
+    group (the earlier chunks' blocks are full, the chunk's own is lower-triangular, so the mask is
+    plain causal) and W_end = W0 - eta K^T E. This equals the chunk rule chunk by chunk, with one
+    state update per group instead of one per chunk."""
+    g = np.random.default_rng(50 + b)
+    d, n, eta = 8, 64, 0.3
+    Q, K, V = (g.standard_normal((n, d)) for _ in range(3))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    W0 = g.standard_normal((d, d)) * 0.3
+    # the chunk rule in dual form, chunk by chunk
+    W, Zc = W0.copy(), np.zeros((n, d))
+    for c0 in range(0, n, b):
+        Qc, Kc, Vc = Q[c0:c0 + b], K[c0:c0 + b], V[c0:c0 + b]
+        E = Kc @ W - Vc
+        Zc[c0:c0 + b] = Qc @ W - eta * np.tril(Qc @ Kc.T) @ E
+        W = W - eta * Kc.T @ E
+    # the group form
+    P = K @ W0 - V
+    E = np.zeros_like(P)
+    for c0 in range(0, n, b):
+        E[c0:c0 + b] = P[c0:c0 + b] - eta * (K[c0:c0 + b] @ K[:c0].T) @ E[:c0]
+    blk = np.arange(n) // b
+    N = np.where(blk[:, None] > blk[None, :], K @ K.T, 0.0)
+    assert np.allclose(E, np.linalg.solve(np.eye(n) + eta * N, P), atol=1e-12)
+    assert np.allclose(Q @ W0 - eta * np.tril(Q @ K.T) @ E, Zc, atol=1e-12)
+    assert np.allclose(W0 - eta * K.T @ E, W, atol=1e-12)
+
+
+def test_per_token_learning_rate_is_a_scaling_of_keys_and_values():
+    """A per-token inner learning rate eta_t >= 0 (gradient of token t scaled by eta_t) equals plain
+    TTT-Linear with eta = 1 on keys and values scaled by sqrt(eta_t), queries unchanged: the error
+    becomes sqrt(eta_t) e_t, so each outer product k^T e and each read-out weight (q . k_i) e_i picks
+    up eta_t exactly once. So the library serves it for any d and b with no new kernel."""
+    import oracle
+    g = np.random.default_rng(9)
+    T, d, b = 13, 4, 4
+    Q, K, V = (g.standard_normal((T, d)) for _ in range(3))
+    et = g.uniform(0.0, 0.5, T)
+    W0 = g.standard_normal((d, d)) * 0.3
+    W, Z = W0.copy(), np.zeros((T, d))
+    for t in range(T):
+        if t % b == 0:
+            Wa = W.copy()
+        W = W - et[t] * np.outer(K[t], K[t] @ Wa - V[t])
+        Z[t] = Q[t] @ W
+    r = np.sqrt(et)[:, None]
+    Zs, Ws = oracle.linear_primal(Q[None, None], (r * K)[None, None], (r * V)[None, None], np.array([1.0]),
+                                  W0[None], b)
+    assert np.allclose(Zs[0, 0], Z, atol=1e-12)
+    assert np.allclose(Ws[0, 0], W, atol=1e-12)
