@@ -94,6 +94,9 @@ ttt_status plan_linear(int B, int H, int T, int d, int b, bool bf16, const ttt_o
       if (len < min_len) len = min_len;
     }
     const long long count = (T + len - 1) / len;
+    // Grids of one read-out CTA per (unit, segment) and 8 combine CTAs per unit
+    // must fit a 32-bit signed count.
+    if (static_cast<long long>(units) * std::max(count, 8LL) > 2147483647LL) return TTT_ERR_UNSUPPORTED;
     if (count >= 2) {
       pl.seg_len = static_cast<int>(len);
       pl.seg_count = static_cast<int>(count);

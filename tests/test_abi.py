@@ -119,6 +119,19 @@ def test_segment_options_are_checked(lib):
     assert call(ttt.ttt_options(0, 0, ttt.PATH_SEGMENTED, 0), b=8) == ttt.TTT_ERR_UNSUPPORTED
 
 
+def test_segment_grid_must_fit_a_launch(lib):
+    """One read-out CTA per (unit, segment) and 8 combine CTAs per unit: a forced segment length
+    whose grids would need 2^31 or more CTAs is refused before anything is enqueued."""
+    plan = ttt.ttt_plan()
+    o = ttt.ttt_options(0, 0, ttt.PATH_SEGMENTED, 16)
+    assert lib.ttt_linear_plan(65536, 1024, 1024, 64, 16, 1, ctypes.byref(o), ctypes.byref(plan)) == \
+        ttt.TTT_ERR_UNSUPPORTED  # 2^26 units x 64 segments
+    assert lib.ttt_linear_plan(65536, 512, 1024, 64, 16, 1, ctypes.byref(o), ctypes.byref(plan)) == \
+        ttt.TTT_ERR_UNSUPPORTED  # exactly 2^31
+    assert lib.ttt_linear_plan(65536, 511, 1024, 64, 16, 1, ctypes.byref(o), ctypes.byref(plan)) == ttt.TTT_OK
+    assert (plan.path, plan.seg_len, plan.seg_count) == (3, 16, 64)  # 2^31 - 2^22 CTAs: still fits
+
+
 def test_mlp_and_decode_reject_bad_arguments(lib):
     vp = ctypes.c_void_p
     st = lib.ttt_mlp_fwd(vp(4096), vp(4096), vp(4096), 1, vp(4096), vp(4096), vp(4096), 1, 1, 16, 64, 16,
