@@ -13,6 +13,8 @@ each segment of chunks (the segment-parallel form), plus one decode token with
 an (anchor, running) weight pair. ``oracle.backward.linear_backward`` (numpy,
 fp64, small cases) is the backward of the TTT-Linear scan: dQ, dK, dV, deta and
 dW0 for upstream dZ and dW_out, pinned in tests/test_oracle_backward.py.
+``oracle.variants`` (numpy, fp64) holds TTT-Linear with a layer norm and a
+residual inside the inner model, pinned in tests/test_oracle_variants.py.
 
 Parity pins live in tests/test_oracle_pins.py (b = 1 delta rule; causal linear
 attention; finite differences and autograd; eta = 0; chaining; b = T closed

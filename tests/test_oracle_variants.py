@@ -1,0 +1,136 @@
+"""The oracle of TTT-Linear with a layer norm and a residual inside f, pinned (CPU only).
+
+oracle/variants.py reads the normalised inner model as f(k; W) = k + LN(k W) and
+trains it with the chunk rule. Its hand-written gradient is checked against
+central finite differences of the loss and against torch autograd through
+torch's own layer_norm; the token-by-token form against the chunk-by-chunk dual
+form; eta = 0 (no update) and gamma = 0 (f no longer depends on W) against their
+closed forms. A dropped mean in the normalisation's chain rule, a missing
+residual or a gradient taken at the running weights each fail one of these.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.variants import LN_EPS, layer_norm, ln_residual_dual, ln_residual_error, ln_residual_primal
+
+
+def rand_case(B, H, T, d, seed):
+    g = np.random.default_rng(seed)
+    Q, K, V = (g.standard_normal((B, H, T, d)) * 0.8 for _ in range(3))
+    eta = g.uniform(0.05, 0.4, H)
+    W0 = g.standard_normal((H, d, d)) * 0.4
+    gamma = 1.0 + 0.3 * g.standard_normal((H, d))
+    beta = 0.2 * g.standard_normal((H, d))
+    return Q, K, V, eta, W0, gamma, beta
+
+
+def loss(k, v, W, gamma, beta):
+    return 0.5 * np.sum((k + layer_norm(k @ W, gamma, beta)[0] - v) ** 2)
+
+
+@pytest.mark.parametrize("d", [2, 3, 8])
+def test_gradient_equals_finite_differences(d):
+    g = np.random.default_rng(d)
+    k, v = g.standard_normal(d), g.standard_normal(d)
+    W = g.standard_normal((d, d)) * 0.5
+    gamma, beta = 1.0 + 0.3 * g.standard_normal(d), 0.2 * g.standard_normal(d)
+    grad = np.outer(k, ln_residual_error(k[None], v[None], W, gamma, beta)[0])
+    h = 1e-6
+    fd = np.zeros_like(W)
+    for i in range(d):
+        for j in range(d):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[i, j] += h
+            Wm[i, j] -= h
+            fd[i, j] = (loss(k, v, Wp, gamma, beta) - loss(k, v, Wm, gamma, beta)) / (2 * h)
+    assert np.allclose(grad, fd, atol=1e-7, rtol=1e-6)
+
+
+def test_gradient_equals_torch_autograd():
+    g = np.random.default_rng(1)
+    n, d = 5, 6
+    k, v = g.standard_normal((n, d)), g.standard_normal((n, d))
+    W = g.standard_normal((d, d)) * 0.5
+    gamma, beta = 1.0 + 0.3 * g.standard_normal(d), 0.2 * g.standard_normal(d)
+    Wt = torch.tensor(W, requires_grad=True)
+    kt, vt = torch.tensor(k), torch.tensor(v)
+    for t in range(n):  # one token's loss at a time: its gradient is k_t^T e_t
+        out = kt[t] + torch.nn.functional.layer_norm(kt[t] @ Wt, (d,), torch.tensor(gamma), torch.tensor(beta),
+                                                     eps=LN_EPS)
+        (gW,) = torch.autograd.grad(0.5 * ((out - vt[t]) ** 2).sum(), Wt)
+        e = ln_residual_error(k[t][None], v[t][None], W, gamma, beta)[0]
+        assert np.allclose(np.outer(k[t], e), gW.numpy(), atol=1e-12, rtol=1e-10)
+
+
+def test_layer_norm_equals_torch():
+    g = np.random.default_rng(2)
+    y = g.standard_normal((7, 5)) * 3 + 1
+    gamma, beta = g.standard_normal(5), g.standard_normal(5)
+    want = torch.nn.functional.layer_norm(torch.tensor(y), (5,), torch.tensor(gamma), torch.tensor(beta), eps=LN_EPS)
+    assert np.allclose(layer_norm(y, gamma, beta)[0], want.numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("T,b", [(9, 1), (9, 4), (12, 12), (10, 3)])
+def test_primal_equals_dual(T, b):
+    args = rand_case(2, 2, T, 4, seed=T + b)
+    Zp, Wp = ln_residual_primal(*args, b)
+    Zd, Wd = ln_residual_dual(*args, b)
+    assert np.allclose(Zp, Zd, atol=1e-12) and np.allclose(Wp, Wd, atol=1e-12)
+
+
+def test_primal_equals_torch_loop():
+    """Per-token loop in torch fp64 with torch's layer_norm and autograd for every gradient."""
+    Q, K, V, eta, W0, gamma, beta = rand_case(1, 1, 8, 3, seed=4)
+    b = 3
+    Z, Wo = ln_residual_primal(Q, K, V, eta, W0, gamma, beta, b)
+    gm, bt = torch.tensor(gamma[0]), torch.tensor(beta[0])
+    f = lambda x, W: x + torch.nn.functional.layer_norm(x @ W, (3,), gm, bt, eps=LN_EPS)
+    W = torch.tensor(W0[0])
+    for t in range(8):
+        if t % b == 0:
+            Wa = W.clone().requires_grad_(True)
+        k, v, q = (torch.tensor(a[0, 0, t]) for a in (K, V, Q))
+        (gW,) = torch.autograd.grad(0.5 * ((f(k, Wa) - v) ** 2).sum(), Wa)
+        W = W - eta[0] * gW
+        assert np.allclose(f(q, W).detach().numpy(), Z[0, 0, t], atol=1e-12)
+    assert np.allclose(W.detach().numpy(), Wo[0, 0], atol=1e-12)
+
+
+def test_eta_zero_is_the_normalised_forward():
+    Q, K, V, _, W0, gamma, beta = rand_case(2, 2, 7, 4, seed=5)
+    Z, Wo = ln_residual_primal(Q, K, V, np.zeros(2), W0, gamma, beta, 3)
+    for h in range(2):
+        assert np.allclose(Z[:, h], Q[:, h] + layer_norm(Q[:, h] @ W0[h], gamma[h], beta[h])[0], atol=1e-13)
+        assert np.array_equal(Wo[:, h], np.broadcast_to(W0[h], Wo[:, h].shape))
+
+
+def test_gamma_zero_leaves_w_untouched():
+    """With gamma = 0, f(k) = k + beta does not depend on W: no gradient, and z = q + beta."""
+    Q, K, V, eta, W0, _, beta = rand_case(1, 2, 6, 4, seed=6)
+    Z, Wo = ln_residual_primal(Q, K, V, eta, W0, np.zeros((2, 4)), beta, 2)
+    assert np.array_equal(Wo[0], W0)
+    assert np.allclose(Z, Q + beta[None, :, None, :], atol=1e-15)
+
+
+def test_planted_mistakes_are_caught():
+    """Variants of the error with one plausible slip each must disagree with torch autograd."""
+    g = np.random.default_rng(8)
+    d = 5
+    k, v = g.standard_normal(d), g.standard_normal(d)
+    W = g.standard_normal((d, d)) * 0.5
+    gamma, beta = 1.0 + 0.3 * g.standard_normal(d), 0.2 * g.standard_normal(d)
+    Wt = torch.tensor(W, requires_grad=True)
+    out = torch.tensor(k) + torch.nn.functional.layer_norm(torch.tensor(k) @ Wt, (d,), torch.tensor(gamma),
+                                                           torch.tensor(beta), eps=LN_EPS)
+    (gW,) = torch.autograd.grad(0.5 * ((out - torch.tensor(v)) ** 2).sum(), Wt)
+    o, x, s = layer_norm(k @ W, gamma, beta)
+    r = k + o - v
+    slips = {
+        "no mean of g": (gamma * r - x * (gamma * r * x).mean()) / s,
+        "no x term": (gamma * r - (gamma * r).mean()) / s,
+        "no residual": (gamma * (o - v) - (gamma * (o - v)).mean() - x * (gamma * (o - v) * x).mean()) / s,
+        "no gamma": (r - r.mean() - x * (r * x).mean()) / s,
+    }
+    for name, e in slips.items():
+        assert not np.allclose(np.outer(k, e), gW.numpy(), atol=1e-6), name
