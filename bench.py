@@ -45,6 +45,7 @@ METRIC = "TTT-Linear scan tokens·heads/sec and % of binding roofline (1×B300)"
 UNIT = "token·heads/s"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
+NOMINAL_HBM_GBS = 7700.0  # B300 HBM3e, vendor figure: context beside the measured copy bandwidth
 # kernel -> (source files whose digest a committed ncu summary must match, summary file)
 KERNEL_PROFILES = {
     "linear_mma_kernel": (("test_sequence_layers_06_b300/csrc/linear_mma.cu",), "profiles/linear_mma_long_b16.md"),
@@ -136,6 +137,32 @@ def profiled_traffic(kernel: str, workload: str):
         return int(float(vals["traffic_bytes_per_launch"]))
     except (KeyError, ValueError):
         return None
+
+
+def roofline_summary(names, kernel_ms, kbytes, ms_per_step: float, step_bytes: int, hbm_gbs: float,
+                     peak_kind: str, traffic_of) -> dict:
+    """The JSON line's roofline block: for each kernel with algorithmic bytes, those bytes over its
+    mean event-timed duration against the HBM peak; the dominant (longest) kernel at the top level;
+    the whole step's fraction; and each fraction also against the nominal HBM bandwidth."""
+    kernels = {}
+    for name, ms, nbytes in zip(names, kernel_ms, kbytes):
+        if nbytes == 0:
+            continue
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        kernels[name] = {"ms": round(ms, 4), "share": round(ms / ms_per_step, 4), "algorithmic_bytes": nbytes,
+                         "achieved_gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 4),
+                         "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4), "traffic": traffic_of(name)}
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    step_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": hbm_gbs,
+            "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": kernels[dom]["traffic"],
+            "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.4 TB/s",
+            "frac_of_nominal": kernels[dom]["frac_of_nominal"], "nominal_gbs": NOMINAL_HBM_GBS,
+            "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes"], "kernel_ms": kernels[dom]["ms"],
+            "kernels": kernels,
+            "step": {"algorithmic_bytes": step_bytes, "ms": round(ms_per_step, 4),
+                     "frac": round(step_gbs / hbm_gbs, 4), "frac_of_nominal": round(step_gbs / NOMINAL_HBM_GBS, 4)}}
 
 
 class ClockSampler:
@@ -379,29 +406,12 @@ def bench_ours(args, world, rank, local):
     # roofline: every kernel's algorithmic bytes over its own mean event-timed duration
     hbm_gbs, _, peak_kind = measured_peaks()
     kernel_ms = [float(np.mean([p[k] for p in per])) for k in range(3)]
-    kbytes = kernel_bytes(w, plan)
     names = ("linear_seg_affine_wy_kernel" if plan["affine"] == 2 else "linear_seg_affine_kernel",
              "linear_seg_combine_kernel", "linear_mma_kernel")
-    kernels = {}
     profile_key = f"{w.name} B{w.B} H{w.H} T{w.T} b{args.b}"
-    for k, name in enumerate(names):
-        if kbytes[k] == 0:
-            continue
-        gbs = kbytes[k] / (kernel_ms[k] * 1e-3) / 1e9
-        kernels[name] = {"ms": round(kernel_ms[k], 4), "share": round(kernel_ms[k] / ms_per_step, 4),
-                         "algorithmic_bytes": kbytes[k], "achieved_gbs": round(gbs, 1),
-                         "frac": round(gbs / hbm_gbs, 4), "traffic": profiled_traffic(name, profile_key)}
-    dom = max(kernels, key=lambda n: kernels[n]["ms"])
-    alg_bytes = algorithmic_bytes(w)
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["achieved_gbs"], "peak": hbm_gbs,
-                "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": kernels[dom]["traffic"],
-                "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS hbm_gbs)" if peak_kind == "measured"
-                else "fallback 6.4 TB/s",
-                "algorithmic_bytes_per_launch": kernels[dom]["algorithmic_bytes"], "kernel_ms": kernels[dom]["ms"],
-                "kernels": kernels,
-                "step": {"algorithmic_bytes": alg_bytes, "ms": round(ms_per_step, 4),
-                         "frac": round(alg_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_gbs, 4)},
-                "flops_per_step": algorithmic_flops(w, args.b)}
+    roofline = roofline_summary(names, kernel_ms, kernel_bytes(w, plan), ms_per_step, algorithmic_bytes(w),
+                                hbm_gbs, peak_kind, lambda name: profiled_traffic(name, profile_key))
+    roofline["flops_per_step"] = algorithmic_flops(w, args.b)
 
     # end to end: pinned host buffers in, Z and W_out back out, through the public call
     e2e = None

@@ -75,3 +75,22 @@ def test_roofline_bytes_and_profile_lookup():
         alg = readout if kernel == "linear_mma_kernel" else affine
         assert traffic is None or 0.95 * alg < traffic < 1.02 * alg, (kernel, traffic, alg)
         assert bench.profiled_traffic(kernel, "linear_long B1 H32 T65536 b16") is None
+
+
+def test_roofline_block_reproduces_a_measured_line():
+    """bench.py's roofline block from one B300 run's per-kernel event times (long-context workload,
+    b16): the same numbers that run printed, plus the fractions of the nominal 7.7 TB/s."""
+    bench = _bench()
+    names = ("linear_seg_affine_wy_kernel", "linear_seg_combine_kernel", "linear_mma_kernel")
+    r = bench.roofline_summary(names, [0.3671, 0.0376, 0.4853], [1063256064, 41418752, 2162163712], 0.8929,
+                               2148532224, 6514.2, "measured", lambda name: None)
+    assert r["kernel"] == "linear_mma_kernel" and r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert (r["achieved"], r["frac"], r["peak"]) == (4455.3, 0.6839, 6514.2)
+    assert r["kernels"]["linear_seg_affine_wy_kernel"]["frac"] == 0.4446
+    assert r["kernels"]["linear_seg_combine_kernel"]["share"] == 0.0421
+    assert r["step"]["frac"] == 0.3694
+    assert r["frac_of_nominal"] == round(4455.3 / 7700.0, 4) and r["step"]["frac_of_nominal"] == 0.3125
+    one_pass = bench.roofline_summary(names, [0.0, 0.0, 3.77], [0, 0, 2162163712], 3.77, 2148532224, 6514.2,
+                                      "fallback", lambda name: 7)
+    assert list(one_pass["kernels"]) == ["linear_mma_kernel"] and one_pass["traffic"] == 7
+    assert one_pass["peak_kind"] == "fallback 6.4 TB/s"
