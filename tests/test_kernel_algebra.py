@@ -281,3 +281,35 @@ def test_per_token_learning_rate_is_a_scaling_of_keys_and_values():
                                   W0[None], b)
     assert np.allclose(Zs[0, 0], Z, atol=1e-12)
     assert np.allclose(Ws[0, 0], W, atol=1e-12)
+
+
+def test_group_maps_compose_in_any_association():
+    """The chain X <- X + M_g X + [0 | Q_g] over a segment's groups is a product of affine maps, so
+    composing them pairwise first, [I+M2 | Q2] o [I+M1 | Q1] = [(I+M2)(I+M1) | (I+M2) Q1 + Q2], and then
+    chaining the pairs gives the same segment map as the group-by-group chain."""
+    g = np.random.default_rng(21)
+    d, n, b, eta, groups = 6, 16, 4, 0.3, 8
+    K = g.standard_normal((groups * n, d))
+    K /= np.linalg.norm(K, axis=1, keepdims=True)
+    V = g.standard_normal((groups * n, d))
+    maps = []
+    for gi in range(groups):  # each group's map from the chunk rule alone
+        Kg, Vg = K[gi * n:(gi + 1) * n], V[gi * n:(gi + 1) * n]
+        A = chunk_rule(Kg, np.zeros_like(Vg), eta, np.eye(d), b)
+        maps.append((A - np.eye(d), chunk_rule(Kg, Vg, eta, np.zeros((d, d)), b)))
+    X = np.hstack([np.eye(d), np.zeros((d, d))])
+    for M, Q in maps:  # the chain, group by group
+        X = X + M @ X + np.hstack([np.zeros((d, d)), Q])
+
+    def compose(second, first):
+        (M2, Q2), (M1, Q1) = second, first
+        return M1 + M2 + M2 @ M1, Q1 + Q2 + M2 @ Q1
+
+    pairs = [compose(maps[i + 1], maps[i]) for i in range(0, groups, 2)]
+    quads = [compose(pairs[i + 1], pairs[i]) for i in range(0, len(pairs), 2)]
+    Y = np.hstack([np.eye(d), np.zeros((d, d))])
+    for M, Q in quads:
+        Y = Y + M @ Y + np.hstack([np.zeros((d, d)), Q])
+    assert np.allclose(Y, X, atol=1e-12)
+    assert np.allclose(X[:, :d], chunk_rule(K, np.zeros_like(V), eta, np.eye(d), b), atol=1e-12)
+    assert np.allclose(X[:, d:], chunk_rule(K, V, eta, np.zeros((d, d)), b), atol=1e-12)
