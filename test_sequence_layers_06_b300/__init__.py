@@ -116,10 +116,17 @@ def _dtype_code(t):
     raise TypeError(f"Q/K/V must be bfloat16 or float32, got {t.dtype}")
 
 
-def _check(t, name, dtype=None, shape=None):
+def _is_device_tensor(t) -> bool:
     import torch
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+    return isinstance(t, torch.Tensor) and t.is_cuda
+
+
+def _check(t, name, dtype=None, shape=None, device=None):
+    """t is a contiguous CUDA tensor of this dtype and shape on this device (None: any)."""
+    if not _is_device_tensor(t):
         raise TypeError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}; the call's tensors are on {device}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -128,9 +135,27 @@ def _check(t, name, dtype=None, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
-def _stream_ptr(stream):
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _on_device(device):
+    """Context that makes `device` current for a call (nothing to do if it already is, as inside
+    a stream capture on that device)."""
+    import contextlib
+
     import torch
-    s = torch.cuda.current_stream() if stream is None else stream
+    if device.index is None or torch.cuda.current_device() == device.index:
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
+def _stream_ptr(stream, device=None):
+    """The stream to enqueue on: `stream`, which must belong to `device`, or the device's current one."""
+    import torch
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    if device is not None and getattr(s, "device", device) != device:
+        raise ValueError(f"stream is on {s.device}; the call's tensors are on {device}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -154,25 +179,28 @@ def ttt_linear_fwd(Q, K, V, eta, W0, b: int, Z=None, W_out=None, workspace=None,
     import torch
     lib = load_library()
     B, H, T, d = Q.shape
+    dev = Q.device
     for n, t in (("Q", Q), ("K", K), ("V", V)):
-        _check(t, n, Q.dtype, (B, H, T, d))
-    _check(eta, "eta", torch.float32, (H,))
-    _check(W0, "W0", torch.float32, (H, d, d))
+        _check(t, n, Q.dtype, (B, H, T, d), dev)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(W0, "W0", torch.float32, (H, d, d), dev)
     if Z is None:
         Z = torch.empty_like(Q)
     if W_out is None:
-        W_out = torch.empty((B, H, d, d), dtype=torch.float32, device=Q.device)
-    _check(Z, "Z", Q.dtype, (B, H, T, d))
-    _check(W_out, "W_out", torch.float32, (B, H, d, d))
-    need = ttt_workspace_bytes(B, H, T, d, b, TTT_VARIANT_LINEAR, options)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
-    args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), B, H, T, d, int(b), _p(Z), _p(W_out),
-            _p(workspace), workspace.numel(), _stream_ptr(stream))
-    if options is None:
-        st = lib.ttt_linear_fwd(*args)
-    else:
-        st = lib.ttt_linear_fwd_ex(*args, _opts(options))
+        W_out = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    _check(Z, "Z", Q.dtype, (B, H, T, d), dev)
+    _check(W_out, "W_out", torch.float32, (B, H, d, d), dev)
+    with _on_device(dev):
+        need = ttt_workspace_bytes(B, H, T, d, b, TTT_VARIANT_LINEAR, options)
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check(workspace, "workspace", device=dev)
+        args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), B, H, T, d, int(b), _p(Z), _p(W_out),
+                _p(workspace), _nbytes(workspace), _stream_ptr(stream, dev))
+        if options is None:
+            st = lib.ttt_linear_fwd(*args)
+        else:
+            st = lib.ttt_linear_fwd_ex(*args, _opts(options))
     if st != TTT_OK:
         raise TTTError("ttt_linear_fwd", st)
     return Z, W_out
@@ -185,26 +213,32 @@ def ttt_mlp_fwd(Q, K, V, eta, W1_0, W2_0, b: int, Z=None, W1_out=None, W2_out=No
     lib = load_library()
     B, H, T, d = Q.shape
     m = 4 * d
+    dev = Q.device
     for n, t in (("Q", Q), ("K", K), ("V", V)):
-        _check(t, n, Q.dtype, (B, H, T, d))
-    _check(eta, "eta", torch.float32, (H,))
-    _check(W1_0, "W1_0", torch.float32, (H, d, m))
-    _check(W2_0, "W2_0", torch.float32, (H, m, d))
+        _check(t, n, Q.dtype, (B, H, T, d), dev)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(W1_0, "W1_0", torch.float32, (H, d, m), dev)
+    _check(W2_0, "W2_0", torch.float32, (H, m, d), dev)
     if Z is None:
         Z = torch.empty_like(Q)
     if W1_out is None:
-        W1_out = torch.empty((B, H, d, m), dtype=torch.float32, device=Q.device)
+        W1_out = torch.empty((B, H, d, m), dtype=torch.float32, device=dev)
     if W2_out is None:
-        W2_out = torch.empty((B, H, m, d), dtype=torch.float32, device=Q.device)
-    need = ttt_workspace_bytes(B, H, T, d, b, TTT_VARIANT_MLP)
-    if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
-    args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W1_0), _p(W2_0), B, H, T, d, int(b), _p(Z),
-            _p(W1_out), _p(W2_out), _p(workspace), workspace.numel(), _stream_ptr(stream))
-    if options is None:
-        st = lib.ttt_mlp_fwd(*args)
-    else:
-        st = lib.ttt_mlp_fwd_ex(*args, _opts(options))
+        W2_out = torch.empty((B, H, m, d), dtype=torch.float32, device=dev)
+    _check(Z, "Z", Q.dtype, (B, H, T, d), dev)
+    _check(W1_out, "W1_out", torch.float32, (B, H, d, m), dev)
+    _check(W2_out, "W2_out", torch.float32, (B, H, m, d), dev)
+    with _on_device(dev):
+        need = ttt_workspace_bytes(B, H, T, d, b, TTT_VARIANT_MLP)
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check(workspace, "workspace", device=dev)
+        args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W1_0), _p(W2_0), B, H, T, d, int(b), _p(Z),
+                _p(W1_out), _p(W2_out), _p(workspace), _nbytes(workspace), _stream_ptr(stream, dev))
+        if options is None:
+            st = lib.ttt_mlp_fwd(*args)
+        else:
+            st = lib.ttt_mlp_fwd_ex(*args, _opts(options))
     if st != TTT_OK:
         raise TTTError("ttt_mlp_fwd", st)
     return Z, W1_out, W2_out
@@ -217,16 +251,21 @@ def ttt_mlp_fwd_noalloc(Q, K, V, eta, W1_0, W2_0, b: int, Z=None, W1_out=None, W
     lib = load_library()
     B, H, T, d = Q.shape
     m = 4 * d
+    dev = Q.device
     for n, t in (("Q", Q), ("K", K), ("V", V)):
-        _check(t, n, Q.dtype, (B, H, T, d))
-    _check(eta, "eta", torch.float32, (H,))
-    _check(W1_0, "W1_0", torch.float32, (H, d, m))
-    _check(W2_0, "W2_0", torch.float32, (H, m, d))
+        _check(t, n, Q.dtype, (B, H, T, d), dev)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(W1_0, "W1_0", torch.float32, (H, d, m), dev)
+    _check(W2_0, "W2_0", torch.float32, (H, m, d), dev)
     Z = torch.empty_like(Q) if Z is None else Z
-    W1_out = torch.empty((B, H, d, m), dtype=torch.float32, device=Q.device) if W1_out is None else W1_out
-    W2_out = torch.empty((B, H, m, d), dtype=torch.float32, device=Q.device) if W2_out is None else W2_out
-    st = lib.ttt_mlp_fwd_noalloc(_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W1_0), _p(W2_0), B, H, T, d,
-                                 int(b), _p(Z), _p(W1_out), _p(W2_out), _stream_ptr(stream))
+    W1_out = torch.empty((B, H, d, m), dtype=torch.float32, device=dev) if W1_out is None else W1_out
+    W2_out = torch.empty((B, H, m, d), dtype=torch.float32, device=dev) if W2_out is None else W2_out
+    _check(Z, "Z", Q.dtype, (B, H, T, d), dev)
+    _check(W1_out, "W1_out", torch.float32, (B, H, d, m), dev)
+    _check(W2_out, "W2_out", torch.float32, (B, H, m, d), dev)
+    with _on_device(dev):
+        st = lib.ttt_mlp_fwd_noalloc(_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W1_0), _p(W2_0), B, H, T,
+                                     d, int(b), _p(Z), _p(W1_out), _p(W2_out), _stream_ptr(stream, dev))
     if st != TTT_OK:
         raise TTTError("ttt_mlp_fwd_noalloc", st)
     return Z, W1_out, W2_out
@@ -237,15 +276,18 @@ def ttt_linear_decode_step(q, k, v, eta, W_anchor, W_run, pos: int, b: int, z=No
     import torch
     lib = load_library()
     B, H, d = q.shape
+    dev = q.device
     for n, t in (("q", q), ("k", k), ("v", v)):
-        _check(t, n, q.dtype, (B, H, d))
-    _check(eta, "eta", torch.float32, (H,))
-    _check(W_anchor, "W_anchor", torch.float32, (B, H, d, d))
-    _check(W_run, "W_run", torch.float32, (B, H, d, d))
+        _check(t, n, q.dtype, (B, H, d), dev)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(W_anchor, "W_anchor", torch.float32, (B, H, d, d), dev)
+    _check(W_run, "W_run", torch.float32, (B, H, d, d), dev)
     if z is None:
         z = torch.empty_like(q)
-    st = lib.ttt_linear_decode_step(_p(q), _p(k), _p(v), _dtype_code(q), _p(eta), _p(W_anchor), _p(W_run),
-                                    B, H, d, int(pos), int(b), _p(z), _stream_ptr(stream))
+    _check(z, "z", q.dtype, (B, H, d), dev)
+    with _on_device(dev):
+        st = lib.ttt_linear_decode_step(_p(q), _p(k), _p(v), _dtype_code(q), _p(eta), _p(W_anchor), _p(W_run),
+                                        B, H, d, int(pos), int(b), _p(z), _stream_ptr(stream, dev))
     if st != TTT_OK:
         raise TTTError("ttt_linear_decode_step", st)
     return z
@@ -261,20 +303,23 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b: int, dZ, dW_out, workspace=None, stream=
     import torch
     lib = load_library()
     B, H, T, d = Q.shape
+    dev = Q.device
     for n, t in (("Q", Q), ("K", K), ("V", V), ("dZ", dZ)):
-        _check(t, n, torch.float32, (B, H, T, d))
-    _check(eta, "eta", torch.float32, (H,))
-    _check(W0, "W0", torch.float32, (H, d, d))
-    _check(dW_out, "dW_out", torch.float32, (B, H, d, d))
+        _check(t, n, torch.float32, (B, H, T, d), dev)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(W0, "W0", torch.float32, (H, d, d), dev)
+    _check(dW_out, "dW_out", torch.float32, (B, H, d, d), dev)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    deta = torch.empty((H,), dtype=torch.float32, device=Q.device)
-    dW0 = torch.empty((H, d, d), dtype=torch.float32, device=Q.device)
+    deta = torch.empty((H,), dtype=torch.float32, device=dev)
+    dW0 = torch.empty((H, d, d), dtype=torch.float32, device=dev)
     need = ttt_linear_bwd_workspace_bytes(B, H, T, d, b)
     if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
-    st = lib.ttt_linear_bwd(_p(Q), _p(K), _p(V), TTT_F32, _p(eta), _p(W0), B, H, T, d, int(b), _p(dZ), _p(dW_out),
-                            _p(dQ), _p(dK), _p(dV), _p(deta), _p(dW0), _p(workspace), workspace.numel(),
-                            _stream_ptr(stream))
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", device=dev)
+    with _on_device(dev):
+        st = lib.ttt_linear_bwd(_p(Q), _p(K), _p(V), TTT_F32, _p(eta), _p(W0), B, H, T, d, int(b), _p(dZ),
+                                _p(dW_out), _p(dQ), _p(dK), _p(dV), _p(deta), _p(dW0), _p(workspace),
+                                _nbytes(workspace), _stream_ptr(stream, dev))
     if st != TTT_OK:
         raise TTTError("ttt_linear_bwd", st)
     return dQ, dK, dV, deta, dW0
@@ -282,4 +327,6 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b: int, dZ, dW_out, workspace=None, stream=
 
 def ttt_last_device_status(workspace, stream=None) -> int:
     """Wait for the stream, then read and clear the workspace's device status word."""
-    return int(load_library().ttt_last_device_status(_p(workspace), _stream_ptr(stream)))
+    _check(workspace, "workspace")
+    with _on_device(workspace.device):
+        return int(load_library().ttt_last_device_status(_p(workspace), _stream_ptr(stream, workspace.device)))
