@@ -7,8 +7,9 @@ include/ttt.h and raise on a non-OK status. There is no CPU fallback: if the
 library is missing or no GPU is present the calls fail loudly.
 
 Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_plan, ttt_linear_fwd,
-ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_linear_decode_step,
-ttt_last_device_status, ttt_status_str.
+ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_linear_decode_step, ttt_linear_bwd_workspace_bytes,
+ttt_linear_bwd, ttt_last_device_status, ttt_status_str. The *_fwd_ex forms are reached
+through the options argument.
 """
 from __future__ import annotations
 
