@@ -35,7 +35,9 @@
  *   (a wait that ran out of time) are written to a status word inside the
  *   workspace; ttt_last_device_status() reads it.
  *
- *   Inputs are never modified. Outputs may not alias inputs.
+ *   Inputs are never modified. Outputs (and the workspace) may overlap
+ *   neither an input nor one another: a call whose buffers do returns
+ *   TTT_ERR_ARG before anything is enqueued. Inputs may alias each other.
  */
 #ifndef TTT_B300_H
 #define TTT_B300_H

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <algorithm>
 #include <cstring>
+#include <initializer_list>
 
 #include "ttt.h"
 #include "kernels.h"
@@ -32,6 +33,35 @@ bool sizes_ok(int B, int H, int T, int d, int b) {
 }
 
 size_t mlp_hidden(int d) { return static_cast<size_t>(4) * d; }
+
+// A buffer the call touches: start and length in bytes.
+struct Span {
+  const void* p;
+  size_t n;
+};
+
+bool overlap(const Span& a, const Span& b) {
+  if (a.p == nullptr || b.p == nullptr || a.n == 0 || b.n == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Outputs (and scratch) may overlap neither an input nor one another; inputs
+// may alias each other, since they are only read.
+bool outputs_disjoint(std::initializer_list<Span> outs, std::initializer_list<Span> ins) {
+  for (auto o = outs.begin(); o != outs.end(); ++o) {
+    for (const Span& i : ins)
+      if (overlap(*o, i)) return false;
+    for (auto o2 = o + 1; o2 != outs.end(); ++o2)
+      if (overlap(*o, *o2)) return false;
+  }
+  return true;
+}
+
+// Bytes of a [n0][n1][n2][n3] tensor with elements of `es` bytes.
+size_t bytes4(int n0, int n1, int n2, int n3, size_t es) {
+  return static_cast<size_t>(n0) * n1 * n2 * n3 * es;
+}
 
 ttt_options defaults(const ttt_options* opt) {
   ttt_options o;
@@ -228,6 +258,12 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
   const ttt_status pst = plan_linear(B, H, T, d, b, dt == TTT_BF16, o, &pl);
   if (pst != TTT_OK) return pst;
   if (ws_bytes < kStatusBytes + seg_scratch_bytes(pl, B * H, d)) return TTT_ERR_ARG;
+  {
+    const size_t seq = bytes4(B, H, T, d, dt == TTT_BF16 ? 2 : 4);
+    if (!outputs_disjoint({{Z, seq}, {W_out, bytes4(B, H, d, d, 4)}, {workspace, ws_bytes}},
+                          {{Q, seq}, {K, seq}, {V, seq}, {eta, bytes4(H, 1, 1, 1, 4)}, {W0, bytes4(H, d, d, 1, 4)}}))
+      return TTT_ERR_ARG;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   ttt::LinearParams p;
@@ -307,6 +343,13 @@ ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype
                         static_cast<const void*>(W2_out), static_cast<const void*>(workspace)})
     if (p && !aligned16(p)) return TTT_ERR_ARG;
   if (ws_bytes < workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP, nullptr)) return TTT_ERR_ARG;
+  {
+    const size_t seq = bytes4(B, H, T, d, dt == TTT_BF16 ? 2 : 4);
+    const size_t w1 = bytes4(d, static_cast<int>(mlp_hidden(d)), 1, 1, 4);
+    if (!outputs_disjoint({{Z, seq}, {W1_out, w1 * B * H}, {W2_out, w1 * B * H}, {workspace, ws_bytes}},
+                          {{Q, seq}, {K, seq}, {V, seq}, {eta, bytes4(H, 1, 1, 1, 4)}, {W1_0, w1 * H}, {W2_0, w1 * H}}))
+      return TTT_ERR_ARG;
+  }
   const ttt_options o = defaults(opt);
   if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -357,10 +400,15 @@ ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, t
   if (B < 1 || H < 1 || d < 1 || b < 1 || pos < 0) return TTT_ERR_ARG;
   if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
   if (!q || !k || !v || !z || !eta || !W_anchor || !W_run) return TTT_ERR_ARG;
-  if (W_anchor == W_run) return TTT_ERR_ARG;
   for (const void* p : {q, k, v, static_cast<const void*>(z), static_cast<const void*>(eta),
                         static_cast<const void*>(W_anchor), static_cast<const void*>(W_run)})
     if (!aligned16(p)) return TTT_ERR_ARG;
+  {
+    const size_t tok = bytes4(B, H, d, 1, dt == TTT_BF16 ? 2 : 4), st = bytes4(B, H, d, d, 4);
+    if (!outputs_disjoint({{z, tok}, {W_anchor, st}, {W_run, st}},
+                          {{q, tok}, {k, tok}, {v, tok}, {eta, bytes4(H, 1, 1, 1, 4)}}))
+      return TTT_ERR_ARG;
+  }
   ttt::DecodeParams p;
   p.q = q; p.k = k; p.v = v; p.z = z; p.eta = eta;
   p.W_anchor = W_anchor; p.W_run = W_run;
@@ -391,6 +439,14 @@ ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype
                         static_cast<const void*>(dW0), static_cast<const void*>(workspace)})
     if (p && !aligned16(p)) return TTT_ERR_ARG;
   if (ws_bytes < ttt_linear_bwd_workspace_bytes(B, H, T, d, b)) return TTT_ERR_ARG;
+  {
+    const size_t seq = bytes4(B, H, T, d, 4), hdd = bytes4(H, d, d, 1, 4);
+    if (!outputs_disjoint({{dQ, seq}, {dK, seq}, {dV, seq}, {deta, bytes4(H, 1, 1, 1, 4)}, {dW0, hdd},
+                           {workspace, ws_bytes}},
+                          {{Q, seq}, {K, seq}, {V, seq}, {dZ, seq}, {eta, bytes4(H, 1, 1, 1, 4)}, {W0, hdd},
+                           {dW_out, bytes4(B, H, d, d, 4)}}))
+      return TTT_ERR_ARG;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ttt::LinearBwdParams p;
   p.Q = static_cast<const float*>(Q);

@@ -73,9 +73,12 @@ def test_linear_plan(lib):
         ttt.ttt_linear_plan(1, 1, 100, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 24})
 
 
+MB = 1 << 20  # fake device addresses 1 MB apart: no two buffers of these small calls overlap
+
+
 def _lin(lib, **kw):
-    a = dict(Q=4096, K=4096, V=4096, dt=1, eta=4096, W0=4096, B=1, H=1, T=16, d=64, b=16, Z=4096, W=4096,
-             ws=4096, wsb=1 << 20, s=0)
+    a = dict(Q=1 * MB, K=2 * MB, V=3 * MB, dt=1, eta=4 * MB, W0=5 * MB, B=1, H=1, T=16, d=64, b=16, Z=6 * MB,
+             W=7 * MB, ws=8 * MB, wsb=1 << 20, s=0)
     a.update(kw)
     vp = ctypes.c_void_p
     return lib.ttt_linear_fwd(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W0"]), a["B"],
@@ -147,8 +150,8 @@ def test_mlp_and_decode_reject_bad_arguments(lib):
 
 
 def _bwd(lib, **kw):
-    a = dict(Q=4096, K=4096, V=4096, dt=0, eta=4096, W0=4096, B=2, H=3, T=40, d=16, b=8, dZ=4096, dW=4096,
-             dQ=4096, dK=4096, dV=4096, deta=4096, dW0=4096, ws=4096, wsb=1 << 24, s=0)
+    a = dict(Q=1 * MB, K=2 * MB, V=3 * MB, dt=0, eta=4 * MB, W0=5 * MB, B=2, H=3, T=40, d=16, b=8, dZ=6 * MB,
+             dW=7 * MB, dQ=8 * MB, dK=9 * MB, dV=10 * MB, deta=11 * MB, dW0=12 * MB, ws=16 * MB, wsb=1 << 24, s=0)
     a.update(kw)
     vp = ctypes.c_void_p
     return lib.ttt_linear_bwd(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W0"]), a["B"],
@@ -178,3 +181,41 @@ def test_no_cpu_fallback_without_a_gpu(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present; this checks the CPU-only failure mode")
     assert _lin(lib) == ttt.TTT_ERR_CUDA
+
+
+@pytest.mark.parametrize("kw", [dict(Z=1 * MB + 1024), dict(Z=3 * MB - 1024), dict(W=5 * MB), dict(ws=4 * MB),
+                                dict(W=6 * MB + 1024), dict(ws=7 * MB)])
+def test_linear_refuses_outputs_that_overlap(lib, kw):
+    """Z, W_out and the workspace may overlap neither an input nor one another (Q holds 2 KB here)."""
+    assert _lin(lib, **kw) == ttt.TTT_ERR_ARG
+
+
+def test_inputs_may_alias_and_outputs_may_abut(lib):
+    """Q = K = V is allowed, and so is Z starting right where Q ends; with no GPU such a call gets past
+    every argument check and fails only at the first CUDA call."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; these fake addresses must not reach a kernel")
+    assert _lin(lib, K=1 * MB, V=1 * MB) == ttt.TTT_ERR_CUDA
+    assert _lin(lib, Z=1 * MB + 2048) == ttt.TTT_ERR_CUDA       # Q is 16 x 64 bf16 = 2048 bytes
+    assert _lin(lib, Z=1 * MB + 2032) == ttt.TTT_ERR_ARG        # one 16-byte step into Q
+
+
+@pytest.mark.parametrize("kw", [dict(dQ=1 * MB), dict(dK=6 * MB + 4096), dict(deta=4 * MB), dict(dW0=7 * MB + 1024),
+                                dict(ws=12 * MB - 1024), dict(dV=9 * MB)])
+def test_backward_refuses_outputs_that_overlap(lib, kw):
+    """Each output moved onto an input (dQ on Q, dK inside dZ, deta on eta, dW0 inside dW_out) or onto
+    another output (the 16 MB workspace over dW0, dV on dK)."""
+    assert _bwd(lib, **kw) == ttt.TTT_ERR_ARG
+
+
+def test_decode_refuses_states_that_overlap():
+    vp = ctypes.c_void_p
+    lib = ttt.load_library()
+
+    def call(q, z, Wa, Wr):
+        return lib.ttt_linear_decode_step(vp(q), vp(q), vp(q), 1, vp(4 * MB), vp(Wa), vp(Wr), 1, 2, 64, 0, 16, vp(z),
+                                          vp(0))
+    assert call(1 * MB, 2 * MB, 5 * MB, 5 * MB + 16 * 1024) == ttt.TTT_ERR_ARG  # W_run inside W_anchor (32 KB)
+    assert call(1 * MB, 1 * MB + 128, 5 * MB, 6 * MB) == ttt.TTT_ERR_ARG       # z inside q (256 bytes)
+    assert call(1 * MB, 2 * MB, 4 * MB, 6 * MB) == ttt.TTT_ERR_ARG             # W_anchor on eta
