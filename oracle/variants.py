@@ -33,6 +33,9 @@ Two forms are given, for the same reason as for plain TTT-Linear:
 Pins (tests/test_oracle_variants.py): the gradient against central finite
 differences of the loss and against torch autograd through torch's own
 layer_norm; primal equals dual; eta = 0 and gamma = 0 in closed form.
+
+Momentum. momentum_primal and momentum_dual hold the E²-TTT-style variant
+(momentum gradient descent with chunk-start gradients); see momentum_primal.
 """
 from __future__ import annotations
 
@@ -110,3 +113,81 @@ def ln_residual_dual(Q, K, V, eta, W0, gamma, beta, b: int):
                 W = W - eta[h] * Kc.T @ E
             W_out[n, h] = W
     return Z, W_out
+
+
+# ---------------------------------------------------------------------------- momentum
+def momentum_primal(Q, K, V, alpha, beta, W0, b: int):
+    """TTT-Linear with momentum gradient descent, token by token.
+
+    The E²-TTT write-up (zhichai, sections 2.3 and 5.1) keeps a momentum state M
+    beside the fast weights W, takes every gradient at the chunk-start weights,
+    and says the chunk's state then follows exactly from a recurrence; its
+    displayed per-chunk update leaves the function f undefined. The reading here
+    is momentum gradient descent at token level with those chunk-start gradients:
+    for chunk c with start state W_a, and for each of its tokens t in order,
+        g_t = k_t^T (k_t W_a - v_t),   M <- beta M + (1 - beta) g_t,   W <- W - alpha M,
+    then z_t = q_t W. M starts at zero for every sequence. With beta = 0 this is
+    the TTT-Linear chunk rule with eta = alpha. (The displayed per-chunk
+    formula, read literally, would instead take one momentum step per chunk.)
+    Parity with the page's own method is unpinned: the page gives neither f nor
+    a read-out, nor any worked value. The pins hold this reading to the
+    mathematics: beta = 0 against the C oracle's TTT-Linear, the gradient
+    against torch autograd, and the primal against the closed-form dual.
+
+    Q, K, V [B,H,T,d]; alpha, beta [H]. W0 [H,d,d]. Returns Z [B,H,T,d] and the
+    final W and M [B,H,d,d], fp64."""
+    Q, K, V, alpha, beta, W0 = map(_f64, (Q, K, V, alpha, beta, W0))
+    B, H, T, d = Q.shape
+    if b < 1:
+        raise ValueError("b must be positive")
+    Z = np.zeros_like(Q)
+    W_out, M_out = np.zeros((B, H, d, d)), np.zeros((B, H, d, d))
+    for n in range(B):
+        for h in range(H):
+            W, M = W0[h].copy(), np.zeros((d, d))
+            Wa = W
+            for t in range(T):
+                if t % b == 0:
+                    Wa = W.copy()
+                g = np.outer(K[n, h, t], K[n, h, t] @ Wa - V[n, h, t])
+                M = beta[h] * M + (1.0 - beta[h]) * g
+                W = W - alpha[h] * M
+                Z[n, h, t] = Q[n, h, t] @ W
+            W_out[n, h], M_out[n, h] = W, M
+    return Z, W_out, M_out
+
+
+def momentum_dual(Q, K, V, alpha, beta, W0, b: int):
+    """The same layer chunk by chunk, from the recurrence solved in closed form.
+
+    Within a chunk with start (W_a, M_a) and errors E = K W_a - V, after its s-th
+    token (s = 1, 2, ...)
+        M_s = beta^s M_a + (1 - beta) sum_{i<=s} beta^(s-i) k_i^T e_i,
+        W_s = W_a - alpha [c_s M_a + sum_{i<=s} (1 - beta^(s-i+1)) k_i^T e_i],
+    with c_s = beta + beta^2 + ... + beta^s. So the read-out is a decay-masked
+    dual form, Z = Q W_a - alpha c * (Q M_a) - alpha (tril(Q K^T) * D) E with
+    D[s][i] = 1 - beta^(s-i+1), and the chunk's end state is the last row."""
+    Q, K, V, alpha, beta, W0 = map(_f64, (Q, K, V, alpha, beta, W0))
+    B, H, T, d = Q.shape
+    if b < 1:
+        raise ValueError("b must be positive")
+    Z = np.zeros_like(Q)
+    W_out, M_out = np.zeros((B, H, d, d)), np.zeros((B, H, d, d))
+    for n in range(B):
+        for h in range(H):
+            a, be = alpha[h], beta[h]
+            W, M = W0[h].copy(), np.zeros((d, d))
+            for c0 in range(0, T, b):
+                Qc, Kc, Vc = Q[n, h, c0:c0 + b], K[n, h, c0:c0 + b], V[n, h, c0:c0 + b]
+                C = len(Kc)
+                s = np.arange(1, C + 1)
+                E = Kc @ W - Vc
+                cs = np.cumsum(be ** s)                                     # c_s
+                D = np.tril(1.0 - be ** np.maximum(s[:, None] - s[None, :] + 1, 1))  # 1 - beta^(s-i+1), i <= s
+                Z[n, h, c0:c0 + C] = Qc @ W - a * cs[:, None] * (Qc @ M) - a * (np.tril(Qc @ Kc.T) * D) @ E
+                G = Kc.T @ (E * (be ** (C - s))[:, None])                   # sum_i beta^(C-i) k_i^T e_i
+                W_new = W - a * (cs[-1] * M + Kc.T @ (E * D[-1][:, None]))
+                M = be ** C * M + (1.0 - be) * G
+                W = W_new
+            W_out[n, h], M_out[n, h] = W, M
+    return Z, W_out, M_out

@@ -7,6 +7,11 @@ torch's own layer_norm; the token-by-token form against the chunk-by-chunk dual
 form; eta = 0 (no update) and gamma = 0 (f no longer depends on W) against their
 closed forms. A dropped mean in the normalisation's chain rule, a missing
 residual or a gradient taken at the running weights each fail one of these.
+
+The momentum variant (momentum gradient descent with chunk-start gradients) is
+checked token by token against its closed-form dual, against the C oracle's
+TTT-Linear at beta = 0, against torch autograd for every gradient, and at a zero
+rate.
 """
 import numpy as np
 import pytest
@@ -134,3 +139,58 @@ def test_planted_mistakes_are_caught():
     }
     for name, e in slips.items():
         assert not np.allclose(np.outer(k, e), gW.numpy(), atol=1e-6), name
+
+
+# ---------------------------------------------------------------------------- momentum
+from oracle.variants import momentum_dual, momentum_primal  # noqa: E402
+
+import oracle  # noqa: E402
+
+
+def momentum_case(B, H, T, d, seed):
+    g = np.random.default_rng(seed)
+    Q, K, V = (g.standard_normal((B, H, T, d)) * 0.8 for _ in range(3))
+    alpha = g.uniform(0.05, 0.3, H)
+    beta = g.uniform(0.1, 0.95, H)
+    W0 = g.standard_normal((H, d, d)) * 0.3
+    return Q, K, V, alpha, beta, W0
+
+
+@pytest.mark.parametrize("T,b", [(11, 1), (11, 3), (12, 4), (9, 9), (10, 16)])
+def test_momentum_primal_equals_closed_form_dual(T, b):
+    args = momentum_case(2, 2, T, 3, seed=T + b)
+    for got, want in zip(momentum_primal(*args, b), momentum_dual(*args, b)):
+        assert np.allclose(got, want, atol=1e-12)
+
+
+@pytest.mark.parametrize("b", [1, 4, 7])
+def test_momentum_without_momentum_is_ttt_linear(b):
+    """beta = 0: the C oracle's TTT-Linear with eta = alpha, by both forms."""
+    Q, K, V, alpha, _, W0 = momentum_case(2, 3, 13, 4, seed=b)
+    Zr, Wr = oracle.linear_primal(Q, K, V, alpha, W0, b)
+    for Z, W, M in (momentum_primal(Q, K, V, alpha, np.zeros(3), W0, b),
+                    momentum_dual(Q, K, V, alpha, np.zeros(3), W0, b)):
+        assert np.allclose(Z, Zr, atol=1e-12) and np.allclose(W, Wr, atol=1e-12)
+
+
+def test_momentum_gradient_equals_torch_autograd():
+    """b = 3: every gradient comes from autograd of 1/2 ||k W_a - v||^2 at the chunk-start W_a."""
+    Q, K, V, alpha, beta, W0 = momentum_case(1, 1, 8, 3, seed=3)
+    b = 3
+    Z, Wo, Mo = momentum_primal(Q, K, V, alpha, beta, W0, b)
+    W, M = torch.tensor(W0[0]), torch.zeros(3, 3, dtype=torch.float64)
+    for t in range(8):
+        if t % b == 0:
+            Wa = W.clone().requires_grad_(True)
+        k, v, q = (torch.tensor(x[0, 0, t]) for x in (K, V, Q))
+        (g,) = torch.autograd.grad(0.5 * ((k @ Wa - v) ** 2).sum(), Wa)
+        M = beta[0] * M + (1 - beta[0]) * g
+        W = W - alpha[0] * M
+        assert np.allclose((q @ W).numpy(), Z[0, 0, t], atol=1e-12)
+    assert np.allclose(W.numpy(), Wo[0, 0], atol=1e-12) and np.allclose(M.numpy(), Mo[0, 0], atol=1e-12)
+
+
+def test_momentum_with_zero_rate_reads_out_w0():
+    Q, K, V, _, beta, W0 = momentum_case(1, 2, 7, 3, seed=4)
+    Z, W, M = momentum_primal(Q, K, V, np.zeros(2), beta, W0, 3)
+    assert np.array_equal(W[0], W0) and np.allclose(Z[0], np.einsum("htd,hde->hte", Q[0], W0), atol=1e-14)
