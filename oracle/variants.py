@@ -119,7 +119,8 @@ def ln_residual_dual(Q, K, V, eta, W0, gamma, beta, b: int):
 def momentum_primal(Q, K, V, alpha, beta, W0, b: int):
     """TTT-Linear with momentum gradient descent, token by token.
 
-    The E²-TTT write-up (zhichai, sections 2.3 and 5.1) keeps a momentum state M
+    "推理时的“临阵磨枪”：Test-Time Training如何教会AI“边做边学”" (zhichai),
+    sections 2.3 and 5.1, describes E²-TTT: it keeps a momentum state M
     beside the fast weights W, takes every gradient at the chunk-start weights,
     and says the chunk's state then follows exactly from a recurrence; its
     displayed per-chunk update leaves the function f undefined. The reading here
