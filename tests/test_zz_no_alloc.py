@@ -4,8 +4,8 @@ scratch array instead). Called through the C ABI and compared with
 ttt_mlp_fwd, which gets a workspace from the caller, on two calls in a row
 with different inputs (the shared array must not carry anything over).
 
-Kept in a file pytest collects last, so that a run stopping at the first
-failure has run every other test before this one."""
+Kept in a file pytest collects after the parity tests, so that a run stopping
+at the first failure has run them before this one."""
 import ctypes
 
 import numpy as np
