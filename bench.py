@@ -45,6 +45,7 @@ METRIC = "TTT-Linear scan tokens·heads/sec and % of binding roofline (1×B300)"
 UNIT = "token·heads/s"
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_HBM_GBS = 6400.0
+REFERENCE_BUDGET_S = 120.0  # wall time of the reference arm's warm-up and timed steps together
 NOMINAL_HBM_GBS = 7700.0  # B300 HBM3e, vendor figure: context beside the measured copy bandwidth
 # kernel -> (source files whose digest a committed ncu summary must match, summary file)
 KERNEL_PROFILES = {
@@ -587,7 +588,7 @@ def bench_reference(args, world, rank):
     # whole run stays within a few minutes
     steps = args.steps
     warm = max(3, args.warmup)
-    budget_s = 120.0
+    budget_s = REFERENCE_BUDGET_S
     threads = oracle.max_threads()
     probe = synth.make_inputs(w.with_(B=1, T=256))
     t0 = time.perf_counter()

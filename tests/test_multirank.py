@@ -94,3 +94,23 @@ def test_roofline_block_reproduces_a_measured_line():
                                       "fallback", lambda name: 7)
     assert list(one_pass["kernels"]) == ["linear_mma_kernel"] and one_pass["traffic"] == 7
     assert one_pass["peak_kind"] == "fallback 6.4 TB/s"
+
+
+def test_reference_arm_prints_on_rank_zero_only(capsys):
+    """bench.py --impl reference: the oracle on a bounded sample of the workload, one JSON line from
+    rank 0 with the reference keys (impl, cpu_baseline, e2e with no copies); other ranks print nothing."""
+    import argparse
+    import json
+    bench = _bench()
+    bench.REFERENCE_BUDGET_S = 0.5
+    args = argparse.Namespace(workload="linear_long", b=16, steps=2, warmup=3)
+    bench.bench_reference(args, 2, 1)
+    assert capsys.readouterr().out == ""
+    bench.bench_reference(args, 2, 0)
+    line = json.loads(capsys.readouterr().out)
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0 and line["dtype"] == "f64"
+    assert line["unit"] == bench.UNIT and line["metric"] == bench.METRIC and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "linear_long" and line["warmup"] >= 3
