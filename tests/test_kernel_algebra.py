@@ -12,8 +12,9 @@ chunk by chunk, on random inputs:
     the chunk-start state, its read-out the running state;
   - the combine: W_start(s+1) = A_s W_start(s) + B_s reproduces the scan;
   - the backward's segment-parallel form (transposed maps);
-  - two restatements for faster kernels: Kh by a finite (nilpotent) series in
-    Horner form, and a read-out that takes a 64-token group of chunks at once;
+  - restatements for faster kernels: Kh by a finite (nilpotent) series in
+    Horner form, a read-out that takes a 64-token group of chunks at once, and
+    group maps composed in pairs (exact, and with the kernel's bf16 rounding);
   - two inner-model variants that reduce to plain TTT-Linear on changed inputs:
     a bias in f (a constant extra input) and a per-token learning rate
     (keys and values scaled by its square root).
@@ -313,3 +314,55 @@ def test_group_maps_compose_in_any_association():
     assert np.allclose(Y, X, atol=1e-12)
     assert np.allclose(X[:, :d], chunk_rule(K, np.zeros_like(V), eta, np.eye(d), b), atol=1e-12)
     assert np.allclose(X[:, d:], chunk_rule(K, V, eta, np.zeros((d, d)), b), atol=1e-12)
+
+
+def test_pairwise_composition_keeps_the_rounding_error_of_the_chain():
+    """The same segment map with bf16 operands and fp32 accumulation at the tcgen05 kernel's rounding
+    points (Kh and the chain's X rounded to bf16; M and Q formed from bf16 operands): composing group
+    maps in pairs once or twice before the chain leaves the error in B (which dominates a segment's start
+    state) within 15 % of the chain's; A's relative error grows, but A itself is negligible."""
+    import torch
+
+    bf = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).to(torch.float64).numpy()
+    f32 = lambda x: x.astype(np.float32).astype(np.float64)
+    g = np.random.default_rng(0)
+    d, n, b, eta, L = 64, 64, 16, 0.1, 4864
+    K = g.standard_normal((L, d))
+    K = bf(K / np.linalg.norm(K, axis=1, keepdims=True))
+    V = bf(g.standard_normal((L, d)))
+    blk = np.arange(n) // b
+    exact, rounded = [], []
+    for g0 in range(0, L, n):
+        Kg, Vg = K[g0:g0 + n], V[g0:g0 + n]
+        N = np.where(blk[:, None] > blk[None, :], Kg @ Kg.T, 0.0)
+        Kh = np.linalg.inv(np.eye(n) + eta * N).T @ Kg
+        exact.append((-eta * Kh.T @ Kg, eta * Kh.T @ Vg))
+        rounded.append((f32(-eta * bf(Kh).T @ bf(Kg)), f32(eta * bf(Kh).T @ bf(Vg))))
+
+    def run(maps, levels, kernel):
+        for _ in range(levels):
+            nxt = []
+            for i in range(0, len(maps), 2):
+                if i + 1 == len(maps):
+                    nxt.append(maps[i])
+                    continue
+                (M1, Q1), (M2, Q2) = maps[i], maps[i + 1]
+                P, R = (bf(M2) @ bf(M1), bf(M2) @ bf(Q1)) if kernel else (M2 @ M1, M2 @ Q1)
+                nxt.append((f32(M1 + M2 + P), f32(Q1 + Q2 + R)) if kernel else (M1 + M2 + P, Q1 + Q2 + R))
+            maps = nxt
+        X = np.hstack([np.eye(d), np.zeros((d, d))])
+        for M, Q in maps:
+            Qx = np.hstack([np.zeros((d, d)), bf(Q) if kernel else Q])
+            X = f32(X + bf(M) @ bf(X) + Qx) if kernel else X + M @ X + Qx
+        return X
+
+    ref = run(exact, 0, False)
+    err = lambda X, part: np.linalg.norm(X[:, part] - ref[:, part]) / np.linalg.norm(ref[:, part])
+    A, B = slice(0, d), slice(d, 2 * d)
+    chain = run(rounded, 0, True)
+    assert err(chain, B) < 5e-3 and err(chain, A) < 1e-2
+    for levels in (1, 2):
+        X = run(rounded, levels, True)
+        assert err(X, B) < 1.15 * err(chain, B)
+        # A's part of a start state, |dA| |W| with |W| ~ |B|, stays below B's own error
+        assert np.linalg.norm(X[:, A] - ref[:, A]) * np.linalg.norm(ref[:, B]) < np.linalg.norm(X[:, B] - ref[:, B])
