@@ -400,3 +400,48 @@ def test_planted_mistakes_are_caught(mistake):
     closed = Q[0, 0] @ W0[0] - eta[0] * np.tril(Q[0, 0] @ K[0, 0].T) @ E
     caught.append(np.max(np.abs(W - (W0[0] - eta[0] * g))) > 1e-6 or rel(Zc, closed) > 1e-9)
     assert any(caught), mistake
+
+
+# ---------------------------------------------------------------- planted slips, TTT-MLP
+def _mlp_planted(Q, K, V, eta, W1, W2, b, mistake):
+    """The TTT-MLP chunk rule token by token with one plausible slip planted (fp64, one unit)."""
+    c, a = np.sqrt(2 / np.pi), 0.044715
+    th = lambda u: np.tanh(c * (u + a * u ** 3))
+    gelu = lambda u: 0.5 * u * (1 + th(u))
+    dgelu = lambda u: 0.5 * (1 + th(u)) + 0.5 * u * (1 - th(u) ** 2) * c * (1 + 3 * a * u * u)
+    if mistake == "erf_gelu":
+        from math import erf
+        gelu = np.vectorize(lambda u: 0.5 * u * (1 + erf(u / np.sqrt(2))))
+    A, Bm = W1.copy(), W2.copy()
+    Z = np.zeros_like(Q)
+    for t in range(len(Q)):
+        if t % b == 0:
+            A0, B0 = A.copy(), Bm.copy()
+        u = K[t] @ A0
+        act = gelu(u)
+        g = act @ B0 - V[t]
+        s1 = gelu(u) if mistake == "sigma_for_derivative" else (1.0 if mistake == "no_derivative" else dgelu(u))
+        delta = (g @ (Bm if mistake == "running_w2" else B0).T) * s1
+        if mistake == "read_first":
+            Z[t] = gelu(Q[t] @ A) @ Bm
+        A = A - eta * np.outer(K[t], delta)
+        Bm = Bm - eta * np.outer(act, g)
+        if mistake != "read_first":
+            Z[t] = gelu(Q[t] @ A) @ Bm
+    return Z, A, Bm
+
+
+@pytest.mark.parametrize("mistake", ["none", "sigma_for_derivative", "no_derivative", "erf_gelu", "running_w2",
+                                     "read_first"])
+def test_mlp_planted_mistakes_are_caught(mistake):
+    """Each slip moves the result far outside the 1e-12 the autograd pins hold the oracle to; the
+    slip-free restatement matches the oracle."""
+    d, m, T, b = 3, 12, 6, 3
+    Q, K, V, eta, W1, W2 = rand_mlp(1, 1, T, d, m, seed=11)
+    Z, A, Bm = oracle.mlp_primal(Q, K, V, eta, W1, W2, b)
+    Zp, Ap, Bp = _mlp_planted(Q[0, 0], K[0, 0], V[0, 0], eta[0], W1[0], W2[0], b, mistake)
+    gap = max(np.max(np.abs(Zp - Z[0, 0])), np.max(np.abs(Ap - A[0, 0])), np.max(np.abs(Bp - Bm[0, 0])))
+    if mistake == "none":
+        assert gap < 1e-12
+    else:
+        assert gap > 1e-6, mistake
