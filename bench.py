@@ -166,14 +166,69 @@ def roofline_summary(names, kernel_ms, kbytes, ms_per_step: float, step_bytes: i
                      "frac": round(step_gbs / hbm_gbs, 4), "frac_of_nominal": round(step_gbs / NOMINAL_HBM_GBS, 4)}}
 
 
+class _Nvml:
+    """The few NVML calls the clock record needs, through ctypes on the driver's
+    libnvidia-ml (no Python NVML package required)."""
+
+    CLOCK_SM = 1
+
+    def __init__(self, uuid: str | None, index: int):
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        ok = False
+        if uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for the device")
+        self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def clock(self) -> int:
+        c = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ctypes.byref(c)) != 0:
+            raise RuntimeError("nvmlDeviceGetClockInfo failed")
+        return int(c.value)
+
+    def max_clock(self) -> int:
+        c = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(c)) != 0:
+            raise RuntimeError("nvmlDeviceGetMaxClockInfo failed")
+        return int(c.value)
+
+    def reasons(self) -> int:
+        r = ctypes.c_ulonglong()
+        if self._reasons(self.h, ctypes.byref(r)) != 0:
+            raise RuntimeError("clock event reasons query failed")
+        return int(r.value)
+
+
+def _device_uuid(index: int):
+    """'GPU-…' UUID of CUDA device `index` (NVML's numbering may differ from CUDA's)."""
+    try:
+        import torch
+        u = getattr(torch.cuda.get_device_properties(index), "uuid", None)
+        if u is None:
+            return None
+        u = str(u)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while the timed region runs."""
+    """Samples the SM clock and the clock event (throttle) reasons while the timed region runs:
+    NVML every ~2 ms (through ctypes), else nvidia-smi every 20 ms. Fewer than 3 samples are
+    reported as unknown, never as clean."""
 
     NAMES = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
              0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
              0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    MIN_SAMPLES = 3
 
-    def __init__(self, index: int, period_s: float = 0.01):
+    def __init__(self, index: int, period_s: float = 0.002):
         self.ok = False
         self.samples = []
         self.reasons = 0
@@ -181,16 +236,13 @@ class ClockSampler:
         self.index = index
         self.mode = None
         self.error = None
+        self.max_mhz = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.nv = _Nvml(_device_uuid(index), index)
+            self.max_mhz = self.nv.max_clock()
             self.ok, self.mode = True, "nvml"
         except Exception as e:  # no NVML: sample nvidia-smi instead
             self.error = repr(e)
-            self.max_mhz = None
             import shutil
             if shutil.which("nvidia-smi"):
                 self.ok, self.mode = True, "nvidia-smi"
@@ -198,8 +250,8 @@ class ClockSampler:
     def _run(self):
         while not self._stop.is_set():
             try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                self.reasons |= self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append(self.nv.clock())
+                self.reasons |= self.nv.reasons()
             except Exception as e:
                 self.error = repr(e)
             time.sleep(self.period)
@@ -222,12 +274,16 @@ class ClockSampler:
     def __enter__(self):
         self._stop = threading.Event()
         if self.mode == "nvml":
+            self.samples.append(self.nv.clock())  # one sample before the timed work is enqueued
+            self.reasons |= self.nv.reasons()
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
         elif self.mode == "nvidia-smi":
             import subprocess
             self._first = threading.Event()
-            self._p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}",
+            uuid = _device_uuid(self.index)
+            self._p = subprocess.Popen(["nvidia-smi", "-i", uuid or str(self.index),
+                                        f"--query-gpu={self.SMI_FIELDS}",
                                         "--format=csv,noheader,nounits", "-lms", "20"],
                                        stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._smi_reader, daemon=True)
@@ -241,6 +297,11 @@ class ClockSampler:
         self._stop.set()
         if self.mode == "nvml":
             self._t.join()
+            try:  # one sample after the timed work has finished
+                self.samples.append(self.nv.clock())
+                self.reasons |= self.nv.reasons()
+            except Exception as e:
+                self.error = repr(e)
         elif self.mode == "nvidia-smi":
             self._p.terminate()
             self._t.join(2.0)
@@ -250,14 +311,19 @@ class ClockSampler:
         med = statistics.median(self.samples) if self.samples else None
         r = {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
              "source": self.mode}
-        if not self.samples and self.error:
+        if len(self.samples) < self.MIN_SAMPLES:
+            r["state"] = "unknown (too few samples in the timed region)"
+        if self.error:
             r["error"] = self.error
         return r
 
-    def rejected(self) -> bool:
+    def rejected(self):
+        """True: throttled or stuck clocks (measure again); None: unknown (too few samples)."""
         r = self.report()
         if set(r["reasons"]) & BAD_REASONS:
             return True
+        if r["samples"] < self.MIN_SAMPLES:
+            return None
         if r["sm_mhz"] and r["sm_max_mhz"] and not r["reasons"] and r["sm_mhz"] < 0.7 * r["sm_max_mhz"]:
             return True
         return False

@@ -173,21 +173,35 @@ TTT_API ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, t
 /*
  * TTT-MLP forward that allocates nothing and takes no workspace. (No
  * counterpart on the pages: it exists for callers that cannot allocate
- * device memory.) The workspace ttt_mlp_fwd needs (a status word and a
- * chunk-start copy of W1, W2 per unit) comes from a fixed 8 MiB array inside
- * the library instead, so at d = 64 at most 64 (batch row, head) units fit;
- * larger requests return TTT_ERR_UNSUPPORTED before anything is enqueued.
+ * device memory, for example code inside a region that must not synchronise
+ * the device, under a memory pool that hands out only the tensors it
+ * manages, or a plain C host that owns just its inputs and outputs.) The
+ * workspace ttt_mlp_fwd needs comes from a fixed array inside the library
+ * instead: a status word, and 8 MiB for the per-unit chunk-start copies of
+ * W1, W2 that only the fp32 SIMT kernel keeps in memory.
+ *   - Limit: the tensor-core kernel (bf16, d = 64, b % 16 == 0) keeps those
+ *     copies on chip and takes any number of units; when the SIMT kernel
+ *     serves the call, at d = 64 at most 64 (batch row, head) units fit.
+ *     Larger requests return TTT_ERR_UNSUPPORTED before anything is enqueued.
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - All calls on a device share it: calls whose kernels overlap on the GPU
  *     race and give wrong results, so order them (one stream, or events).
  *   - The first call on a device looks up the array's address with that
  *     device current; make that first call before any stream capture.
+ *   - A wait that runs out inside the kernel is recorded in the array's own
+ *     status word: read it with ttt_mlp_noalloc_last_device_status().
  * Arguments and results as ttt_mlp_fwd; TTT_ERR_CUDA if the lookup fails.
  */
 TTT_API ttt_status ttt_mlp_fwd_noalloc(const void* Q, const void* K, const void* V, ttt_dtype dt,
                                        const float* eta, const float* W1_0, const float* W2_0, int B,
                                        int H, int T, int d, int b, void* Z, float* W1_out,
                                        float* W2_out, void* stream);
+
+/* Waits for `stream`, then reads and clears the status word of the fixed array
+ * that ttt_mlp_fwd_noalloc uses on the current device: TTT_OK, or the first
+ * error a kernel of the latest such call recorded (TTT_ERR_TIMEOUT). (No
+ * counterpart on the pages.) Allocates nothing. */
+TTT_API ttt_status ttt_mlp_noalloc_last_device_status(void* stream);
 
 /*
  * One TTT-Linear decode token per (batch row, head), in O(d^2) per head.

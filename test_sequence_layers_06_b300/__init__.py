@@ -7,7 +7,7 @@ include/ttt.h and raise on a non-OK status. There is no CPU fallback: if the
 library is missing or no GPU is present the calls fail loudly.
 
 Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_plan, ttt_linear_fwd,
-ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_linear_decode_step, ttt_linear_bwd_workspace_bytes,
+ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_mlp_noalloc_last_device_status, ttt_linear_decode_step, ttt_linear_bwd_workspace_bytes,
 ttt_linear_bwd, ttt_last_device_status, ttt_status_str. The *_fwd_ex forms are reached
 through the options argument.
 """
@@ -26,7 +26,7 @@ PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_SEGMENTED = 0, 1, 2, 3
 
 # Every entry point include/ttt.h declares.
 EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_plan", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
-           "ttt_mlp_fwd_noalloc", "ttt_linear_decode_step", "ttt_linear_bwd_workspace_bytes", "ttt_linear_bwd",
+           "ttt_mlp_fwd_noalloc", "ttt_mlp_noalloc_last_device_status", "ttt_linear_decode_step", "ttt_linear_bwd_workspace_bytes", "ttt_linear_bwd",
            "ttt_last_device_status", "ttt_status_str")
 
 
@@ -73,6 +73,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_mlp_fwd.argtypes = mlp
     lib.ttt_mlp_fwd_ex.argtypes = mlp + [ctypes.POINTER(ttt_options)]
     lib.ttt_mlp_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
+    lib.ttt_mlp_noalloc_last_device_status.argtypes = [vp]
     lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp]
     lib.ttt_last_device_status.argtypes = [vp, vp]
     lib.ttt_linear_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -81,6 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_status_str.argtypes = [i]
     lib.ttt_status_str.restype = ctypes.c_char_p
     for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex", "ttt_mlp_fwd_noalloc",
+              "ttt_mlp_noalloc_last_device_status",
               "ttt_linear_decode_step", "ttt_linear_bwd", "ttt_last_device_status"):
         getattr(lib, f).restype = i
     _lib = lib
@@ -246,8 +248,9 @@ def ttt_mlp_fwd(Q, K, V, eta, W1_0, W2_0, b: int, Z=None, W1_out=None, W2_out=No
 
 
 def ttt_mlp_fwd_noalloc(Q, K, V, eta, W1_0, W2_0, b: int, Z=None, W1_out=None, W2_out=None, stream=None):
-    """TTT-MLP without a workspace (the library's fixed 8 MiB scratch array; at d = 64 up to 64 units).
-    For callers that cannot allocate device memory; calls that overlap on the GPU race."""
+    """TTT-MLP without a workspace, for callers that cannot allocate device memory: the library's fixed
+    scratch array serves instead (any number of units on the tensor-core kernel; at d = 64 up to 64 units
+    on the fp32 SIMT kernel). Calls that overlap on the GPU race on that array."""
     import torch
     lib = load_library()
     B, H, T, d = Q.shape
@@ -270,6 +273,15 @@ def ttt_mlp_fwd_noalloc(Q, K, V, eta, W1_0, W2_0, b: int, Z=None, W1_out=None, W
     if st != TTT_OK:
         raise TTTError("ttt_mlp_fwd_noalloc", st)
     return Z, W1_out, W2_out
+
+
+def ttt_mlp_noalloc_last_device_status(stream=None, device=None) -> int:
+    """Wait for the stream, then read and clear the status word of ttt_mlp_fwd_noalloc's fixed array
+    on `device` (default: the current device)."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with _on_device(dev):
+        return int(load_library().ttt_mlp_noalloc_last_device_status(_stream_ptr(stream, dev)))
 
 
 def ttt_linear_decode_step(q, k, v, eta, W_anchor, W_run, pos: int, b: int, z=None, stream=None):

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ttt.h"
+
 namespace ttt {
 
 struct StatusBlock;
@@ -114,6 +116,20 @@ bool mlp_mma_supported(const MlpParams& p);
 int mlp_mma_tile_rows();
 cudaError_t launch_mlp_mma(const MlpParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            cudaStream_t stream);
+
+// The TTT-MLP forward behind ttt_mlp_fwd(_ex) and ttt_mlp_fwd_noalloc (ttt_api.cu):
+// argument checks, workspace layout and launch. With ws_by_path the workspace
+// need only cover the kernel that serves the call (mlp_workspace_bytes_for_path);
+// otherwise it must cover ttt_workspace_bytes(), which sizes for every kernel.
+ttt_status mlp_forward(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                       const float* W1_0, const float* W2_0, int B, int H, int T, int d, int b, void* Z,
+                       float* W1_out, float* W2_out, void* workspace, size_t ws_bytes, void* stream,
+                       const ttt_options* opt, bool ws_by_path);
+// Whether the tensor-core kernel serves such a call (it keeps the chunk-start
+// weights on chip and uses only the status block of the workspace).
+bool mlp_uses_mma(int T, int d, int b, ttt_dtype dt, const ttt_options* opt);
+// Workspace bytes the kernel that serves such a call uses (0 for invalid sizes).
+size_t mlp_workspace_bytes_for_path(int B, int H, int T, int d, int b, ttt_dtype dt, const ttt_options* opt);
 
 // General fp32-arithmetic TTT-MLP.
 size_t mlp_simt_snapshot_bytes(int units, int d, int m);

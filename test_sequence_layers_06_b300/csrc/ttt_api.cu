@@ -199,6 +199,91 @@ ttt_status reset_status(void* ws, cudaStream_t s) {
 
 }  // namespace
 
+namespace ttt {
+
+// Whether the tensor-core TTT-MLP kernel serves a call with these arguments.
+bool mlp_uses_mma(int T, int d, int b, ttt_dtype dt, const ttt_options* opt) {
+  MlpParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.bf16 = dt == TTT_BF16;
+  p.d = d;
+  p.m = static_cast<int>(mlp_hidden(d));
+  p.b = b;
+  return mlp_mma_supported(p) && T > 0 && (opt == nullptr || opt->force_path != 1);
+}
+
+size_t mlp_workspace_bytes_for_path(int B, int H, int T, int d, int b, ttt_dtype dt, const ttt_options* opt) {
+  if (!sizes_ok(B, H, T, d, b)) return 0;
+  if (mlp_uses_mma(T, d, b, dt, opt)) return kStatusBytes;  // chunk-start copies stay on chip
+  return workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP, nullptr);
+}
+
+// Checks, workspace layout and launch of a TTT-MLP forward. With ws_by_path the
+// workspace need only cover the kernel that serves the call; otherwise it must
+// cover ttt_workspace_bytes() (every kernel).
+ttt_status mlp_forward(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                       const float* W1_0, const float* W2_0, int B, int H, int T, int d, int b, void* Z,
+                       float* W1_out, float* W2_out, void* workspace, size_t ws_bytes, void* stream,
+                       const ttt_options* opt, bool ws_by_path) {
+  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
+  if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
+  if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
+  if (!eta || !W1_0 || !W2_0 || !W1_out || !W2_out || !workspace) return TTT_ERR_ARG;
+  if (T > 0 && (!Q || !K || !V || !Z)) return TTT_ERR_ARG;
+  for (const void* p : {static_cast<const void*>(Q), static_cast<const void*>(K), static_cast<const void*>(V),
+                        static_cast<const void*>(Z), static_cast<const void*>(eta), static_cast<const void*>(W1_0),
+                        static_cast<const void*>(W2_0), static_cast<const void*>(W1_out),
+                        static_cast<const void*>(W2_out), static_cast<const void*>(workspace)})
+    if (p && !aligned16(p)) return TTT_ERR_ARG;
+  const ttt_options o = defaults(opt);
+  if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
+  const size_t need = ws_by_path ? mlp_workspace_bytes_for_path(B, H, T, d, b, dt, opt)
+                                 : workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP, nullptr);
+  if (need == 0 || ws_bytes < need) return TTT_ERR_ARG;
+  {
+    const size_t seq = bytes4(B, H, T, d, dt == TTT_BF16 ? 2 : 4);
+    const size_t w1 = bytes4(d, static_cast<int>(mlp_hidden(d)), 1, 1, 4);
+    if (!outputs_disjoint({{Z, seq}, {W1_out, w1 * B * H}, {W2_out, w1 * B * H}, {workspace, ws_bytes}},
+                          {{Q, seq}, {K, seq}, {V, seq}, {eta, bytes4(H, 1, 1, 1, 4)}, {W1_0, w1 * H}, {W2_0, w1 * H}}))
+      return TTT_ERR_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  ttt::MlpParams p;
+  p.Q = Q; p.K = K; p.V = V; p.Z = Z;
+  p.eta = eta; p.W1_0 = W1_0; p.W2_0 = W2_0; p.W1_out = W1_out; p.W2_out = W2_out;
+  p.snap = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+  p.B = B; p.H = H; p.T = T; p.d = d; p.m = static_cast<int>(mlp_hidden(d)); p.b = b;
+  p.units = B * H;
+  p.bf16 = (dt == TTT_BF16);
+  p.status = static_cast<ttt::StatusBlock*>(workspace);
+  p.timeout_ns = o.wait_timeout_ns;
+  p.inject_stall = o.inject_stall;
+
+  const bool mma_ok = ttt::mlp_mma_supported(p);
+  if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
+  const bool use_mma = mma_ok && o.force_path != 1 && T > 0;
+
+  ttt_status st = reset_status(workspace, s);
+  if (st != TTT_OK) return st;
+  cudaError_t err;
+  if (use_mma) {
+    CUtensorMap mq, mk, mv;
+    const int rows = ttt::mlp_mma_tile_rows();
+    if (!encode_3d(&mq, Q, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mk, K, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
+      return TTT_ERR_CUDA;
+    err = ttt::launch_mlp_mma(p, mq, mk, mv, s);
+  } else {
+    err = ttt::launch_mlp_simt(p, s);
+  }
+  return err == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+
+}  // namespace ttt
+
 extern "C" {
 
 size_t ttt_workspace_bytes(int B, int H, int T, int d, int b, int variant) {
@@ -332,58 +417,8 @@ ttt_status ttt_mlp_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype
                           const float* W1_0, const float* W2_0, int B, int H, int T, int d, int b, void* Z,
                           float* W1_out, float* W2_out, void* workspace, size_t ws_bytes, void* stream,
                           const ttt_options* opt) {
-  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
-  if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
-  if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
-  if (!eta || !W1_0 || !W2_0 || !W1_out || !W2_out || !workspace) return TTT_ERR_ARG;
-  if (T > 0 && (!Q || !K || !V || !Z)) return TTT_ERR_ARG;
-  for (const void* p : {static_cast<const void*>(Q), static_cast<const void*>(K), static_cast<const void*>(V),
-                        static_cast<const void*>(Z), static_cast<const void*>(eta), static_cast<const void*>(W1_0),
-                        static_cast<const void*>(W2_0), static_cast<const void*>(W1_out),
-                        static_cast<const void*>(W2_out), static_cast<const void*>(workspace)})
-    if (p && !aligned16(p)) return TTT_ERR_ARG;
-  if (ws_bytes < workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP, nullptr)) return TTT_ERR_ARG;
-  {
-    const size_t seq = bytes4(B, H, T, d, dt == TTT_BF16 ? 2 : 4);
-    const size_t w1 = bytes4(d, static_cast<int>(mlp_hidden(d)), 1, 1, 4);
-    if (!outputs_disjoint({{Z, seq}, {W1_out, w1 * B * H}, {W2_out, w1 * B * H}, {workspace, ws_bytes}},
-                          {{Q, seq}, {K, seq}, {V, seq}, {eta, bytes4(H, 1, 1, 1, 4)}, {W1_0, w1 * H}, {W2_0, w1 * H}}))
-      return TTT_ERR_ARG;
-  }
-  const ttt_options o = defaults(opt);
-  if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  ttt::MlpParams p;
-  p.Q = Q; p.K = K; p.V = V; p.Z = Z;
-  p.eta = eta; p.W1_0 = W1_0; p.W2_0 = W2_0; p.W1_out = W1_out; p.W2_out = W2_out;
-  p.snap = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
-  p.B = B; p.H = H; p.T = T; p.d = d; p.m = static_cast<int>(mlp_hidden(d)); p.b = b;
-  p.units = B * H;
-  p.bf16 = (dt == TTT_BF16);
-  p.status = static_cast<ttt::StatusBlock*>(workspace);
-  p.timeout_ns = o.wait_timeout_ns;
-  p.inject_stall = o.inject_stall;
-
-  const bool mma_ok = ttt::mlp_mma_supported(p);
-  if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
-  const bool use_mma = mma_ok && o.force_path != 1 && T > 0;
-
-  ttt_status st = reset_status(workspace, s);
-  if (st != TTT_OK) return st;
-  cudaError_t err;
-  if (use_mma) {
-    CUtensorMap mq, mk, mv;
-    const int rows = ttt::mlp_mma_tile_rows();
-    if (!encode_3d(&mq, Q, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&mk, K, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
-      return TTT_ERR_CUDA;
-    err = ttt::launch_mlp_mma(p, mq, mk, mv, s);
-  } else {
-    err = ttt::launch_mlp_simt(p, s);
-  }
-  return err == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+  return ttt::mlp_forward(Q, K, V, dt, eta, W1_0, W2_0, B, H, T, d, b, Z, W1_out, W2_out, workspace, ws_bytes,
+                          stream, opt, false);
 }
 
 ttt_status ttt_mlp_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,

@@ -12,7 +12,7 @@ import torch
 import synth
 import test_sequence_layers_06_b300 as ttt
 from oracle.backward import linear_backward
-from ttt_testlib import rel_l2, to64, torch_inputs
+from ttt_testlib import rel_err, rel_l2, to64, torch_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +42,7 @@ def test_backward_matches_oracle(B, H, T, d, b, eta):
     for name, g, r in zip(("dQ", "dK", "dV", "deta", "dW0"), got, want):
         g = to64(g)
         assert np.all(np.isfinite(g)), name
-        assert rel_l2(g, r) <= 1e-4, (name, rel_l2(g, r))
+        assert rel_err(name, g, r, 1e-4) <= 1e-4, (name, rel_l2(g, r))
 
 
 def test_backward_empty_sequence():

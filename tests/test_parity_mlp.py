@@ -6,7 +6,7 @@ import torch
 
 import synth
 import test_sequence_layers_06_b300 as ttt
-from ttt_testlib import oracle_mlp, rel_l2, to64, tolerance, torch_inputs
+from ttt_testlib import oracle_mlp, rel_err, rel_l2, to64, tolerance, torch_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -28,8 +28,8 @@ def test_mlp_small(T, b, dtype, d):
     Z, W1, W2 = run_mlp(inp, b)
     Zr, W1r, W2r = oracle_mlp(inp, b)
     tol = 1e-4 if dtype == "f32" else tolerance(w)
-    for x, r in ((Z, Zr), (W1, W1r), (W2, W2r)):
-        assert rel_l2(x, r) <= tol, rel_l2(x, r)
+    for name, x, r in (("Z", Z, Zr), ("W1", W1, W1r), ("W2", W2, W2r)):
+        assert rel_err(name, x, r, tol) <= tol, rel_l2(x, r)
 
 
 @pytest.mark.parametrize("T,b", [(96, 32), (80, 48), (130, 64)])
@@ -43,8 +43,8 @@ def test_mlp_tensor_path_chunks_of_several_tiles(T, b):
                                 options={"force_path": ttt.PATH_TENSOR})
     torch.cuda.synchronize()
     Zr, W1r, W2r = oracle_mlp(inp, b)
-    for x, r in ((Z, Zr), (W1, W1r), (W2, W2r)):
-        assert rel_l2(to64(x), r) <= tolerance(w), rel_l2(to64(x), r)
+    for name, x, r in (("Z", Z, Zr), ("W1", W1, W1r), ("W2", W2, W2r)):
+        assert rel_err(name, to64(x), r, tolerance(w)) <= tolerance(w), rel_l2(to64(x), r)
 
 
 def test_mlp_simt_path_bf16_agrees_with_tensor_path():
@@ -72,7 +72,7 @@ def test_mlp_full_size_sampled():
     sub = synth.make_inputs(w, units=units)
     Zr, W1r, W2r = oracle_mlp(sub, w.b)
     for k, (n, h) in enumerate(units):
-        assert rel_l2(to64(Z[n, h]), Zr[0, k]) <= tolerance(w)
-        assert rel_l2(to64(W1[n, h]), W1r[0, k]) <= tolerance(w)
-        assert rel_l2(to64(W2[n, h]), W2r[0, k]) <= tolerance(w)
+        assert rel_err(f"Z unit {n},{h}", to64(Z[n, h]), Zr[0, k], tolerance(w)) <= tolerance(w)
+        assert rel_err(f"W1 unit {n},{h}", to64(W1[n, h]), W1r[0, k], tolerance(w)) <= tolerance(w)
+        assert rel_err(f"W2 unit {n},{h}", to64(W2[n, h]), W2r[0, k], tolerance(w)) <= tolerance(w)
     assert bool(torch.isfinite(Z.float()).all())

@@ -2,6 +2,8 @@
 the library through its binding, call the oracle, compare."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 import oracle
@@ -13,6 +15,22 @@ def rel_l2(x, ref) -> float:
     ref = np.asarray(ref, dtype=np.float64)
     n = np.linalg.norm(ref)
     return float(np.linalg.norm(x - ref) / (n if n > 0 else 1.0))
+
+
+# Every parity comparison's measured error, printed by conftest.py at the end of the run.
+MARGINS: list = []
+
+
+def record_margin(what: str, err: float, bar: float) -> float:
+    """Keep one comparison's rel-L2 and its bar for the end-of-run margin table; returns err."""
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    MARGINS.append({"test": test, "what": what, "err": float(err), "bar": float(bar)})
+    return err
+
+
+def rel_err(what: str, x, ref, bar: float) -> float:
+    """rel_l2(x, ref), recorded against `bar` (the caller still asserts)."""
+    return record_margin(what, rel_l2(x, ref), bar)
 
 
 def worst_unit_rel(x, ref) -> float:
