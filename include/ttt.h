@@ -88,7 +88,13 @@ typedef struct {
                                records on `stream` before its first kernel, after the
                                affine-map kernel, after the combine kernel and after
                                the read-out kernel. On the one-pass path the first
-                               three are recorded back to back. */
+                               three are recorded back to back. Given events, the
+                               segment-parallel form runs in one piece (no overlap). */
+  int32_t pieces;           /* segment-parallel form only: 0 = automatic; 1 = the
+                               three kernels one after another over all segments;
+                               n > 1 = the segments are cut into n pieces and the
+                               affine maps of piece p + 1 run beside the read-out of
+                               piece p (a second stream inside the call) */
 } ttt_options;
 
 /* How a TTT-Linear call with these arguments runs (filled by ttt_linear_plan). */
@@ -99,6 +105,7 @@ typedef struct {
   int32_t kernels;    /* kernels one call enqueues (besides a 16-byte status reset) */
   int32_t affine;     /* path 3: 1 = affine maps by warp-level MMAs (16-token tiles),
                          2 = by tcgen05 tensor cores (64-token steps); else 0 */
+  int32_t pieces;     /* path 3: pieces the segments are cut into (1 = no overlap); else 1 */
 } ttt_plan;
 
 /* Bytes of workspace a call with these sizes needs on the current device
@@ -126,7 +133,10 @@ TTT_API size_t ttt_workspace_bytes_ex(int B, int H, int T, int d, int b, int var
  * the maps are chained from W0 to give every segment's start state, and the
  * segments are then read out side by side. Exact algebra on the chunk update
  * ("5 · TestingTime 训练与长上下文", section 4); results agree with the one-pass
- * form within bf16 rounding. Three kernels are enqueued; otherwise one.
+ * form within bf16 rounding. Three kernels are enqueued, three per piece
+ * when the segments are cut into pieces whose affine maps overlap the
+ * previous piece's read-out (ttt_options.pieces; work on a second stream
+ * that the call joins back into `stream`); otherwise one.
  *   Q, K, V  [B][H][T][d], dtype dt.  eta [H] float32 (per-head inner learning rate).
  *   W0       [H][d][d] float32: initial state per head, shared by the batch
  *            (an outer-loop parameter); every batch row restarts from it.

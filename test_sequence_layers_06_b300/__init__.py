@@ -39,12 +39,12 @@ class TTTError(RuntimeError):
 class ttt_options(ctypes.Structure):
     _fields_ = [("wait_timeout_ns", ctypes.c_uint64), ("inject_stall", ctypes.c_int32),
                 ("force_path", ctypes.c_int32), ("seg_len", ctypes.c_int32),
-                ("phase_events", ctypes.c_void_p)]
+                ("phase_events", ctypes.c_void_p), ("pieces", ctypes.c_int32)]
 
 
 class ttt_plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("seg_len", ctypes.c_int32), ("seg_count", ctypes.c_int32),
-                ("kernels", ctypes.c_int32), ("affine", ctypes.c_int32)]
+                ("kernels", ctypes.c_int32), ("affine", ctypes.c_int32), ("pieces", ctypes.c_int32)]
 
 
 _lib = None
@@ -102,7 +102,7 @@ def ttt_workspace_bytes(B: int, H: int, T: int, d: int, b: int, variant: int = T
 
 
 def ttt_linear_plan(B: int, H: int, T: int, d: int, b: int, dtype: int = TTT_BF16, options=None) -> dict:
-    """How ttt_linear_fwd runs for these sizes: {path, seg_len, seg_count, kernels, affine}."""
+    """How ttt_linear_fwd runs for these sizes: {path, seg_len, seg_count, kernels, affine, pieces}."""
     out = ttt_plan()
     st = load_library().ttt_linear_plan(B, H, T, d, b, dtype, _opts(options), ctypes.byref(out))
     if st != TTT_OK:

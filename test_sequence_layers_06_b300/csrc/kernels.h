@@ -31,6 +31,12 @@ struct LinearParams {
   // shorter) that run side by side from start states the combine step computes.
   int seg_len;
   int seg_count;
+  // The segments one launch covers: [seg_first, seg_first + seg_num) (segments
+  // for the read-out, maps for the affine and combine kernels). A call may
+  // split the range over several launches so that the affine maps of later
+  // segments overlap the read-out of earlier ones.
+  int seg_first;
+  int seg_num;
   float* seg_maps;     // workspace [units][seg_count-1][2][d][d]: (A_s, B_s)
   float* seg_starts;   // workspace [units][seg_count-1][d][d]: start state of segment s+1
   int affine_wy;       // affine maps on the tcgen05 kernel (64-token steps); else warp-level MMAs

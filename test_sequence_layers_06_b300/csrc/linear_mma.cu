@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint64_t* sready = empty + kStages;  // the tile's S fragments are written
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
 
-  const int unit = blockIdx.x / p.seg_count;
-  const int seg = blockIdx.x % p.seg_count;
+  const int unit = blockIdx.x / p.seg_num;
+  const int seg = p.seg_first + blockIdx.x % p.seg_num;
   const int h = unit % p.H;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -283,10 +283,6 @@ __global__ void __launch_bounds__(kThreads, 3)
       mma_bf16_16816(z[0], wr[k], qb0);
       mma_bf16_16816(z[1], wr[k], qb1);
     }
-    // All reads of this stage are in registers: hand it back to the producer.
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       e[nt][0] += e2[nt][0];
@@ -309,6 +305,15 @@ __global__ void __launch_bounds__(kThreads, 3)
     // Read-out part 2: Z^T += (-eta E^T) S^T.
     mma_bf16_16816(z[0], ea, sb0);
     mma_bf16_16816(z[1], ea, sb1);
+
+    // Hand the stage back to the producer, whose next TMA load overwrites it. Only
+    // now has every register loaded from it (K^T for the update, S^T) been consumed,
+    // so no load from the stage is still outstanding; the proxy fence orders these
+    // generic-proxy reads before that async-proxy write. (Releasing it right after
+    // issuing the last ldmatrix let a delayed load read the next tile's K.)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
 
     // Z^T (rows j, columns t) -> Z[t][j] (16 x 16 bf16) in the warp's staging tile
     // by a transposing stmatrix, then one 16-byte store per lane: rows of 32 bytes.
@@ -347,7 +352,8 @@ bool linear_mma_supported(const LinearParams& p) { return p.d == kD && p.b % kTi
 cudaError_t launch_linear_mma(const LinearParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& mv, cudaStream_t stream) {
   if (p.units == 0) return cudaSuccess;
-  linear_mma_kernel<<<p.units * p.seg_count, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (p.seg_num == 0) return cudaSuccess;
+  linear_mma_kernel<<<p.units * p.seg_num, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

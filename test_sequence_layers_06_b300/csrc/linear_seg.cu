@@ -55,8 +55,8 @@ __global__ void __launch_bounds__(kAffThreads, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAffAbortOff);
 
   const int maps = p.seg_count - 1;       // the last segment needs no map
-  const int unit = blockIdx.x / maps;
-  const int seg = blockIdx.x % maps;
+  const int unit = blockIdx.x / p.seg_num;
+  const int seg = p.seg_first + blockIdx.x % p.seg_num;
   const int h = unit % p.H;
   const int t0 = seg * p.seg_len;
   const int num_tiles = p.seg_len / kTile;  // segments with a map are full
@@ -187,9 +187,6 @@ __global__ void __launch_bounds__(kAffThreads, 2)
       kbt[2 * qq + 1][0] = r[2];
       kbt[2 * qq + 1][1] = r[3];
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-
     uint32_t ea[4];
     ea[0] = pack_bf16(neta * (e[0][0] + e2[0][0]), neta * (e[0][1] + e2[0][1]));
     ea[1] = pack_bf16(neta * (e[0][2] + e2[0][2]), neta * (e[0][3] + e2[0][3]));
@@ -198,6 +195,12 @@ __global__ void __launch_bounds__(kAffThreads, 2)
     // X^T += (-eta E^T) K: the chunk's gradient step on both halves.
 #pragma unroll
     for (int q = 0; q < 8; ++q) mma_bf16_16816(Xt[q], ea, kbt[q]);
+    // Release the stage only once every register loaded from it has been consumed
+    // (no load from it outstanding); the proxy fence orders these generic-proxy
+    // reads before the producer's async-proxy refill.
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
 
   // (A_s or B_s)[i][j] = X^T[j][i].
@@ -212,7 +215,8 @@ __global__ void __launch_bounds__(kAffThreads, 2)
   }
 }
 
-// W_start(s + 1) = A_s W_start(s) + B_s for s = 0 .. S-2, with W_start(0) = W0,
+// W_start(s + 1) = A_s W_start(s) + B_s for the maps s of the launch's range
+// (seg_first ..), starting from W0 for the first segment,
 // in fp32. The columns of W are independent, so a CTA serves 8 columns of one
 // unit and a unit's 64 columns spread over 8 CTAs. Thread (i, c) holds row i,
 // columns 4c .. 4c+3 of its CTA's slice.
@@ -232,9 +236,12 @@ __global__ void __launch_bounds__(kCmbThreads) linear_seg_combine_kernel(LinearP
   const int i = tid >> 1;
   const int c = (tid & 1) * 4;
 
-  // W_start(0) = W0[h], this CTA's columns.
-  *reinterpret_cast<float4*>(&sW[i * kCmbCols + c]) =
-      *reinterpret_cast<const float4*>(p.W0 + static_cast<size_t>(h) * kD * kD + i * kD + j0 + c);
+  // W_start(seg_first): W0[h] for the first segment, else what the combine of the
+  // previous maps wrote (this CTA's columns).
+  const float* Ws = p.seg_first == 0
+                        ? p.W0 + static_cast<size_t>(h) * kD * kD
+                        : p.seg_starts + (static_cast<size_t>(unit) * maps + p.seg_first - 1) * kD * kD;
+  *reinterpret_cast<float4*>(&sW[i * kCmbCols + c]) = __ldcg(reinterpret_cast<const float4*>(Ws + i * kD + j0 + c));
 
   // Registers that carry map s into shared memory: A (4096 floats, 8 float4 per
   // thread) and this thread's four entries of B.
@@ -246,8 +253,9 @@ __global__ void __launch_bounds__(kCmbThreads) linear_seg_combine_kernel(LinearP
     for (int r = 0; r < 8; ++r) ra[r] = __ldcg(reinterpret_cast<const float4*>(A) + tid + kCmbThreads * r);
     rb = __ldcg(reinterpret_cast<const float4*>(A + kD * kD + i * kD + j0 + c));
   };
-  if (maps > 0) fetch(0);
-  for (int s = 0; s < maps; ++s) {
+  const int s_end = p.seg_first + p.seg_num;
+  if (p.seg_num > 0) fetch(p.seg_first);
+  for (int s = p.seg_first; s < s_end; ++s) {
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const int f = (tid + kCmbThreads * r) * 4;
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kCmbThreads) linear_seg_combine_kernel(LinearP
     }
     const float4 b = rb;
     __syncthreads();  // sA complete; sW holds W_start(s)
-    if (s + 1 < maps) fetch(s + 1);
+    if (s + 1 < s_end) fetch(s + 1);
     float acc[2][4] = {{b.x, b.y, b.z, b.w}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int k = 0; k < kD; k += 4) {
@@ -286,14 +294,14 @@ bool linear_seg_supported(const LinearParams& p) { return p.d == kD && p.b % kTi
 
 cudaError_t launch_linear_seg_affine(const LinearParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                                      cudaStream_t stream) {
-  const int items = p.units * (p.seg_count - 1);
+  const int items = p.units * p.seg_num;
   if (items == 0) return cudaSuccess;
   linear_seg_affine_kernel<<<items, kAffThreads, kAffSmemBytes, stream>>>(mk, mv, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_linear_seg_combine(const LinearParams& p, cudaStream_t stream) {
-  if (p.seg_count < 2 || p.units == 0) return cudaSuccess;
+  if (p.seg_count < 2 || p.units == 0 || p.seg_num == 0) return cudaSuccess;
   linear_seg_combine_kernel<<<p.units * (kD / kCmbCols), kCmbThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -218,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   int* n_loaded = reinterpret_cast<int*>(smem + kMiscOff + 8);
 
   const int maps = p.seg_count - 1;
-  const int unit = blockIdx.x / maps;
-  const int seg = blockIdx.x % maps;
+  const int unit = blockIdx.x / p.seg_num;
+  const int seg = p.seg_first + blockIdx.x % p.seg_num;
   const int h = unit % p.H;
   const int t0 = seg * p.seg_len;
   const int n = p.seg_len / kStep;                // TMA steps
@@ -499,7 +499,7 @@ int linear_seg_wy_rows() { return kStep; }
 
 cudaError_t launch_linear_seg_affine_wy(const LinearParams& p, const CUtensorMap& mk64, const CUtensorMap& mv64,
                                         cudaStream_t stream) {
-  const int items = p.units * (p.seg_count - 1);
+  const int items = p.units * p.seg_num;
   if (items == 0) return cudaSuccess;
   // The attribute belongs to the current device: set it on every launch, as the
   // other large-shared-memory launchers do (a process may drive several GPUs).

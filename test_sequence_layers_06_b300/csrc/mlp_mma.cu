@@ -233,6 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) report_error(p.status, TTT_ERR_TIMEOUT, kWhereMlpLoad, unit);
       ok = false;
     }
+    // Every thread's reads of the other stage (the previous tile) are complete at the
+    // barrier below; the proxy fence also orders them before the async-proxy TMA write
+    // that refills that stage next.
+    fence_proxy_async_smem();
     if (__syncthreads_or(!ok)) {
       // This tile's load may still be in flight: let it land before the CTA exits.
       if (tid == 0) (void)mbar_wait_bounded(&full[s], (u >> 1) & 1, p.timeout_ns);

@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cstring>
 #include <initializer_list>
+#include <mutex>
 
 #include "ttt.h"
 #include "kernels.h"
@@ -87,14 +88,17 @@ struct LinearPlan {
   int seg_len;    // tokens per segment (a multiple of b)
   int seg_count;  // segments per (batch row, head)
   bool affine_wy; // affine maps on tcgen05 in 64-token steps (else warp-level MMAs)
+  int pieces;     // segment pieces: the affine maps of piece p + 1 overlap the read-out of piece p
 };
 
 constexpr int kSegMinTokens = 256;  // shortest segment the automatic plan makes
 constexpr int kSegWavesTarget = 2;  // read-out work items per resident CTA slot (at most)
 constexpr int kMmaCtasPerSm = 3;    // linear_mma_kernel's occupancy (its launch bounds)
+constexpr int kAutoPieces = 1;      // pieces of the automatic plan
 
 ttt_status plan_linear(int B, int H, int T, int d, int b, bool bf16, const ttt_options& o, LinearPlan* out) {
-  LinearPlan pl{false, T > 0 ? T : 1, 1, false};
+  LinearPlan pl{false, T > 0 ? T : 1, 1, false, 1};
+  if (o.pieces < 0) return TTT_ERR_ARG;
   const bool mma_ok = d == 64 && b % 16 == 0 && bf16;
   if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
   if (o.force_path == 3 && !mma_ok) return TTT_ERR_UNSUPPORTED;
@@ -131,6 +135,9 @@ ttt_status plan_linear(int B, int H, int T, int d, int b, bool bf16, const ttt_o
       pl.seg_len = static_cast<int>(len);
       pl.seg_count = static_cast<int>(count);
       pl.affine_wy = ttt::linear_seg_wy_supported(b, pl.seg_len);
+      // Phase events time each kernel over all segments, so they ask for one piece.
+      const int want = o.phase_events ? 1 : (o.pieces > 0 ? o.pieces : kAutoPieces);
+      pl.pieces = std::max(1, std::min(want, pl.seg_count));
     }
   }
   *out = pl;
@@ -191,6 +198,66 @@ bool encode_3d(CUtensorMap* map, const void* base, int units, int T, int d, int 
                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+
+// A second stream per device for the overlapped segment pieces (created once,
+// non-blocking; work on it is ordered against the caller's stream by events).
+cudaStream_t side_stream() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static cudaStream_t streams[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (streams[dev] == nullptr && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+    streams[dev] = nullptr;
+  return streams[dev];
+}
+
+// The segment-parallel form in `pieces` pieces. Read-out piece p covers segments
+// [r_p, r_{p+1}); it needs the start states up to segment r_{p+1} - 1, i.e. the
+// maps [0, r_{p+1} - 1). Map piece p covers [max(r_p - 1, 0), r_{p+1} - 1) and its
+// combine continues the chain from the start state the previous piece wrote.
+//   stream s:    maps 0, combine 0, read-out 0, wait(combine 1), read-out 1, ...
+//   side stream: wait(maps 0), maps 1, wait(combine 0), combine 1, maps 2, combine 2, ...
+// so the affine maps of piece p + 1 run beside the read-out of piece p. Every
+// kernel waits only for work enqueued before it (stream order and events); no
+// kernel waits for another that runs at the same time.
+template <class MapsFn, class CombineFn, class ReadFn>
+cudaError_t run_in_pieces(int S, int pieces, cudaStream_t s, MapsFn maps, CombineFn combine, ReadFn readout) {
+  constexpr int kMaxPieces = 64;
+  pieces = std::min(pieces, kMaxPieces);
+  cudaStream_t x = side_stream();
+  if (x == nullptr) return cudaErrorUnknown;
+  auto bound = [&](int p) { return static_cast<int>((static_cast<long long>(S) * p) / pieces); };
+  // done[p]: the start states of piece p are written; done[pieces]: maps of piece 0 done.
+  cudaEvent_t done[kMaxPieces + 1] = {};
+  cudaError_t err = cudaSuccess;
+  int made = 0;
+  for (; made <= pieces && err == cudaSuccess; ++made)
+    err = cudaEventCreateWithFlags(&done[made], cudaEventDisableTiming);
+  if (err == cudaSuccess) {
+    const int m1 = bound(1) - 1;
+    if (m1 > 0) err = maps(0, m1, s);
+    if (err == cudaSuccess) err = cudaEventRecord(done[pieces], s);
+    if (err == cudaSuccess && m1 > 0) err = combine(0, m1, s);
+    if (err == cudaSuccess) err = cudaEventRecord(done[0], s);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(x, done[pieces], 0);
+    for (int p = 1; p < pieces && err == cudaSuccess; ++p) {
+      const int m0 = bound(p) - 1, m1p = bound(p + 1) - 1;
+      if (m1p > m0) err = maps(m0, m1p, x);
+      if (err == cudaSuccess) err = cudaStreamWaitEvent(x, done[p - 1], 0);
+      if (err == cudaSuccess && m1p > m0) err = combine(m0, m1p, x);
+      if (err == cudaSuccess) err = cudaEventRecord(done[p], x);
+    }
+    for (int p = 0; p < pieces && err == cudaSuccess; ++p) {
+      if (p > 0) err = cudaStreamWaitEvent(s, done[p], 0);
+      if (err == cudaSuccess) err = readout(bound(p), bound(p + 1), s);
+    }
+  }
+  for (int i = 0; i < made; ++i) cudaEventDestroy(done[i]);  // released once their work completes
+  return err;
 }
 
 ttt_status reset_status(void* ws, cudaStream_t s) {
@@ -322,6 +389,8 @@ ttt_status ttt_linear_plan(int B, int H, int T, int d, int b, ttt_dtype dt, cons
   out->seg_count = pl.seg_count;
   out->kernels = T == 0 ? 0 : (pl.seg_count > 1 ? 3 : 1);
   out->affine = pl.seg_count > 1 ? (pl.affine_wy ? 2 : 1) : 0;
+  out->pieces = pl.pieces;
+  if (pl.seg_count > 1) out->kernels = 3 * pl.pieces;
   return TTT_OK;
 }
 
@@ -365,6 +434,8 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
   p.seg_maps = nullptr;
   p.seg_starts = nullptr;
   p.affine_wy = pl.affine_wy ? 1 : 0;
+  p.seg_first = 0;
+  p.seg_num = pl.seg_count;
   if (pl.seg_count > 1) {
     const size_t per = static_cast<size_t>(p.units) * (pl.seg_count - 1) * d * d;
     p.seg_maps = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
@@ -382,23 +453,44 @@ ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V, ttt_dt
         !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
       return TTT_ERR_CUDA;
     cudaEvent_t* ev = static_cast<cudaEvent_t*>(o.phase_events);
-    err = ev ? cudaEventRecord(ev[0], s) : cudaSuccess;
-    if (err == cudaSuccess && pl.seg_count > 1) {
-      if (pl.affine_wy) {
-        CUtensorMap mk64, mv64;
-        const int rows64 = ttt::linear_seg_wy_rows();
-        if (!encode_3d(&mk64, K, p.units, T, d, rows64, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_3d(&mv64, V, p.units, T, d, rows64, d, CU_TENSOR_MAP_SWIZZLE_128B))
-          return TTT_ERR_CUDA;
-        err = ttt::launch_linear_seg_affine_wy(p, mk64, mv64, s);
-      } else {
-        err = ttt::launch_linear_seg_affine(p, mk, mv, s);
-      }
+    CUtensorMap mk64, mv64;
+    if (pl.seg_count > 1 && pl.affine_wy) {
+      const int rows64 = ttt::linear_seg_wy_rows();
+      if (!encode_3d(&mk64, K, p.units, T, d, rows64, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_3d(&mv64, V, p.units, T, d, rows64, d, CU_TENSOR_MAP_SWIZZLE_128B))
+        return TTT_ERR_CUDA;
     }
-    if (err == cudaSuccess && ev) err = cudaEventRecord(ev[1], s);
-    if (err == cudaSuccess && pl.seg_count > 1) err = ttt::launch_linear_seg_combine(p, s);
-    if (err == cudaSuccess && ev) err = cudaEventRecord(ev[2], s);
-    if (err == cudaSuccess) err = ttt::launch_linear_mma(p, mq, mk, mv, s);
+    // Affine maps [m0, m1), and their combine, on stream `st`.
+    auto maps = [&](int m0, int m1, cudaStream_t st) -> cudaError_t {
+      ttt::LinearParams q = p;
+      q.seg_first = m0;
+      q.seg_num = m1 - m0;
+      return pl.affine_wy ? ttt::launch_linear_seg_affine_wy(q, mk64, mv64, st)
+                          : ttt::launch_linear_seg_affine(q, mk, mv, st);
+    };
+    auto combine = [&](int m0, int m1, cudaStream_t st) -> cudaError_t {
+      ttt::LinearParams q = p;
+      q.seg_first = m0;
+      q.seg_num = m1 - m0;
+      return ttt::launch_linear_seg_combine(q, st);
+    };
+    auto readout = [&](int s0, int s1, cudaStream_t st) -> cudaError_t {
+      ttt::LinearParams q = p;
+      q.seg_first = s0;
+      q.seg_num = s1 - s0;
+      return ttt::launch_linear_mma(q, mq, mk, mv, st);
+    };
+    err = ev ? cudaEventRecord(ev[0], s) : cudaSuccess;
+    if (err == cudaSuccess && pl.seg_count > 1 && pl.pieces > 1) {
+      err = run_in_pieces(pl.seg_count, pl.pieces, s, maps, combine, readout);
+    } else {
+      const int m = pl.seg_count - 1;
+      if (err == cudaSuccess && m > 0) err = maps(0, m, s);
+      if (err == cudaSuccess && ev) err = cudaEventRecord(ev[1], s);
+      if (err == cudaSuccess && m > 0) err = combine(0, m, s);
+      if (err == cudaSuccess && ev) err = cudaEventRecord(ev[2], s);
+      if (err == cudaSuccess) err = readout(0, pl.seg_count, s);
+    }
     if (err == cudaSuccess && ev) err = cudaEventRecord(ev[3], s);
   } else {
     err = ttt::launch_linear_simt(p, s);

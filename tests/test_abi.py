@@ -62,7 +62,15 @@ def test_workspace_bytes_for_the_segment_parallel_form(lib):
 def test_linear_plan(lib):
     assert ttt.ttt_linear_plan(1, 32, 131072, 64, 16)["path"] == 3
     p = ttt.ttt_linear_plan(2, 3, 1000, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 256})
-    assert p == {"path": 3, "seg_len": 256, "seg_count": 4, "kernels": 3, "affine": 2}
+    assert p == {"path": 3, "seg_len": 256, "seg_count": 4, "kernels": 3, "affine": 2, "pieces": 1}
+    # pieces: clamped to the segment count; three kernels per piece; -1 is refused
+    p = ttt.ttt_linear_plan(2, 3, 1000, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 256,
+                                                         "pieces": 3})
+    assert p["pieces"] == 3 and p["kernels"] == 9
+    assert ttt.ttt_linear_plan(2, 3, 1000, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 256,
+                                                            "pieces": 9})["pieces"] == 4
+    with pytest.raises(ttt.TTTError):
+        ttt.ttt_linear_plan(2, 3, 1000, 64, 16, options={"pieces": -1})
     p = ttt.ttt_linear_plan(2, 3, 1000, 64, 16, options={"force_path": ttt.PATH_SEGMENTED, "seg_len": 48})
     assert p["affine"] == 1  # 48-token segments are not whole 64-token steps
     assert ttt.ttt_linear_plan(1, 1, 100, 64, 16)["path"] == 2       # too short to cut

@@ -34,12 +34,14 @@ int main(void) {
   FIELD(ttt_options, force_path);
   FIELD(ttt_options, seg_len);
   FIELD(ttt_options, phase_events);
+  FIELD(ttt_options, pieces);
   printf("sizeof.ttt_plan=%zu\n", sizeof(ttt_plan));
   FIELD(ttt_plan, path);
   FIELD(ttt_plan, seg_len);
   FIELD(ttt_plan, seg_count);
   FIELD(ttt_plan, kernels);
   FIELD(ttt_plan, affine);
+  FIELD(ttt_plan, pieces);
   printf("str.ok=%s\n", ttt_status_str(TTT_OK));
   printf("str.timeout=%s\n", ttt_status_str(TTT_ERR_TIMEOUT));
   printf("ws.linear=%zu\n", ttt_workspace_bytes(2, 3, 100, 64, 16, TTT_VARIANT_LINEAR));

@@ -96,6 +96,58 @@ def test_segment_parallel_path(T, b, seg):
     assert ez <= tolerance(w) and ew <= tolerance(w), (ez, ew, worst_unit_rel(to64(Z), Zr))
 
 
+@pytest.mark.parametrize("pieces,T,seg", [(2, 4096, 512), (3, 4096, 512), (5, 2560, 256), (8, 2048, 256)])
+def test_segment_pieces_are_bit_identical_to_one_piece(pieces, T, seg):
+    """Cutting the segments into pieces (the affine maps of piece p + 1 on a second
+    stream beside the read-out of piece p, the combine continued piece by piece from
+    the stored start states) changes only when each kernel runs, not what it computes:
+    Z and W_out are bit-identical to the one-piece run, and that run matches the oracle."""
+    w = W["linear_125m"].with_(B=2, H=3, T=T, seed=500 + pieces)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    base = {"force_path": ttt.PATH_SEGMENTED, "seg_len": seg}
+    assert ttt.ttt_linear_plan(w.B, w.H, T, w.d, 16, options=dict(base, pieces=pieces))["pieces"] == pieces
+    Z1, W1 = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16, options=dict(base, pieces=1))
+    Zp, Wp = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16, options=dict(base, pieces=pieces))
+    torch.cuda.synchronize()
+    assert torch.equal(Z1.view(torch.int16), Zp.view(torch.int16)) and torch.equal(W1, Wp)
+    Zr, Wr = oracle_linear(inp, 16)
+    assert rel_err("Z", to64(Zp), Zr, tolerance(w)) <= tolerance(w)
+    assert rel_err("W_out", to64(Wp), Wr, tolerance(w)) <= tolerance(w)
+
+
+def test_concurrent_calls_on_two_streams_are_bit_identical():
+    """Two independent calls on two streams at once, and the piecewise form, put tcgen05
+    affine-map CTAs on the same SMs as read-out CTAs. Every result must be bit-identical to a
+    lone call. (A read-out warp that released its stage to the next TMA load before its last
+    load from that stage had completed read the next tile's K once in about eight such runs;
+    a stage is now released only after all of its loaded registers are consumed.)"""
+    w = W["linear_long"].with_(T=32768, seed=61)
+    t = torch_inputs(synth.make_inputs(w, want_exact=False))
+    opts = {"force_path": ttt.PATH_SEGMENTED, "seg_len": 1024}
+
+    def call(stream=None, **extra):
+        Z = torch.empty_like(t["Q"])
+        Wo = torch.empty((w.B, w.H, w.d, w.d), device="cuda")
+        ws = torch.empty(ttt.ttt_workspace_bytes(w.B, w.H, w.T, w.d, w.b, 0, opts), dtype=torch.uint8, device="cuda")
+        ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], w.b, Z=Z, W_out=Wo, workspace=ws,
+                           stream=stream, options=dict(opts, **extra))
+        return Z, Wo, ws
+
+    Zr, Wr, _ = call()
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    runs = []
+    for _ in range(24):
+        runs += [call(s1), call(s2)]
+    for _ in range(8):
+        runs.append(call(pieces=4))
+    torch.cuda.synchronize()
+    for Z, Wo, ws in runs:
+        assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+        assert torch.equal(Z.view(torch.int16), Zr.view(torch.int16)) and torch.equal(Wo, Wr)
+
+
 def test_segment_parallel_equals_one_pass():
     """The two tensor-core forms agree with each other within bf16 rounding."""
     w = W["linear_small"].with_(B=2, H=4, T=2048, seed=41)
