@@ -59,6 +59,9 @@ static_assert(3 * kSmemBytes <= 227 * 1024, "three CTAs per SM");
 
 enum : int { kWhereProducer = 1, kWhereConsumer = 2 };
 
+// kTileChunk: every 16-token tile is a whole chunk (b = 16), so the chunk-start
+// copy of W^T is the running one and no second copy is kept.
+template <bool kTileChunk>
 __global__ void __launch_bounds__(kThreads, 3)
     linear_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                       const __grid_constant__ CUtensorMap mv,
@@ -194,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
 
-  uint32_t wa[4][4];  // bf16 A fragments of the chunk-start W^T (k-step s covers i in [16s, 16s+16))
-  uint32_t wr[4][4];  // bf16 A fragments of the running W^T (read-out)
+  uint32_t wr[4][4];  // bf16 A fragments of the running W^T at the tile start (k-step s: i in [16s, 16s+16))
+  uint32_t wa[4][4];  // ... and of the chunk-start W^T (not kept when every tile is a chunk)
 
   for (int u = 0; u < num_tiles; ++u) {
     const int s = u % kStages;
@@ -212,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 3)
     const uint32_t sK = sQ + kTileBytes;
     const uint32_t sV = sQ + 2 * kTileBytes;
 
-    const bool starts_chunk = ((u * kTile) % p.b) == 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       wr[k][0] = pack_bf16(Wt[2 * k][0], Wt[2 * k][1]);
@@ -220,11 +222,13 @@ __global__ void __launch_bounds__(kThreads, 3)
       wr[k][2] = pack_bf16(Wt[2 * k + 1][0], Wt[2 * k + 1][1]);
       wr[k][3] = pack_bf16(Wt[2 * k + 1][2], Wt[2 * k + 1][3]);
     }
-    if (starts_chunk) {
+    if constexpr (!kTileChunk) {
+      if (((u * kTile) % p.b) == 0) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) wa[k][r] = wr[k][r];
+          for (int r = 0; r < 4; ++r) wa[k][r] = wr[k][r];
+      }
     }
 
     // -V^T as the accumulator of E^T. ldmatrix.trans of the V tile's 8x8 blocks
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
     for (int k = 0; k < 4; ++k)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(k < 2 ? e[nt] : e2[nt], wa[k], kb[nt][k]);
+      for (int nt = 0; nt < 2; ++nt) mma_bf16_16816(k < 2 ? e[nt] : e2[nt], kTileChunk ? wr[k] : wa[k], kb[nt][k]);
 
     // K^T-side B operand for the update (k = t, n = i): kbt[q] for i in [8q, 8q+8).
     uint32_t kbt[8][2];
@@ -273,16 +277,6 @@ __global__ void __launch_bounds__(kThreads, 3)
       kbt[2 * qq + 1][1] = r[3];
     }
 
-    // Read-out part 1: Z^T = W_run^T Q^T (Q as B operand, like K).
-    float z[2][4] = {};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint32_t r[4];
-      ldsm_x4(r, sQ + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
-      uint32_t qb0[2] = {r[0], r[1]}, qb1[2] = {r[2], r[3]};
-      mma_bf16_16816(z[0], wr[k], qb0);
-      mma_bf16_16816(z[1], wr[k], qb1);
-    }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       e[nt][0] += e2[nt][0];
@@ -300,6 +294,19 @@ __global__ void __launch_bounds__(kThreads, 3)
     // W^T += (-eta E^T) K: the state update of the chunk's gradient step.
 #pragma unroll
     for (int q = 0; q < 8; ++q) mma_bf16_16816(Wt[q], ea, kbt[q]);
+
+    // The read-out's products come after the update, so that the update (the serial
+    // chain to the next tile) is issued first; they use the tile-start copy wr.
+    // Read-out part 1: Z^T = W_run^T Q^T (Q as B operand, like K).
+    float z[2][4] = {};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t r[4];
+      ldsm_x4(r, sQ + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
+      uint32_t qb0[2] = {r[0], r[1]}, qb1[2] = {r[2], r[3]};
+      mma_bf16_16816(z[0], wr[k], qb0);
+      mma_bf16_16816(z[1], wr[k], qb1);
+    }
 
     const uint32_t sb0[2] = {sv.x, sv.y}, sb1[2] = {sv.z, sv.w};
     // Read-out part 2: Z^T += (-eta E^T) S^T.
@@ -353,7 +360,10 @@ cudaError_t launch_linear_mma(const LinearParams& p, const CUtensorMap& mq, cons
                               const CUtensorMap& mv, cudaStream_t stream) {
   if (p.units == 0) return cudaSuccess;
   if (p.seg_num == 0) return cudaSuccess;
-  linear_mma_kernel<<<p.units * p.seg_num, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (p.b == kTile)
+    linear_mma_kernel<true><<<p.units * p.seg_num, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    linear_mma_kernel<false><<<p.units * p.seg_num, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
