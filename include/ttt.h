@@ -229,6 +229,59 @@ TTT_API ttt_status ttt_linear_decode_step(const void* q, const void* k, const vo
                                   int d, int pos, int b, void* z, void* stream);
 
 /*
+ * Inner-model variants of TTT-Linear. The pages name these ingredients without
+ * formulas; each call states the reading it computes. All four run one fp32
+ * CUDA kernel per call (linear_variants.cu): one CTA per (batch row, head),
+ * the state in shared memory, any d <= 64 and any b, Q/K/V/Z fp32 or bf16
+ * (dt). They take no workspace (the kernel has no waits and no status word).
+ * Q, K, V, Z, eta, W0, W_out and the per-call arrays follow ttt_linear_fwd's
+ * conventions; per-head vectors are [H][d] float32, shared by the batch rows.
+ * Errors: TTT_ERR_ARG for null/misaligned pointers, bad sizes or outputs that
+ * overlap an input or each other; TTT_ERR_UNSUPPORTED for d > 64;
+ * TTT_ERR_CUDA if the launch fails.
+ *
+ * ttt_linear_bias_fwd: f(k) = k W + beta ("Test-Time Training (TTT) guide",
+ * section 3, writes f(W, x) = W x + b). (W, beta) are trained together by the
+ * chunk rule on 1/2 ||k W + beta - v||^2: e = k W_a + beta_a - v at the
+ * chunk-start weights, W -= eta k^T e, beta -= eta e; read-out
+ * z_t = q_t W_t + beta_t. beta0 [H][d] in, beta_out [B][H][d] out.
+ */
+TTT_API ttt_status ttt_linear_bias_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                       const float* eta, const float* W0, const float* beta0, int B,
+                                       int H, int T, int d, int b, void* Z, float* W_out,
+                                       float* beta_out, void* stream);
+
+/* ttt_linear_token_eta_fwd: a learning rate per token ("5 · TestingTime
+ * 训练与长上下文", section 3.1, lists a learnable learning rate). eta_tok
+ * [B][H][T] float32 >= 0 scales token t's gradient in the chunk rule:
+ * W -= eta_t k_t^T (k_t W_a - v_t); read-out z_t = q_t W_t. */
+TTT_API ttt_status ttt_linear_token_eta_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                            const float* eta_tok, const float* W0, int B, int H, int T,
+                                            int d, int b, void* Z, float* W_out, void* stream);
+
+/* ttt_linear_ln_fwd: a layer norm and a residual inside f (same page, section
+ * 3.1): f(k) = k + LN(k W), LN(y) = gamma (y - mean y) / sqrt(var y + 1e-6)
+ * + beta over the d features of a token (biased variance), gamma, beta [H][d].
+ * Trained by the chunk rule on 1/2 ||f(k) - v||^2 (gradient through LN at the
+ * chunk-start W); read-out z_t = q_t + LN(q_t W_t). */
+TTT_API ttt_status ttt_linear_ln_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                     const float* eta, const float* W0, const float* gamma,
+                                     const float* beta, int B, int H, int T, int d, int b, void* Z,
+                                     float* W_out, void* stream);
+
+/* ttt_linear_momentum_fwd: momentum gradient descent with chunk-start
+ * gradients ("推理时的“临阵磨枪”：Test-Time Training如何教会AI“边做边学”",
+ * sections 2.3 and 5.1, keep a momentum state beside W; the page leaves its
+ * update function undefined). Per token t of a chunk with start state W_a:
+ * g_t = k_t^T (k_t W_a - v_t), M = beta M + (1 - beta) g_t, W -= alpha M,
+ * z_t = q_t W. M starts at zero for every sequence and carries across chunks.
+ * alpha, beta [H]; M_out [B][H][d][d] the final momentum. */
+TTT_API ttt_status ttt_linear_momentum_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                           const float* alpha, const float* beta, const float* W0, int B,
+                                           int H, int T, int d, int b, void* Z, float* W_out, float* M_out,
+                                           void* stream);
+
+/*
  * Backward of ttt_linear_fwd: the vector-Jacobian product of (Z, W_out) with
  * respect to (Q, K, V, eta, W0), for training the outer loop ("5 · TestingTime
  * 训练与长上下文", section 2.2: W0 and the projections that make Q, K, V are

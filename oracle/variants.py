@@ -36,6 +36,17 @@ layer_norm; primal equals dual; eta = 0 and gamma = 0 in closed form.
 
 Momentum. momentum_primal and momentum_dual hold the E²-TTT-style variant
 (momentum gradient descent with chunk-start gradients); see momentum_primal.
+
+Bias. "Test-Time Training (TTT) guide" (section 3) writes the linear inner
+model with a bias, f(W, x) = W x + b. bias_primal trains (W, beta) together by
+the same chunk rule on 1/2 ||k W + beta - v||^2 (row vectors): the gradient of
+one token is (k^T e, e) with e = k W_a + beta_a - v at the chunk-start
+weights, and the read-out is z_t = q_t W_t + beta_t.
+
+Per-token learning rate. The ablation ladder of "5 · TestingTime 训练与长上下文"
+(section 3.1) names a learnable learning rate. token_eta_primal reads it as a
+rate eta_t per token (per batch row and head) that scales that token's gradient
+in the chunk rule: W <- W - eta_t k_t^T (k_t W_a - v_t), read-out q_t W_t.
 """
 from __future__ import annotations
 
@@ -192,3 +203,54 @@ def momentum_dual(Q, K, V, alpha, beta, W0, b: int):
                 W = W_new
             W_out[n, h], M_out[n, h] = W, M
     return Z, W_out, M_out
+
+
+# ---------------------------------------------------------------------------- bias
+def bias_primal(Q, K, V, eta, W0, beta0, b: int):
+    """TTT-Linear with a bias, f(k) = k W + beta, token by token (see the module
+    docstring). Q, K, V [B,H,T,d]; eta [H]; W0 [H,d,d]; beta0 [H,d] (shared by the
+    batch rows, like W0). Returns Z [B,H,T,d], the final W [B,H,d,d] and beta [B,H,d]."""
+    Q, K, V, eta, W0, beta0 = map(_f64, (Q, K, V, eta, W0, beta0))
+    B, H, T, d = Q.shape
+    if b < 1:
+        raise ValueError("b must be positive")
+    Z = np.zeros_like(Q)
+    W_out, beta_out = np.zeros((B, H, d, d)), np.zeros((B, H, d))
+    for n in range(B):
+        for h in range(H):
+            W, be = W0[h].copy(), beta0[h].copy()
+            Wa, ba = W, be
+            for t in range(T):
+                if t % b == 0:
+                    Wa, ba = W.copy(), be.copy()
+                e = K[n, h, t] @ Wa + ba - V[n, h, t]
+                W = W - eta[h] * np.outer(K[n, h, t], e)
+                be = be - eta[h] * e
+                Z[n, h, t] = Q[n, h, t] @ W + be
+            W_out[n, h], beta_out[n, h] = W, be
+    return Z, W_out, beta_out
+
+
+# ---------------------------------------------------------------------------- per-token rate
+def token_eta_primal(Q, K, V, eta_t, W0, b: int):
+    """TTT-Linear with a learning rate per token, token by token (see the module
+    docstring). Q, K, V [B,H,T,d]; eta_t [B,H,T]; W0 [H,d,d]. Returns Z [B,H,T,d]
+    and the final W [B,H,d,d]."""
+    Q, K, V, eta_t, W0 = map(_f64, (Q, K, V, eta_t, W0))
+    B, H, T, d = Q.shape
+    assert eta_t.shape == (B, H, T)
+    if b < 1:
+        raise ValueError("b must be positive")
+    Z = np.zeros_like(Q)
+    W_out = np.zeros((B, H, d, d))
+    for n in range(B):
+        for h in range(H):
+            W = W0[h].copy()
+            Wa = W
+            for t in range(T):
+                if t % b == 0:
+                    Wa = W.copy()
+                W = W - eta_t[n, h, t] * np.outer(K[n, h, t], K[n, h, t] @ Wa - V[n, h, t])
+                Z[n, h, t] = Q[n, h, t] @ W
+            W_out[n, h] = W
+    return Z, W_out

@@ -7,6 +7,7 @@ include/ttt.h and raise on a non-OK status. There is no CPU fallback: if the
 library is missing or no GPU is present the calls fail loudly.
 
 Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_plan, ttt_linear_fwd,
+ttt_linear_bias_fwd, ttt_linear_token_eta_fwd, ttt_linear_ln_fwd, ttt_linear_momentum_fwd,
 ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_mlp_noalloc_last_device_status, ttt_linear_decode_step, ttt_linear_bwd_workspace_bytes,
 ttt_linear_bwd, ttt_last_device_status, ttt_status_str. The *_fwd_ex forms are reached
 through the options argument.
@@ -27,7 +28,8 @@ PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_SEGMENTED = 0, 1, 2, 3
 # Every entry point include/ttt.h declares.
 EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_plan", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
            "ttt_mlp_fwd_noalloc", "ttt_mlp_noalloc_last_device_status", "ttt_linear_decode_step", "ttt_linear_bwd_workspace_bytes", "ttt_linear_bwd",
-           "ttt_last_device_status", "ttt_status_str")
+           "ttt_last_device_status", "ttt_status_str", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
+           "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd")
 
 
 class TTTError(RuntimeError):
@@ -79,10 +81,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_linear_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.ttt_linear_bwd_workspace_bytes.restype = sz
     lib.ttt_linear_bwd.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.ttt_linear_bias_fwd.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
+    lib.ttt_linear_token_eta_fwd.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp]
+    lib.ttt_linear_ln_fwd.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, i, vp, vp, vp]
+    lib.ttt_linear_momentum_fwd.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
     lib.ttt_status_str.argtypes = [i]
     lib.ttt_status_str.restype = ctypes.c_char_p
     for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex", "ttt_mlp_fwd_noalloc",
-              "ttt_mlp_noalloc_last_device_status",
+              "ttt_mlp_noalloc_last_device_status", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
+              "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd",
               "ttt_linear_decode_step", "ttt_linear_bwd", "ttt_last_device_status"):
         getattr(lib, f).restype = i
     _lib = lib
@@ -282,6 +289,71 @@ def ttt_mlp_noalloc_last_device_status(stream=None, device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with _on_device(dev):
         return int(load_library().ttt_mlp_noalloc_last_device_status(_stream_ptr(stream, dev)))
+
+
+def _variant_prologue(Q, K, V, W0):
+    import torch
+    B, H, T, d = Q.shape
+    dev = Q.device
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _check(t, n, Q.dtype, (B, H, T, d), dev)
+    _check(W0, "W0", torch.float32, (H, d, d), dev)
+    Z = torch.empty_like(Q)
+    W_out = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    return B, H, T, d, dev, Z, W_out
+
+
+def _variant_call(name, *args, dev):
+    with _on_device(dev):
+        st = getattr(load_library(), name)(*args)
+    if st != TTT_OK:
+        raise TTTError(name, st)
+
+
+def ttt_linear_bias_fwd(Q, K, V, eta, W0, beta0, b: int, stream=None):
+    """TTT-Linear with f(k) = k W + beta; returns (Z, W_out, beta_out)."""
+    import torch
+    B, H, T, d, dev, Z, W_out = _variant_prologue(Q, K, V, W0)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(beta0, "beta0", torch.float32, (H, d), dev)
+    beta_out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    _variant_call("ttt_linear_bias_fwd", _p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), _p(beta0), B, H, T,
+                  d, int(b), _p(Z), _p(W_out), _p(beta_out), _stream_ptr(stream, dev), dev=dev)
+    return Z, W_out, beta_out
+
+
+def ttt_linear_token_eta_fwd(Q, K, V, eta_tok, W0, b: int, stream=None):
+    """TTT-Linear with a learning rate per token, eta_tok [B, H, T]; returns (Z, W_out)."""
+    import torch
+    B, H, T, d, dev, Z, W_out = _variant_prologue(Q, K, V, W0)
+    _check(eta_tok, "eta_tok", torch.float32, (B, H, T), dev)
+    _variant_call("ttt_linear_token_eta_fwd", _p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta_tok), _p(W0), B, H, T, d,
+                  int(b), _p(Z), _p(W_out), _stream_ptr(stream, dev), dev=dev)
+    return Z, W_out
+
+
+def ttt_linear_ln_fwd(Q, K, V, eta, W0, gamma, beta, b: int, stream=None):
+    """TTT-Linear with f(k) = k + LN(k W) (gamma, beta [H, d]); returns (Z, W_out)."""
+    import torch
+    B, H, T, d, dev, Z, W_out = _variant_prologue(Q, K, V, W0)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(gamma, "gamma", torch.float32, (H, d), dev)
+    _check(beta, "beta", torch.float32, (H, d), dev)
+    _variant_call("ttt_linear_ln_fwd", _p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), _p(gamma), _p(beta), B,
+                  H, T, d, int(b), _p(Z), _p(W_out), _stream_ptr(stream, dev), dev=dev)
+    return Z, W_out
+
+
+def ttt_linear_momentum_fwd(Q, K, V, alpha, beta, W0, b: int, stream=None):
+    """TTT-Linear with momentum gradient descent (alpha, beta [H]); returns (Z, W_out, M_out)."""
+    import torch
+    B, H, T, d, dev, Z, W_out = _variant_prologue(Q, K, V, W0)
+    _check(alpha, "alpha", torch.float32, (H,), dev)
+    _check(beta, "beta", torch.float32, (H,), dev)
+    M_out = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    _variant_call("ttt_linear_momentum_fwd", _p(Q), _p(K), _p(V), _dtype_code(Q), _p(alpha), _p(beta), _p(W0), B, H,
+                  T, d, int(b), _p(Z), _p(W_out), _p(M_out), _stream_ptr(stream, dev), dev=dev)
+    return Z, W_out, M_out
 
 
 def ttt_linear_decode_step(q, k, v, eta, W_anchor, W_run, pos: int, b: int, z=None, stream=None):

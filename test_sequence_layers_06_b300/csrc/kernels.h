@@ -82,6 +82,28 @@ struct LinearBwdParams {
   float* partial;  // workspace [units][d*d + 1]: per-unit dW0, then d eta
 };
 
+// Inner-model variants of TTT-Linear (linear_variants.cu), fp32 arithmetic.
+enum : int { kVarBias = 1, kVarTokenEta = 2, kVarLn = 3, kVarMomentum = 4 };
+struct VariantParams {
+  const void* Q;
+  const void* K;
+  const void* V;
+  void* Z;
+  const float* rate;      // [H]: eta (bias, LN) or alpha (momentum); unused for per-token rates
+  const float* mbeta;     // [H]: momentum coefficient beta (momentum only)
+  const float* tok_rate;  // [B][H][T]: per-token learning rate (per-token variant only)
+  const float* W0;        // [H][d][d]
+  const float* vec0;      // [H][d]: beta0 (bias) or gamma (LN)
+  const float* vec1;      // [H][d]: beta (LN)
+  float* W_out;           // [B][H][d][d]
+  float* aux_out;         // [B][H][d] final bias, or [B][H][d][d] final momentum
+  int B, H, T, d, b;
+  int units;
+  bool bf16;
+  int variant;            // kVar*
+};
+cudaError_t launch_linear_variant(const VariantParams& p, cudaStream_t stream);
+
 struct DecodeParams {
   const void* q;
   const void* k;

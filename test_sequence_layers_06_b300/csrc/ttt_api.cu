@@ -546,6 +546,76 @@ ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, t
                                                                                            : TTT_ERR_CUDA;
 }
 
+// Shared checks and launch of the inner-model variants (linear_variants.cu).
+static ttt_status variant_fwd(int variant, const void* Q, const void* K, const void* V, ttt_dtype dt,
+                              const float* rate, const float* mbeta, const float* tok_rate, const float* W0,
+                              const float* vec0, const float* vec1, int B, int H, int T, int d, int b, void* Z,
+                              float* W_out, float* aux_out, void* stream) {
+  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
+  if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
+  if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
+  const bool needs_rate = variant != ttt::kVarTokenEta, needs_beta = variant == ttt::kVarMomentum;
+  const bool needs_tok = variant == ttt::kVarTokenEta;
+  const bool needs_v0 = variant == ttt::kVarBias || variant == ttt::kVarLn, needs_v1 = variant == ttt::kVarLn;
+  const bool needs_aux = variant == ttt::kVarBias || variant == ttt::kVarMomentum;
+  if (!W0 || !W_out || (needs_rate && !rate) || (needs_beta && !mbeta) || (needs_v0 && !vec0) ||
+      (needs_v1 && !vec1) || (needs_aux && !aux_out))
+    return TTT_ERR_ARG;
+  if (T > 0 && (!Q || !K || !V || !Z || (needs_tok && !tok_rate))) return TTT_ERR_ARG;
+  for (const void* p : {Q, K, V, static_cast<const void*>(Z), static_cast<const void*>(rate),
+                        static_cast<const void*>(mbeta), static_cast<const void*>(tok_rate),
+                        static_cast<const void*>(W0), static_cast<const void*>(vec0),
+                        static_cast<const void*>(vec1), static_cast<const void*>(W_out),
+                        static_cast<const void*>(aux_out)})
+    if (p && !aligned16(p)) return TTT_ERR_ARG;
+  {
+    const size_t seq = bytes4(B, H, T, d, dt == TTT_BF16 ? 2 : 4), hv = bytes4(H, 1, 1, 1, 4);
+    const size_t aux = variant == ttt::kVarBias ? bytes4(B, H, d, 1, 4) : bytes4(B, H, d, d, 4);
+    if (!outputs_disjoint({{Z, seq}, {W_out, bytes4(B, H, d, d, 4)}, {aux_out, needs_aux ? aux : 0}},
+                          {{Q, seq}, {K, seq}, {V, seq}, {rate, needs_rate ? hv : 0}, {mbeta, needs_beta ? hv : 0},
+                           {tok_rate, needs_tok ? bytes4(B, H, T, 1, 4) : 0}, {W0, bytes4(H, d, d, 1, 4)},
+                           {vec0, needs_v0 ? bytes4(H, d, 1, 1, 4) : 0}, {vec1, needs_v1 ? bytes4(H, d, 1, 1, 4) : 0}}))
+      return TTT_ERR_ARG;
+  }
+  ttt::VariantParams p;
+  p.Q = Q; p.K = K; p.V = V; p.Z = Z;
+  p.rate = rate; p.mbeta = mbeta; p.tok_rate = tok_rate; p.W0 = W0; p.vec0 = vec0; p.vec1 = vec1;
+  p.W_out = W_out; p.aux_out = aux_out;
+  p.B = B; p.H = H; p.T = T; p.d = d; p.b = b;
+  p.units = B * H;
+  p.bf16 = dt == TTT_BF16;
+  p.variant = variant;
+  return ttt::launch_linear_variant(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_linear_bias_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                               const float* W0, const float* beta0, int B, int H, int T, int d, int b, void* Z,
+                               float* W_out, float* beta_out, void* stream) {
+  return variant_fwd(ttt::kVarBias, Q, K, V, dt, eta, nullptr, nullptr, W0, beta0, nullptr, B, H, T, d, b, Z, W_out,
+                     beta_out, stream);
+}
+
+ttt_status ttt_linear_token_eta_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta_tok,
+                                    const float* W0, int B, int H, int T, int d, int b, void* Z, float* W_out,
+                                    void* stream) {
+  return variant_fwd(ttt::kVarTokenEta, Q, K, V, dt, nullptr, nullptr, eta_tok, W0, nullptr, nullptr, B, H, T, d, b,
+                     Z, W_out, nullptr, stream);
+}
+
+ttt_status ttt_linear_ln_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                             const float* W0, const float* gamma, const float* beta, int B, int H, int T, int d,
+                             int b, void* Z, float* W_out, void* stream) {
+  return variant_fwd(ttt::kVarLn, Q, K, V, dt, eta, nullptr, nullptr, W0, gamma, beta, B, H, T, d, b, Z, W_out,
+                     nullptr, stream);
+}
+
+ttt_status ttt_linear_momentum_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* alpha,
+                                   const float* beta, const float* W0, int B, int H, int T, int d, int b, void* Z,
+                                   float* W_out, float* M_out, void* stream) {
+  return variant_fwd(ttt::kVarMomentum, Q, K, V, dt, alpha, beta, nullptr, W0, nullptr, nullptr, B, H, T, d, b, Z,
+                     W_out, M_out, stream);
+}
+
 size_t ttt_linear_bwd_workspace_bytes(int B, int H, int T, int d, int b) {
   if (!sizes_ok(B, H, T, d, b)) return 0;
   return kStatusBytes + round_up(ttt::linear_bwd_scratch_bytes(B * H, T, d, b), 16);

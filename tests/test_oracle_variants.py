@@ -12,6 +12,14 @@ The momentum variant (momentum gradient descent with chunk-start gradients) is
 checked token by token against its closed-form dual, against the C oracle's
 TTT-Linear at beta = 0, against torch autograd for every gradient, and at a zero
 rate.
+
+The bias variant (f(k) = k W + beta) is checked against the C oracle's plain
+TTT-Linear on keys and queries extended by a constant 1 (an independent
+implementation of the same chunk rule), its gradient against central finite
+differences of 1/2 ||k W + beta - v||^2, and at eta = 0 against q W0 + beta0.
+The per-token learning rate is checked against the C oracle at a constant rate,
+against the C oracle with keys and values scaled by sqrt(eta_t) (the gradient of
+token t picks up eta_t exactly once), and at eta_t = 0.
 """
 import numpy as np
 import pytest
@@ -194,3 +202,90 @@ def test_momentum_with_zero_rate_reads_out_w0():
     Q, K, V, _, beta, W0 = momentum_case(1, 2, 7, 3, seed=4)
     Z, W, M = momentum_primal(Q, K, V, np.zeros(2), beta, W0, 3)
     assert np.array_equal(W[0], W0) and np.allclose(Z[0], np.einsum("htd,hde->hte", Q[0], W0), atol=1e-14)
+
+
+# ---------------------------------------------------------------------------- bias
+def _bias_case(B, H, T, d, seed):
+    g = np.random.default_rng(seed)
+    Q, K, V = (g.standard_normal((B, H, T, d)) * 0.7 for _ in range(3))
+    return Q, K, V, g.uniform(0.05, 0.4, H), g.standard_normal((H, d, d)) * 0.3, g.standard_normal((H, d)) * 0.3
+
+
+@pytest.mark.parametrize("T,b", [(13, 1), (17, 4), (20, 20)])
+def test_bias_equals_c_oracle_on_a_constant_extra_input(T, b):
+    import oracle
+    from oracle.variants import bias_primal
+    B, H, d = 2, 2, 5
+    Q, K, V, eta, W0, beta0 = _bias_case(B, H, T, d, 70 + T + b)
+    Z, W, be = bias_primal(Q, K, V, eta, W0, beta0, b)
+    one, zero = np.ones((B, H, T, 1)), np.zeros((B, H, T, 1))
+    W0x = np.zeros((H, d + 1, d + 1))
+    W0x[:, :d, :d], W0x[:, d, :d] = W0, beta0
+    Zx, Wx = oracle.linear_primal(np.concatenate([Q, one], 3), np.concatenate([K, one], 3),
+                                  np.concatenate([V, zero], 3), eta, W0x, b)
+    assert np.allclose(Zx[..., :d], Z, atol=1e-12)
+    assert np.allclose(Wx[:, :, :d, :d], W, atol=1e-12) and np.allclose(Wx[:, :, d, :d], be, atol=1e-12)
+
+
+def test_bias_gradient_equals_finite_differences():
+    """One token, b = 1: the step taken equals -eta times the central-difference gradient of
+    1/2 ||k W + beta - v||^2 with respect to W and beta."""
+    from oracle.variants import bias_primal
+    g = np.random.default_rng(3)
+    d, eta = 4, 0.3
+    q, k, v = (g.standard_normal(d) for _ in range(3))
+    W, be = g.standard_normal((d, d)) * 0.4, g.standard_normal(d) * 0.4
+    _, W1, b1 = bias_primal(q[None, None, None], k[None, None, None], v[None, None, None], np.array([eta]),
+                            W[None], be[None], 1)
+    f = lambda W_, b_: 0.5 * np.sum((k @ W_ + b_ - v) ** 2)
+    h = 1e-6
+    gW = np.zeros_like(W)
+    for i in range(d):
+        for j in range(d):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[i, j] += h
+            Wm[i, j] -= h
+            gW[i, j] = (f(Wp, be) - f(Wm, be)) / (2 * h)
+    gb = np.array([(f(W, be + h * np.eye(d)[j]) - f(W, be - h * np.eye(d)[j])) / (2 * h) for j in range(d)])
+    assert np.allclose(W1[0, 0], W - eta * gW, atol=1e-8)
+    assert np.allclose(b1[0, 0], be - eta * gb, atol=1e-8)
+
+
+def test_bias_eta_zero_reads_out_the_initial_model():
+    from oracle.variants import bias_primal
+    Q, K, V, _, W0, beta0 = _bias_case(1, 2, 9, 4, 5)
+    Z, W, be = bias_primal(Q, K, V, np.zeros(2), W0, beta0, 3)
+    assert np.allclose(Z, np.einsum("nhti,hij->nhtj", Q, W0) + beta0[None, :, None, :], atol=1e-14)
+    assert np.array_equal(W[0], W0) and np.array_equal(be[0], beta0)
+
+
+# ---------------------------------------------------------------------------- per-token rate
+@pytest.mark.parametrize("T,b", [(11, 1), (19, 4), (16, 16)])
+def test_token_eta_equals_c_oracle_at_a_constant_rate(T, b):
+    import oracle
+    from oracle.variants import token_eta_primal
+    B, H, d = 2, 3, 4
+    Q, K, V, eta, W0, _ = _bias_case(B, H, T, d, 90 + T)
+    et = np.broadcast_to(eta[None, :, None], (B, H, T)).copy()
+    Z, W = token_eta_primal(Q, K, V, et, W0, b)
+    Zr, Wr = oracle.linear_primal(Q, K, V, eta, W0, b)
+    assert np.allclose(Z, Zr, atol=1e-12) and np.allclose(W, Wr, atol=1e-12)
+
+
+def test_token_eta_equals_c_oracle_on_scaled_keys_and_values():
+    import oracle
+    from oracle.variants import token_eta_primal
+    B, H, T, d, b = 2, 2, 23, 5, 4
+    Q, K, V, _, W0, _ = _bias_case(B, H, T, d, 11)
+    et = np.random.default_rng(12).uniform(0.0, 0.5, (B, H, T))
+    Z, W = token_eta_primal(Q, K, V, et, W0, b)
+    r = np.sqrt(et)[..., None]
+    Zs, Ws = oracle.linear_primal(Q, r * K, r * V, np.ones(H), W0, b)
+    assert np.allclose(Z, Zs, atol=1e-12) and np.allclose(W, Ws, atol=1e-12)
+
+
+def test_token_eta_zero_reads_out_w0():
+    from oracle.variants import token_eta_primal
+    Q, K, V, _, W0, _ = _bias_case(1, 2, 7, 3, 13)
+    Z, W = token_eta_primal(Q, K, V, np.zeros((1, 2, 7)), W0, 2)
+    assert np.allclose(Z, np.einsum("nhti,hij->nhtj", Q, W0), atol=1e-14) and np.array_equal(W[0], W0)

@@ -1,0 +1,121 @@
+"""Inner-model variants of TTT-Linear on the GPU (through the C ABI) against the
+fp64 oracle of oracle/variants.py (pinned in test_oracle_variants.py): a bias in
+f, a learning rate per token, a layer norm and a residual inside f, and
+momentum gradient descent with chunk-start gradients. Bars: rel-L2 <= 1e-4 with
+fp32 operands, <= 2e-2 with bf16 operands (fp32 state and arithmetic)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import test_sequence_layers_06_b300 as ttt
+from oracle.variants import bias_primal, ln_residual_primal, momentum_primal, token_eta_primal
+from ttt_testlib import rel_err, to64, tolerance, torch_inputs
+
+pytestmark = pytest.mark.gpu
+
+CASES = [(16, 40, 16, "f32"), (64, 70, 5, "f32"), (32, 37, 1, "f32"), (64, 100, 16, "bf16"), (63, 50, 64, "bf16"),
+         (64, 130, 64, "f32")]
+
+
+def inputs(d, T, dtype, seed, B=2, H=3):
+    w = synth.WORKLOADS["linear_small"].with_(B=B, H=H, T=T, d=d, dtype=dtype, seed=seed)
+    inp = synth.make_inputs(w)
+    return w, inp, torch_inputs(inp)
+
+
+def check(name, got, want, w):
+    bar = tolerance(w)
+    for label, g, r in zip(name.split(","), got, want):
+        assert np.all(np.isfinite(to64(g))), label
+        assert rel_err(label, to64(g), r, bar) <= bar, label
+
+
+@pytest.mark.parametrize("d,T,b,dtype", CASES)
+def test_bias_matches_oracle(d, T, b, dtype):
+    w, inp, t = inputs(d, T, dtype, 700 + d + T + b)
+    beta0 = np.random.default_rng(d + T).standard_normal((w.H, d)).astype(np.float32) * 0.3
+    got = ttt.ttt_linear_bias_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(beta0).cuda(), b)
+    torch.cuda.synchronize()
+    want = bias_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, beta0, b)
+    check("Z,W_out,beta_out", got, want, w)
+
+
+@pytest.mark.parametrize("d,T,b,dtype", CASES)
+def test_token_eta_matches_oracle(d, T, b, dtype):
+    w, inp, t = inputs(d, T, dtype, 710 + d + T + b)
+    et = np.random.default_rng(T).uniform(0.0, 0.5, (w.B, w.H, T)).astype(np.float32)
+    got = ttt.ttt_linear_token_eta_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(et).cuda(), t["W0"], b)
+    torch.cuda.synchronize()
+    want = token_eta_primal(inp.q64, inp.k64, inp.v64, et, inp.W0_64, b)
+    check("Z,W_out", got, want, w)
+
+
+@pytest.mark.parametrize("d,T,b,dtype", CASES)
+def test_layer_norm_residual_matches_oracle(d, T, b, dtype):
+    w, inp, t = inputs(d, T, dtype, 720 + d + T + b)
+    g = np.random.default_rng(d * T)
+    gamma = (1.0 + 0.2 * g.standard_normal((w.H, d))).astype(np.float32)
+    beta = (0.1 * g.standard_normal((w.H, d))).astype(np.float32)
+    got = ttt.ttt_linear_ln_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(gamma).cuda(),
+                                torch.from_numpy(beta).cuda(), b)
+    torch.cuda.synchronize()
+    want = ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma, beta, b)
+    check("Z,W_out", got, want, w)
+
+
+@pytest.mark.parametrize("d,T,b,dtype", CASES)
+def test_momentum_matches_oracle(d, T, b, dtype):
+    w, inp, t = inputs(d, T, dtype, 730 + d + T + b)
+    g = np.random.default_rng(d + 2 * T)
+    alpha = g.uniform(0.05, 0.3, w.H).astype(np.float32)
+    beta = g.uniform(0.5, 0.9, w.H).astype(np.float32)
+    got = ttt.ttt_linear_momentum_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(alpha).cuda(),
+                                      torch.from_numpy(beta).cuda(), t["W0"], b)
+    torch.cuda.synchronize()
+    want = momentum_primal(inp.q64, inp.k64, inp.v64, alpha, beta, inp.W0_64, b)
+    check("Z,W_out,M_out", got, want, w)
+
+
+def test_variants_reduce_to_plain_ttt_linear():
+    """Two variants at settings where they are plain TTT-Linear (a per-token rate equal to the
+    head's eta everywhere; momentum with beta = 0 and alpha = eta) equal the library's plain
+    fp32 SIMT path on the same inputs within fp32 rounding."""
+    w, inp, t = inputs(64, 96, "f32", 741)
+    Zp, Wp = ttt.ttt_linear_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16,
+                                options={"force_path": ttt.PATH_SIMT})
+    et = t["eta"][None, :, None].expand(w.B, w.H, w.T).contiguous()
+    Zt, Wt = ttt.ttt_linear_token_eta_fwd(t["Q"], t["K"], t["V"], et, t["W0"], 16)
+    Zm, Wm, _ = ttt.ttt_linear_momentum_fwd(t["Q"], t["K"], t["V"], t["eta"], torch.zeros_like(t["eta"]), t["W0"], 16)
+    torch.cuda.synchronize()
+    for Z, Wo in ((Zt, Wt), (Zm, Wm)):
+        assert float((Z - Zp).abs().max()) < 1e-5 and float((Wo - Wp).abs().max()) < 1e-5
+
+
+@pytest.mark.parametrize("variant", ["bias", "token_eta", "ln", "momentum"])
+def test_variants_medium_bf16(variant):
+    """B1 H2 T1024 d64 b16, bf16 operands: every unit against the oracle."""
+    w, inp, t = inputs(64, 1024, "bf16", 750, B=1, H=2)
+    g = np.random.default_rng(7)
+    if variant == "bias":
+        beta0 = (0.3 * g.standard_normal((w.H, 64))).astype(np.float32)
+        got = ttt.ttt_linear_bias_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(beta0).cuda(), 16)
+        want, names = bias_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, beta0, 16), "Z,W_out,beta_out"
+    elif variant == "token_eta":
+        et = g.uniform(0.0, 0.5, (1, w.H, w.T)).astype(np.float32)
+        got = ttt.ttt_linear_token_eta_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(et).cuda(), t["W0"], 16)
+        want, names = token_eta_primal(inp.q64, inp.k64, inp.v64, et, inp.W0_64, 16), "Z,W_out"
+    elif variant == "ln":
+        gamma = (1.0 + 0.2 * g.standard_normal((w.H, 64))).astype(np.float32)
+        beta = (0.1 * g.standard_normal((w.H, 64))).astype(np.float32)
+        got = ttt.ttt_linear_ln_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(gamma).cuda(),
+                                    torch.from_numpy(beta).cuda(), 16)
+        want, names = ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma, beta, 16), "Z,W_out"
+    else:
+        alpha = np.full(w.H, 0.1, np.float32)
+        beta = np.array([0.6, 0.9], np.float32)
+        got = ttt.ttt_linear_momentum_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(alpha).cuda(),
+                                          torch.from_numpy(beta).cuda(), t["W0"], 16)
+        want, names = momentum_primal(inp.q64, inp.k64, inp.v64, alpha, beta, inp.W0_64, 16), "Z,W_out,M_out"
+    torch.cuda.synchronize()
+    check(names, got, want, w)
