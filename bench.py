@@ -602,6 +602,27 @@ def bench_extras(ttt, dev, stream):
     flops = w.token_heads * (16 * w.d * m + 4 * 16 * (w.d + m))
     out["mlp_125m_b16"] = {"ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
                            "tensor_frac": round(flops / (ms * 1e-3) / (tflops * 1e12), 5)}
+    # inner-model variants (fp32 SIMT kernel, one CTA per unit) on the small workload's shape
+    try:
+        w = synth.WORKLOADS["linear_small"]
+        inp, Q, K, V, eta = dev_inputs(w)
+        W0 = torch.from_numpy(inp.W0).to(dev)
+        vec = torch.zeros((w.H, w.d), device=dev)
+        gam = torch.ones((w.H, w.d), device=dev)
+        et = torch.full((w.B, w.H, w.T), 0.1, device=dev)
+        calls = {"bias": lambda: ttt.ttt_linear_bias_fwd(Q, K, V, eta, W0, vec, 16, stream=stream),
+                 "token_eta": lambda: ttt.ttt_linear_token_eta_fwd(Q, K, V, et, W0, 16, stream=stream),
+                 "ln_residual": lambda: ttt.ttt_linear_ln_fwd(Q, K, V, eta, W0, gam, vec, 16, stream=stream),
+                 "momentum": lambda: ttt.ttt_linear_momentum_fwd(Q, K, V, eta, eta, W0, 16, stream=stream)}
+        for name, fn in calls.items():
+            ms = t_ms(fn, 3)
+            out[f"variant_{name}_small_b16"] = {
+                "ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                "hbm_frac": round(algorithmic_bytes(w) / (ms * 1e-3) / 1e9 / hbm_gbs, 5),
+                "note": "B2 H4 T2048 d64 bf16 in, fp32 SIMT kernel, one CTA per (batch row, head)"}
+        del Q, K, V
+    except Exception as exc:  # reported in the line, never silently dropped
+        out["variants"] = {"error": f"{type(exc).__name__}: {exc}"}
     # backward of TTT-Linear (fp32 operands, the first GPU form: one CTA per unit)
     try:
         w = synth.WORKLOADS["linear_small"].with_(dtype="f32")
