@@ -288,12 +288,17 @@ TTT_API ttt_status ttt_linear_momentum_fwd(const void* Q, const void* K, const v
  * outer-loop parameters). Per chunk c with start state W:
  *   E = K_c W - V_c,  S = tril(Q_c K_c^T),  Z_c = Q_c W - eta S E,  W' = W - eta K_c^T E,
  * reversed from G = dW_out (G: gradient of the next chunk's start state).
- *   Q, K, V, dZ [B][H][T][d] float32 (dt must be TTT_F32); eta [H]; W0 [H][d][d];
- *   dW_out [B][H][d][d]. Outputs dQ, dK, dV [B][H][T][d] float32, deta [H] and
- *   dW0 [H][d][d] (summed over the batch rows, which share eta and W0).
- *   Supported: d <= 64 and b <= 64, else TTT_ERR_UNSUPPORTED (also for bf16).
+ *   Q, K, V, dZ [B][H][T][d] of dtype dt; eta [H]; W0 [H][d][d];
+ *   dW_out [B][H][d][d]. Outputs dQ, dK, dV [B][H][T][d] of dtype dt, deta [H] and
+ *   dW0 [H][d][d] float32 (summed over the batch rows, which share eta and W0).
+ *   Kernels: bf16 with d = 64 and b = 16 runs on the tensor cores (state and
+ *   products fp32-accumulated, W checkpointed every 64 tokens in the workspace);
+ *   every other case with d <= 64 and b <= 64 runs the fp32 SIMT kernel (fp32 or
+ *   bf16 operands); anything else returns TTT_ERR_UNSUPPORTED.
  *   workspace: ttt_linear_bwd_workspace_bytes(B, H, T, d, b) bytes (a status
- *   word, every chunk-start state, per-unit partial sums), 16-byte aligned.
+ *   word, the kept states, per-unit partial sums), 16-byte aligned. A wait in the
+ *   tensor-core kernel that runs out records TTT_ERR_TIMEOUT there
+ *   (ttt_last_device_status).
  * All pointers are device memory, 16-byte aligned, caller-owned; work is
  * enqueued on `stream`. Argument errors return before anything is enqueued.
  */

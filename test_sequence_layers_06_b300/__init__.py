@@ -383,14 +383,15 @@ def ttt_linear_bwd_workspace_bytes(B: int, H: int, T: int, d: int, b: int) -> in
 
 
 def ttt_linear_bwd(Q, K, V, eta, W0, b: int, dZ, dW_out, workspace=None, stream=None):
-    """Backward of ttt_linear_fwd (float32 operands): returns (dQ, dK, dV, deta, dW0) for
-    upstream gradients dZ [B, H, T, d] and dW_out [B, H, d, d]. Asynchronous on `stream`."""
+    """Backward of ttt_linear_fwd: returns (dQ, dK, dV, deta, dW0) for upstream gradients
+    dZ [B, H, T, d] (the dtype of Q: float32 or bfloat16) and dW_out [B, H, d, d] float32;
+    dQ, dK, dV come in the dtype of Q. Asynchronous on `stream`."""
     import torch
     lib = load_library()
     B, H, T, d = Q.shape
     dev = Q.device
     for n, t in (("Q", Q), ("K", K), ("V", V), ("dZ", dZ)):
-        _check(t, n, torch.float32, (B, H, T, d), dev)
+        _check(t, n, Q.dtype, (B, H, T, d), dev)
     _check(eta, "eta", torch.float32, (H,), dev)
     _check(W0, "W0", torch.float32, (H, d, d), dev)
     _check(dW_out, "dW_out", torch.float32, (B, H, d, d), dev)
@@ -402,7 +403,7 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b: int, dZ, dW_out, workspace=None, stream=
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _check(workspace, "workspace", device=dev)
     with _on_device(dev):
-        st = lib.ttt_linear_bwd(_p(Q), _p(K), _p(V), TTT_F32, _p(eta), _p(W0), B, H, T, d, int(b), _p(dZ),
+        st = lib.ttt_linear_bwd(_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), B, H, T, d, int(b), _p(dZ),
                                 _p(dW_out), _p(dQ), _p(dK), _p(dV), _p(deta), _p(dW0), _p(workspace),
                                 _nbytes(workspace), _stream_ptr(stream, dev))
     if st != TTT_OK:

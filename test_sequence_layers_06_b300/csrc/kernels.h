@@ -61,25 +61,29 @@ struct MlpParams {
   int inject_stall;
 };
 
-// Backward of TTT-Linear (fp32 operands): upstream dZ, dW_out -> dQ, dK, dV,
+// Backward of TTT-Linear: upstream dZ, dW_out -> dQ, dK, dV (the dtype of Q),
 // d eta [H] and dW0 [H][d][d] (summed over batch rows).
 struct LinearBwdParams {
-  const float* Q;
-  const float* K;
-  const float* V;
-  const float* dZ;
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* dZ;
   const float* eta;
   const float* W0;
   const float* dW_out;
-  float* dQ;
-  float* dK;
-  float* dV;
+  void* dQ;
+  void* dK;
+  void* dV;
   float* deta;
   float* dW0;
   int B, H, T, d, b;
   int units;
-  float* states;   // workspace [units][ceil(T/b)][d][d]: chunk-start states
+  bool bf16;       // Q, K, V, dZ, dQ, dK, dV are bf16 (else fp32)
+  float* states;   // workspace [units][ceil(T/b)][d][d]: chunk-start states (tensor-core kernel:
+                   // the state at the start of every 64-token block)
   float* partial;  // workspace [units][d*d + 1]: per-unit dW0, then d eta
+  StatusBlock* status;
+  uint64_t timeout_ns;
 };
 
 // Inner-model variants of TTT-Linear (linear_variants.cu), fp32 arithmetic.
@@ -166,10 +170,19 @@ cudaError_t launch_mlp_simt(const MlpParams& p, cudaStream_t stream);
 // Decode token.
 cudaError_t launch_linear_decode(const DecodeParams& p, cudaStream_t stream);
 
-// Backward of TTT-Linear, fp32, d <= 64, b <= 64 (linear_bwd.cu).
+// Backward of TTT-Linear in fp32 arithmetic, fp32 or bf16 operands, d <= 64, b <= 64
+// (linear_bwd.cu), and the sum of the per-unit dW0, d eta shares over batch rows.
 bool linear_bwd_supported(int d, int b);
 size_t linear_bwd_smem_bytes(int d, int b);
 size_t linear_bwd_scratch_bytes(int units, int T, int d, int b);  // states + partials, bytes
 cudaError_t launch_linear_bwd(const LinearBwdParams& p, cudaStream_t stream);
+cudaError_t launch_linear_bwd_reduce(const LinearBwdParams& p, cudaStream_t stream);
+
+// Backward of TTT-Linear on the tensor cores (linear_bwd_mma.cu): bf16, d = 64, b = 16.
+// Tensor maps over Q, K, V, dZ with linear_bwd_mma_rows()-row boxes.
+bool linear_bwd_mma_supported(int d, int b, bool bf16);
+int linear_bwd_mma_rows();
+cudaError_t launch_linear_bwd_mma(const LinearBwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                  const CUtensorMap& mv, const CUtensorMap& mdz, cudaStream_t stream);
 
 }  // namespace ttt

@@ -1,4 +1,5 @@
-// Backward of the chunked TTT-Linear scan, fp32 operands, d <= 64, b <= 64.
+// Backward of the chunked TTT-Linear scan in fp32 arithmetic: fp32 or bf16
+// operands (dQ, dK, dV in the operands' dtype), d <= 64, b <= 64.
 //
 // The outer loop trains W0 and the projections that make Q, K, V by
 // backpropagating through the inner loop ("5 · TestingTime 训练与长上下文",
@@ -20,8 +21,8 @@
 // Design: one CTA per (batch row, head). A forward pass keeps every
 // chunk-start state in the workspace; the backward pass reloads them in
 // reverse. Every matrix of a chunk sits in shared memory and every product is
-// a plain fp32 loop spread over the CTA's threads: this is the first GPU form
-// of the backward, built for parity, not speed.
+// a plain fp32 loop spread over the CTA's threads: the general form, for the
+// 1e-4 bar of fp32 operands and the shapes linear_bwd_mma.cu does not take.
 #include "ttt_device.cuh"
 #include "kernels.h"
 
@@ -30,6 +31,16 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 
+template <typename T>
+__device__ __forceinline__ float ldv(const void* p, size_t i) {
+  return static_cast<float>(static_cast<const T*>(p)[i]);
+}
+template <typename T>
+__device__ __forceinline__ void stv(void* p, size_t i, float v) {
+  static_cast<T*>(p)[i] = static_cast<T>(v);
+}
+
+template <typename Tin>
 __global__ void __launch_bounds__(kBwdThreads) linear_bwd_kernel(LinearBwdParams p) {
   extern __shared__ __align__(16) float bsm[];
   const int d = p.d, b = p.b, T = p.T;
@@ -60,8 +71,8 @@ __global__ void __launch_bounds__(kBwdThreads) linear_bwd_kernel(LinearBwdParams
     const int c0 = c * b, n = min(b, T - c0);
     for (int i = tid; i < d * d; i += kBwdThreads) states[static_cast<size_t>(c) * d * d + i] = W[i];
     for (int x = tid; x < n * d; x += kBwdThreads) {
-      Kc[x] = p.K[base + static_cast<size_t>(c0) * d + x];
-      Vc[x] = p.V[base + static_cast<size_t>(c0) * d + x];
+      Kc[x] = ldv<Tin>(p.K, base + static_cast<size_t>(c0) * d + x);
+      Vc[x] = ldv<Tin>(p.V, base + static_cast<size_t>(c0) * d + x);
     }
     __syncthreads();
     for (int x = tid; x < n * d; x += kBwdThreads) {  // E = K_c W - V_c
@@ -89,10 +100,10 @@ __global__ void __launch_bounds__(kBwdThreads) linear_bwd_kernel(LinearBwdParams
     const size_t off = base + static_cast<size_t>(c0) * d;
     for (int i = tid; i < d * d; i += kBwdThreads) W[i] = states[static_cast<size_t>(c) * d * d + i];
     for (int x = tid; x < n * d; x += kBwdThreads) {
-      Qc[x] = p.Q[off + x];
-      Kc[x] = p.K[off + x];
-      Vc[x] = p.V[off + x];
-      dZc[x] = p.dZ[off + x];
+      Qc[x] = ldv<Tin>(p.Q, off + x);
+      Kc[x] = ldv<Tin>(p.K, off + x);
+      Vc[x] = ldv<Tin>(p.V, off + x);
+      dZc[x] = ldv<Tin>(p.dZ, off + x);
     }
     __syncthreads();
     for (int x = tid; x < n * d; x += kBwdThreads) {  // E = K_c W - V_c, KG = K_c G
@@ -140,9 +151,9 @@ __global__ void __launch_bounds__(kBwdThreads) linear_bwd_kernel(LinearBwdParams
       }
       for (int t2 = 0; t2 <= t; ++t2) aq = fmaf(P[t * n + t2], Kc[t2 * d + i], aq);
       for (int t2 = t; t2 < n; ++t2) ak = fmaf(P[t2 * n + t], Qc[t2 * d + i], ak);
-      p.dQ[off + x] = aq;
-      p.dK[off + x] = ak - eta * eg;
-      p.dV[off + x] = -dE[x];
+      stv<Tin>(p.dQ, off + x, aq);
+      stv<Tin>(p.dK, off + x, ak - eta * eg);
+      stv<Tin>(p.dV, off + x, -dE[x]);
     }
     __syncthreads();  // G is read above; update it only now
     for (int x = tid; x < d * d; x += kBwdThreads) {  // G += Q_c^T dZ_c + K_c^T dE
@@ -200,14 +211,16 @@ size_t linear_bwd_scratch_bytes(int units, int T, int d, int b) {
 
 cudaError_t launch_linear_bwd(const LinearBwdParams& p, cudaStream_t stream) {
   const size_t smem = linear_bwd_smem_bytes(p.d, p.b);
+  auto kern = p.bf16 ? linear_bwd_kernel<__nv_bfloat16> : linear_bwd_kernel<float>;
   if (smem > 48 * 1024) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(linear_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  linear_bwd_kernel<<<p.units, kBwdThreads, smem, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  kern<<<p.units, kBwdThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_linear_bwd_reduce(const LinearBwdParams& p, cudaStream_t stream) {
   linear_bwd_reduce_kernel<<<p.H, kBwdThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }

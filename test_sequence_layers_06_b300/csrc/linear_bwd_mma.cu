@@ -1,0 +1,658 @@
+// Backward of the chunked TTT-Linear scan on the tensor cores: bf16 Q, K, V,
+// dZ (dQ, dK, dV written in bf16), fp32 state and accumulation, d = 64, b = 16.
+//
+// The outer loop trains W0, eta and the projections that make Q, K, V by
+// backpropagating through the inner loop ("5 · TestingTime 训练与长上下文",
+// section 2.2). For chunk c with start state W and G the gradient of the next
+// chunk's start state (G = dW_out after the last chunk):
+//   E = K W - V,  S = tril(Q K^T),  P = -eta tril(dZ E^T)
+//   dE = -eta (K G + S^T dZ),  dV = -dE
+//   dQ = dZ W^T + P K,  dK = -eta E G^T + P^T Q + dE W^T
+//   d eta += -sum(E .* K G) - sum(S .* dZ E^T)
+//   G <- G + Q^T dZ + K^T dE,   and dW0 = G after the first chunk
+// (the same recurrence as linear_bwd.cu, which serves fp32 and other shapes).
+//
+// Design. The chunk rule splits over the output columns j of W, and so do E, G
+// and dE: each of 4 consumer warps owns 16 columns and keeps G^T (16 x 64) as
+// fp32 mma.sync accumulator fragments for the whole sequence. dQ, dK and P sum
+// over all columns, so each warp forms its columns' share and the four shares
+// are added through shared memory.
+//   Pass 1 walks the sequence forward (K, V only), keeping W in fragments as the
+//   forward kernel does, and writes W at the start of every 64-token block to
+//   the workspace (fp32).
+//   Pass 2 walks the blocks in reverse. For a block it reloads W, recomputes the
+//   four chunk states and errors (bf16 copies in shared memory), then runs the
+//   backward of its four chunks, last first.
+// A producer warp streams the 64-token blocks by TMA (K, V for pass 1; Q, K, V,
+// dZ for pass 2, double-buffered) and forms, per chunk, S = tril(Q K^T) and
+// S^T = triu(K Q^T) as the consumers' B fragments. Every wait is bounded in
+// wall-clock time; a role that gives up sets a shared flag the others see.
+#include "ttt_device.cuh"
+#include "kernels.h"
+
+namespace ttt {
+namespace {
+
+constexpr int kD = 64;
+constexpr int kTile = 16;               // = b
+constexpr int kBlk = 64;                // tokens per block (4 chunks)
+constexpr int kWarps = 4;               // consumer warps; one more produces
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kTileBytes = kTile * kD * 2;   // 2 KB
+constexpr int kBlkBytes = kBlk * kD * 2;     // 8 KB
+// shared memory map (bytes from a 1024-aligned base)
+constexpr int kP1 = 0;                                  // pass 1: [2 stages][K, V] blocks
+constexpr int kP2 = kP1 + 2 * 2 * kBlkBytes;            // pass 2: [2 stages][Q, K, V, dZ] blocks
+constexpr int kSb = kP2 + 2 * 4 * kBlkBytes;            // [2 stages][4 chunks][S, S^T] B fragments, 512 B each
+constexpr int kWc = kSb + 2 * 4 * 2 * 512;              // [4 chunks] W bf16 [i][j]
+constexpr int kEc = kWc + 4 * kD * kD * 2;              // [4 chunks] E bf16 [t][j]
+constexpr int kGc = kEc + 4 * kTileBytes;               // G bf16 [i][j]
+constexpr int kDE = kGc + kD * kD * 2;                  // dE bf16 [t][j]
+constexpr int kOut = kDE + kTileBytes;                  // [4 warps][2] 16 x 16 bf16 output staging
+constexpr int kPp = kOut + kWarps * 2 * 512;            // P shares fp32 [4 warps][16][16]
+constexpr int kPad = 68;                                // fp32 row stride of the dQ/dK shares
+constexpr int kQp = kPp + kWarps * kTile * kTile * 4;   // dQ shares fp32 [4][16][kPad]
+constexpr int kKp = kQp + kWarps * kTile * kPad * 4;    // dK shares fp32 [4][16][kPad]
+constexpr int kRed = kKp + kWarps * kTile * kPad * 4;   // d eta per warp
+constexpr int kBar = kRed + 64;
+constexpr int kNumBars = 12;
+constexpr int kMisc = kBar + kNumBars * 8;              // abort flag
+constexpr int kSmemBytes = kMisc + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "fits one CTA per SM");
+
+enum : int { kWhereBwdProducer = 20, kWhereBwdPass1 = 21, kWhereBwdPass2 = 22, kWhereBwdSync = 23 };
+
+__device__ __forceinline__ void unpack4(uint4 v, float (&s)[2][4]) {
+  // the producer packs C fragments as {(nt0: r0, r1), (nt1: r0, r1), (nt0: r2, r3), (nt1: r2, r3)}
+  s[0][0] = bf16_lo(v.x); s[0][1] = bf16_hi(v.x);
+  s[1][0] = bf16_lo(v.y); s[1][1] = bf16_hi(v.y);
+  s[0][2] = bf16_lo(v.z); s[0][3] = bf16_hi(v.z);
+  s[1][2] = bf16_lo(v.w); s[1][3] = bf16_hi(v.w);
+}
+
+// A fragments (bf16) of a 16 x 64 block of X^T held as fp32 C fragments xt[8][4]
+// (rows m, columns 8q + 2tg): k-step s covers columns [16s, 16s + 16).
+__device__ __forceinline__ void pack_a(const float (&xt)[8][4], uint32_t (&a)[4][4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a[k][0] = pack_bf16(xt[2 * k][0], xt[2 * k][1]);
+    a[k][1] = pack_bf16(xt[2 * k][2], xt[2 * k][3]);
+    a[k][2] = pack_bf16(xt[2 * k + 1][0], xt[2 * k + 1][1]);
+    a[k][3] = pack_bf16(xt[2 * k + 1][2], xt[2 * k + 1][3]);
+  }
+}
+
+// Writes X (64 x 64, [i][j], 128-byte swizzled rows) columns [16w, 16w + 16) from
+// the A fragments of X^T rows j (a transposing stmatrix per 16 x 16 block).
+__device__ __forceinline__ void store_t(uint32_t base, const uint32_t (&a)[4][4], int warp, int lane) {
+  const int mi = lane >> 3, mr = lane & 7;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) stsm_x4_t(base + swz128(16 * s + ((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)), a[s]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_bwd_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdz,
+                          LinearBwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full1 = reinterpret_cast<uint64_t*>(sm + kBar);
+  uint64_t* empty1 = full1 + 2;
+  uint64_t* full2 = full1 + 4;
+  uint64_t* ready2 = full1 + 6;
+  uint64_t* empty2 = full1 + 8;
+  uint64_t* sync1 = full1 + 10;  // P shares written (4 warps)
+  uint64_t* sync2 = full1 + 11;  // dQ, dK shares written (4 warps)
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc);
+  const uint32_t s0 = smem_u32(sm);
+
+  const int unit = blockIdx.x;
+  const int h = unit % p.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tg = lane & 3, mi = lane >> 3, mr = lane & 7;
+  const int T = p.T;
+  const int ntiles = (T + kTile - 1) / kTile;
+  const int nblk = (T + kBlk - 1) / kBlk;
+  const float eta = p.eta[h];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full1[i], 1);
+      mbar_init(&empty1[i], kWarps);
+      mbar_init(&full2[i], 1);
+      mbar_init(&ready2[i], 1);
+      mbar_init(&empty2[i], kWarps);
+    }
+    mbar_init(sync1, kWarps);
+    mbar_init(sync2, kWarps);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ---------------------------------------------------------------- producer
+    bool ok = true;
+    int issued1 = 0, issued2 = 0, seen2 = 0;  // lane 0's TMA blocks, and those seen to land
+    if (lane == 0) {
+      prefetch_tmap(&mk);
+      prefetch_tmap(&mv);
+      prefetch_tmap(&mq);
+      prefetch_tmap(&mdz);
+      for (int bk = 0; bk < nblk && ok; ++bk) {
+        const int s = bk & 1;
+        if (bk >= 2) ok = mbar_wait_or_abort(&empty1[s], ((bk >> 1) - 1) & 1, p.timeout_ns, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&full1[s], 2 * kBlkBytes);
+        tma_load_3d(sm + kP1 + s * 2 * kBlkBytes, &mk, &full1[s], 0, bk * kBlk, unit);
+        tma_load_3d(sm + kP1 + s * 2 * kBlkBytes + kBlkBytes, &mv, &full1[s], 0, bk * kBlk, unit);
+        issued1 = bk + 1;
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    for (int r = 0; r < nblk && ok; ++r) {
+      const int bk = nblk - 1 - r, s = r & 1;
+      if (lane == 0) {
+        if (r >= 2) ok = mbar_wait_or_abort(&empty2[s], ((r >> 1) - 1) & 1, p.timeout_ns, abort_flag);
+        if (ok) {
+          uint8_t* st = sm + kP2 + s * 4 * kBlkBytes;
+          mbar_arrive_expect_tx(&full2[s], 4 * kBlkBytes);
+          tma_load_3d(st, &mq, &full2[s], 0, bk * kBlk, unit);
+          tma_load_3d(st + kBlkBytes, &mk, &full2[s], 0, bk * kBlk, unit);
+          tma_load_3d(st + 2 * kBlkBytes, &mv, &full2[s], 0, bk * kBlk, unit);
+          tma_load_3d(st + 3 * kBlkBytes, &mdz, &full2[s], 0, bk * kBlk, unit);
+          issued2 = r + 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&full2[s], (r >> 1) & 1, p.timeout_ns, abort_flag));
+      if (!ok) break;
+      seen2 = r + 1;
+      // S = tril(Q K^T) and S^T = triu(K Q^T) of each chunk, as packed C fragments.
+      const uint32_t sQb = s0 + kP2 + s * 4 * kBlkBytes, sKb = sQb + kBlkBytes;
+#pragma unroll 1
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t sQ = sQb + u * kTileBytes, sK = sKb + u * kTileBytes;
+        float sa[2][4] = {}, sb[2][4] = {};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t qa[4], ka[4], rq[4], rk[4];
+          ldsm_x4(qa, sQ + swz128(((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));  // Q as A (m = t, k = i)
+          ldsm_x4(ka, sK + swz128(((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));  // K as A
+          ldsm_x4(rk, sK + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));  // K as B (k = i, n = t')
+          ldsm_x4(rq, sQ + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));  // Q as B
+          const uint32_t kb0[2] = {rk[0], rk[1]}, kb1[2] = {rk[2], rk[3]};
+          const uint32_t qb0[2] = {rq[0], rq[1]}, qb1[2] = {rq[2], rq[3]};
+          mma_bf16_16816(sa[0], qa, kb0);
+          mma_bf16_16816(sa[1], qa, kb1);
+          mma_bf16_16816(sb[0], ka, qb0);
+          mma_bf16_16816(sb[1], ka, qb1);
+        }
+        // element (row g (+8), column 8nt + 2tg (+1)): keep column <= row in S, column >= row in S^T
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int c = 8 * nt + 2 * tg;
+          if (c > g) sa[nt][0] = 0.f;
+          if (c + 1 > g) sa[nt][1] = 0.f;
+          if (c > g + 8) sa[nt][2] = 0.f;
+          if (c + 1 > g + 8) sa[nt][3] = 0.f;
+          if (c < g) sb[nt][0] = 0.f;
+          if (c + 1 < g) sb[nt][1] = 0.f;
+          if (c < g + 8) sb[nt][2] = 0.f;
+          if (c + 1 < g + 8) sb[nt][3] = 0.f;
+        }
+        uint8_t* dst = sm + kSb + ((s * 4 + u) * 2) * 512 + lane * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16(sa[0][0], sa[0][1]), pack_bf16(sa[1][0], sa[1][1]),
+                                                    pack_bf16(sa[0][2], sa[0][3]), pack_bf16(sa[1][2], sa[1][3]));
+        *reinterpret_cast<uint4*>(dst + 512) = make_uint4(pack_bf16(sb[0][0], sb[0][1]), pack_bf16(sb[1][0], sb[1][1]),
+                                                          pack_bf16(sb[0][2], sb[0][3]), pack_bf16(sb[1][2], sb[1][3]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready2[s]);
+    }
+    if (lane == 0) {
+      if (!ok) {
+        if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdProducer, unit);
+        *abort_flag = 1;
+      }
+      // Loads still in flight must land before the CTA may exit.
+      for (int bk = (issued1 > 2 ? issued1 - 2 : 0); bk < issued1; ++bk)
+        (void)mbar_wait_bounded(&full1[bk & 1], (bk >> 1) & 1, p.timeout_ns);
+      for (int r = seen2; r < issued2; ++r) (void)mbar_wait_bounded(&full2[r & 1], (r >> 1) & 1, p.timeout_ns);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int jw = 16 * warp;
+  bool ok = true;
+  float Wt[8][4];  // W^T rows j = jw + g (+8), columns i = 8q + 2tg (+1)
+  {
+    const float* W0 = p.W0 + static_cast<size_t>(h) * kD * kD;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = 8 * q + 2 * tg;
+      Wt[q][0] = W0[i * kD + jw + g];
+      Wt[q][1] = W0[(i + 1) * kD + jw + g];
+      Wt[q][2] = W0[i * kD + jw + g + 8];
+      Wt[q][3] = W0[(i + 1) * kD + jw + g + 8];
+    }
+  }
+  float* ckpt = p.states + static_cast<size_t>(unit) * nblk * kD * kD;
+  auto save_w = [&](float* dst) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = 8 * q + 2 * tg;
+      dst[i * kD + jw + g] = Wt[q][0];
+      dst[(i + 1) * kD + jw + g] = Wt[q][1];
+      dst[i * kD + jw + g + 8] = Wt[q][2];
+      dst[(i + 1) * kD + jw + g + 8] = Wt[q][3];
+    }
+  };
+  auto load_w = [&](const float* src) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = 8 * q + 2 * tg;
+      Wt[q][0] = __ldcg(src + i * kD + jw + g);
+      Wt[q][1] = __ldcg(src + (i + 1) * kD + jw + g);
+      Wt[q][2] = __ldcg(src + i * kD + jw + g + 8);
+      Wt[q][3] = __ldcg(src + (i + 1) * kD + jw + g + 8);
+    }
+  };
+  // One chunk of the forward rule on the fragments: E^T = W^T K^T - V^T, W^T -= eta E^T K.
+  // Returns E^T (C fragments) and the bf16 A fragments of W^T used.
+  auto chunk_forward = [&](uint32_t sK, uint32_t sV, bool update, float (&e)[2][4], uint32_t (&wa)[4][4]) {
+    pack_a(Wt, wa);
+    float e2[2][4];
+    {
+      uint32_t vt[4];
+      ldsm_x4_t(vt, sV + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        e[nt][0] = -bf16_lo(vt[2 * nt]);
+        e[nt][1] = -bf16_hi(vt[2 * nt]);
+        e[nt][2] = -bf16_lo(vt[2 * nt + 1]);
+        e[nt][3] = -bf16_hi(vt[2 * nt + 1]);
+        e2[nt][0] = e2[nt][1] = e2[nt][2] = e2[nt][3] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t r[4];
+      ldsm_x4(r, sK + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
+      const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
+      mma_bf16_16816(k < 2 ? e[0] : e2[0], wa[k], b0);
+      mma_bf16_16816(k < 2 ? e[1] : e2[1], wa[k], b1);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) e[nt][r] += e2[nt][r];
+    if (update) {
+      uint32_t ea[4];
+      ea[0] = pack_bf16(-eta * e[0][0], -eta * e[0][1]);
+      ea[1] = pack_bf16(-eta * e[0][2], -eta * e[0][3]);
+      ea[2] = pack_bf16(-eta * e[1][0], -eta * e[1][1]);
+      ea[3] = pack_bf16(-eta * e[1][2], -eta * e[1][3]);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        uint32_t r[4];
+        ldsm_x4_t(r, sK + swz128(((mi & 1) << 3) + mr, 2 * qq + (mi >> 1)));
+        const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
+        mma_bf16_16816(Wt[2 * qq], ea, b0);
+        mma_bf16_16816(Wt[2 * qq + 1], ea, b1);
+      }
+    }
+  };
+
+  // ---------------------------------------------------------------- pass 1: checkpoints
+  for (int bk = 0; bk < nblk; ++bk) {
+    const int s = bk & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&full1[s], (bk >> 1) & 1, p.timeout_ns, abort_flag))) {
+      if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdPass1, unit);
+      *abort_flag = 1;
+      ok = false;
+      break;
+    }
+    save_w(ckpt + static_cast<size_t>(bk) * kD * kD);
+    const uint32_t sK = s0 + kP1 + s * 2 * kBlkBytes, sV = sK + kBlkBytes;
+    const int nt = min(4, ntiles - 4 * bk);
+    for (int u = 0; u < nt; ++u) {
+      float e[2][4];
+      uint32_t wa[4][4];
+      chunk_forward(sK + u * kTileBytes, sV + u * kTileBytes, true, e, wa);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty1[s]);
+  }
+
+  // ---------------------------------------------------------------- pass 2: the backward
+  float Gt[8][4];  // G^T rows j = jw + g (+8), columns i = 8q + 2tg (+1)
+  {
+    const float* G0 = p.dW_out + static_cast<size_t>(unit) * kD * kD;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = 8 * q + 2 * tg;
+      Gt[q][0] = G0[i * kD + jw + g];
+      Gt[q][1] = G0[(i + 1) * kD + jw + g];
+      Gt[q][2] = G0[i * kD + jw + g + 8];
+      Gt[q][3] = G0[(i + 1) * kD + jw + g + 8];
+    }
+  }
+  float deta = 0.f;
+  // The stores of pass 1 must be visible to this CTA's loads of the checkpoints.
+  __threadfence_block();
+  int ktile = 0;  // chunks done in pass 2 (phase of sync1 / sync2)
+  __nv_bfloat16* dQg = static_cast<__nv_bfloat16*>(p.dQ);
+  __nv_bfloat16* dKg = static_cast<__nv_bfloat16*>(p.dK);
+  __nv_bfloat16* dVg = static_cast<__nv_bfloat16*>(p.dV);
+  const size_t base = static_cast<size_t>(unit) * T * kD;
+  float* ppart = reinterpret_cast<float*>(sm + kPp);
+  float* qpart = reinterpret_cast<float*>(sm + kQp);
+  float* kpart = reinterpret_cast<float*>(sm + kKp);
+
+  for (int r = 0; ok && r < nblk; ++r) {
+    const int bk = nblk - 1 - r, s = r & 1;
+    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&ready2[s], (r >> 1) & 1, p.timeout_ns, abort_flag))) {
+      if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdPass2, unit);
+      *abort_flag = 1;
+      ok = false;
+      break;
+    }
+    const uint32_t sQb = s0 + kP2 + s * 4 * kBlkBytes, sKb = sQb + kBlkBytes, sVb = sQb + 2 * kBlkBytes,
+                   sZb = sQb + 3 * kBlkBytes;
+    const int nt = min(4, ntiles - 4 * bk);
+    // Recompute the block's chunk states and errors from its checkpoint.
+    load_w(ckpt + static_cast<size_t>(bk) * kD * kD);
+    for (int u = 0; u < nt; ++u) {
+      float e[2][4];
+      uint32_t wa[4][4];
+      chunk_forward(sKb + u * kTileBytes, sVb + u * kTileBytes, u + 1 < nt, e, wa);
+      store_t(s0 + kWc + u * kD * kD * 2, wa, warp, lane);  // W_u [i][j], this warp's columns
+      // E_u [t][j]: E^T (rows j, columns t) through a transposing stmatrix.
+      const uint32_t ev[4] = {pack_bf16(e[0][0], e[0][1]), pack_bf16(e[0][2], e[0][3]), pack_bf16(e[1][0], e[1][1]),
+                              pack_bf16(e[1][2], e[1][3])};
+      stsm_x4_t(s0 + kEc + u * kTileBytes + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)), ev);
+    }
+    __syncwarp();
+
+    for (int u = nt - 1; u >= 0; --u, ++ktile) {
+      const uint32_t sQ = sQb + u * kTileBytes, sK = sKb + u * kTileBytes, sZ = sZb + u * kTileBytes;
+      const uint32_t sW = s0 + kWc + u * kD * kD * 2, sE = s0 + kEc + u * kTileBytes;
+      const uint8_t* sfr = sm + kSb + ((s * 4 + u) * 2) * 512 + lane * 16;
+      const uint4 sv = *reinterpret_cast<const uint4*>(sfr);        // S (rows t, columns t')
+      const uint4 stv = *reinterpret_cast<const uint4*>(sfr + 512); // S^T (rows t, columns t')
+
+      // G (bf16, [i][j]) for this warp's columns: the B operand of E G^T.
+      uint32_t ga[4][4];
+      pack_a(Gt, ga);
+      store_t(s0 + kGc, ga, warp, lane);
+
+      // (K G)^T = G^T K^T (rows j, columns t).
+      float kg[2][4] = {};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t rr[4];
+        ldsm_x4(rr, sK + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
+        const uint32_t b0[2] = {rr[0], rr[1]}, b1[2] = {rr[2], rr[3]};
+        mma_bf16_16816(kg[0], ga[k], b0);
+        mma_bf16_16816(kg[1], ga[k], b1);
+      }
+      // dZ^T as A (m = j, k = t') and (S^T dZ)^T = dZ^T S (B[k = t'][n = t] = S[t'][t]: S^T's C fragment).
+      uint32_t zt[4];
+      ldsm_x4_t(zt, sZ + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
+      float de[2][4];
+      {
+        float zs[2][4] = {};
+        const uint32_t b0[2] = {stv.x, stv.y}, b1[2] = {stv.z, stv.w};
+        mma_bf16_16816(zs[0], zt, b0);
+        mma_bf16_16816(zs[1], zt, b1);
+#pragma unroll
+        for (int nt2 = 0; nt2 < 2; ++nt2)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) de[nt2][q] = -eta * (kg[nt2][q] + zs[nt2][q]);
+      }
+      // d eta: -sum(E .* K G) over this warp's columns (E^T in the C layout of kg).
+      {
+        uint32_t et[4];
+        ldsm_x4_t(et, sE + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
+#pragma unroll
+        for (int nt2 = 0; nt2 < 2; ++nt2)
+          deta -= bf16_lo(et[2 * nt2]) * kg[nt2][0] + bf16_hi(et[2 * nt2]) * kg[nt2][1] +
+                  bf16_lo(et[2 * nt2 + 1]) * kg[nt2][2] + bf16_hi(et[2 * nt2 + 1]) * kg[nt2][3];
+      }
+      // dE (bf16, [t][j]) for this warp's columns; dV = -dE goes out from it.
+      const uint32_t dea[4] = {pack_bf16(de[0][0], de[0][1]), pack_bf16(de[0][2], de[0][3]),
+                               pack_bf16(de[1][0], de[1][1]), pack_bf16(de[1][2], de[1][3])};
+      stsm_x4_t(s0 + kDE + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)), dea);
+
+      // This warp's share of P: dZ[:, own] E[:, own]^T (rows t, columns t').
+      uint32_t za[4];
+      ldsm_x4(za, sZ + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));  // dZ as A (m = t, k = j)
+      {
+        float pw[2][4] = {};
+        uint32_t rr[4];
+        ldsm_x4(rr, sE + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));  // E as B (k = j, n = t')
+        const uint32_t b0[2] = {rr[0], rr[1]}, b1[2] = {rr[2], rr[3]};
+        mma_bf16_16816(pw[0], za, b0);
+        mma_bf16_16816(pw[1], za, b1);
+        float sf[2][4];
+        unpack4(sv, sf);
+#pragma unroll
+        for (int nt2 = 0; nt2 < 2; ++nt2)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) deta -= sf[nt2][q] * pw[nt2][q];
+        float* dst = ppart + warp * kTile * kTile;
+#pragma unroll
+        for (int nt2 = 0; nt2 < 2; ++nt2) {
+          const int c = 8 * nt2 + 2 * tg;
+          *reinterpret_cast<float2*>(dst + g * kTile + c) = make_float2(pw[nt2][0], pw[nt2][1]);
+          *reinterpret_cast<float2*>(dst + (g + 8) * kTile + c) = make_float2(pw[nt2][2], pw[nt2][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sync1);
+
+      // G^T += dZ^T Q + dE^T K (this warp's rows j), from the chunk's own tiles.
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        uint32_t rq[4], rk[4];
+        ldsm_x4_t(rq, sQ + swz128(((mi & 1) << 3) + mr, 2 * qq + (mi >> 1)));
+        ldsm_x4_t(rk, sK + swz128(((mi & 1) << 3) + mr, 2 * qq + (mi >> 1)));
+        const uint32_t q0[2] = {rq[0], rq[1]}, q1[2] = {rq[2], rq[3]};
+        const uint32_t k0[2] = {rk[0], rk[1]}, k1[2] = {rk[2], rk[3]};
+        mma_bf16_16816(Gt[2 * qq], zt, q0);
+        mma_bf16_16816(Gt[2 * qq + 1], zt, q1);
+        mma_bf16_16816(Gt[2 * qq], dea, k0);
+        mma_bf16_16816(Gt[2 * qq + 1], dea, k1);
+      }
+
+      // Every warp's P share is written: P = -eta tril(sum of shares), as A fragments of P
+      // and of P^T (rows t, k = t').
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(sync1, ktile & 1, p.timeout_ns, abort_flag))) {
+        if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdSync, unit);
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      uint32_t pa[4], pta[4];
+      {
+        auto P = [&](int t, int t2) -> float {
+          if (t2 > t) return 0.f;
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) v += ppart[w * kTile * kTile + t * kTile + t2];
+          return -eta * v;
+        };
+        // A fragment of a 16 x 16 X: {(g, 2tg), (g + 8, 2tg), (g, 2tg + 8), (g + 8, 2tg + 8)} pairs
+        pa[0] = pack_bf16(P(g, 2 * tg), P(g, 2 * tg + 1));
+        pa[1] = pack_bf16(P(g + 8, 2 * tg), P(g + 8, 2 * tg + 1));
+        pa[2] = pack_bf16(P(g, 2 * tg + 8), P(g, 2 * tg + 9));
+        pa[3] = pack_bf16(P(g + 8, 2 * tg + 8), P(g + 8, 2 * tg + 9));
+        pta[0] = pack_bf16(P(2 * tg, g), P(2 * tg + 1, g));
+        pta[1] = pack_bf16(P(2 * tg, g + 8), P(2 * tg + 1, g + 8));
+        pta[2] = pack_bf16(P(2 * tg + 8, g), P(2 * tg + 9, g));
+        pta[3] = pack_bf16(P(2 * tg + 8, g + 8), P(2 * tg + 9, g + 8));
+      }
+      // The shares of the previous chunk have been read by every warp (they all passed sync1
+      // of this chunk after summing them), so the buffers may be rewritten.
+      // This warp's shares of dQ (dZ W^T) and dK (dE W^T - eta E G^T) over its columns.
+      {
+        uint32_t dza[4], ea[4];
+        ldsm_x4(dza, s0 + kDE + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));  // dE as A (m = t, k = j)
+        ldsm_x4(ea, sE + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));        // E as A
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ea[q] = pack_bf16(-eta * bf16_lo(ea[q]), -eta * bf16_hi(ea[q]));
+        float acc[8][4];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {  // W rows i in [16pp, 16pp + 16) as B (k = j, n = i)
+          uint32_t rr[4];
+          ldsm_x4(rr, sW + swz128(16 * pp + ((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
+          const uint32_t b0[2] = {rr[0], rr[1]}, b1[2] = {rr[2], rr[3]};
+          mma_bf16_16816(acc[2 * pp], za, b0);
+          mma_bf16_16816(acc[2 * pp + 1], za, b1);
+        }
+        float* dq = qpart + warp * kTile * kPad;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = 8 * q + 2 * tg;
+          *reinterpret_cast<float2*>(dq + g * kPad + c) = make_float2(acc[q][0], acc[q][1]);
+          *reinterpret_cast<float2*>(dq + (g + 8) * kPad + c) = make_float2(acc[q][2], acc[q][3]);
+          acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+        }
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+          uint32_t rw[4], rg[4];
+          ldsm_x4(rw, sW + swz128(16 * pp + ((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
+          ldsm_x4(rg, s0 + kGc + swz128(16 * pp + ((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
+          const uint32_t w0[2] = {rw[0], rw[1]}, w1[2] = {rw[2], rw[3]};
+          const uint32_t g0[2] = {rg[0], rg[1]}, g1[2] = {rg[2], rg[3]};
+          mma_bf16_16816(acc[2 * pp], dza, w0);
+          mma_bf16_16816(acc[2 * pp + 1], dza, w1);
+          mma_bf16_16816(acc[2 * pp], ea, g0);
+          mma_bf16_16816(acc[2 * pp + 1], ea, g1);
+        }
+        float* dk = kpart + warp * kTile * kPad;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = 8 * q + 2 * tg;
+          *reinterpret_cast<float2*>(dk + g * kPad + c) = make_float2(acc[q][0], acc[q][1]);
+          *reinterpret_cast<float2*>(dk + (g + 8) * kPad + c) = make_float2(acc[q][2], acc[q][3]);
+        }
+      }
+
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sync2);
+      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(sync2, ktile & 1, p.timeout_ns, abort_flag))) {
+        if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdSync, unit);
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      // This warp's output columns i in [16w, 16w + 16): sum of the shares + P K (dQ) and P^T Q (dK).
+      {
+        float oq[2][4], ok2[2][4];
+#pragma unroll
+        for (int nt2 = 0; nt2 < 2; ++nt2) {
+          const int c = jw + 8 * nt2 + 2 * tg;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int t = g + 8 * half;
+            float2 sq = make_float2(0.f, 0.f), sk = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+              const float2 a = *reinterpret_cast<const float2*>(qpart + w * kTile * kPad + t * kPad + c);
+              const float2 b = *reinterpret_cast<const float2*>(kpart + w * kTile * kPad + t * kPad + c);
+              sq.x += a.x;
+              sq.y += a.y;
+              sk.x += b.x;
+              sk.y += b.y;
+            }
+            oq[nt2][2 * half] = sq.x;
+            oq[nt2][2 * half + 1] = sq.y;
+            ok2[nt2][2 * half] = sk.x;
+            ok2[nt2][2 * half + 1] = sk.y;
+          }
+        }
+        uint32_t rk[4], rq[4];  // K and Q as B (k = t', n = i) for i in [16w, 16w + 16)
+        ldsm_x4_t(rk, sK + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));
+        ldsm_x4_t(rq, sQ + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));
+        const uint32_t k0[2] = {rk[0], rk[1]}, k1[2] = {rk[2], rk[3]};
+        const uint32_t q0[2] = {rq[0], rq[1]}, q1[2] = {rq[2], rq[3]};
+        mma_bf16_16816(oq[0], pa, k0);
+        mma_bf16_16816(oq[1], pa, k1);
+        mma_bf16_16816(ok2[0], pta, q0);
+        mma_bf16_16816(ok2[1], pta, q1);
+        // Out through the warp's staging tile ([t][16 i], 32-byte rows), one 16-byte store per lane.
+        const int tok0 = 64 * bk + 16 * u;
+        auto emit = [&](const float (&o)[2][4], __nv_bfloat16* dst, int buf) {
+          uint8_t* stg = sm + kOut + (warp * 2 + buf) * 512;
+          const uint32_t v[4] = {pack_bf16(o[0][0], o[0][1]), pack_bf16(o[0][2], o[0][3]), pack_bf16(o[1][0], o[1][1]),
+                                 pack_bf16(o[1][2], o[1][3])};
+          stsm_x4(smem_u32(stg) + ((mi & 1) * 8 + mr) * 32 + (mi >> 1) * 16, v);
+          __syncwarp();
+          const int tok = tok0 + (lane >> 1);
+          const uint4 x = *reinterpret_cast<const uint4*>(stg + (lane >> 1) * 32 + (lane & 1) * 16);
+          if (tok < T) *reinterpret_cast<uint4*>(dst + base + static_cast<size_t>(tok) * kD + jw + 8 * (lane & 1)) = x;
+        };
+        emit(oq, dQg, 0);
+        emit(ok2, dKg, 1);
+        // dV = -dE for this warp's columns j (the same 16-column band), from the dE tile.
+        {
+          const int tok = tok0 + (lane >> 1);
+          uint4 x = *reinterpret_cast<const uint4*>(sm + kDE + swz128(lane >> 1, 2 * warp + (lane & 1)));
+          x.x ^= 0x80008000u;
+          x.y ^= 0x80008000u;
+          x.z ^= 0x80008000u;
+          x.w ^= 0x80008000u;
+          if (tok < T) *reinterpret_cast<uint4*>(dVg + base + static_cast<size_t>(tok) * kD + jw + 8 * (lane & 1)) = x;
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok) break;
+    // Every read of this block's tiles is done: hand the stage back.
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty2[s]);
+  }
+
+  // dW0 share of this unit (G after the first chunk) and d eta.
+  float* part = p.partial + static_cast<size_t>(unit) * (kD * kD + 1);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int i = 8 * q + 2 * tg;
+    part[i * kD + jw + g] = Gt[q][0];
+    part[(i + 1) * kD + jw + g] = Gt[q][1];
+    part[i * kD + jw + g + 8] = Gt[q][2];
+    part[(i + 1) * kD + jw + g + 8] = Gt[q][3];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) deta += __shfl_xor_sync(0xffffffffu, deta, o);
+  float* red = reinterpret_cast<float*>(sm + kRed);
+  if (lane == 0) red[warp] = deta;
+  asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // the four consumer warps only
+  if (threadIdx.x == 0) part[kD * kD] = red[0] + red[1] + red[2] + red[3];
+  if (!ok && lane == 0 && !*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdPass2, unit);
+}
+
+}  // namespace
+
+bool linear_bwd_mma_supported(int d, int b, bool bf16) { return bf16 && d == kD && b == kTile; }
+
+int linear_bwd_mma_rows() { return kBlk; }
+
+cudaError_t launch_linear_bwd_mma(const LinearBwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                  const CUtensorMap& mv, const CUtensorMap& mdz, cudaStream_t stream) {
+  if (p.units == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(linear_bwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  linear_bwd_mma_kernel<<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdz, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ttt

@@ -627,7 +627,9 @@ ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype
                           void* stream) {
   if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
   if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
-  if (dt != TTT_F32 || !ttt::linear_bwd_supported(d, b)) return TTT_ERR_UNSUPPORTED;
+  const bool bf16 = dt == TTT_BF16;
+  const bool mma = ttt::linear_bwd_mma_supported(d, b, bf16) && T > 0;
+  if (!mma && !ttt::linear_bwd_supported(d, b)) return TTT_ERR_UNSUPPORTED;
   if (!eta || !W0 || !dW_out || !deta || !dW0 || !workspace) return TTT_ERR_ARG;
   if (T > 0 && (!Q || !K || !V || !dZ || !dQ || !dK || !dV)) return TTT_ERR_ARG;
   for (const void* p : {Q, K, V, dZ, static_cast<const void*>(dQ), static_cast<const void*>(dK),
@@ -637,7 +639,7 @@ ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype
     if (p && !aligned16(p)) return TTT_ERR_ARG;
   if (ws_bytes < ttt_linear_bwd_workspace_bytes(B, H, T, d, b)) return TTT_ERR_ARG;
   {
-    const size_t seq = bytes4(B, H, T, d, 4), hdd = bytes4(H, d, d, 1, 4);
+    const size_t seq = bytes4(B, H, T, d, bf16 ? 2 : 4), hdd = bytes4(H, d, d, 1, 4);
     if (!outputs_disjoint({{dQ, seq}, {dK, seq}, {dV, seq}, {deta, bytes4(H, 1, 1, 1, 4)}, {dW0, hdd},
                            {workspace, ws_bytes}},
                           {{Q, seq}, {K, seq}, {V, seq}, {dZ, seq}, {eta, bytes4(H, 1, 1, 1, 4)}, {W0, hdd},
@@ -646,26 +648,38 @@ ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ttt::LinearBwdParams p;
-  p.Q = static_cast<const float*>(Q);
-  p.K = static_cast<const float*>(K);
-  p.V = static_cast<const float*>(V);
-  p.dZ = static_cast<const float*>(dZ);
+  p.Q = Q; p.K = K; p.V = V; p.dZ = dZ;
   p.eta = eta;
   p.W0 = W0;
   p.dW_out = dW_out;
-  p.dQ = static_cast<float*>(dQ);
-  p.dK = static_cast<float*>(dK);
-  p.dV = static_cast<float*>(dV);
+  p.dQ = dQ; p.dK = dK; p.dV = dV;
   p.deta = deta;
   p.dW0 = dW0;
   p.B = B; p.H = H; p.T = T; p.d = d; p.b = b;
   p.units = B * H;
+  p.bf16 = bf16;
   p.states = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
   const size_t nch = (static_cast<size_t>(T) + b - 1) / b;
   p.partial = p.states + static_cast<size_t>(p.units) * nch * d * d;
+  p.status = static_cast<ttt::StatusBlock*>(workspace);
+  p.timeout_ns = kDefaultTimeoutNs;
   const ttt_status st = reset_status(workspace, s);
   if (st != TTT_OK) return st;
-  return ttt::launch_linear_bwd(p, s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+  cudaError_t err;
+  if (mma) {
+    CUtensorMap mq, mk, mv, mdz;
+    const int rows = ttt::linear_bwd_mma_rows();
+    if (!encode_3d(&mq, Q, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mk, K, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&mdz, dZ, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
+      return TTT_ERR_CUDA;
+    err = ttt::launch_linear_bwd_mma(p, mq, mk, mv, mdz, s);
+  } else {
+    err = ttt::launch_linear_bwd(p, s);
+  }
+  if (err == cudaSuccess) err = ttt::launch_linear_bwd_reduce(p, s);
+  return err == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
 ttt_status ttt_last_device_status(void* workspace, void* stream) {

@@ -177,7 +177,7 @@ def test_backward_workspace_bytes(lib):
 @pytest.mark.parametrize("kw,want", [(dict(Q=0), ttt.TTT_ERR_ARG), (dict(dZ=0), ttt.TTT_ERR_ARG),
                                      (dict(deta=0), ttt.TTT_ERR_ARG), (dict(dW0=4100), ttt.TTT_ERR_ARG),
                                      (dict(wsb=4096), ttt.TTT_ERR_ARG), (dict(b=0), ttt.TTT_ERR_ARG),
-                                     (dict(dt=5), ttt.TTT_ERR_ARG), (dict(dt=1), ttt.TTT_ERR_UNSUPPORTED),
+                                     (dict(dt=5), ttt.TTT_ERR_ARG), (dict(dt=1, b=65), ttt.TTT_ERR_UNSUPPORTED),
                                      (dict(d=65), ttt.TTT_ERR_UNSUPPORTED), (dict(b=65), ttt.TTT_ERR_UNSUPPORTED)])
 def test_backward_rejects_bad_arguments(lib, kw, want):
     assert _bwd(lib, **kw) == want

@@ -3,7 +3,9 @@
 ttt_linear_bwd returns dQ, dK, dV, d eta and dW0 for upstream dZ and dW_out;
 oracle.backward.linear_backward (pinned by finite differences and autograd in
 test_oracle_backward.py) computes the same in fp64 from the same fp32 inputs.
-Bar: rel-L2 <= 1e-4 per output (fp32 operands).
+Bars: rel-L2 <= 1e-4 per output with fp32 operands, <= 2e-2 with bf16 operands.
+bf16 with d = 64 and b = 16 runs the tensor-core kernel (linear_bwd_mma.cu); other
+bf16 shapes and every fp32 case run the fp32 SIMT kernel.
 """
 import numpy as np
 import pytest
@@ -57,3 +59,50 @@ def test_backward_empty_sequence():
     torch.cuda.synchronize()
     assert np.array_equal(deta.cpu().numpy(), np.zeros(2, np.float32))
     assert np.allclose(dW0.cpu().numpy(), dW.sum(0), atol=1e-6)
+
+
+def bf16_round(a):
+    return torch.from_numpy(a).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+@pytest.mark.parametrize("B,H,T,d,b", [(1, 1, 16, 64, 16), (1, 2, 64, 64, 16), (2, 2, 100, 64, 16),
+                                       (1, 3, 130, 64, 16), (2, 1, 257, 64, 16), (1, 2, 1000, 64, 16),
+                                       (2, 2, 70, 32, 5), (1, 2, 50, 64, 32)])
+def test_backward_bf16_matches_oracle(B, H, T, d, b):
+    """bf16 operands: the tensor-core kernel (d = 64, b = 16: single chunks, ragged tails, one
+    and several 64-token blocks) and the SIMT kernel on other shapes, against the fp64 backward
+    of the same bf16 values."""
+    w = W["linear_small"].with_(B=B, H=H, T=T, d=d, b=b, eta=("uniform", 0.05, 0.5), seed=60 + T + d + b)
+    inp = synth.make_inputs(w)
+    g = np.random.default_rng(T + 3 * b)
+    dZ = bf16_round(g.standard_normal((B, H, T, d)).astype(np.float32))
+    dW = g.standard_normal((B, H, d, d)).astype(np.float32)
+    t = torch_inputs(inp)
+    dev = t["Q"].device
+    got = ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], b,
+                             torch.from_numpy(dZ).to(dev).to(torch.bfloat16), torch.from_numpy(dW).to(dev))
+    torch.cuda.synchronize()
+    assert got[0].dtype == torch.bfloat16
+    want = linear_backward(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, b, dZ, dW)
+    for name, gg, r in zip(("dQ", "dK", "dV", "deta", "dW0"), got, want):
+        gg = to64(gg)
+        assert np.all(np.isfinite(gg)), name
+        assert rel_err(f"bf16 {name}", gg, r, 2e-2) <= 2e-2, (name, rel_l2(gg, r))
+
+
+def test_backward_bf16_125m_shape_sampled_heads():
+    """B2 H12 T2048 (125M-shaped heads, shorter sequence), bf16, b = 16, per-head eta in
+    [0.05, 0.5]: the tensor-core kernel over every unit, the oracle on every unit too."""
+    w = W["linear_125m"].with_(B=2, H=12, T=2048, seed=65)
+    inp = synth.make_inputs(w)
+    g = np.random.default_rng(66)
+    dZ = bf16_round(g.standard_normal((w.B, w.H, w.T, w.d)).astype(np.float32))
+    dW = g.standard_normal((w.B, w.H, w.d, w.d)).astype(np.float32)
+    t = torch_inputs(inp)
+    dev = t["Q"].device
+    got = ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16,
+                             torch.from_numpy(dZ).to(dev).to(torch.bfloat16), torch.from_numpy(dW).to(dev))
+    torch.cuda.synchronize()
+    want = linear_backward(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, 16, dZ, dW)
+    for name, gg, r in zip(("dQ", "dK", "dV", "deta", "dW0"), got, want):
+        assert rel_err(f"bf16 125m {name}", to64(gg), r, 2e-2) <= 2e-2, name
