@@ -623,7 +623,25 @@ def bench_extras(ttt, dev, stream):
         del Q, K, V
     except Exception as exc:  # reported in the line, never silently dropped
         out["variants"] = {"error": f"{type(exc).__name__}: {exc}"}
-    # backward of TTT-Linear (fp32 operands, the first GPU form: one CTA per unit)
+    # backward of TTT-Linear on the tensor cores (bf16, b = 16), 125M-shaped: B8 H12 T8192
+    try:
+        w = synth.WORKLOADS["linear_125m"]
+        inp, Q, K, V, eta = dev_inputs(w)
+        W0 = torch.from_numpy(inp.W0).to(dev)
+        dZ = torch.randn_like(Q, dtype=torch.float32).to(torch.bfloat16)
+        dW = torch.randn(w.B, w.H, w.d, w.d, device=dev)
+        ws = torch.empty(ttt.ttt_linear_bwd_workspace_bytes(w.B, w.H, w.T, w.d, 16), dtype=torch.uint8, device=dev)
+        ms = t_ms(lambda: ttt.ttt_linear_bwd(Q, K, V, eta, W0, 16, dZ, dW, workspace=ws, stream=stream), 5)
+        # algorithmic bytes: Q, K, V, dZ read and dQ, dK, dV written once (bf16), states aside
+        bwd_bytes = w.token_heads * 7 * w.d * 2
+        out["linear_bwd_125m_bf16_b16"] = {"ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                                           "hbm_frac": round(bwd_bytes / (ms * 1e-3) / 1e9 / hbm_gbs, 4),
+                                           "note": "B8 H12 T8192 d64 bf16; tensor-core backward, one CTA per "
+                                                   "(batch row, head), W kept every 64 tokens"}
+        del Q, K, V, dZ
+    except Exception as exc:  # reported in the line, never silently dropped
+        out["linear_bwd_125m_bf16_b16"] = {"error": f"{type(exc).__name__}: {exc}"}
+    # backward of TTT-Linear, fp32 operands (the SIMT kernel: one CTA per unit)
     try:
         w = synth.WORKLOADS["linear_small"].with_(dtype="f32")
         inp = synth.make_inputs(w, want_exact=False)

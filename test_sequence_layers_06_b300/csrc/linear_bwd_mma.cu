@@ -15,8 +15,11 @@
 // Design. The chunk rule splits over the output columns j of W, and so do E, G
 // and dE: each of 4 consumer warps owns 16 columns and keeps G^T (16 x 64) as
 // fp32 mma.sync accumulator fragments for the whole sequence. dQ, dK and P sum
-// over all columns, so each warp forms its columns' share and the four shares
-// are added through shared memory.
+// over all columns: once every warp has written its columns of G and dE (bf16,
+// shared memory), each warp forms the full P and the dQ, dK of its own band of
+// 16 input features from those full-width copies, so a chunk needs one meeting
+// of the four warps. The copies of W, E (per block) and of G, dE (per chunk)
+// are kept twice, so that the next one can be written while the last is read.
 //   Pass 1 walks the sequence forward (K, V only), keeping W in fragments as the
 //   forward kernel does, and writes W at the start of every 64-token block to
 //   the workspace (fp32).
@@ -44,18 +47,16 @@ constexpr int kBlkBytes = kBlk * kD * 2;     // 8 KB
 constexpr int kP1 = 0;                                  // pass 1: [2 stages][K, V] blocks
 constexpr int kP2 = kP1 + 2 * 2 * kBlkBytes;            // pass 2: [2 stages][Q, K, V, dZ] blocks
 constexpr int kSb = kP2 + 2 * 4 * kBlkBytes;            // [2 stages][4 chunks][S, S^T] B fragments, 512 B each
-constexpr int kWc = kSb + 2 * 4 * 2 * 512;              // [4 chunks] W bf16 [i][j]
-constexpr int kEc = kWc + 4 * kD * kD * 2;              // [4 chunks] E bf16 [t][j]
-constexpr int kGc = kEc + 4 * kTileBytes;               // G bf16 [i][j]
-constexpr int kDE = kGc + kD * kD * 2;                  // dE bf16 [t][j]
-constexpr int kOut = kDE + kTileBytes;                  // [4 warps][2] 16 x 16 bf16 output staging
-constexpr int kPp = kOut + kWarps * 2 * 512;            // P shares fp32 [4 warps][16][16]
-constexpr int kPad = 68;                                // fp32 row stride of the dQ/dK shares
-constexpr int kQp = kPp + kWarps * kTile * kTile * 4;   // dQ shares fp32 [4][16][kPad]
-constexpr int kKp = kQp + kWarps * kTile * kPad * 4;    // dK shares fp32 [4][16][kPad]
-constexpr int kRed = kKp + kWarps * kTile * kPad * 4;   // d eta per warp
+constexpr int kWcBytes = 4 * kD * kD * 2;             // [4 chunks] W bf16 [i][j]
+constexpr int kEcBytes = 4 * kTileBytes;                // [4 chunks] E bf16 [t][j]
+constexpr int kWc = kSb + 2 * 4 * 2 * 512;              // [2 blocks] W copies
+constexpr int kEc = kWc + 2 * kWcBytes;                 // [2 blocks] E copies
+constexpr int kGc = kEc + 2 * kEcBytes;                 // [2 chunks] G bf16 [i][j]
+constexpr int kDE = kGc + 2 * kD * kD * 2;              // [2 chunks] dE bf16 [t][j]
+constexpr int kOut = kDE + 2 * kTileBytes;              // [4 warps][2] 16 x 16 bf16 output staging
+constexpr int kRed = kOut + kWarps * 2 * 512;           // d eta per warp
 constexpr int kBar = kRed + 64;
-constexpr int kNumBars = 12;
+constexpr int kNumBars = 11;
 constexpr int kMisc = kBar + kNumBars * 8;              // abort flag
 constexpr int kSmemBytes = kMisc + 16 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "fits one CTA per SM");
@@ -68,6 +69,13 @@ __device__ __forceinline__ void unpack4(uint4 v, float (&s)[2][4]) {
   s[1][0] = bf16_lo(v.y); s[1][1] = bf16_hi(v.y);
   s[0][2] = bf16_lo(v.z); s[0][3] = bf16_hi(v.z);
   s[1][2] = bf16_lo(v.w); s[1][3] = bf16_hi(v.w);
+}
+
+// Transpose of an 8 x 8 bf16 matrix held one row pair per thread (the fragment layout).
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
 
 // A fragments (bf16) of a 16 x 64 block of X^T held as fp32 C fragments xt[8][4]
@@ -101,8 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full2 = full1 + 4;
   uint64_t* ready2 = full1 + 6;
   uint64_t* empty2 = full1 + 8;
-  uint64_t* sync1 = full1 + 10;  // P shares written (4 warps)
-  uint64_t* sync2 = full1 + 11;  // dQ, dK shares written (4 warps)
+  uint64_t* sync1 = full1 + 10;  // the four consumer warps meet (copies of W, E, G, dE written)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc);
   const uint32_t s0 = smem_u32(sm);
 
@@ -124,7 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty2[i], kWarps);
     }
     mbar_init(sync1, kWarps);
-    mbar_init(sync2, kWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -342,16 +348,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   float deta = 0.f;
-  // The stores of pass 1 must be visible to this CTA's loads of the checkpoints.
-  __threadfence_block();
-  int ktile = 0;  // chunks done in pass 2 (phase of sync1 / sync2)
+  int nsync = 0;  // uses of the consumers' sync barrier (its phase)
+  auto sync_all = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sync1);
+    const bool done = __all_sync(0xffffffffu, mbar_wait_or_abort(sync1, nsync & 1, p.timeout_ns, abort_flag));
+    ++nsync;
+    return done;
+  };
   __nv_bfloat16* dQg = static_cast<__nv_bfloat16*>(p.dQ);
   __nv_bfloat16* dKg = static_cast<__nv_bfloat16*>(p.dK);
   __nv_bfloat16* dVg = static_cast<__nv_bfloat16*>(p.dV);
   const size_t base = static_cast<size_t>(unit) * T * kD;
-  float* ppart = reinterpret_cast<float*>(sm + kPp);
-  float* qpart = reinterpret_cast<float*>(sm + kQp);
-  float* kpart = reinterpret_cast<float*>(sm + kKp);
+  int ktile = 0;  // chunks done in pass 2 (which G and dE copy)
 
   for (int r = 0; ok && r < nblk; ++r) {
     const int bk = nblk - 1 - r, s = r & 1;
@@ -364,34 +373,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQb = s0 + kP2 + s * 4 * kBlkBytes, sKb = sQb + kBlkBytes, sVb = sQb + 2 * kBlkBytes,
                    sZb = sQb + 3 * kBlkBytes;
     const int nt = min(4, ntiles - 4 * bk);
-    // Recompute the block's chunk states and errors from its checkpoint.
+    // Recompute the block's chunk states and errors from its checkpoint into this block's
+    // copies (two sets, by block parity: the other set may still be read for the previous block).
+    const uint32_t sWc = s0 + kWc + (r & 1) * kWcBytes, sEc = s0 + kEc + (r & 1) * kEcBytes;
     load_w(ckpt + static_cast<size_t>(bk) * kD * kD);
     for (int u = 0; u < nt; ++u) {
       float e[2][4];
       uint32_t wa[4][4];
       chunk_forward(sKb + u * kTileBytes, sVb + u * kTileBytes, u + 1 < nt, e, wa);
-      store_t(s0 + kWc + u * kD * kD * 2, wa, warp, lane);  // W_u [i][j], this warp's columns
-      // E_u [t][j]: E^T (rows j, columns t) through a transposing stmatrix.
+      store_t(sWc + u * kD * kD * 2, wa, warp, lane);  // W_u [i][j], this warp's columns
       const uint32_t ev[4] = {pack_bf16(e[0][0], e[0][1]), pack_bf16(e[0][2], e[0][3]), pack_bf16(e[1][0], e[1][1]),
                               pack_bf16(e[1][2], e[1][3])};
-      stsm_x4_t(s0 + kEc + u * kTileBytes + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)), ev);
+      stsm_x4_t(sEc + u * kTileBytes + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)), ev);  // E_u [t][j]
     }
-    __syncwarp();
+    if (!sync_all()) {  // every warp's columns of W_u and E_u are in place
+      ok = false;
+      break;
+    }
 
     for (int u = nt - 1; u >= 0; --u, ++ktile) {
       const uint32_t sQ = sQb + u * kTileBytes, sK = sKb + u * kTileBytes, sZ = sZb + u * kTileBytes;
-      const uint32_t sW = s0 + kWc + u * kD * kD * 2, sE = s0 + kEc + u * kTileBytes;
+      const uint32_t sW = sWc + u * kD * kD * 2, sE = sEc + u * kTileBytes;
+      const uint32_t sG = s0 + kGc + (ktile & 1) * kD * kD * 2, sDE = s0 + kDE + (ktile & 1) * kTileBytes;
       const uint8_t* sfr = sm + kSb + ((s * 4 + u) * 2) * 512 + lane * 16;
-      const uint4 sv = *reinterpret_cast<const uint4*>(sfr);        // S (rows t, columns t')
-      const uint4 stv = *reinterpret_cast<const uint4*>(sfr + 512); // S^T (rows t, columns t')
 
-      // G (bf16, [i][j]) for this warp's columns: the B operand of E G^T.
+      // ---- this warp's output columns j: dE, dV, its part of d eta, and the G update.
       uint32_t ga[4][4];
       pack_a(Gt, ga);
-      store_t(s0 + kGc, ga, warp, lane);
-
-      // (K G)^T = G^T K^T (rows j, columns t).
-      float kg[2][4] = {};
+      store_t(sG, ga, warp, lane);  // G [i][j] before this chunk's update, this warp's columns
+      float kg[2][4] = {};          // (K G)^T = G^T K^T (rows j, columns t)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t rr[4];
@@ -400,62 +410,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16_16816(kg[0], ga[k], b0);
         mma_bf16_16816(kg[1], ga[k], b1);
       }
-      // dZ^T as A (m = j, k = t') and (S^T dZ)^T = dZ^T S (B[k = t'][n = t] = S[t'][t]: S^T's C fragment).
-      uint32_t zt[4];
+      uint32_t zt[4];  // dZ^T as A (m = j, k = t')
       ldsm_x4_t(zt, sZ + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
       float de[2][4];
       {
+        const uint4 stv = *reinterpret_cast<const uint4*>(sfr + 512);  // S^T: B[k = t'][n = t] = S[t'][t]
         float zs[2][4] = {};
         const uint32_t b0[2] = {stv.x, stv.y}, b1[2] = {stv.z, stv.w};
         mma_bf16_16816(zs[0], zt, b0);
         mma_bf16_16816(zs[1], zt, b1);
 #pragma unroll
-        for (int nt2 = 0; nt2 < 2; ++nt2)
+        for (int n2 = 0; n2 < 2; ++n2)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) de[nt2][q] = -eta * (kg[nt2][q] + zs[nt2][q]);
+          for (int q = 0; q < 4; ++q) de[n2][q] = -eta * (kg[n2][q] + zs[n2][q]);
       }
-      // d eta: -sum(E .* K G) over this warp's columns (E^T in the C layout of kg).
-      {
+      {  // d eta: -sum(E .* K G) over this warp's columns
         uint32_t et[4];
         ldsm_x4_t(et, sE + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
 #pragma unroll
-        for (int nt2 = 0; nt2 < 2; ++nt2)
-          deta -= bf16_lo(et[2 * nt2]) * kg[nt2][0] + bf16_hi(et[2 * nt2]) * kg[nt2][1] +
-                  bf16_lo(et[2 * nt2 + 1]) * kg[nt2][2] + bf16_hi(et[2 * nt2 + 1]) * kg[nt2][3];
+        for (int n2 = 0; n2 < 2; ++n2)
+          deta -= bf16_lo(et[2 * n2]) * kg[n2][0] + bf16_hi(et[2 * n2]) * kg[n2][1] +
+                  bf16_lo(et[2 * n2 + 1]) * kg[n2][2] + bf16_hi(et[2 * n2 + 1]) * kg[n2][3];
       }
-      // dE (bf16, [t][j]) for this warp's columns; dV = -dE goes out from it.
       const uint32_t dea[4] = {pack_bf16(de[0][0], de[0][1]), pack_bf16(de[0][2], de[0][3]),
                                pack_bf16(de[1][0], de[1][1]), pack_bf16(de[1][2], de[1][3])};
-      stsm_x4_t(s0 + kDE + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)), dea);
-
-      // This warp's share of P: dZ[:, own] E[:, own]^T (rows t, columns t').
-      uint32_t za[4];
-      ldsm_x4(za, sZ + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));  // dZ as A (m = t, k = j)
-      {
-        float pw[2][4] = {};
-        uint32_t rr[4];
-        ldsm_x4(rr, sE + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));  // E as B (k = j, n = t')
-        const uint32_t b0[2] = {rr[0], rr[1]}, b1[2] = {rr[2], rr[3]};
-        mma_bf16_16816(pw[0], za, b0);
-        mma_bf16_16816(pw[1], za, b1);
-        float sf[2][4];
-        unpack4(sv, sf);
-#pragma unroll
-        for (int nt2 = 0; nt2 < 2; ++nt2)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) deta -= sf[nt2][q] * pw[nt2][q];
-        float* dst = ppart + warp * kTile * kTile;
-#pragma unroll
-        for (int nt2 = 0; nt2 < 2; ++nt2) {
-          const int c = 8 * nt2 + 2 * tg;
-          *reinterpret_cast<float2*>(dst + g * kTile + c) = make_float2(pw[nt2][0], pw[nt2][1]);
-          *reinterpret_cast<float2*>(dst + (g + 8) * kTile + c) = make_float2(pw[nt2][2], pw[nt2][3]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sync1);
-
-      // G^T += dZ^T Q + dE^T K (this warp's rows j), from the chunk's own tiles.
+      stsm_x4_t(sDE + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)), dea);  // dE [t][j]
+      // G^T += dZ^T Q + dE^T K (the copy in sG keeps the G this chunk's products need).
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         uint32_t rq[4], rk[4];
@@ -468,150 +448,105 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16_16816(Gt[2 * qq], dea, k0);
         mma_bf16_16816(Gt[2 * qq + 1], dea, k1);
       }
-
-      // Every warp's P share is written: P = -eta tril(sum of shares), as A fragments of P
-      // and of P^T (rows t, k = t').
-      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(sync1, ktile & 1, p.timeout_ns, abort_flag))) {
-        if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdSync, unit);
-        *abort_flag = 1;
+      const int tok0 = 64 * bk + 16 * u;
+      {  // dV = -dE for this warp's columns
+        __syncwarp();
+        const int tok = tok0 + (lane >> 1);
+        uint4 x = *reinterpret_cast<const uint4*>(sm + (sDE - s0) + swz128(lane >> 1, 2 * warp + (lane & 1)));
+        x.x ^= 0x80008000u;
+        x.y ^= 0x80008000u;
+        x.z ^= 0x80008000u;
+        x.w ^= 0x80008000u;
+        if (tok < T) *reinterpret_cast<uint4*>(dVg + base + static_cast<size_t>(tok) * kD + jw + 8 * (lane & 1)) = x;
+      }
+      if (!sync_all()) {  // every warp's columns of G and dE are in place
         ok = false;
         break;
       }
+
+      // ---- this warp's band of input features i in [16w, 16w + 16): P, dQ, dK over all columns.
+      uint32_t za[4][4];  // dZ as A (m = t, k = j), k-step k: j in [16k, 16k + 16)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ldsm_x4(za[k], sZ + swz128(((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));
       uint32_t pa[4], pta[4];
-      {
-        auto P = [&](int t, int t2) -> float {
-          if (t2 > t) return 0.f;
-          float v = 0.f;
+      {  // P = -eta tril(dZ E^T), the full 16 x 16 (every warp forms it)
+        float pc[2][4] = {};
 #pragma unroll
-          for (int w = 0; w < kWarps; ++w) v += ppart[w * kTile * kTile + t * kTile + t2];
-          return -eta * v;
-        };
-        // A fragment of a 16 x 16 X: {(g, 2tg), (g + 8, 2tg), (g, 2tg + 8), (g + 8, 2tg + 8)} pairs
-        pa[0] = pack_bf16(P(g, 2 * tg), P(g, 2 * tg + 1));
-        pa[1] = pack_bf16(P(g + 8, 2 * tg), P(g + 8, 2 * tg + 1));
-        pa[2] = pack_bf16(P(g, 2 * tg + 8), P(g, 2 * tg + 9));
-        pa[3] = pack_bf16(P(g + 8, 2 * tg + 8), P(g + 8, 2 * tg + 9));
-        pta[0] = pack_bf16(P(2 * tg, g), P(2 * tg + 1, g));
-        pta[1] = pack_bf16(P(2 * tg, g + 8), P(2 * tg + 1, g + 8));
-        pta[2] = pack_bf16(P(2 * tg + 8, g), P(2 * tg + 9, g));
-        pta[3] = pack_bf16(P(2 * tg + 8, g + 8), P(2 * tg + 9, g + 8));
-      }
-      // The shares of the previous chunk have been read by every warp (they all passed sync1
-      // of this chunk after summing them), so the buffers may be rewritten.
-      // This warp's shares of dQ (dZ W^T) and dK (dE W^T - eta E G^T) over its columns.
-      {
-        uint32_t dza[4], ea[4];
-        ldsm_x4(dza, s0 + kDE + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));  // dE as A (m = t, k = j)
-        ldsm_x4(ea, sE + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));        // E as A
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ea[q] = pack_bf16(-eta * bf16_lo(ea[q]), -eta * bf16_hi(ea[q]));
-        float acc[8][4];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {  // W rows i in [16pp, 16pp + 16) as B (k = j, n = i)
+        for (int k = 0; k < 4; ++k) {
           uint32_t rr[4];
-          ldsm_x4(rr, sW + swz128(16 * pp + ((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
+          ldsm_x4(rr, sE + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));  // E as B (k = j, n = t')
           const uint32_t b0[2] = {rr[0], rr[1]}, b1[2] = {rr[2], rr[3]};
-          mma_bf16_16816(acc[2 * pp], za, b0);
-          mma_bf16_16816(acc[2 * pp + 1], za, b1);
+          mma_bf16_16816(pc[0], za[k], b0);
+          mma_bf16_16816(pc[1], za[k], b1);
         }
-        float* dq = qpart + warp * kTile * kPad;
+        if (warp == 0) {  // d eta: -sum(S .* dZ E^T), once
+          float sf[2][4];
+          unpack4(*reinterpret_cast<const uint4*>(sfr), sf);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = 8 * q + 2 * tg;
-          *reinterpret_cast<float2*>(dq + g * kPad + c) = make_float2(acc[q][0], acc[q][1]);
-          *reinterpret_cast<float2*>(dq + (g + 8) * kPad + c) = make_float2(acc[q][2], acc[q][3]);
-          acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+          for (int n2 = 0; n2 < 2; ++n2)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) deta -= sf[n2][q] * pc[n2][q];
         }
 #pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          uint32_t rw[4], rg[4];
-          ldsm_x4(rw, sW + swz128(16 * pp + ((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
-          ldsm_x4(rg, s0 + kGc + swz128(16 * pp + ((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
-          const uint32_t w0[2] = {rw[0], rw[1]}, w1[2] = {rw[2], rw[3]};
-          const uint32_t g0[2] = {rg[0], rg[1]}, g1[2] = {rg[2], rg[3]};
-          mma_bf16_16816(acc[2 * pp], dza, w0);
-          mma_bf16_16816(acc[2 * pp + 1], dza, w1);
-          mma_bf16_16816(acc[2 * pp], ea, g0);
-          mma_bf16_16816(acc[2 * pp + 1], ea, g1);
+        for (int n2 = 0; n2 < 2; ++n2) {  // keep t' <= t, scale by -eta
+          const int c = 8 * n2 + 2 * tg;
+          pc[n2][0] = c > g ? 0.f : -eta * pc[n2][0];
+          pc[n2][1] = c + 1 > g ? 0.f : -eta * pc[n2][1];
+          pc[n2][2] = c > g + 8 ? 0.f : -eta * pc[n2][2];
+          pc[n2][3] = c + 1 > g + 8 ? 0.f : -eta * pc[n2][3];
         }
-        float* dk = kpart + warp * kTile * kPad;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = 8 * q + 2 * tg;
-          *reinterpret_cast<float2*>(dk + g * kPad + c) = make_float2(acc[q][0], acc[q][1]);
-          *reinterpret_cast<float2*>(dk + (g + 8) * kPad + c) = make_float2(acc[q][2], acc[q][3]);
-        }
+        pa[0] = pack_bf16(pc[0][0], pc[0][1]);
+        pa[1] = pack_bf16(pc[0][2], pc[0][3]);
+        pa[2] = pack_bf16(pc[1][0], pc[1][1]);
+        pa[3] = pack_bf16(pc[1][2], pc[1][3]);
+        pta[0] = movm_t(pa[0]);  // P^T's 8 x 8 blocks are the transposed blocks of P
+        pta[1] = movm_t(pa[2]);
+        pta[2] = movm_t(pa[1]);
+        pta[3] = movm_t(pa[3]);
       }
-
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sync2);
-      if (!__all_sync(0xffffffffu, mbar_wait_or_abort(sync2, ktile & 1, p.timeout_ns, abort_flag))) {
-        if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdSync, unit);
-        *abort_flag = 1;
-        ok = false;
-        break;
-      }
-      // This warp's output columns i in [16w, 16w + 16): sum of the shares + P K (dQ) and P^T Q (dK).
+      float oq[2][4] = {}, ok2[2][4] = {};
       {
-        float oq[2][4], ok2[2][4];
-#pragma unroll
-        for (int nt2 = 0; nt2 < 2; ++nt2) {
-          const int c = jw + 8 * nt2 + 2 * tg;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int t = g + 8 * half;
-            float2 sq = make_float2(0.f, 0.f), sk = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-              const float2 a = *reinterpret_cast<const float2*>(qpart + w * kTile * kPad + t * kPad + c);
-              const float2 b = *reinterpret_cast<const float2*>(kpart + w * kTile * kPad + t * kPad + c);
-              sq.x += a.x;
-              sq.y += a.y;
-              sk.x += b.x;
-              sk.y += b.y;
-            }
-            oq[nt2][2 * half] = sq.x;
-            oq[nt2][2 * half + 1] = sq.y;
-            ok2[nt2][2 * half] = sk.x;
-            ok2[nt2][2 * half + 1] = sk.y;
-          }
-        }
-        uint32_t rk[4], rq[4];  // K and Q as B (k = t', n = i) for i in [16w, 16w + 16)
+        uint32_t rk[4], rq[4];  // K and Q as B (k = t', n = i in the band)
         ldsm_x4_t(rk, sK + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));
         ldsm_x4_t(rq, sQ + swz128(((mi & 1) << 3) + mr, 2 * warp + (mi >> 1)));
         const uint32_t k0[2] = {rk[0], rk[1]}, k1[2] = {rk[2], rk[3]};
         const uint32_t q0[2] = {rq[0], rq[1]}, q1[2] = {rq[2], rq[3]};
-        mma_bf16_16816(oq[0], pa, k0);
+        mma_bf16_16816(oq[0], pa, k0);   // P K
         mma_bf16_16816(oq[1], pa, k1);
-        mma_bf16_16816(ok2[0], pta, q0);
+        mma_bf16_16816(ok2[0], pta, q0); // P^T Q
         mma_bf16_16816(ok2[1], pta, q1);
-        // Out through the warp's staging tile ([t][16 i], 32-byte rows), one 16-byte store per lane.
-        const int tok0 = 64 * bk + 16 * u;
-        auto emit = [&](const float (&o)[2][4], __nv_bfloat16* dst, int buf) {
-          uint8_t* stg = sm + kOut + (warp * 2 + buf) * 512;
-          const uint32_t v[4] = {pack_bf16(o[0][0], o[0][1]), pack_bf16(o[0][2], o[0][3]), pack_bf16(o[1][0], o[1][1]),
-                                 pack_bf16(o[1][2], o[1][3])};
-          stsm_x4(smem_u32(stg) + ((mi & 1) * 8 + mr) * 32 + (mi >> 1) * 16, v);
-          __syncwarp();
-          const int tok = tok0 + (lane >> 1);
-          const uint4 x = *reinterpret_cast<const uint4*>(stg + (lane >> 1) * 32 + (lane & 1) * 16);
-          if (tok < T) *reinterpret_cast<uint4*>(dst + base + static_cast<size_t>(tok) * kD + jw + 8 * (lane & 1)) = x;
-        };
-        emit(oq, dQg, 0);
-        emit(ok2, dKg, 1);
-        // dV = -dE for this warp's columns j (the same 16-column band), from the dE tile.
-        {
-          const int tok = tok0 + (lane >> 1);
-          uint4 x = *reinterpret_cast<const uint4*>(sm + kDE + swz128(lane >> 1, 2 * warp + (lane & 1)));
-          x.x ^= 0x80008000u;
-          x.y ^= 0x80008000u;
-          x.z ^= 0x80008000u;
-          x.w ^= 0x80008000u;
-          if (tok < T) *reinterpret_cast<uint4*>(dVg + base + static_cast<size_t>(tok) * kD + jw + 8 * (lane & 1)) = x;
-        }
       }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // sums over the columns j in [16k, 16k + 16)
+        uint32_t rw[4], rg[4], ea[4], da[4];
+        ldsm_x4(rw, sW + swz128(jw + ((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));  // W rows i as B (k = j, n = i)
+        ldsm_x4(rg, sG + swz128(jw + ((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));  // G rows i as B
+        ldsm_x4(ea, sE + swz128(((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));       // E as A (m = t, k = j)
+        ldsm_x4(da, sDE + swz128(((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));      // dE as A
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ea[q] = pack_bf16(-eta * bf16_lo(ea[q]), -eta * bf16_hi(ea[q]));
+        const uint32_t w0[2] = {rw[0], rw[1]}, w1[2] = {rw[2], rw[3]};
+        const uint32_t g0[2] = {rg[0], rg[1]}, g1[2] = {rg[2], rg[3]};
+        mma_bf16_16816(oq[0], za[k], w0);  // dZ W^T
+        mma_bf16_16816(oq[1], za[k], w1);
+        mma_bf16_16816(ok2[0], da, w0);    // dE W^T
+        mma_bf16_16816(ok2[1], da, w1);
+        mma_bf16_16816(ok2[0], ea, g0);    // -eta E G^T
+        mma_bf16_16816(ok2[1], ea, g1);
+      }
+      // Out through the warp's staging tile ([t][16 i], 32-byte rows), one 16-byte store per lane.
+      auto emit = [&](const float (&o)[2][4], __nv_bfloat16* dst, int buf) {
+        uint8_t* stg = sm + kOut + (warp * 2 + buf) * 512;
+        const uint32_t v[4] = {pack_bf16(o[0][0], o[0][1]), pack_bf16(o[0][2], o[0][3]), pack_bf16(o[1][0], o[1][1]),
+                               pack_bf16(o[1][2], o[1][3])};
+        stsm_x4(smem_u32(stg) + ((mi & 1) * 8 + mr) * 32 + (mi >> 1) * 16, v);
+        __syncwarp();
+        const int tok = tok0 + (lane >> 1);
+        const uint4 x = *reinterpret_cast<const uint4*>(stg + (lane >> 1) * 32 + (lane & 1) * 16);
+        if (tok < T) *reinterpret_cast<uint4*>(dst + base + static_cast<size_t>(tok) * kD + jw + 8 * (lane & 1)) = x;
+      };
+      emit(oq, dQg, 0);
+      emit(ok2, dKg, 1);
       __syncwarp();
     }
     if (!ok) break;
@@ -620,6 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty2[s]);
   }
+  if (!ok && !*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdSync, unit);
+  if (!ok) *abort_flag = 1;
 
   // dW0 share of this unit (G after the first chunk) and d eta.
   float* part = p.partial + static_cast<size_t>(unit) * (kD * kD + 1);
@@ -637,7 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (lane == 0) red[warp] = deta;
   asm volatile("bar.sync 1, %0;" ::"n"(kWarps * 32) : "memory");  // the four consumer warps only
   if (threadIdx.x == 0) part[kD * kD] = red[0] + red[1] + red[2] + red[3];
-  if (!ok && lane == 0 && !*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdPass2, unit);
 }
 
 }  // namespace
