@@ -681,10 +681,18 @@ def bench_extras(ttt, dev, stream):
             for i in range(100):
                 ttt.ttt_linear_decode_step(q, q, q, e32, Wa, Wr, 5 + i, 16, z=z, stream=side)
         gms = t_ms(graph.replay, 10) / 100
+        per_launch = {}
+        for n in (16, 128):  # n tokens per launch (ttt_linear_decode), state kept in registers between them
+            qn = torch.randn(1, 32, n, 64, device=dev).to(torch.bfloat16)
+            zn = torch.empty_like(qn)
+            per_launch[str(n)] = round(t_ms(lambda: ttt.ttt_linear_decode(qn, qn, qn, e32, Wa, Wr, 5, 16, z=zn,
+                                                                          stream=stream), 20) * 1e3 / n, 3)
         out["decode_long_1tok"] = {"us_per_step": round(ms * 1e3, 2),
                                    "us_per_step_cuda_graph": round(gms * 1e3, 2),
-                                   "note": "B1 H32 d64 bf16, one token per call; first through the Python "
-                                           "binding per call, second 100 calls replayed from a CUDA graph"}
+                                   "us_per_token_n_per_launch": per_launch,
+                                   "note": "B1 H32 d64 bf16: one token per call through the Python binding, "
+                                           "100 one-token calls replayed from a CUDA graph, and n tokens per "
+                                           "ttt_linear_decode launch (us per token); floor ~0.25 us (state bytes)"}
     except Exception as exc:  # reported in the line, never silently dropped
         out["decode_long_1tok"] = {"error": f"{type(exc).__name__}: {exc}"}
     return out

@@ -228,6 +228,16 @@ TTT_API ttt_status ttt_linear_decode_step(const void* q, const void* k, const vo
                                   const float* eta, float* W_anchor, float* W_run, int B, int H,
                                   int d, int pos, int b, void* z, void* stream);
 
+/* N decode tokens per (batch row, head) in one launch: tokens pos .. pos + N - 1,
+ * each exactly as ttt_linear_decode_step (the chunk-start anchor moves whenever
+ * a token completes a chunk). q, k, v, z [B][H][N][d], dtype dt; W_anchor, W_run
+ * as above (in/out). N = 0 enqueues nothing. Calling it equals N calls of
+ * ttt_linear_decode_step with positions pos, pos + 1, ..., and amortises the
+ * launch over the N tokens. */
+TTT_API ttt_status ttt_linear_decode(const void* q, const void* k, const void* v, ttt_dtype dt,
+                                     const float* eta, float* W_anchor, float* W_run, int B, int H,
+                                     int N, int d, int pos, int b, void* z, void* stream);
+
 /*
  * Inner-model variants of TTT-Linear. The pages name these ingredients without
  * formulas; each call states the reading it computes. All four run one fp32

@@ -29,7 +29,7 @@ PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_SEGMENTED = 0, 1, 2, 3
 EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_plan", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
            "ttt_mlp_fwd_noalloc", "ttt_mlp_noalloc_last_device_status", "ttt_linear_decode_step", "ttt_linear_bwd_workspace_bytes", "ttt_linear_bwd",
            "ttt_last_device_status", "ttt_status_str", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
-           "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd")
+           "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode")
 
 
 class TTTError(RuntimeError):
@@ -77,6 +77,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_mlp_fwd_noalloc.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
     lib.ttt_mlp_noalloc_last_device_status.argtypes = [vp]
     lib.ttt_linear_decode_step.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp]
+    lib.ttt_linear_decode.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.ttt_last_device_status.argtypes = [vp, vp]
     lib.ttt_linear_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.ttt_linear_bwd_workspace_bytes.restype = sz
@@ -89,7 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_status_str.restype = ctypes.c_char_p
     for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex", "ttt_mlp_fwd_noalloc",
               "ttt_mlp_noalloc_last_device_status", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
-              "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd",
+              "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode",
               "ttt_linear_decode_step", "ttt_linear_bwd", "ttt_last_device_status"):
         getattr(lib, f).restype = i
     _lib = lib
@@ -375,6 +376,29 @@ def ttt_linear_decode_step(q, k, v, eta, W_anchor, W_run, pos: int, b: int, z=No
                                         B, H, d, int(pos), int(b), _p(z), _stream_ptr(stream, dev))
     if st != TTT_OK:
         raise TTTError("ttt_linear_decode_step", st)
+    return z
+
+
+def ttt_linear_decode(q, k, v, eta, W_anchor, W_run, pos: int, b: int, z=None, stream=None):
+    """N decode tokens per (batch row, head) in one launch; q, k, v [B, H, N, d]. Updates
+    W_anchor/W_run in place; returns z [B, H, N, d]."""
+    import torch
+    lib = load_library()
+    B, H, N, d = q.shape
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check(t, n, q.dtype, (B, H, N, d), dev)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(W_anchor, "W_anchor", torch.float32, (B, H, d, d), dev)
+    _check(W_run, "W_run", torch.float32, (B, H, d, d), dev)
+    if z is None:
+        z = torch.empty_like(q)
+    _check(z, "z", q.dtype, (B, H, N, d), dev)
+    with _on_device(dev):
+        st = lib.ttt_linear_decode(_p(q), _p(k), _p(v), _dtype_code(q), _p(eta), _p(W_anchor), _p(W_run), B, H, N, d,
+                                   int(pos), int(b), _p(z), _stream_ptr(stream, dev))
+    if st != TTT_OK:
+        raise TTTError("ttt_linear_decode", st)
     return z
 
 

@@ -1,22 +1,31 @@
-// TTT-Linear decode: one token per (batch row, head), O(d^2) work and memory
-// per head ("Test-Time Training (TTT) guide", section 3: constant time and
-// memory per decoded token).
+// TTT-Linear decode: N tokens per (batch row, head) in one launch, O(d^2) work
+// and memory per token ("Test-Time Training (TTT) guide", section 3: constant
+// time and memory per decoded token).
 //
 // The pair (W_anchor, W_run) is the chunk-start and the running state, so a
 // token inside a chunk still takes its gradient at the chunk-start weights:
 //   e = k W_anchor - v;  W_run <- W_run - eta k^T e;  z = q W_run
 // and z is formed from the old W_run as q W_run - eta (q . k) e, so the read
-// does not wait for the write. When the token completes a chunk, W_anchor
-// takes the new W_run.
+// does not wait for the write. When a token completes a chunk, W_anchor takes
+// the new W_run.
+//
+// Every one of these is a function of one output column j of the state, so a
+// head's d columns are split over CTAs of 16 columns (4 CTAs per head at
+// d = 64). A CTA holds its columns of W_anchor and W_run in registers for all
+// N tokens: thread (i, c) keeps row i, columns 4c .. 4c + 3 of the slice of each
+// state. Per token the column sums over i are a shuffle reduction within each
+// warp plus a sum of the warps' partials in shared memory.
 #include "kernels.h"
 #include "ttt_device.cuh"
 
 namespace ttt {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kCols = 16;                   // state columns per CTA
 constexpr int kMaxD = 64;
-constexpr int kParts = kThreads / kMaxD;  // 4 partial sums per column
+constexpr int kThreads = kMaxD * kCols / 4;  // one float4 of each state per thread at d = 64
+constexpr int kWarpsD = kThreads / 32;
+constexpr int kTokBuf = 32;                 // tokens whose q, k, v are staged at once
 
 template <typename T>
 __device__ __forceinline__ float ld(const T* p);
@@ -27,76 +36,120 @@ __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16* p) { ret
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) linear_decode_kernel(DecodeParams p) {
-  __shared__ float qs[kMaxD], ks[kMaxD], vs[kMaxD], es[kMaxD];
-  __shared__ float pe[kParts][kMaxD], pz[kParts][kMaxD];
-  __shared__ float qk;
-  const int unit = blockIdx.x;
+  __shared__ float qs[kTokBuf][kMaxD], ks[kTokBuf][kMaxD], vs[kTokBuf][kCols];
+  __shared__ float part[2][kWarpsD][kCols];  // per-warp column sums of k W_anchor and q W_run
+  __shared__ float es[kCols];
+  __shared__ float qk[kTokBuf];
+  const int groups = (p.d + kCols - 1) / kCols;
+  const int unit = blockIdx.x / groups;
+  const int j0 = (blockIdx.x % groups) * kCols;
   const int h = unit % p.H;
   const int d = p.d;
   const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int i = tid >> 2;        // state row
+  const int c = (tid & 3) * 4;   // first of this thread's 4 columns within the slice
+  const bool row_ok = i < d;
   const float eta = p.eta[h];
-  const T* q = static_cast<const T*>(p.q) + static_cast<size_t>(unit) * d;
-  const T* k = static_cast<const T*>(p.k) + static_cast<size_t>(unit) * d;
-  const T* v = static_cast<const T*>(p.v) + static_cast<size_t>(unit) * d;
   float* Wa = p.W_anchor + static_cast<size_t>(unit) * d * d;
   float* Wr = p.W_run + static_cast<size_t>(unit) * d * d;
 
-  if (tid < d) {
-    qs[tid] = ld<T>(q + tid);
-    ks[tid] = ld<T>(k + tid);
-    vs[tid] = ld<T>(v + tid);
-  }
-  __syncthreads();
-  if (tid < 32) {
-    float s = 0.f;
-    for (int i = tid; i < d; i += 32) s = fmaf(qs[i], ks[i], s);
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (tid == 0) qk = s;
-  }
-  const int j = tid % kMaxD;
-  const int part = tid / kMaxD;
-  if (j < d) {
-    float se = 0.f, sz = 0.f;
-    for (int i = part; i < d; i += kParts) {
-      se = fmaf(ks[i], Wa[i * d + j], se);
-      sz = fmaf(qs[i], Wr[i * d + j], sz);
+  // This thread's 4 columns of row i (fewer at the right edge when d % 16 != 0).
+  float wa[4] = {0.f, 0.f, 0.f, 0.f}, wr[4] = {0.f, 0.f, 0.f, 0.f};
+  auto col_ok = [&](int q) { return row_ok && j0 + c + q < d; };
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (col_ok(q)) {
+      wa[q] = Wa[i * d + j0 + c + q];
+      wr[q] = Wr[i * d + j0 + c + q];
     }
-    pe[part][j] = se;
-    pz[part][j] = sz;
-  }
-  __syncthreads();
-  if (tid < d) {
-    float se = 0.f, sz = 0.f;
-    for (int r = 0; r < kParts; ++r) {
-      se += pe[r][tid];
-      sz += pz[r][tid];
+
+  for (int n0 = 0; n0 < p.N; n0 += kTokBuf) {
+    const int nb = min(kTokBuf, p.N - n0);
+    // Stage the q, k (all d) and v (this slice) of the next nb tokens.
+    for (int x = tid; x < nb * d; x += kThreads) {
+      const int t = x / d, f = x % d;
+      const size_t g = (static_cast<size_t>(unit) * p.N + n0 + t) * d + f;
+      qs[t][f] = ld<T>(static_cast<const T*>(p.q) + g);
+      ks[t][f] = ld<T>(static_cast<const T*>(p.k) + g);
+      if (f >= j0 && f < j0 + kCols) vs[t][f - j0] = ld<T>(static_cast<const T*>(p.v) + g);
     }
-    const float e = se - vs[tid];
-    es[tid] = e;
-    const float z = sz - eta * qk * e;
-    if (p.bf16)
-      static_cast<__nv_bfloat16*>(p.z)[static_cast<size_t>(unit) * d + tid] = __float2bfloat16_rn(z);
-    else
-      static_cast<float*>(p.z)[static_cast<size_t>(unit) * d + tid] = z;
+    __syncthreads();
+    for (int t = warp; t < nb; t += kWarpsD) {  // q . k per token, a warp each
+      float s = 0.f;
+      for (int f = lane; f < d; f += 32) s = fmaf(qs[t][f], ks[t][f], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) qk[t] = s;
+    }
+    for (int t = 0; t < nb; ++t) {
+      const float kv = row_ok ? ks[t][i] : 0.f, qv = row_ok ? qs[t][i] : 0.f;
+      float se[4], sz[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        se[q] = kv * wa[q];
+        sz[q] = qv * wr[q];
+      }
+      // sum over the warp's 8 rows (lanes with equal lane % 4 hold the same columns)
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          se[q] += __shfl_xor_sync(0xffffffffu, se[q], o);
+          sz[q] += __shfl_xor_sync(0xffffffffu, sz[q], o);
+        }
+      if (lane < 4)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          part[0][warp][4 * lane + q] = se[q];
+          part[1][warp][4 * lane + q] = sz[q];
+        }
+      __syncthreads();
+      if (tid < kCols) {
+        float a = 0.f, z = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarpsD; ++w) {
+          a += part[0][w][tid];
+          z += part[1][w][tid];
+        }
+        const float e = a - vs[t][tid];
+        es[tid] = e;
+        if (j0 + tid < d) {
+          const size_t o = (static_cast<size_t>(unit) * p.N + n0 + t) * d + j0 + tid;
+          const float zz = z - eta * qk[t] * e;
+          if (p.bf16)
+            static_cast<__nv_bfloat16*>(p.z)[o] = __float2bfloat16_rn(zz);
+          else
+            static_cast<float*>(p.z)[o] = zz;
+        }
+      }
+      __syncthreads();
+      const bool completes = ((p.pos + n0 + t + 1) % p.b) == 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        wr[q] -= eta * kv * es[c + q];
+        if (completes) wa[q] = wr[q];
+      }
+    }
+    __syncthreads();  // the staged tokens are read; the next batch may overwrite them
   }
-  __syncthreads();
-  const bool completes = ((p.pos + 1) % p.b) == 0;
-  for (int x = tid; x < d * d; x += kThreads) {
-    const int i = x / d, jj = x % d;
-    const float w = Wr[x] - eta * ks[i] * es[jj];
-    Wr[x] = w;
-    if (completes) Wa[x] = w;
-  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (col_ok(q)) {
+      Wa[i * d + j0 + c + q] = wa[q];
+      Wr[i * d + j0 + c + q] = wr[q];
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_linear_decode(const DecodeParams& p, cudaStream_t stream) {
-  if (p.units == 0) return cudaSuccess;
+  if (p.units == 0 || p.N == 0) return cudaSuccess;
+  const int grid = p.units * ((p.d + kCols - 1) / kCols);
   if (p.bf16)
-    linear_decode_kernel<__nv_bfloat16><<<p.units, kThreads, 0, stream>>>(p);
+    linear_decode_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(p);
   else
-    linear_decode_kernel<float><<<p.units, kThreads, 0, stream>>>(p);
+    linear_decode_kernel<float><<<grid, kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

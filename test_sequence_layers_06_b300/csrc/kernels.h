@@ -117,6 +117,7 @@ struct DecodeParams {
   float* W_anchor;
   float* W_run;
   int B, H, d, pos, b;
+  int N;               // tokens per (batch row, head); q, k, v, z are [B][H][N][d]
   int units;
   bool bf16;
 };

@@ -520,18 +520,20 @@ ttt_status ttt_mlp_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt
                         stream, nullptr);
 }
 
-ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, ttt_dtype dt, const float* eta,
-                                  float* W_anchor, float* W_run, int B, int H, int d, int pos, int b, void* z,
-                                  void* stream) {
+ttt_status ttt_linear_decode(const void* q, const void* k, const void* v, ttt_dtype dt, const float* eta,
+                             float* W_anchor, float* W_run, int B, int H, int N, int d, int pos, int b, void* z,
+                             void* stream) {
   if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
-  if (B < 1 || H < 1 || d < 1 || b < 1 || pos < 0) return TTT_ERR_ARG;
+  if (B < 1 || H < 1 || N < 0 || d < 1 || b < 1 || pos < 0) return TTT_ERR_ARG;
+  if (static_cast<long double>(B) * H * N * d >= 9.0e18L || static_cast<long long>(B) * H * 4 >= 2147483647LL)
+    return TTT_ERR_ARG;
   if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !z || !eta || !W_anchor || !W_run) return TTT_ERR_ARG;
+  if (!eta || !W_anchor || !W_run || (N > 0 && (!q || !k || !v || !z))) return TTT_ERR_ARG;
   for (const void* p : {q, k, v, static_cast<const void*>(z), static_cast<const void*>(eta),
                         static_cast<const void*>(W_anchor), static_cast<const void*>(W_run)})
-    if (!aligned16(p)) return TTT_ERR_ARG;
+    if (p && !aligned16(p)) return TTT_ERR_ARG;
   {
-    const size_t tok = bytes4(B, H, d, 1, dt == TTT_BF16 ? 2 : 4), st = bytes4(B, H, d, d, 4);
+    const size_t tok = bytes4(B, H, N, d, dt == TTT_BF16 ? 2 : 4), st = bytes4(B, H, d, d, 4);
     if (!outputs_disjoint({{z, tok}, {W_anchor, st}, {W_run, st}},
                           {{q, tok}, {k, tok}, {v, tok}, {eta, bytes4(H, 1, 1, 1, 4)}}))
       return TTT_ERR_ARG;
@@ -540,10 +542,17 @@ ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, t
   p.q = q; p.k = k; p.v = v; p.z = z; p.eta = eta;
   p.W_anchor = W_anchor; p.W_run = W_run;
   p.B = B; p.H = H; p.d = d; p.pos = pos; p.b = b;
+  p.N = N;
   p.units = B * H;
   p.bf16 = (dt == TTT_BF16);
-  return ttt::launch_linear_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TTT_OK
-                                                                                           : TTT_ERR_CUDA;
+  return ttt::launch_linear_decode(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, ttt_dtype dt, const float* eta,
+                                  float* W_anchor, float* W_run, int B, int H, int d, int pos, int b, void* z,
+                                  void* stream) {
+  if (!q || !k || !v || !z) return TTT_ERR_ARG;
+  return ttt_linear_decode(q, k, v, dt, eta, W_anchor, W_run, B, H, 1, d, pos, b, z, stream);
 }
 
 // Shared checks and launch of the inner-model variants (linear_variants.cu).

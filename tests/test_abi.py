@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 18
+    assert len(names) == 19
     assert set(names) == set(ttt.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n

@@ -275,6 +275,38 @@ def test_decode_continues_forward():
     assert rel_err("W_run", to64(Wr), Wref, 2e-2) <= 2e-2
 
 
+@pytest.mark.parametrize("dtype,d,N", [("bf16", 64, 37), ("f32", 64, 50), ("f32", 40, 21), ("bf16", 64, 1)])
+def test_decode_many_tokens_in_one_launch_continues_forward(dtype, d, N):
+    """Prefill T1 (b | T1), then decode N tokens in one ttt_linear_decode launch (the
+    anchor moves at every chunk boundary inside the launch): equals the oracle over
+    T1 + N; a state width that is not a multiple of 16 leaves a partial column slice."""
+    T1, b = 32, 16
+    w = W["linear_small"].with_(B=2, H=3, T=T1 + N, d=d, dtype=dtype, seed=90 + N + d)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    sl = lambda x, a, e: x[:, :, a:e].contiguous()
+    _, Wp = ttt.ttt_linear_fwd(sl(t["Q"], 0, T1), sl(t["K"], 0, T1), sl(t["V"], 0, T1), t["eta"], t["W0"], b)
+    Wa, Wr = Wp.clone(), Wp.clone()
+    z = ttt.ttt_linear_decode(sl(t["Q"], T1, T1 + N), sl(t["K"], T1, T1 + N), sl(t["V"], T1, T1 + N), t["eta"],
+                              Wa, Wr, T1, b)
+    torch.cuda.synchronize()
+    Zr, Wref = oracle_linear(inp, b)
+    bar = tolerance(w)
+    assert rel_err("decoded z (one launch)", to64(z), Zr[:, :, T1:], bar) <= bar
+    assert rel_err("W_run (one launch)", to64(Wr), Wref, bar) <= bar
+    # the anchor is the state at the start of the current chunk
+    n_full = ((T1 + N) // b) * b
+    _, Wanc = oracle.linear_primal(inp.q64[:, :, :n_full], inp.k64[:, :, :n_full], inp.v64[:, :, :n_full],
+                                   inp.eta64, inp.W0_64, b)
+    assert rel_l2(to64(Wa), Wanc) <= bar
+    # no tokens: nothing changes
+    Wa2, Wr2 = Wa.clone(), Wr.clone()
+    e = torch.empty((w.B, w.H, 0, d), dtype=t["Q"].dtype, device="cuda")
+    ttt.ttt_linear_decode(e, e, e, t["eta"], Wa2, Wr2, T1 + N, b)
+    torch.cuda.synchronize()
+    assert torch.equal(Wa2, Wa) and torch.equal(Wr2, Wr)
+
+
 def test_decode_fp32_single_token_matches_oracle():
     g = np.random.default_rng(3)
     B, H, d = 2, 4, 64
