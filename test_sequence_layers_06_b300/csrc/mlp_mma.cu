@@ -348,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < 4; ++r) w2[2 * q + nt][r] = fmaf(-eta, acc[nt][r], w2[2 * q + nt][r]);
       }
     }
-    __syncthreads();
+    // D's columns [16w, +16) are written and read by this warp alone: no CTA barrier.
+    __syncwarp();
 
     // (4) Hq = Q W1 - eta tril(Q K^T) D, Aq = gelu(Hq);  W1 -= eta K^T D (this warp's columns).
     {
@@ -385,10 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < 4; ++r) w1[mt][nt][r] = fmaf(-eta, acc[nt][r], w1[mt][nt][r]);
       }
     }
-    __syncthreads();  // Aq complete; every read of the running W1 copy is done
-
+    // Columns [16w, +16) of the W1 copies are read by this warp alone (U, Hq): rewrite them now.
+    __syncwarp();
     TTT_STORE_W1(sm + kW1b);
     if (snap && chunk_end) TTT_STORE_W1(W1s);
+    __syncthreads();  // Aq complete
     // (5) Z partials (value columns [16(w&3), +16), hidden quarter w>>2) and
     //     tril(Aq A^T) partials (hidden [16w, +16)).
     {
@@ -457,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint32_t*>(Z) = pack_bf16(fmaf(-eta, r.x, z.x), fmaf(-eta, r.y, z.y));
       }
     }
-    __syncthreads();
+    // No barrier here: the next tile first meets at its start barrier, and the buffers read
+    // above (part, gf, saf) are written again only after that.
   }
   // Final state.
   float* W1o = p.W1_out + static_cast<size_t>(unit) * kD * kM;
