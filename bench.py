@@ -72,6 +72,8 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--mode", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd: time the TTT-Linear backward (ttt_linear_bwd) on the workload instead")
     return ap.parse_args()
 
 
@@ -777,11 +779,59 @@ def bench_mlp(args, world, rank, local):
                                        "peak_kind": f"{kind} bf16 burst"}}), flush=True)
 
 
+def bench_bwd(args, world, rank, local):
+    """The TTT-Linear backward through ttt_linear_bwd on a workload (secondary; used for the
+    backward's profiles). Reports against the HBM roofline of its algorithmic bytes: Q, K, V, dZ
+    read and dQ, dK, dV written once."""
+    import torch
+    import test_sequence_layers_06_b300 as ttt
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload].with_(b=args.b)
+    if args.T:
+        w = w.with_(T=args.T)
+    inp = synth.make_inputs(w, want_exact=False)
+    cv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev))
+    Q, K, V = cv(inp.q), cv(inp.k), cv(inp.v)
+    eta, W0 = torch.from_numpy(inp.eta).to(dev), torch.from_numpy(inp.W0).to(dev)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    dZ = torch.randn(Q.shape, device=dev, generator=g).to(torch.bfloat16)
+    dW = torch.randn((w.B, w.H, w.d, w.d), device=dev, generator=g)
+    ws = torch.empty(ttt.ttt_linear_bwd_workspace_bytes(w.B, w.H, w.T, w.d, args.b), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: ttt.ttt_linear_bwd(Q, K, V, eta, W0, args.b, dZ, dW, workspace=ws, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    if ttt.ttt_last_device_status(ws, stream) != 0:
+        raise RuntimeError("device status not OK after the timed region")
+    ms = a.elapsed_time(e) / args.steps
+    hbm_gbs, _, kind = measured_peaks()
+    nbytes = w.token_heads * 7 * w.d * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({"metric": "TTT-Linear backward tokens·heads/sec", "value": w.token_heads / (ms * 1e-3),
+                          "unit": UNIT, "n_gpus": world, "steps": args.steps, "ms_per_step": round(ms, 4),
+                          "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                          "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "b": args.b},
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                                       "frac": round(gbs / hbm_gbs, 4), "algorithmic_bytes": nbytes,
+                                       "peak_kind": kind}}), flush=True)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
         bench_reference(args, world, rank)
+    elif args.mode == "bwd":
+        bench_bwd(args, world, rank, local)
     elif synth.WORKLOADS[args.workload].variant == "mlp":
         bench_mlp(args, world, rank, local)
     else:
