@@ -303,10 +303,13 @@ TTT_API ttt_status ttt_linear_momentum_fwd(const void* Q, const void* K, const v
  *   dW0 [H][d][d] float32 (summed over the batch rows, which share eta and W0).
  *   Kernels: bf16 with d = 64 and b = 16 runs on the tensor cores (state and
  *   products fp32-accumulated, W checkpointed every 64 tokens in the workspace);
- *   every other case with d <= 64 and b <= 64 runs the fp32 SIMT kernel (fp32 or
- *   bf16 operands); anything else returns TTT_ERR_UNSUPPORTED.
+ *   every other case with d <= 64 runs the fp32 SIMT kernel (fp32 or bf16
+ *   operands; chunks longer than 64 tokens are walked in 32-token blocks, with
+ *   the chunk's E and dE kept in the workspace); d > 64 returns
+ *   TTT_ERR_UNSUPPORTED.
  *   workspace: ttt_linear_bwd_workspace_bytes(B, H, T, d, b) bytes (a status
- *   word, the kept states, per-unit partial sums), 16-byte aligned. A wait in the
+ *   word, the kept states, per-unit partial sums and, for b > 64, one chunk's
+ *   E and dE per unit), 16-byte aligned. A wait in the
  *   tensor-core kernel that runs out records TTT_ERR_TIMEOUT there
  *   (ttt_last_device_status).
  * All pointers are device memory, 16-byte aligned, caller-owned; work is

@@ -82,6 +82,7 @@ struct LinearBwdParams {
   float* states;   // workspace [units][ceil(T/b)][d][d]: chunk-start states (tensor-core kernel:
                    // the state at the start of every 64-token block)
   float* partial;  // workspace [units][d*d + 1]: per-unit dW0, then d eta
+  float* chunk_buf;  // workspace [units][2][min(b, T)][d]: E, dE of one chunk (chunks longer than 64)
   StatusBlock* status;
   uint64_t timeout_ns;
 };
@@ -176,6 +177,7 @@ cudaError_t launch_linear_decode(const DecodeParams& p, cudaStream_t stream);
 bool linear_bwd_supported(int d, int b);
 size_t linear_bwd_smem_bytes(int d, int b);
 size_t linear_bwd_scratch_bytes(int units, int T, int d, int b);  // states + partials, bytes
+float* linear_bwd_chunk_buf(float* partial, int units, int d);       // where chunk_buf starts
 cudaError_t launch_linear_bwd(const LinearBwdParams& p, cudaStream_t stream);
 cudaError_t launch_linear_bwd_reduce(const LinearBwdParams& p, cudaStream_t stream);
 

@@ -1,5 +1,5 @@
 // Backward of the chunked TTT-Linear scan in fp32 arithmetic: fp32 or bf16
-// operands (dQ, dK, dV in the operands' dtype), d <= 64, b <= 64.
+// operands (dQ, dK, dV in the operands' dtype), d <= 64, any chunk size.
 //
 // The outer loop trains W0 and the projections that make Q, K, V by
 // backpropagating through the inner loop ("5 · TestingTime 训练与长上下文",
@@ -20,9 +20,12 @@
 //
 // Design: one CTA per (batch row, head). A forward pass keeps every
 // chunk-start state in the workspace; the backward pass reloads them in
-// reverse. Every matrix of a chunk sits in shared memory and every product is
-// a plain fp32 loop spread over the CTA's threads: the general form, for the
+// reverse. For b <= 64 every matrix of a chunk sits in shared memory; longer
+// chunks are walked in blocks (linear_bwd_wide_kernel). Every product is a
+// plain fp32 loop spread over the CTA's threads: the general form, for the
 // 1e-4 bar of fp32 operands and the shapes linear_bwd_mma.cu does not take.
+#include <algorithm>
+
 #include "ttt_device.cuh"
 #include "kernels.h"
 
@@ -177,6 +180,246 @@ __global__ void __launch_bounds__(kBwdThreads) linear_bwd_kernel(LinearBwdParams
   if (tid == 0) part[d * d] = red[0];
 }
 
+// Chunks longer than 64 tokens (the large-chunk regime): the same recurrence,
+// with a chunk walked in blocks of kSub tokens. E and dE of the chunk live in
+// the workspace; S = tril(Q_c K_c^T) and P = -eta tril(dZ_c E^T) are formed one
+// kSub x kSub block at a time, only on and below the diagonal, and applied at
+// once: the sums over later (dE, dK) or earlier (dQ) tokens of the chunk run
+// over blocks, the block's own entries masked by absolute token index.
+constexpr int kSub = 32;
+
+template <typename Tin>
+__global__ void __launch_bounds__(kBwdThreads) linear_bwd_wide_kernel(LinearBwdParams p) {
+  extern __shared__ __align__(16) float bsm[];
+  const int d = p.d, b = p.b, T = p.T;
+  const int unit = blockIdx.x;
+  const int h = unit % p.H;
+  const int tid = threadIdx.x;
+  const float eta = p.eta[h];
+  const int nch = (T + b - 1) / b;
+  const int cap = min(b, T);     // tokens of the longest chunk
+  float* W = bsm;                // [d][d]   chunk-start state
+  float* G = W + d * d;          // [d][d]   gradient of the next chunk's start state
+  float* R1 = G + d * d;         // [kSub][d] operands of the row block (tokens t)
+  float* R2 = R1 + kSub * d;
+  float* C1 = R2 + kSub * d;     // [kSub][d] operands of the column block (tokens t2)
+  float* C2 = C1 + kSub * d;
+  float* Acc = C2 + kSub * d;    // [kSub][d] the row block's result
+  float* Sb = Acc + kSub * d;    // [kSub][kSub] one block of S or P
+  float* red = Sb + kSub * kSub; // [kBwdThreads]
+  const size_t base = static_cast<size_t>(unit) * T * d;
+  float* states = p.states + static_cast<size_t>(unit) * nch * d * d;
+  float* Ec = p.chunk_buf + static_cast<size_t>(unit) * 2 * cap * d;  // [cap][d]
+  float* dEc = Ec + static_cast<size_t>(cap) * d;                      // [cap][d]
+
+  auto load = [&](float* dst, const void* src, size_t off, int m) {
+    for (int x = tid; x < m * d; x += kBwdThreads) dst[x] = ldv<Tin>(src, off + x);
+  };
+  auto load_ws = [&](float* dst, const float* src, int m) {
+    for (int x = tid; x < m * d; x += kBwdThreads) dst[x] = src[x];
+  };
+  // Ec = K_c W - V_c for the n tokens of the chunk at `off`.
+  auto chunk_errors = [&](size_t off, int n) {
+    for (int r0 = 0; r0 < n; r0 += kSub) {
+      const int m = min(kSub, n - r0);
+      load(R1, p.K, off + static_cast<size_t>(r0) * d, m);
+      load(R2, p.V, off + static_cast<size_t>(r0) * d, m);
+      __syncthreads();
+      for (int x = tid; x < m * d; x += kBwdThreads) {
+        const int t = x / d, j = x % d;
+        float acc = -R2[x];
+        for (int k = 0; k < d; ++k) acc = fmaf(R1[t * d + k], W[k * d + j], acc);
+        Ec[r0 * d + x] = acc;
+      }
+      __syncthreads();
+    }
+  };
+
+  // ---------------------------------------------------------------- forward: chunk-start states
+  for (int i = tid; i < d * d; i += kBwdThreads) W[i] = p.W0[static_cast<size_t>(h) * d * d + i];
+  __syncthreads();
+  for (int c = 0; c < nch; ++c) {
+    const int c0 = c * b, n = min(b, T - c0);
+    const size_t off = base + static_cast<size_t>(c0) * d;
+    for (int i = tid; i < d * d; i += kBwdThreads) states[static_cast<size_t>(c) * d * d + i] = W[i];
+    chunk_errors(off, n);
+    for (int r0 = 0; r0 < n; r0 += kSub) {  // W -= eta K_c^T E, block by block
+      const int m = min(kSub, n - r0);
+      load(R1, p.K, off + static_cast<size_t>(r0) * d, m);
+      load_ws(R2, Ec + r0 * d, m);
+      __syncthreads();
+      for (int x = tid; x < d * d; x += kBwdThreads) {
+        const int i = x / d, j = x % d;
+        float acc = 0.f;
+        for (int t = 0; t < m; ++t) acc = fmaf(R1[t * d + i], R2[t * d + j], acc);
+        W[x] -= eta * acc;
+      }
+      __syncthreads();
+    }
+  }
+
+  // ---------------------------------------------------------------- backward, last chunk first
+  for (int i = tid; i < d * d; i += kBwdThreads) G[i] = p.dW_out[static_cast<size_t>(unit) * d * d + i];
+  float deta = 0.f;
+  __syncthreads();
+  for (int c = nch - 1; c >= 0; --c) {
+    const int c0 = c * b, n = min(b, T - c0);
+    const size_t off = base + static_cast<size_t>(c0) * d;
+    for (int i = tid; i < d * d; i += kBwdThreads) W[i] = states[static_cast<size_t>(c) * d * d + i];
+    __syncthreads();
+    chunk_errors(off, n);
+
+    // dE_t = -eta (k_t G + sum_{t2 >= t} (q_t2 . k_t) dz_t2); d eta -= E . (K G)
+    for (int r0 = 0; r0 < n; r0 += kSub) {
+      const int m = min(kSub, n - r0);
+      load(R1, p.K, off + static_cast<size_t>(r0) * d, m);
+      __syncthreads();
+      for (int x = tid; x < m * d; x += kBwdThreads) {
+        const int t = x / d, j = x % d;
+        float kg = 0.f;
+        for (int k = 0; k < d; ++k) kg = fmaf(R1[t * d + k], G[k * d + j], kg);
+        deta -= Ec[r0 * d + x] * kg;
+        Acc[x] = kg;
+      }
+      for (int q0 = r0; q0 < n; q0 += kSub) {
+        const int mq = min(kSub, n - q0);
+        load(C1, p.Q, off + static_cast<size_t>(q0) * d, mq);
+        load(C2, p.dZ, off + static_cast<size_t>(q0) * d, mq);
+        __syncthreads();
+        for (int x = tid; x < mq * m; x += kBwdThreads) {  // Sb[t2][t] = q_t2 . k_t for t2 >= t
+          const int t2 = x / m, t = x % m;
+          float s = 0.f;
+          if (q0 + t2 >= r0 + t)
+            for (int k = 0; k < d; ++k) s = fmaf(C1[t2 * d + k], R1[t * d + k], s);
+          Sb[t2 * kSub + t] = s;
+        }
+        __syncthreads();
+        for (int x = tid; x < m * d; x += kBwdThreads) {
+          const int t = x / d, j = x % d;
+          float acc = Acc[x];
+          for (int t2 = 0; t2 < mq; ++t2) acc = fmaf(Sb[t2 * kSub + t], C2[t2 * d + j], acc);
+          Acc[x] = acc;
+        }
+        __syncthreads();
+      }
+      for (int x = tid; x < m * d; x += kBwdThreads) dEc[r0 * d + x] = -eta * Acc[x];
+      __syncthreads();
+    }
+
+    // dQ_t = dz_t W^T + sum_{t2 <= t} P[t][t2] k_t2, P[t][t2] = -eta dz_t . e_t2;
+    // d eta -= sum_{t2 <= t} (q_t . k_t2)(dz_t . e_t2)
+    for (int r0 = 0; r0 < n; r0 += kSub) {
+      const int m = min(kSub, n - r0);
+      load(R1, p.dZ, off + static_cast<size_t>(r0) * d, m);
+      load(R2, p.Q, off + static_cast<size_t>(r0) * d, m);
+      __syncthreads();
+      for (int x = tid; x < m * d; x += kBwdThreads) {
+        const int t = x / d, i = x % d;
+        float acc = 0.f;
+        for (int j = 0; j < d; ++j) acc = fmaf(R1[t * d + j], W[i * d + j], acc);
+        Acc[x] = acc;
+      }
+      for (int k0 = 0; k0 <= r0; k0 += kSub) {
+        const int mk = min(kSub, n - k0);
+        load_ws(C1, Ec + k0 * d, mk);
+        load(C2, p.K, off + static_cast<size_t>(k0) * d, mk);
+        __syncthreads();
+        for (int x = tid; x < m * mk; x += kBwdThreads) {
+          const int t = x / mk, t2 = x % mk;
+          float pv = 0.f;
+          if (k0 + t2 <= r0 + t) {
+            float s = 0.f;
+            for (int j = 0; j < d; ++j) {
+              pv = fmaf(R1[t * d + j], C1[t2 * d + j], pv);
+              s = fmaf(R2[t * d + j], C2[t2 * d + j], s);
+            }
+            deta -= s * pv;
+          }
+          Sb[t * kSub + t2] = -eta * pv;
+        }
+        __syncthreads();
+        for (int x = tid; x < m * d; x += kBwdThreads) {
+          const int t = x / d, i = x % d;
+          float acc = Acc[x];
+          for (int t2 = 0; t2 < mk; ++t2) acc = fmaf(Sb[t * kSub + t2], C2[t2 * d + i], acc);
+          Acc[x] = acc;
+        }
+        __syncthreads();
+      }
+      for (int x = tid; x < m * d; x += kBwdThreads) stv<Tin>(p.dQ, off + static_cast<size_t>(r0) * d + x, Acc[x]);
+      __syncthreads();
+    }
+
+    // dK_t = dE_t W^T - eta e_t G^T + sum_{t2 >= t} P[t2][t] q_t2;  dV = -dE
+    for (int r0 = 0; r0 < n; r0 += kSub) {
+      const int m = min(kSub, n - r0);
+      load_ws(R1, dEc + r0 * d, m);
+      load_ws(R2, Ec + r0 * d, m);
+      __syncthreads();
+      for (int x = tid; x < m * d; x += kBwdThreads) {
+        const int t = x / d, i = x % d;
+        float ak = 0.f, eg = 0.f;
+        for (int j = 0; j < d; ++j) {
+          ak = fmaf(R1[t * d + j], W[i * d + j], ak);
+          eg = fmaf(R2[t * d + j], G[i * d + j], eg);
+        }
+        Acc[x] = ak - eta * eg;
+        stv<Tin>(p.dV, off + static_cast<size_t>(r0) * d + x, -R1[x]);
+      }
+      for (int q0 = r0; q0 < n; q0 += kSub) {
+        const int mq = min(kSub, n - q0);
+        load(C1, p.dZ, off + static_cast<size_t>(q0) * d, mq);
+        load(C2, p.Q, off + static_cast<size_t>(q0) * d, mq);
+        __syncthreads();
+        for (int x = tid; x < mq * m; x += kBwdThreads) {  // Sb[t2][t] = P[t2][t] for t2 >= t
+          const int t2 = x / m, t = x % m;
+          float pv = 0.f;
+          if (q0 + t2 >= r0 + t)
+            for (int j = 0; j < d; ++j) pv = fmaf(C1[t2 * d + j], R2[t * d + j], pv);
+          Sb[t2 * kSub + t] = -eta * pv;
+        }
+        __syncthreads();
+        for (int x = tid; x < m * d; x += kBwdThreads) {
+          const int t = x / d, i = x % d;
+          float acc = Acc[x];
+          for (int t2 = 0; t2 < mq; ++t2) acc = fmaf(Sb[t2 * kSub + t], C2[t2 * d + i], acc);
+          Acc[x] = acc;
+        }
+        __syncthreads();
+      }
+      for (int x = tid; x < m * d; x += kBwdThreads) stv<Tin>(p.dK, off + static_cast<size_t>(r0) * d + x, Acc[x]);
+      __syncthreads();
+    }
+
+    // G += Q_c^T dZ_c + K_c^T dE (G was last read above)
+    for (int r0 = 0; r0 < n; r0 += kSub) {
+      const int m = min(kSub, n - r0);
+      load(R1, p.Q, off + static_cast<size_t>(r0) * d, m);
+      load(R2, p.dZ, off + static_cast<size_t>(r0) * d, m);
+      load(C1, p.K, off + static_cast<size_t>(r0) * d, m);
+      load_ws(C2, dEc + r0 * d, m);
+      __syncthreads();
+      for (int x = tid; x < d * d; x += kBwdThreads) {
+        const int i = x / d, j = x % d;
+        float acc = 0.f;
+        for (int t = 0; t < m; ++t) acc = fmaf(R1[t * d + i], R2[t * d + j], fmaf(C1[t * d + i], C2[t * d + j], acc));
+        G[x] += acc;
+      }
+      __syncthreads();
+    }
+  }
+
+  float* part = p.partial + static_cast<size_t>(unit) * (d * d + 1);
+  for (int i = tid; i < d * d; i += kBwdThreads) part[i] = G[i];
+  red[tid] = deta;
+  __syncthreads();
+  for (int s = kBwdThreads / 2; s > 0; s >>= 1) {
+    if (tid < s) red[tid] += red[tid + s];
+    __syncthreads();
+  }
+  if (tid == 0) part[d * d] = red[0];
+}
+
 // dW0[h] and d eta[h]: sums over the batch rows of the per-unit partials.
 __global__ void __launch_bounds__(kBwdThreads) linear_bwd_reduce_kernel(LinearBwdParams p) {
   const int h = blockIdx.x;
@@ -199,19 +442,33 @@ size_t linear_bwd_smem_bytes(int d, int b) {
          sizeof(float);
 }
 
-bool linear_bwd_supported(int d, int b) {
-  return d >= 1 && d <= 64 && b >= 1 && b <= 64 && linear_bwd_smem_bytes(d, b) <= 227 * 1024;
+static size_t wide_smem_bytes(int d) {
+  return (static_cast<size_t>(2) * d * d + static_cast<size_t>(5) * kSub * d + kSub * kSub + kBwdThreads) *
+         sizeof(float);
 }
+
+static bool short_chunks(int d, int b) { return b <= 64 && linear_bwd_smem_bytes(d, b) <= 227 * 1024; }
+
+bool linear_bwd_supported(int d, int b) { return d >= 1 && d <= 64 && b >= 1; }
 
 size_t linear_bwd_scratch_bytes(int units, int T, int d, int b) {
   const size_t nch = (static_cast<size_t>(T) + b - 1) / b;
-  return static_cast<size_t>(units) * nch * d * d * sizeof(float) +
-         static_cast<size_t>(units) * (static_cast<size_t>(d) * d + 1) * sizeof(float);
+  size_t bytes = static_cast<size_t>(units) * nch * d * d * sizeof(float) +
+                 static_cast<size_t>(units) * (static_cast<size_t>(d) * d + 1) * sizeof(float);
+  if (!short_chunks(d, b))  // E and dE of one chunk per unit
+    bytes += static_cast<size_t>(units) * 2 * std::min(b, T) * d * sizeof(float);
+  return bytes;
+}
+
+float* linear_bwd_chunk_buf(float* partial, int units, int d) {
+  return partial + static_cast<size_t>(units) * (static_cast<size_t>(d) * d + 1);
 }
 
 cudaError_t launch_linear_bwd(const LinearBwdParams& p, cudaStream_t stream) {
-  const size_t smem = linear_bwd_smem_bytes(p.d, p.b);
-  auto kern = p.bf16 ? linear_bwd_kernel<__nv_bfloat16> : linear_bwd_kernel<float>;
+  const bool wide = !short_chunks(p.d, p.b);
+  const size_t smem = wide ? wide_smem_bytes(p.d) : linear_bwd_smem_bytes(p.d, p.b);
+  auto kern = wide ? (p.bf16 ? linear_bwd_wide_kernel<__nv_bfloat16> : linear_bwd_wide_kernel<float>)
+                   : (p.bf16 ? linear_bwd_kernel<__nv_bfloat16> : linear_bwd_kernel<float>);
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -670,6 +670,7 @@ ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype
   p.states = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
   const size_t nch = (static_cast<size_t>(T) + b - 1) / b;
   p.partial = p.states + static_cast<size_t>(p.units) * nch * d * d;
+  p.chunk_buf = ttt::linear_bwd_chunk_buf(p.partial, p.units, d);
   p.status = static_cast<ttt::StatusBlock*>(workspace);
   p.timeout_ns = kDefaultTimeoutNs;
   const ttt_status st = reset_status(workspace, s);

@@ -172,13 +172,17 @@ def test_backward_workspace_bytes(lib):
     assert ttt.ttt_linear_bwd_workspace_bytes(2, 3, 40, 16, 8) == 256 + 6 * 5 * 16 * 16 * 4 + 6 * (16 * 16 + 1) * 4 + 8
     assert ttt.ttt_linear_bwd_workspace_bytes(1, 1, 0, 16, 8) == 256 + 1 * (16 * 16 + 1) * 4 + 12
     assert ttt.ttt_linear_bwd_workspace_bytes(0, 1, 8, 16, 8) == 0
+    # chunks longer than 64 tokens add one chunk's E and dE per unit (at most T tokens of them)
+    states, part = 6 * 2 * 16 * 16 * 4, 6 * (16 * 16 + 1) * 4
+    assert ttt.ttt_linear_bwd_workspace_bytes(2, 3, 130, 16, 100) == 256 + states + part + 6 * 2 * 100 * 16 * 4 + 8
+    assert ttt.ttt_linear_bwd_workspace_bytes(2, 3, 70, 16, 128) == 256 + 6 * 16 * 16 * 4 + part + 6 * 2 * 70 * 16 * 4 + 8
 
 
 @pytest.mark.parametrize("kw,want", [(dict(Q=0), ttt.TTT_ERR_ARG), (dict(dZ=0), ttt.TTT_ERR_ARG),
                                      (dict(deta=0), ttt.TTT_ERR_ARG), (dict(dW0=4100), ttt.TTT_ERR_ARG),
                                      (dict(wsb=4096), ttt.TTT_ERR_ARG), (dict(b=0), ttt.TTT_ERR_ARG),
-                                     (dict(dt=5), ttt.TTT_ERR_ARG), (dict(dt=1, b=65), ttt.TTT_ERR_UNSUPPORTED),
-                                     (dict(d=65), ttt.TTT_ERR_UNSUPPORTED), (dict(b=65), ttt.TTT_ERR_UNSUPPORTED)])
+                                     (dict(dt=5), ttt.TTT_ERR_ARG), (dict(dt=1, d=65), ttt.TTT_ERR_UNSUPPORTED),
+                                     (dict(d=65), ttt.TTT_ERR_UNSUPPORTED), (dict(b=65, wsb=4096), ttt.TTT_ERR_ARG)])
 def test_backward_rejects_bad_arguments(lib, kw, want):
     assert _bwd(lib, **kw) == want
 

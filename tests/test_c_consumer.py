@@ -53,7 +53,7 @@ int main(void) {
   printf("fwd.width=%d\n", (int)ttt_linear_fwd(dummy, dummy, dummy, TTT_F32, dummy, dummy, 1, 1, 16, 65, 16,
                                                dummy, dummy, dummy, 1u << 20, NULL));
   printf("plan.bad=%d\n", (int)ttt_linear_plan(1, 1, 16, 64, 0, TTT_BF16, &opt, &plan));
-  printf("bwd.b65=%d\n", (int)ttt_linear_bwd(dummy, dummy, dummy, TTT_BF16, dummy, dummy, 1, 1, 16, 64, 65,
+  printf("bwd.d65=%d\n", (int)ttt_linear_bwd(dummy, dummy, dummy, TTT_BF16, dummy, dummy, 1, 1, 16, 65, 16,
                                               dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 1u << 20,
                                               NULL));
   return 0;
@@ -99,4 +99,4 @@ def test_argument_errors_from_c(c_output):
     assert int(c_output["fwd.null"]) == -1      # TTT_ERR_ARG: null pointers
     assert int(c_output["fwd.width"]) == -2     # TTT_ERR_UNSUPPORTED: d > 64
     assert int(c_output["plan.bad"]) == -1      # b < 1
-    assert int(c_output["bwd.b65"]) == -2       # no backward kernel takes chunks longer than 64
+    assert int(c_output["bwd.d65"]) == -2       # no backward kernel takes d > 64

@@ -30,8 +30,14 @@ def upstream(w, seed):
 
 @pytest.mark.parametrize("B,H,T,d,b,eta", [(1, 1, 64, 16, 16, ("const", 0.5)), (2, 3, 37, 16, 5, ("uniform", 0.05, 0.5)),
                                            (1, 2, 64, 64, 16, ("const", 0.1)), (2, 2, 50, 32, 64, ("const", 0.1)),
-                                           (1, 1, 9, 8, 1, ("const", 0.3)), (2, 1, 130, 64, 64, ("const", 0.05))])
+                                           (1, 1, 9, 8, 1, ("const", 0.3)), (2, 1, 130, 64, 64, ("const", 0.05)),
+                                           (1, 2, 200, 16, 100, ("const", 0.05)), (2, 1, 300, 64, 128, ("const", 0.02)),
+                                           (1, 1, 70, 32, 256, ("const", 0.05)), (1, 2, 257, 64, 65, ("const", 0.03)),
+                                           (1, 1, 512, 64, 512, ("const", 0.01))])
 def test_backward_matches_oracle(B, H, T, d, b, eta):
+    """fp32 operands. b <= 64 keeps a chunk in shared memory; b > 64 walks it in 32-token blocks
+    (ragged last block and chunk, one chunk longer than the sequence, one chunk of the whole
+    sequence). eta shrinks as b grows so that each chunk's update stays a contraction."""
     w = W["linear_tiny_f32"].with_(B=B, H=H, T=T, d=d, b=b, eta=eta, w_std=0.02, seed=40 + T + d + b)
     inp = synth.make_inputs(w)
     dZ, dW = upstream(w, seed=T + b)
@@ -47,14 +53,15 @@ def test_backward_matches_oracle(B, H, T, d, b, eta):
         assert rel_err(name, g, r, 1e-4) <= 1e-4, (name, rel_l2(g, r))
 
 
-def test_backward_empty_sequence():
+@pytest.mark.parametrize("b", [16, 128])
+def test_backward_empty_sequence(b):
     """T = 0: no tokens, so dW0 is dW_out summed over the batch rows and d eta is 0."""
     w = W["linear_tiny_f32"].with_(B=2, H=2, T=0, d=16, seed=3)
     inp = synth.make_inputs(w)
     dZ, dW = upstream(w, seed=1)
     t = torch_inputs(inp)
     dev = t["W0"].device
-    _, _, _, deta, dW0 = ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16,
+    _, _, _, deta, dW0 = ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], b,
                                             torch.from_numpy(dZ).to(dev), torch.from_numpy(dW).to(dev))
     torch.cuda.synchronize()
     assert np.array_equal(deta.cpu().numpy(), np.zeros(2, np.float32))
@@ -67,12 +74,13 @@ def bf16_round(a):
 
 @pytest.mark.parametrize("B,H,T,d,b", [(1, 1, 16, 64, 16), (1, 2, 64, 64, 16), (2, 2, 100, 64, 16),
                                        (1, 3, 130, 64, 16), (2, 1, 257, 64, 16), (1, 2, 1000, 64, 16),
-                                       (2, 2, 70, 32, 5), (1, 2, 50, 64, 32)])
+                                       (2, 2, 70, 32, 5), (1, 2, 50, 64, 32), (2, 2, 300, 64, 128)])
 def test_backward_bf16_matches_oracle(B, H, T, d, b):
     """bf16 operands: the tensor-core kernel (d = 64, b = 16: single chunks, ragged tails, one
     and several 64-token blocks) and the SIMT kernel on other shapes, against the fp64 backward
-    of the same bf16 values."""
-    w = W["linear_small"].with_(B=B, H=H, T=T, d=d, b=b, eta=("uniform", 0.05, 0.5), seed=60 + T + d + b)
+    of the same bf16 values; b = 128 walks its chunks in blocks, at a smaller eta."""
+    eta = ("uniform", 0.05, 0.5) if b <= 64 else ("const", 0.02)
+    w = W["linear_small"].with_(B=B, H=H, T=T, d=d, b=b, eta=eta, seed=60 + T + d + b)
     inp = synth.make_inputs(w)
     g = np.random.default_rng(T + 3 * b)
     dZ = bf16_round(g.standard_normal((B, H, T, d)).astype(np.float32))
