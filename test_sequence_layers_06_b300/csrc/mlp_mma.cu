@@ -21,7 +21,9 @@
 // (rewritten after every update, 128-byte XOR swizzle), so every product reads
 // whatever fragment layout it needs with ldmatrix, transposed or not. Q, K, V
 // tiles arrive by TMA, double-buffered. Products over the hidden dimension
-// (G, Z, tril(Aq A^T)) are split across warps and summed through shared memory.
+// (G, Z) are split across warps by hidden quarter and summed through shared
+// memory; tril(Aq A^T) is linear in its hidden terms, so each quarter applies
+// its own part of it to G before that sum.
 #include "kernels.h"
 #include "ttt_device.cuh"
 
@@ -46,10 +48,7 @@ constexpr int kGb = kAqb + kTile * kRowM;            // G, bf16 [16][64]
 constexpr int kSb = kGb + kTile * 128;               // tril(Q K^T), bf16 [16][16] in 128-byte rows
 constexpr int kPart = kSb + kTile * 128;             // partial sums, fp32: G or Z [4][16][kPad]
 constexpr int kPad = 68;                             // fp32 row stride of the partial buffers
-constexpr int kSap = kPart + 4 * kTile * kPad * 4;   // tril(Aq A^T) partials [16][16][16] fp32
-constexpr int kGf = kSap + kWarps * kTile * kTile * 4;  // G fp32 [16][kPad]
-constexpr int kSaf = kGf + kTile * kPad * 4;         // tril(Aq A^T) fp32 [16][16]
-constexpr int kBar = kSaf + kTile * kTile * 4;       // 2 mbarriers
+constexpr int kBar = kPart + 4 * kTile * kPad * 4;   // 2 mbarriers
 constexpr int kBaseBytes = kBar + 64;
 constexpr int kW1s = kBaseBytes;                     // chunk-start copies (b > 16 only)
 constexpr int kW2s = kW1s + kD * kRowM;
@@ -132,9 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* W1s = snap ? sm + kW1s : sm + kW1b;
   uint8_t* W2s = snap ? sm + kW2s : sm + kW2b;
   float* part = reinterpret_cast<float*>(sm + kPart);
-  float* sap = reinterpret_cast<float*>(sm + kSap);
-  float* gf = reinterpret_cast<float*>(sm + kGf);
-  float* saf = reinterpret_cast<float*>(sm + kSaf);
 
   const int unit = blockIdx.x;
   const int h = unit % p.H;
@@ -259,24 +255,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int r = 0; r < 4; ++r) gelu2(cu[nt][r], cu[nt][r], cp[nt][r]);
     st_tile(sm + kAb, kRowM, 0, warp, cu, lane);
-    if (warp == 0) {
-      float cs[2][4] = {};
+    if (warp < 2) {  // warp nt forms columns [8nt, 8nt + 8) of S
+      const int nt = warp;
+      float cs[4] = {};
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         uint32_t a[4], b[4];
         ldA(a, sQ, 128, 0, 2 * ks, lane);
         ldB(b, sK, 128, 0, 2 * ks, lane);
-        mma2(cs, a, b);
+        const uint32_t bn[2] = {b[2 * nt], b[2 * nt + 1]};
+        mma_bf16_16816(cs, a, bn);
       }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {  // keep column <= row (update, then read)
-        const int c = 8 * nt + 2 * tg;
-        if (c > g) cs[nt][0] = 0.f;
-        if (c + 1 > g) cs[nt][1] = 0.f;
-        if (c > g + 8) cs[nt][2] = 0.f;
-        if (c + 1 > g + 8) cs[nt][3] = 0.f;
-      }
-      st_tile(sm + kSb, 128, 0, 0, cs, lane);
+      const int c = 8 * nt + 2 * tg;  // keep column <= row (update, then read)
+      if (c > g) cs[0] = 0.f;
+      if (c + 1 > g) cs[1] = 0.f;
+      if (c > g + 8) cs[2] = 0.f;
+      if (c + 1 > g + 8) cs[3] = 0.f;
+      *reinterpret_cast<uint32_t*>(sm + kSb + swz(g, nt, 128) + 4 * tg) = pack_bf16(cs[0], cs[1]);
+      *reinterpret_cast<uint32_t*>(sm + kSb + swz(g + 8, nt, 128) + 4 * tg) = pack_bf16(cs[2], cs[3]);
     }
     __syncthreads();
 
@@ -313,7 +309,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t vv = *reinterpret_cast<const uint32_t*>(sVp + swz(t, j >> 3, 128) + (j & 7) * 2);
       acc.x -= bf16_lo(vv);
       acc.y -= bf16_hi(vv);
-      *reinterpret_cast<float2*>(gf + t * kPad + j) = acc;
       *reinterpret_cast<uint32_t*>(sm + kGb + swz(t, j >> 3, 128) + (j & 7) * 2) = pack_bf16(acc.x, acc.y);
     }
     __syncthreads();
@@ -391,18 +386,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     TTT_STORE_W1(sm + kW1b);
     if (snap && chunk_end) TTT_STORE_W1(W1s);
     __syncthreads();  // Aq complete
-    // (5) Z partials (value columns [16(w&3), +16), hidden quarter w>>2) and
-    //     tril(Aq A^T) partials (hidden [16w, +16)).
+    // (5) Z partials: warp -> value columns [16(w&3), +16), hidden quarter kq = w>>2:
+    //     Aq_kq W2_kq - eta tril(Aq_kq A_kq^T) G, the second term by the quarter's own
+    //     16 x 16 block of tril(Aq A^T) (the four quarters' blocks sum to the whole).
     {
       const int np = warp & 3, kq = warp >> 2;
-      float cz[2][4] = {};
+      float cz[2][4] = {}, csa[2][4] = {};
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        uint32_t a[4], b[4];
+        uint32_t a[4], b[4], ba[4];
         ldA(a, Aqb, kRowM, 0, 8 * kq + 2 * ks, lane);
         ldBT(b, W2b, 128, 64 * kq + 16 * ks, 2 * np, lane);
+        ldB(ba, Ab, kRowM, 0, 8 * kq + 2 * ks, lane);
         mma2(cz, a, b);
+        mma2(csa, a, ba);
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {  // keep t2 <= t, scale by -eta
+        const int c = 8 * nt + 2 * tg;
+        csa[nt][0] = c > g ? 0.f : -eta * csa[nt][0];
+        csa[nt][1] = c + 1 > g ? 0.f : -eta * csa[nt][1];
+        csa[nt][2] = c > g + 8 ? 0.f : -eta * csa[nt][2];
+        csa[nt][3] = c + 1 > g + 8 ? 0.f : -eta * csa[nt][3];
+      }
+      // The C fragment of the 16 x 16 block is the A fragment (m = t, k = t2) of the next product.
+      const uint32_t sa[4] = {pack_bf16(csa[0][0], csa[0][1]), pack_bf16(csa[0][2], csa[0][3]),
+                              pack_bf16(csa[1][0], csa[1][1]), pack_bf16(csa[1][2], csa[1][3])};
+      uint32_t bg[4];
+      ldBT(bg, Gb, 128, 0, 2 * np, lane);
+      mma2(cz, sa, bg);
       float* dst = part + kq * kTile * kPad;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -410,32 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float2*>(dst + g * kPad + c) = make_float2(cz[nt][0], cz[nt][1]);
         *reinterpret_cast<float2*>(dst + (g + 8) * kPad + c) = make_float2(cz[nt][2], cz[nt][3]);
       }
-      float csa[2][4] = {};
-      uint32_t a[4], b[4];
-      ldA(a, Aqb, kRowM, 0, 2 * warp, lane);
-      ldB(b, Ab, kRowM, 0, 2 * warp, lane);
-      mma2(csa, a, b);
-      float* sd = sap + warp * kTile * kTile;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int c = 8 * nt + 2 * tg;
-        *reinterpret_cast<float2*>(sd + g * kTile + c) = make_float2(csa[nt][0], csa[nt][1]);
-        *reinterpret_cast<float2*>(sd + (g + 8) * kTile + c) = make_float2(csa[nt][2], csa[nt][3]);
-      }
     }
-    __syncthreads();  // every read of the running W2 copy is done
+    __syncthreads();  // every read of the running W2 copy is done; the Z partials are written
 
     TTT_STORE_W2(sm + kW2b);
     if (snap && chunk_end) TTT_STORE_W2(W2s);
-    if (tid < kTile * kTile) {
-      const int t = tid >> 4, t2 = tid & 15;
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) v += sap[w * kTile * kTile + tid];
-      saf[tid] = t2 <= t ? v : 0.f;
-    }
-    __syncthreads();
-    // Z = sum of the quarters - eta tril(Aq A^T) G, written for the rows inside the sequence.
+    // Z = sum of the quarters, written for the rows inside the sequence.
     {
       const int t = tid >> 5, j = (tid & 31) * 2;
       float2 z = make_float2(0.f, 0.f);
@@ -445,22 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         z.x += v.x;
         z.y += v.y;
       }
-      float2 r = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int t2 = 0; t2 < kTile; ++t2) {
-        const float sv = saf[t * kTile + t2];
-        const float2 gv = *reinterpret_cast<const float2*>(gf + t2 * kPad + j);
-        r.x = fmaf(sv, gv.x, r.x);
-        r.y = fmaf(sv, gv.y, r.y);
-      }
       const int tt = u * kTile + t;
       if (tt < p.T) {
         __nv_bfloat16* Z = static_cast<__nv_bfloat16*>(p.Z) + (static_cast<size_t>(unit) * p.T + tt) * kD + j;
-        *reinterpret_cast<uint32_t*>(Z) = pack_bf16(fmaf(-eta, r.x, z.x), fmaf(-eta, r.y, z.y));
+        *reinterpret_cast<uint32_t*>(Z) = pack_bf16(z.x, z.y);
       }
     }
-    // No barrier here: the next tile first meets at its start barrier, and the buffers read
-    // above (part, gf, saf) are written again only after that.
+    // No barrier here: the next tile first meets at its start barrier, and the buffer read
+    // above (part) is written again only after that.
   }
   // Final state.
   float* W1o = p.W1_out + static_cast<size_t>(unit) * kD * kM;
