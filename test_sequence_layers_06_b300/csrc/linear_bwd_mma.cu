@@ -71,13 +71,6 @@ __device__ __forceinline__ void unpack4(uint4 v, float (&s)[2][4]) {
   s[1][2] = bf16_lo(v.w); s[1][3] = bf16_hi(v.w);
 }
 
-// Transpose of an 8 x 8 bf16 matrix held one row pair per thread (the fragment layout).
-__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
-  uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
-  return d;
-}
-
 // A fragments (bf16) of a 16 x 64 block of X^T held as fp32 C fragments xt[8][4]
 // (rows m, columns 8q + 2tg): k-step s covers columns [16s, 16s + 16).
 __device__ __forceinline__ void pack_a(const float (&xt)[8][4], uint32_t (&a)[4][4]) {

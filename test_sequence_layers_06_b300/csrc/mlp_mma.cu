@@ -42,8 +42,7 @@ constexpr int kQKV = 0;                              // [2 stages][Q, K, V] tile
 constexpr int kW1b = kQKV + 2 * 3 * kTileBytes;      // W1 running, bf16 [64][256]
 constexpr int kW2b = kW1b + kD * kRowM;              // W2 running, bf16 [256][64]
 constexpr int kAb = kW2b + kM * 128;                 // A, bf16 [16][256]
-constexpr int kDb = kAb + kTile * kRowM;             // D
-constexpr int kAqb = kDb + kTile * kRowM;            // Aq
+constexpr int kAqb = kAb + kTile * kRowM;            // Aq
 constexpr int kGb = kAqb + kTile * kRowM;            // G, bf16 [16][64]
 constexpr int kSb = kGb + kTile * 128;               // tril(Q K^T), bf16 [16][16] in 128-byte rows
 constexpr int kPart = kSb + kTile * 128;             // partial sums, fp32: G or Z [4][16][kPad]
@@ -215,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const uint32_t W1b = s0 + kW1b, W2b = s0 + kW2b, W1sa = smem_u32(W1s), W2sa = smem_u32(W2s);
-  const uint32_t Ab = s0 + kAb, Db = s0 + kDb, Aqb = s0 + kAqb, Gb = s0 + kGb, Sb = s0 + kSb;
+  const uint32_t Ab = s0 + kAb, Aqb = s0 + kAqb, Gb = s0 + kGb, Sb = s0 + kSb;
   bool ok = true;
 
   for (int u = 0; u < n_tiles; ++u) {
@@ -314,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // (3) D = (G W2a^T) .* P for hidden [16w, +16);  W2 -= eta A^T G (this warp's rows).
+    uint32_t bd[4];
     {
       float cd[2][4] = {};
 #pragma unroll
@@ -327,7 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) cd[nt][r] *= cp[nt][r];
-      st_tile(sm + kDb, kRowM, 0, warp, cd, lane);
+      // D as the B operand (k = t, n = hidden) of S D and K^T D: the transposed 8 x 8
+      // blocks of its C fragment, in registers (no other warp reads this warp's D).
+      bd[0] = movm_t(pack_bf16(cd[0][0], cd[0][1]));
+      bd[1] = movm_t(pack_bf16(cd[0][2], cd[0][3]));
+      bd[2] = movm_t(pack_bf16(cd[1][0], cd[1][1]));
+      bd[3] = movm_t(pack_bf16(cd[1][2], cd[1][3]));
 
       uint32_t a[4];
       ldAT(a, Ab, kRowM, 0, 2 * warp, lane);
@@ -343,8 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = 0; r < 4; ++r) w2[2 * q + nt][r] = fmaf(-eta, acc[nt][r], w2[2 * q + nt][r]);
       }
     }
-    // D's columns [16w, +16) are written and read by this warp alone: no CTA barrier.
-    __syncwarp();
 
     // (4) Hq = Q W1 - eta tril(Q K^T) D, Aq = gelu(Hq);  W1 -= eta K^T D (this warp's columns).
     {
@@ -356,8 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ldBT(b, W1b, kRowM, 16 * ks, 2 * warp, lane);
         mma2(ch, a, b);
       }
-      uint32_t bd[4];
-      ldBT(bd, Db, kRowM, 0, 2 * warp, lane);
       {
         uint32_t a[4];
         ldA(a, Sb, 128, 0, 0, lane);

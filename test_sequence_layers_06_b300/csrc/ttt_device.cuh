@@ -156,6 +156,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t* r, uint32_t addr) {
                : "r"(addr));
 }
 
+// Transpose of an 8 x 8 bf16 matrix held one row pair per thread (the fragment layout).
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
 __device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t* r) {
   asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
                "r"(r[2]), "r"(r[3])
