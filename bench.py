@@ -623,6 +623,32 @@ def bench_extras(ttt, dev, stream):
                 "hbm_frac": round(algorithmic_bytes(w) / (ms * 1e-3) / 1e9 / hbm_gbs, 5),
                 "note": "B2 H4 T2048 d64 bf16 in, fp32 SIMT kernel, one CTA per (batch row, head)"}
         del Q, K, V
+        # The bias (d = 63, padded to 64) and the per-token rate (d = 64) on the tensor-core
+        # kernels, long-context shape: prep pass + ttt_linear_fwd's plan + copy-out.
+        for name in ("bias", "token_eta"):
+            d = 63 if name == "bias" else 64
+            w = synth.WORKLOADS["linear_long"].with_(d=d)
+            inp, Q, K, V, eta = dev_inputs(w)
+            W0 = torch.from_numpy(inp.W0).to(dev)
+            code = ttt.TTT_INNER_BIAS if name == "bias" else ttt.TTT_INNER_TOKEN_ETA
+            vws = torch.empty(ttt.ttt_linear_variant_workspace_bytes(code, ttt.TTT_BF16, w.B, w.H, w.T, d, 16),
+                              dtype=torch.uint8, device=dev)
+            if name == "bias":
+                vec = torch.zeros((w.H, d), dtype=torch.float32, device=dev)
+                fn = lambda: ttt.ttt_linear_bias_fwd(Q, K, V, eta, W0, vec, 16, stream=stream, fast=True, workspace=vws)
+            else:
+                et = torch.full((w.B, w.H, w.T), 0.1, dtype=torch.float32, device=dev)
+                fn = lambda: ttt.ttt_linear_token_eta_fwd(Q, K, V, et, W0, 16, stream=stream, fast=True,
+                                                          workspace=vws)
+            ms = t_ms(fn, 5)
+            if ttt.ttt_last_device_status(vws, stream) != 0:
+                raise RuntimeError(f"variant {name}: device status not OK")
+            out[f"variant_{name}_fast_long_b16"] = {
+                "ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                "hbm_frac": round(algorithmic_bytes(w) / (ms * 1e-3) / 1e9 / hbm_gbs, 4),
+                "note": f"B1 H32 T131072 d{d} bf16: changed inputs (padded to 64 features) through the "
+                        "tensor-core segment-parallel path; bytes counted at d"}
+            del Q, K, V, vws
     except Exception as exc:  # reported in the line, never silently dropped
         out["variants"] = {"error": f"{type(exc).__name__}: {exc}"}
     # backward of TTT-Linear on the tensor cores (bf16, b = 16), 125M-shaped: B8 H12 T8192

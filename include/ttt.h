@@ -71,6 +71,14 @@ typedef enum {
 
 typedef enum { TTT_VARIANT_LINEAR = 0, TTT_VARIANT_MLP = 1 } ttt_variant;
 
+/* Inner-model variants of TTT-Linear (the ttt_linear_*_fwd calls below). */
+typedef enum {
+  TTT_INNER_BIAS = 1,
+  TTT_INNER_TOKEN_ETA = 2,
+  TTT_INNER_LN = 3,
+  TTT_INNER_MOMENTUM = 4
+} ttt_inner_variant;
+
 /* Options for the *_ex calls. Zero-initialise, then set fields. */
 typedef struct {
   uint64_t wait_timeout_ns; /* limit for every wait inside a kernel; 0 = 2 s */
@@ -240,8 +248,8 @@ TTT_API ttt_status ttt_linear_decode(const void* q, const void* k, const void* v
 
 /*
  * Inner-model variants of TTT-Linear. The pages name these ingredients without
- * formulas; each call states the reading it computes. All four run one fp32
- * CUDA kernel per call (linear_variants.cu): one CTA per (batch row, head),
+ * formulas; each call states the reading it computes. The four plain calls run
+ * one fp32 CUDA kernel per call (linear_variants.cu): one CTA per (batch row, head),
  * the state in shared memory, any d <= 64 and any b, Q/K/V/Z fp32 or bf16
  * (dt). They take no workspace (the kernel has no waits and no status word).
  * Q, K, V, Z, eta, W0, W_out and the per-call arrays follow ttt_linear_fwd's
@@ -268,6 +276,42 @@ TTT_API ttt_status ttt_linear_bias_fwd(const void* Q, const void* K, const void*
 TTT_API ttt_status ttt_linear_token_eta_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt,
                                             const float* eta_tok, const float* W0, int B, int H, int T,
                                             int d, int b, void* Z, float* W_out, void* stream);
+
+/*
+ * The bias and the per-token rate on the tensor-core kernels. Both variants are
+ * the plain chunk rule on changed inputs, padded to 64 features:
+ *   bias (d <= 63): q' = [q | 1 | 0], k' = [k | 1 | 0], v' = [v | 0] and
+ *     W0' = [[W0, 0]; [beta0, 0]; [0, 0]]; the state's row d is beta, its
+ *     padded columns stay 0, and z' = [q W + beta | 0];
+ *   per-token rate (d <= 64): k' = sqrt(eta_t) k, v' = sqrt(eta_t) v, eta = 1;
+ *     q is unchanged (zero-padded when d < 64).
+ * The *_ex calls take a workspace of ttt_linear_variant_workspace_bytes(variant,
+ * dt, B, H, T, d, b) bytes (16-byte aligned, disjoint from every input and
+ * output): a status word, the changed inputs and the inner ttt_linear_fwd's own
+ * workspace. With bf16 operands and b % 16 == 0 they write the changed inputs
+ * (one elementwise kernel), run ttt_linear_fwd's kernels on them (one pass or
+ * segment-parallel, by its automatic plan) and copy Z, W_out and beta_out out
+ * of the padded results; otherwise (fp32, b % 16 != 0, d too large for the
+ * padding) they run the fp32 variant kernel like the plain calls, and the
+ * workspace holds only the status word. Results equal the plain calls' up to
+ * rounding: k' and v' are rounded to bf16 again after the scaling.
+ * ttt_last_device_status(workspace, stream) reports the inner forward's bounded
+ * waits and, for the per-token rate, TTT_ERR_DEVICE_CHECK when some eta_t < 0
+ * (that unit's results are then undefined).
+ * ttt_linear_variant_workspace_bytes returns 0 for bad sizes or a variant
+ * without an *_ex call (TTT_INNER_LN, TTT_INNER_MOMENTUM).
+ */
+TTT_API size_t ttt_linear_variant_workspace_bytes(int variant, ttt_dtype dt, int B, int H, int T, int d, int b);
+
+TTT_API ttt_status ttt_linear_bias_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                          const float* eta, const float* W0, const float* beta0, int B,
+                                          int H, int T, int d, int b, void* Z, float* W_out, float* beta_out,
+                                          void* workspace, size_t ws_bytes, void* stream);
+
+TTT_API ttt_status ttt_linear_token_eta_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                               const float* eta_tok, const float* W0, int B, int H, int T,
+                                               int d, int b, void* Z, float* W_out, void* workspace,
+                                               size_t ws_bytes, void* stream);
 
 /* ttt_linear_ln_fwd: a layer norm and a residual inside f (same page, section
  * 3.1): f(k) = k + LN(k W), LN(y) = gamma (y - mean y) / sqrt(var y + 1e-6)

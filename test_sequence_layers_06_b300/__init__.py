@@ -8,6 +8,7 @@ library is missing or no GPU is present the calls fail loudly.
 
 Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_plan, ttt_linear_fwd,
 ttt_linear_bias_fwd, ttt_linear_token_eta_fwd, ttt_linear_ln_fwd, ttt_linear_momentum_fwd,
+ttt_linear_variant_workspace_bytes (the bias and per-token-rate *_ex calls are reached through fast=True),
 ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_mlp_noalloc_last_device_status, ttt_linear_decode_step, ttt_linear_bwd_workspace_bytes,
 ttt_linear_bwd, ttt_last_device_status, ttt_status_str. The *_fwd_ex forms are reached
 through the options argument.
@@ -23,13 +24,15 @@ LIB_PATH = os.path.join(HERE, "libttt_b300.so")
 TTT_OK, TTT_ERR_ARG, TTT_ERR_UNSUPPORTED, TTT_ERR_CUDA, TTT_ERR_TIMEOUT, TTT_ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
 TTT_F32, TTT_BF16 = 0, 1
 TTT_VARIANT_LINEAR, TTT_VARIANT_MLP = 0, 1
+TTT_INNER_BIAS, TTT_INNER_TOKEN_ETA, TTT_INNER_LN, TTT_INNER_MOMENTUM = 1, 2, 3, 4
 PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_SEGMENTED = 0, 1, 2, 3
 
 # Every entry point include/ttt.h declares.
 EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_plan", "ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex",
            "ttt_mlp_fwd_noalloc", "ttt_mlp_noalloc_last_device_status", "ttt_linear_decode_step", "ttt_linear_bwd_workspace_bytes", "ttt_linear_bwd",
            "ttt_last_device_status", "ttt_status_str", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
-           "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode")
+           "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode",
+           "ttt_linear_variant_workspace_bytes", "ttt_linear_bias_fwd_ex", "ttt_linear_token_eta_fwd_ex")
 
 
 class TTTError(RuntimeError):
@@ -86,11 +89,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_linear_token_eta_fwd.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp]
     lib.ttt_linear_ln_fwd.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, i, vp, vp, vp]
     lib.ttt_linear_momentum_fwd.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
+    lib.ttt_linear_variant_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    lib.ttt_linear_variant_workspace_bytes.restype = sz
+    lib.ttt_linear_bias_fwd_ex.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+    lib.ttt_linear_token_eta_fwd_ex.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, sz, vp]
     lib.ttt_status_str.argtypes = [i]
     lib.ttt_status_str.restype = ctypes.c_char_p
     for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex", "ttt_mlp_fwd_noalloc",
               "ttt_mlp_noalloc_last_device_status", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
-              "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode",
+              "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode", "ttt_linear_bias_fwd_ex",
+              "ttt_linear_token_eta_fwd_ex",
               "ttt_linear_decode_step", "ttt_linear_bwd", "ttt_last_device_status"):
         getattr(lib, f).restype = i
     _lib = lib
@@ -311,25 +319,49 @@ def _variant_call(name, *args, dev):
         raise TTTError(name, st)
 
 
-def ttt_linear_bias_fwd(Q, K, V, eta, W0, beta0, b: int, stream=None):
-    """TTT-Linear with f(k) = k W + beta; returns (Z, W_out, beta_out)."""
+def ttt_linear_variant_workspace_bytes(variant: int, dtype: int, B: int, H: int, T: int, d: int, b: int) -> int:
+    return int(load_library().ttt_linear_variant_workspace_bytes(variant, dtype, B, H, T, d, b))
+
+
+def _variant_workspace(variant, Q, B, H, T, d, b, dev, workspace):
+    import torch
+    need = ttt_linear_variant_workspace_bytes(variant, _dtype_code(Q), B, H, T, d, b)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    return workspace
+
+
+def ttt_linear_bias_fwd(Q, K, V, eta, W0, beta0, b: int, stream=None, fast=False, workspace=None):
+    """TTT-Linear with f(k) = k W + beta; returns (Z, W_out, beta_out). fast=True calls
+    ttt_linear_bias_fwd_ex (the tensor-core path on padded inputs where it applies)."""
     import torch
     B, H, T, d, dev, Z, W_out = _variant_prologue(Q, K, V, W0)
     _check(eta, "eta", torch.float32, (H,), dev)
     _check(beta0, "beta0", torch.float32, (H, d), dev)
     beta_out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
-    _variant_call("ttt_linear_bias_fwd", _p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), _p(beta0), B, H, T,
-                  d, int(b), _p(Z), _p(W_out), _p(beta_out), _stream_ptr(stream, dev), dev=dev)
+    args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), _p(beta0), B, H, T, d, int(b), _p(Z), _p(W_out),
+            _p(beta_out))
+    if fast:
+        ws = _variant_workspace(TTT_INNER_BIAS, Q, B, H, T, d, b, dev, workspace)
+        _variant_call("ttt_linear_bias_fwd_ex", *args, _p(ws), ws.numel(), _stream_ptr(stream, dev), dev=dev)
+    else:
+        _variant_call("ttt_linear_bias_fwd", *args, _stream_ptr(stream, dev), dev=dev)
     return Z, W_out, beta_out
 
 
-def ttt_linear_token_eta_fwd(Q, K, V, eta_tok, W0, b: int, stream=None):
-    """TTT-Linear with a learning rate per token, eta_tok [B, H, T]; returns (Z, W_out)."""
+def ttt_linear_token_eta_fwd(Q, K, V, eta_tok, W0, b: int, stream=None, fast=False, workspace=None):
+    """TTT-Linear with a learning rate per token, eta_tok [B, H, T]; returns (Z, W_out).
+    fast=True calls ttt_linear_token_eta_fwd_ex (the tensor-core path on scaled inputs where it
+    applies)."""
     import torch
     B, H, T, d, dev, Z, W_out = _variant_prologue(Q, K, V, W0)
     _check(eta_tok, "eta_tok", torch.float32, (B, H, T), dev)
-    _variant_call("ttt_linear_token_eta_fwd", _p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta_tok), _p(W0), B, H, T, d,
-                  int(b), _p(Z), _p(W_out), _stream_ptr(stream, dev), dev=dev)
+    args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta_tok), _p(W0), B, H, T, d, int(b), _p(Z), _p(W_out))
+    if fast:
+        ws = _variant_workspace(TTT_INNER_TOKEN_ETA, Q, B, H, T, d, b, dev, workspace)
+        _variant_call("ttt_linear_token_eta_fwd_ex", *args, _p(ws), ws.numel(), _stream_ptr(stream, dev), dev=dev)
+    else:
+        _variant_call("ttt_linear_token_eta_fwd", *args, _stream_ptr(stream, dev), dev=dev)
     return Z, W_out
 
 

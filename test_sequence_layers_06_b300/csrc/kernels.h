@@ -88,7 +88,8 @@ struct LinearBwdParams {
 };
 
 // Inner-model variants of TTT-Linear (linear_variants.cu), fp32 arithmetic.
-enum : int { kVarBias = 1, kVarTokenEta = 2, kVarLn = 3, kVarMomentum = 4 };
+enum : int { kVarBias = TTT_INNER_BIAS, kVarTokenEta = TTT_INNER_TOKEN_ETA, kVarLn = TTT_INNER_LN,
+              kVarMomentum = TTT_INNER_MOMENTUM };
 struct VariantParams {
   const void* Q;
   const void* K;
@@ -108,6 +109,39 @@ struct VariantParams {
   int variant;            // kVar*
 };
 cudaError_t launch_linear_variant(const VariantParams& p, cudaStream_t stream);
+
+// The bias and per-token-rate variants as the plain rule on changed inputs
+// (linear_prep.cu): padded to 64 features, bf16.
+struct VariantPrepParams {
+  const void* Q;            // [units][T][d] bf16
+  const void* K;
+  const void* V;
+  const float* tok_rate;    // [units][T] (per-token rate; null: none)
+  void* Qp;                 // [units][T][64] bf16; null: Q is used as it is
+  void* Kp;
+  void* Vp;
+  const float* W0;          // [H][d][d]
+  const float* beta0;       // [H][d] (bias)
+  float* W0p;               // [H][64][64]
+  const float* eta;         // [H]; null: ones
+  float* etap;              // [H]
+  int units, H, T, d;
+  bool bias;
+  StatusBlock* status;
+};
+cudaError_t launch_variant_prep(const VariantPrepParams& p, cudaStream_t stream);
+
+struct VariantPostParams {
+  const void* Zp;           // [units][T][64] bf16; null: Z was written in place
+  void* Z;                  // [units][T][d] bf16
+  const float* Wp;          // [units][64][64]; null: W_out was written in place
+  float* W_out;             // [units][d][d]
+  float* beta_out;          // [units][d] (bias) or null
+  int units, T, d;
+  StatusBlock* status;      // the call's status word
+  const StatusBlock* sub;   // the inner forward's
+};
+cudaError_t launch_variant_post(const VariantPostParams& p, cudaStream_t stream);
 
 struct DecodeParams {
   const void* q;

@@ -1,0 +1,138 @@
+// Two inner-model variants of TTT-Linear on the tensor-core kernels, by changing
+// their inputs (bf16 operands). Both are the plain chunk rule of the dual form
+// ("5 · TestingTime 训练与长上下文", sections 1.1 and 3.1; "Test-Time Training
+// (TTT) guide", section 3) on other Q, K, V and W0:
+//
+//   bias, f(k) = k W + beta (d <= 63): append a constant-1 feature to q and k,
+//     pad every row to 64 features, and stack beta under W:
+//       q' = [q | 1 | 0],  k' = [k | 1 | 0],  v' = [v | 0],  W0' = [[W0, 0]; [beta0, 0]; [0, 0]].
+//     Then e' = k' W' - v' = [k W + beta - v | 0], the update of W' is the
+//     updates of W (rows < d) and of beta (row d), the padded columns of W'
+//     stay 0, and z' = q' W' = [q W + beta | 0].
+//   learning rate per token, eta_t >= 0 (d <= 64): scale k and v by sqrt(eta_t)
+//     and run with eta = 1, since sqrt(eta_t) k^T (sqrt(eta_t) k W - sqrt(eta_t) v)
+//     = eta_t k^T (k W - v); q is unchanged (padded with zeros when d < 64).
+//
+// variant_prep_kernel writes the changed inputs (bf16, 64 features per row) and
+// W0' (fp32); variant_post_kernel copies Z, W_out and beta_out back out of the
+// padded results and merges the status words. Both are elementwise passes with
+// one warp per token row.
+#include <algorithm>
+
+#include "ttt_device.cuh"
+#include "kernels.h"
+
+namespace ttt {
+namespace {
+
+constexpr int kPrepThreads = 256;
+constexpr int kP = 64;  // padded width
+
+enum : int { kWhereNegativeRate = 20 };
+
+__device__ __forceinline__ float ldbf(const void* p, size_t i) {
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+__device__ __forceinline__ void stbf(void* p, size_t i, float v) {
+  static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+}
+
+// Blocks [0, H): W0' and eta' of head h. Blocks from H on: token rows, one warp
+// per row, grid-stride.
+__global__ void __launch_bounds__(kPrepThreads) variant_prep_kernel(VariantPrepParams p) {
+  const int d = p.d;
+  if (static_cast<int>(blockIdx.x) < p.H) {
+    const int h = blockIdx.x;
+    for (int x = threadIdx.x; x < kP * kP; x += kPrepThreads) {
+      const int i = x / kP, j = x % kP;
+      float w = 0.f;
+      if (i < d && j < d)
+        w = p.W0[(static_cast<size_t>(h) * d + i) * d + j];
+      else if (p.bias && i == d && j < d)
+        w = p.beta0[static_cast<size_t>(h) * d + j];
+      p.W0p[static_cast<size_t>(h) * kP * kP + x] = w;
+    }
+    if (threadIdx.x == 0) p.etap[h] = p.eta ? p.eta[h] : 1.f;
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(p.units) * p.T;
+  const long long warps = static_cast<long long>(gridDim.x - p.H) * (kPrepThreads / 32);
+  for (long long r = static_cast<long long>(blockIdx.x - p.H) * (kPrepThreads / 32) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
+    float s = 1.f;
+    if (p.tok_rate) {
+      const float et = p.tok_rate[r];
+      if (et < 0.f) {
+        if (lane == 0) report_error(p.status, TTT_ERR_DEVICE_CHECK, kWhereNegativeRate, static_cast<int>(r / p.T));
+        s = 0.f;
+      } else {
+        s = sqrtf(et);
+      }
+    }
+    const size_t in = static_cast<size_t>(r) * d, out = static_cast<size_t>(r) * kP;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int f = lane + 32 * half;
+      const float one = (p.bias && f == d) ? 1.f : 0.f;
+      if (p.Qp) stbf(p.Qp, out + f, f < d ? ldbf(p.Q, in + f) : one);
+      stbf(p.Kp, out + f, f < d ? s * ldbf(p.K, in + f) : one);
+      stbf(p.Vp, out + f, f < d ? s * ldbf(p.V, in + f) : 0.f);
+    }
+  }
+}
+
+// Blocks [0, units): W_out (and beta_out) of a unit from the padded state; block 0
+// also merges the status word of the inner forward into the call's. Blocks from
+// units on: Z rows, one warp per row, grid-stride.
+__global__ void __launch_bounds__(kPrepThreads) variant_post_kernel(VariantPostParams p) {
+  const int d = p.d;
+  if (static_cast<int>(blockIdx.x) < p.units) {
+    const int unit = blockIdx.x;
+    if (unit == 0 && threadIdx.x == 0 && p.sub->code != 0) report_error(p.status, p.sub->code, p.sub->where, p.sub->unit);
+    if (p.Wp == nullptr) return;
+    const float* Wu = p.Wp + static_cast<size_t>(unit) * kP * kP;
+    for (int x = threadIdx.x; x < d * d; x += kPrepThreads) {
+      const int i = x / d, j = x % d;
+      p.W_out[static_cast<size_t>(unit) * d * d + x] = Wu[i * kP + j];
+    }
+    if (p.beta_out)
+      for (int j = threadIdx.x; j < d; j += kPrepThreads) p.beta_out[static_cast<size_t>(unit) * d + j] = Wu[d * kP + j];
+    return;
+  }
+  if (p.Zp == nullptr) return;
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(p.units) * p.T;
+  const long long warps = static_cast<long long>(gridDim.x - p.units) * (kPrepThreads / 32);
+  for (long long r = static_cast<long long>(blockIdx.x - p.units) * (kPrepThreads / 32) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
+    const size_t in = static_cast<size_t>(r) * kP, out = static_cast<size_t>(r) * d;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int f = lane + 32 * half;
+      if (f < d) static_cast<__nv_bfloat16*>(p.Z)[out + f] = static_cast<const __nv_bfloat16*>(p.Zp)[in + f];
+    }
+  }
+}
+
+int row_blocks(long long rows) {
+  const long long want = (rows + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
+  return static_cast<int>(std::min<long long>(want, 148LL * 16));
+}
+
+}  // namespace
+
+cudaError_t launch_variant_prep(const VariantPrepParams& p, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.units) * p.T;
+  variant_prep_kernel<<<p.H + (rows > 0 ? row_blocks(rows) : 0), kPrepThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_variant_post(const VariantPostParams& p, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.units) * p.T;
+  const int zblocks = (p.Zp != nullptr && rows > 0) ? row_blocks(rows) : 0;
+  variant_post_kernel<<<p.units + zblocks, kPrepThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ttt

@@ -556,10 +556,10 @@ ttt_status ttt_linear_decode_step(const void* q, const void* k, const void* v, t
 }
 
 // Shared checks and launch of the inner-model variants (linear_variants.cu).
-static ttt_status variant_fwd(int variant, const void* Q, const void* K, const void* V, ttt_dtype dt,
-                              const float* rate, const float* mbeta, const float* tok_rate, const float* W0,
-                              const float* vec0, const float* vec1, int B, int H, int T, int d, int b, void* Z,
-                              float* W_out, float* aux_out, void* stream) {
+static ttt_status variant_check(int variant, const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                const float* rate, const float* mbeta, const float* tok_rate, const float* W0,
+                                const float* vec0, const float* vec1, int B, int H, int T, int d, int b,
+                                const void* Z, const float* W_out, const float* aux_out) {
   if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
   if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
   if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
@@ -586,6 +586,13 @@ static ttt_status variant_fwd(int variant, const void* Q, const void* K, const v
                            {vec0, needs_v0 ? bytes4(H, d, 1, 1, 4) : 0}, {vec1, needs_v1 ? bytes4(H, d, 1, 1, 4) : 0}}))
       return TTT_ERR_ARG;
   }
+  return TTT_OK;
+}
+
+static ttt_status variant_simt(int variant, const void* Q, const void* K, const void* V, ttt_dtype dt,
+                               const float* rate, const float* mbeta, const float* tok_rate, const float* W0,
+                               const float* vec0, const float* vec1, int B, int H, int T, int d, int b, void* Z,
+                               float* W_out, float* aux_out, void* stream) {
   ttt::VariantParams p;
   p.Q = Q; p.K = K; p.V = V; p.Z = Z;
   p.rate = rate; p.mbeta = mbeta; p.tok_rate = tok_rate; p.W0 = W0; p.vec0 = vec0; p.vec1 = vec1;
@@ -595,6 +602,141 @@ static ttt_status variant_fwd(int variant, const void* Q, const void* K, const v
   p.bf16 = dt == TTT_BF16;
   p.variant = variant;
   return ttt::launch_linear_variant(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+static ttt_status variant_fwd(int variant, const void* Q, const void* K, const void* V, ttt_dtype dt,
+                              const float* rate, const float* mbeta, const float* tok_rate, const float* W0,
+                              const float* vec0, const float* vec1, int B, int H, int T, int d, int b, void* Z,
+                              float* W_out, float* aux_out, void* stream) {
+  const ttt_status st = variant_check(variant, Q, K, V, dt, rate, mbeta, tok_rate, W0, vec0, vec1, B, H, T, d, b, Z,
+                                      W_out, aux_out);
+  if (st != TTT_OK) return st;
+  return variant_simt(variant, Q, K, V, dt, rate, mbeta, tok_rate, W0, vec0, vec1, B, H, T, d, b, Z, W_out, aux_out,
+                      stream);
+}
+
+// ---------------------------------------------------------------- bias and per-token rate on the
+// tensor-core path: the plain rule on changed inputs (linear_prep.cu), padded to 64 features.
+namespace {
+
+constexpr int kPadD = 64;
+
+bool variant_fast_ok(int variant, ttt_dtype dt, int d, int b) {
+  if (dt != TTT_BF16 || b % 16 != 0) return false;
+  if (variant == ttt::kVarBias) return d <= kPadD - 1;
+  if (variant == ttt::kVarTokenEta) return d <= kPadD;
+  return false;
+}
+
+// Byte offsets in the workspace: [status][inner forward's workspace][Q'][K'][V'][Z'][W0'][W_out'][eta'].
+// Q', Z' and W_out' exist only when the rows are padded (the bias, or d < 64).
+struct VariantLayout {
+  size_t sub, sub_bytes, qp, kp, vp, zp, w0p, wp, etap, total;
+};
+
+VariantLayout variant_layout(int variant, int B, int H, int T, int d, int b) {
+  VariantLayout L{};
+  const size_t units = static_cast<size_t>(B) * H;
+  const size_t seq = round_up(units * static_cast<size_t>(T) * kPadD * 2, 256);
+  const bool pad = variant == ttt::kVarBias || d < kPadD;
+  size_t off = kStatusBytes;
+  L.sub = off;
+  L.sub_bytes = round_up(workspace_bytes_impl(B, H, T, kPadD, b, TTT_VARIANT_LINEAR, nullptr), 256);
+  off += L.sub_bytes;
+  if (pad) { L.qp = off; off += seq; }
+  L.kp = off; off += seq;
+  L.vp = off; off += seq;
+  if (pad) { L.zp = off; off += seq; }
+  L.w0p = off; off += round_up(static_cast<size_t>(H) * kPadD * kPadD * 4, 256);
+  if (pad) { L.wp = off; off += round_up(units * kPadD * kPadD * 4, 256); }
+  L.etap = off; off += round_up(static_cast<size_t>(H) * 4, 256);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+size_t ttt_linear_variant_workspace_bytes(int variant, ttt_dtype dt, int B, int H, int T, int d, int b) {
+  if (!sizes_ok(B, H, T, d, b) || !sizes_ok(B, H, T, kPadD, b)) return 0;
+  if (variant != ttt::kVarBias && variant != ttt::kVarTokenEta) return 0;
+  if (!variant_fast_ok(variant, dt, d, b)) return kStatusBytes;
+  return variant_layout(variant, B, H, T, d, b).total;
+}
+
+static ttt_status variant_ex(int variant, const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                             const float* tok_rate, const float* W0, const float* beta0, int B, int H, int T, int d,
+                             int b, void* Z, float* W_out, float* beta_out, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  ttt_status st = variant_check(variant, Q, K, V, dt, eta, nullptr, tok_rate, W0, beta0, nullptr, B, H, T, d, b, Z,
+                                W_out, beta_out);
+  if (st != TTT_OK) return st;
+  const size_t need = ttt_linear_variant_workspace_bytes(variant, dt, B, H, T, d, b);
+  if (need == 0) return TTT_ERR_ARG;
+  if (!workspace || !aligned16(workspace) || ws_bytes < need) return TTT_ERR_ARG;
+  {
+    const size_t seq = bytes4(B, H, T, d, dt == TTT_BF16 ? 2 : 4);
+    if (!outputs_disjoint({{Z, seq}, {W_out, bytes4(B, H, d, d, 4)},
+                           {beta_out, variant == ttt::kVarBias ? bytes4(B, H, d, 1, 4) : 0}, {workspace, ws_bytes}},
+                          {{Q, seq}, {K, seq}, {V, seq}, {eta, variant == ttt::kVarBias ? bytes4(H, 1, 1, 1, 4) : 0},
+                           {tok_rate, variant == ttt::kVarTokenEta ? bytes4(B, H, T, 1, 4) : 0},
+                           {W0, bytes4(H, d, d, 1, 4)}, {beta0, variant == ttt::kVarBias ? bytes4(H, d, 1, 1, 4) : 0}}))
+      return TTT_ERR_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = reset_status(workspace, s);
+  if (st != TTT_OK) return st;
+  if (!variant_fast_ok(variant, dt, d, b))
+    return variant_simt(variant, Q, K, V, dt, eta, nullptr, tok_rate, W0, beta0, nullptr, B, H, T, d, b, Z, W_out,
+                        beta_out, stream);
+
+  const VariantLayout L = variant_layout(variant, B, H, T, d, b);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  ttt::VariantPrepParams pp;
+  pp.Q = Q; pp.K = K; pp.V = V;
+  pp.tok_rate = variant == ttt::kVarTokenEta ? tok_rate : nullptr;
+  pp.Qp = L.qp ? ws + L.qp : nullptr;
+  pp.Kp = ws + L.kp;
+  pp.Vp = ws + L.vp;
+  pp.W0 = W0;
+  pp.beta0 = variant == ttt::kVarBias ? beta0 : nullptr;
+  pp.W0p = reinterpret_cast<float*>(ws + L.w0p);
+  pp.eta = variant == ttt::kVarBias ? eta : nullptr;
+  pp.etap = reinterpret_cast<float*>(ws + L.etap);
+  pp.units = B * H; pp.H = H; pp.T = T; pp.d = d;
+  pp.bias = variant == ttt::kVarBias;
+  pp.status = static_cast<ttt::StatusBlock*>(workspace);
+  if (ttt::launch_variant_prep(pp, s) != cudaSuccess) return TTT_ERR_CUDA;
+
+  void* Zin = L.zp ? static_cast<void*>(ws + L.zp) : Z;
+  float* Win = L.wp ? reinterpret_cast<float*>(ws + L.wp) : W_out;
+  st = ttt_linear_fwd_ex(pp.Qp ? pp.Qp : Q, pp.Kp, pp.Vp, TTT_BF16, pp.etap, pp.W0p, B, H, T, kPadD, b, Zin, Win,
+                         ws + L.sub, L.sub_bytes, stream, nullptr);
+  if (st != TTT_OK) return st;
+
+  ttt::VariantPostParams po;
+  po.Zp = L.zp ? ws + L.zp : nullptr;
+  po.Z = Z;
+  po.Wp = L.wp ? reinterpret_cast<const float*>(ws + L.wp) : nullptr;
+  po.W_out = W_out;
+  po.beta_out = variant == ttt::kVarBias ? beta_out : nullptr;
+  po.units = B * H; po.T = T; po.d = d;
+  po.status = static_cast<ttt::StatusBlock*>(workspace);
+  po.sub = reinterpret_cast<const ttt::StatusBlock*>(ws + L.sub);
+  return ttt::launch_variant_post(po, s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_linear_bias_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                                  const float* W0, const float* beta0, int B, int H, int T, int d, int b, void* Z,
+                                  float* W_out, float* beta_out, void* workspace, size_t ws_bytes, void* stream) {
+  return variant_ex(ttt::kVarBias, Q, K, V, dt, eta, nullptr, W0, beta0, B, H, T, d, b, Z, W_out, beta_out, workspace,
+                    ws_bytes, stream);
+}
+
+ttt_status ttt_linear_token_eta_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                       const float* eta_tok, const float* W0, int B, int H, int T, int d, int b,
+                                       void* Z, float* W_out, void* workspace, size_t ws_bytes, void* stream) {
+  return variant_ex(ttt::kVarTokenEta, Q, K, V, dt, nullptr, eta_tok, W0, nullptr, B, H, T, d, b, Z, W_out, nullptr,
+                    workspace, ws_bytes, stream);
 }
 
 ttt_status ttt_linear_bias_fwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,

@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 19
+    assert len(names) == 22
     assert set(names) == set(ttt.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -231,3 +231,52 @@ def test_decode_refuses_states_that_overlap():
     assert call(1 * MB, 2 * MB, 5 * MB, 5 * MB + 16 * 1024) == ttt.TTT_ERR_ARG  # W_run inside W_anchor (32 KB)
     assert call(1 * MB, 1 * MB + 128, 5 * MB, 6 * MB) == ttt.TTT_ERR_ARG       # z inside q (256 bytes)
     assert call(1 * MB, 2 * MB, 4 * MB, 6 * MB) == ttt.TTT_ERR_ARG             # W_anchor on eta
+
+
+def test_variant_workspace_bytes(lib):
+    """Status word, the inner forward's workspace, the changed inputs (padded to 64 features) and
+    W0'; Q', Z' and W_out' only where rows are padded. Shapes without the tensor-core path need the
+    status word alone; LN and momentum have no workspace call."""
+    bf, f32 = ttt.TTT_BF16, ttt.TTT_F32
+    seq = 6 * 40 * 64 * 2
+    padded = 256 + 256 + 4 * seq + 3 * 64 * 64 * 4 + 6 * 64 * 64 * 4 + 256
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_BIAS, bf, 2, 3, 40, 16, 16) == padded
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_TOKEN_ETA, bf, 2, 3, 40, 32, 16) == padded
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_TOKEN_ETA, bf, 2, 3, 40, 64, 16) == \
+        256 + 256 + 2 * seq + 3 * 64 * 64 * 4 + 256
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_BIAS, bf, 2, 3, 40, 64, 16) == 256   # no room for 1
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_BIAS, f32, 2, 3, 40, 16, 16) == 256
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_TOKEN_ETA, bf, 2, 3, 40, 64, 5) == 256
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_LN, bf, 2, 3, 40, 64, 16) == 0
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_MOMENTUM, bf, 2, 3, 40, 64, 16) == 0
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_BIAS, bf, 0, 3, 40, 16, 16) == 0
+    # the long-context shape: the inner forward's segment scratch is part of it
+    inner = ttt.ttt_workspace_bytes(1, 32, 131072, 64, 16)
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_TOKEN_ETA, bf, 1, 32, 131072, 64, 16) == \
+        256 + -(-inner // 256) * 256 + 2 * 32 * 131072 * 64 * 2 + 32 * 64 * 64 * 4 + 256
+
+
+def _var_ex(lib, name, **kw):
+    a = dict(Q=1 * MB, K=2 * MB, V=3 * MB, dt=1, eta=4 * MB, W0=5 * MB, beta0=6 * MB, B=2, H=3, T=40, d=16, b=16,
+             Z=8 * MB, W=9 * MB, beta=10 * MB, ws=16 * MB, wsb=1 << 24, s=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    if name == "bias":
+        return lib.ttt_linear_bias_fwd_ex(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W0"]),
+                                          vp(a["beta0"]), a["B"], a["H"], a["T"], a["d"], a["b"], vp(a["Z"]),
+                                          vp(a["W"]), vp(a["beta"]), vp(a["ws"]), a["wsb"], vp(a["s"]))
+    return lib.ttt_linear_token_eta_fwd_ex(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W0"]),
+                                           a["B"], a["H"], a["T"], a["d"], a["b"], vp(a["Z"]), vp(a["W"]), vp(a["ws"]),
+                                           a["wsb"], vp(a["s"]))
+
+
+@pytest.mark.parametrize("name", ["bias", "token_eta"])
+@pytest.mark.parametrize("kw,want", [(dict(ws=0), ttt.TTT_ERR_ARG), (dict(ws=16 * MB + 8), ttt.TTT_ERR_ARG),
+                                     (dict(wsb=4096), ttt.TTT_ERR_ARG), (dict(Q=0), ttt.TTT_ERR_ARG),
+                                     (dict(ws=2 * MB), ttt.TTT_ERR_ARG), (dict(Z=16 * MB + 4096), ttt.TTT_ERR_ARG),
+                                     (dict(d=65), ttt.TTT_ERR_UNSUPPORTED), (dict(dt=7), ttt.TTT_ERR_ARG),
+                                     (dict(b=0), ttt.TTT_ERR_ARG)])
+def test_variant_fast_calls_reject_bad_arguments(lib, name, kw, want):
+    """No workspace, a misaligned or too small one, a null input, the workspace over an input or an
+    output inside the workspace, d > 64, a bad dtype or chunk size: refused before anything runs."""
+    assert _var_ex(lib, name, **kw) == want

@@ -119,3 +119,73 @@ def test_variants_medium_bf16(variant):
         want, names = momentum_primal(inp.q64, inp.k64, inp.v64, alpha, beta, inp.W0_64, 16), "Z,W_out,M_out"
     torch.cuda.synchronize()
     check(names, got, want, w)
+
+
+FAST_BIAS = [(63, 50, 16, 2, 3), (16, 40, 16, 2, 3), (32, 130, 64, 2, 2), (1, 33, 16, 1, 2), (48, 2048, 16, 1, 2)]
+
+
+@pytest.mark.parametrize("d,T,b,B,H", FAST_BIAS)
+def test_bias_fast_path_matches_oracle(d, T, b, B, H):
+    """ttt_linear_bias_fwd_ex with bf16 operands: padded inputs through the tensor-core kernels
+    (T = 2048 takes the segment-parallel plan), against the oracle; the status word is clean."""
+    w, inp, t = inputs(d, T, "bf16", 760 + d + T + b, B=B, H=H)
+    beta0 = np.random.default_rng(d + T).standard_normal((w.H, d)).astype(np.float32) * 0.3
+    need = ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_BIAS, ttt.TTT_BF16, B, H, T, d, b)
+    assert need > 256
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    got = ttt.ttt_linear_bias_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(beta0).cuda(), b,
+                                  fast=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    want = bias_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, beta0, b)
+    check("Z,W_out,beta_out", got, want, w)
+
+
+FAST_TOK = [(64, 100, 16, 2, 3), (64, 2048, 16, 1, 2), (40, 70, 32, 2, 2), (64, 37, 64, 1, 3), (16, 48, 16, 1, 1)]
+
+
+@pytest.mark.parametrize("d,T,b,B,H", FAST_TOK)
+def test_token_eta_fast_path_matches_oracle(d, T, b, B, H):
+    """ttt_linear_token_eta_fwd_ex with bf16 operands: sqrt(eta_t)-scaled keys and values through
+    the tensor-core kernels (in place at d = 64, padded below), against the oracle."""
+    w, inp, t = inputs(d, T, "bf16", 770 + d + T + b, B=B, H=H)
+    et = np.random.default_rng(T + d).uniform(0.0, 0.5, (B, H, T)).astype(np.float32)
+    ws = torch.empty(ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_TOKEN_ETA, ttt.TTT_BF16, B, H, T, d, b),
+                     dtype=torch.uint8, device="cuda")
+    got = ttt.ttt_linear_token_eta_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(et).cuda(), t["W0"], b, fast=True,
+                                       workspace=ws)
+    torch.cuda.synchronize()
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    want = token_eta_primal(inp.q64, inp.k64, inp.v64, et, inp.W0_64, b)
+    check("Z,W_out", got, want, w)
+
+
+@pytest.mark.parametrize("d,T,b,dtype", [(16, 40, 16, "f32"), (64, 70, 5, "bf16")])
+def test_fast_calls_run_the_variant_kernel_where_padding_does_not_apply(d, T, b, dtype):
+    """fp32 operands or b % 16 != 0: the *_ex calls take the fp32 variant kernel (a 256-byte
+    workspace) and match the oracle at that dtype's bar."""
+    w, inp, t = inputs(d, T, dtype, 780 + d + T + b)
+    et = np.random.default_rng(T).uniform(0.0, 0.5, (w.B, w.H, T)).astype(np.float32)
+    code = ttt.TTT_BF16 if dtype == "bf16" else ttt.TTT_F32
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_TOKEN_ETA, code, w.B, w.H, T, d, b) == 256
+    got = ttt.ttt_linear_token_eta_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(et).cuda(), t["W0"], b, fast=True)
+    torch.cuda.synchronize()
+    check("Z,W_out", got, token_eta_primal(inp.q64, inp.k64, inp.v64, et, inp.W0_64, b), w)
+
+
+def test_fast_token_eta_reports_a_negative_rate():
+    """A negative per-token rate has no square root: the call finishes and the status word says
+    TTT_ERR_DEVICE_CHECK; the next call with valid rates is clean again."""
+    w, inp, t = inputs(64, 48, "bf16", 790, B=1, H=2)
+    et = np.full((1, 2, 48), 0.2, np.float32)
+    et[0, 1, 17] = -0.1
+    ws = torch.empty(ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_TOKEN_ETA, ttt.TTT_BF16, 1, 2, 48, 64, 16),
+                     dtype=torch.uint8, device="cuda")
+    ttt.ttt_linear_token_eta_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(et).cuda(), t["W0"], 16, fast=True,
+                                 workspace=ws)
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_ERR_DEVICE_CHECK
+    et[0, 1, 17] = 0.1
+    got = ttt.ttt_linear_token_eta_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(et).cuda(), t["W0"], 16, fast=True,
+                                       workspace=ws)
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    check("Z,W_out", got, token_eta_primal(inp.q64, inp.k64, inp.v64, et, inp.W0_64, 16), w)
