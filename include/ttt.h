@@ -367,6 +367,36 @@ TTT_API ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, t
                                   float* deta, float* dW0, void* workspace, size_t ws_bytes,
                                   void* stream);
 
+/*
+ * Backward of ttt_mlp_fwd: the vector-Jacobian product of (Z, W1_out, W2_out)
+ * with respect to (Q, K, V, eta, W1_0, W2_0), for training the outer loop
+ * ("5 · TestingTime 训练与长上下文", section 2.2). Per chunk with start weights
+ * P1 [d][m], P2 [m][d] (m = 4d) the forward is
+ *   U = K P1, A = s(U), G = A P2 - V, D = (G P2^T) .* s'(U),
+ *   Z = s(Q P1 - eta tril(Q K^T) D) P2 - eta tril(Aq A^T) G,
+ *   P1' = P1 - eta K^T D,  P2' = P2 - eta A^T G   (s: tanh-GELU),
+ * reversed chunk by chunk from dW1_out, dW2_out (s'' enters through D).
+ *   Q, K, V, dZ [B][H][T][d] of dtype dt; eta [H]; W1_0 [H][d][m]; W2_0
+ *   [H][m][d]; dW1_out [B][H][d][m]; dW2_out [B][H][m][d]. Outputs dQ, dK, dV
+ *   [B][H][T][d] of dtype dt; deta [H], dW1 [H][d][m], dW2 [H][m][d] float32,
+ *   summed over the batch rows (which share eta and the initial weights).
+ *   d <= 64, any b (a final partial chunk included). One fp32 CUDA kernel, one
+ *   CTA per (batch row, head), plus a reduction over the batch rows: a parity
+ *   form, whose workspace keeps every chunk-start (W1, W2) and one chunk's
+ *   matrices per unit.
+ *   workspace: ttt_mlp_bwd_workspace_bytes(B, H, T, d, b) bytes, 16-byte aligned.
+ *   Errors: TTT_ERR_ARG for null/misaligned pointers, bad sizes, a short
+ *   workspace or outputs that overlap an input or each other;
+ *   TTT_ERR_UNSUPPORTED for d > 64.
+ */
+TTT_API size_t ttt_mlp_bwd_workspace_bytes(int B, int H, int T, int d, int b);
+
+TTT_API ttt_status ttt_mlp_bwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                               const float* W1_0, const float* W2_0, int B, int H, int T, int d, int b,
+                               const void* dZ, const float* dW1_out, const float* dW2_out, void* dQ, void* dK,
+                               void* dV, float* deta, float* dW1, float* dW2, void* workspace,
+                               size_t ws_bytes, void* stream);
+
 /* Waits for `stream`, then reads and clears the status word of `workspace`.
  * Every call that takes a workspace (the *_fwd calls and ttt_linear_bwd)
  * clears that word when it is enqueued, so this reports the kernels of the

@@ -10,7 +10,7 @@ Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_plan, ttt_l
 ttt_linear_bias_fwd, ttt_linear_token_eta_fwd, ttt_linear_ln_fwd, ttt_linear_momentum_fwd,
 ttt_linear_variant_workspace_bytes (the bias and per-token-rate *_ex calls are reached through fast=True),
 ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_mlp_noalloc_last_device_status, ttt_linear_decode_step, ttt_linear_bwd_workspace_bytes,
-ttt_linear_bwd, ttt_last_device_status, ttt_status_str. The *_fwd_ex forms are reached
+ttt_linear_bwd, ttt_mlp_bwd_workspace_bytes, ttt_mlp_bwd, ttt_last_device_status, ttt_status_str. The *_fwd_ex forms are reached
 through the options argument.
 """
 from __future__ import annotations
@@ -32,7 +32,8 @@ EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_plan", "
            "ttt_mlp_fwd_noalloc", "ttt_mlp_noalloc_last_device_status", "ttt_linear_decode_step", "ttt_linear_bwd_workspace_bytes", "ttt_linear_bwd",
            "ttt_last_device_status", "ttt_status_str", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
            "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode",
-           "ttt_linear_variant_workspace_bytes", "ttt_linear_bias_fwd_ex", "ttt_linear_token_eta_fwd_ex")
+           "ttt_linear_variant_workspace_bytes", "ttt_linear_bias_fwd_ex", "ttt_linear_token_eta_fwd_ex",
+           "ttt_mlp_bwd_workspace_bytes", "ttt_mlp_bwd")
 
 
 class TTTError(RuntimeError):
@@ -89,6 +90,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_linear_token_eta_fwd.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp]
     lib.ttt_linear_ln_fwd.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, i, vp, vp, vp]
     lib.ttt_linear_momentum_fwd.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp]
+    lib.ttt_mlp_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.ttt_mlp_bwd_workspace_bytes.restype = sz
+    lib.ttt_mlp_bwd.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                vp]
     lib.ttt_linear_variant_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     lib.ttt_linear_variant_workspace_bytes.restype = sz
     lib.ttt_linear_bias_fwd_ex.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
@@ -98,7 +103,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex", "ttt_mlp_fwd_noalloc",
               "ttt_mlp_noalloc_last_device_status", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
               "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode", "ttt_linear_bias_fwd_ex",
-              "ttt_linear_token_eta_fwd_ex",
+              "ttt_linear_token_eta_fwd_ex", "ttt_mlp_bwd",
               "ttt_linear_decode_step", "ttt_linear_bwd", "ttt_last_device_status"):
         getattr(lib, f).restype = i
     _lib = lib
@@ -465,6 +470,42 @@ def ttt_linear_bwd(Q, K, V, eta, W0, b: int, dZ, dW_out, workspace=None, stream=
     if st != TTT_OK:
         raise TTTError("ttt_linear_bwd", st)
     return dQ, dK, dV, deta, dW0
+
+
+def ttt_mlp_bwd_workspace_bytes(B: int, H: int, T: int, d: int, b: int) -> int:
+    return int(load_library().ttt_mlp_bwd_workspace_bytes(B, H, T, d, b))
+
+
+def ttt_mlp_bwd(Q, K, V, eta, W1_0, W2_0, b: int, dZ, dW1_out, dW2_out, workspace=None, stream=None):
+    """Backward of ttt_mlp_fwd: returns (dQ, dK, dV, deta, dW1, dW2) for upstream gradients dZ
+    [B, H, T, d] (the dtype of Q), dW1_out [B, H, d, 4d] and dW2_out [B, H, 4d, d] float32.
+    Asynchronous on `stream`."""
+    import torch
+    lib = load_library()
+    B, H, T, d = Q.shape
+    m = 4 * d
+    dev = Q.device
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("dZ", dZ)):
+        _check(t, n, Q.dtype, (B, H, T, d), dev)
+    _check(eta, "eta", torch.float32, (H,), dev)
+    _check(W1_0, "W1_0", torch.float32, (H, d, m), dev)
+    _check(W2_0, "W2_0", torch.float32, (H, m, d), dev)
+    _check(dW1_out, "dW1_out", torch.float32, (B, H, d, m), dev)
+    _check(dW2_out, "dW2_out", torch.float32, (B, H, m, d), dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    deta = torch.empty((H,), dtype=torch.float32, device=dev)
+    dW1 = torch.empty((H, d, m), dtype=torch.float32, device=dev)
+    dW2 = torch.empty((H, m, d), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(ttt_mlp_bwd_workspace_bytes(B, H, T, d, b), 256), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", device=dev)
+    with _on_device(dev):
+        st = lib.ttt_mlp_bwd(_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W1_0), _p(W2_0), B, H, T, d, int(b),
+                             _p(dZ), _p(dW1_out), _p(dW2_out), _p(dQ), _p(dK), _p(dV), _p(deta), _p(dW1), _p(dW2),
+                             _p(workspace), _nbytes(workspace), _stream_ptr(stream, dev))
+    if st != TTT_OK:
+        raise TTTError("ttt_mlp_bwd", st)
+    return dQ, dK, dV, deta, dW1, dW2
 
 
 def ttt_last_device_status(workspace, stream=None) -> int:

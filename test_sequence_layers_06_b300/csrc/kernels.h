@@ -87,6 +87,40 @@ struct LinearBwdParams {
   uint64_t timeout_ns;
 };
 
+// Backward of TTT-MLP (mlp_bwd.cu), fp32 arithmetic, d <= 64, hidden m = 4d, any b.
+struct MlpBwdParams {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* dZ;
+  const float* eta;
+  const float* W1_0;     // [H][d][m]
+  const float* W2_0;     // [H][m][d]
+  const float* dW1_out;  // [B][H][d][m]
+  const float* dW2_out;  // [B][H][m][d]
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* deta;           // [H]
+  float* dW1;            // [H][d][m]
+  float* dW2;            // [H][m][d]
+  int B, H, T, d, m, b;
+  int units;
+  bool bf16;             // Q, K, V, dZ, dQ, dK, dV are bf16 (else fp32)
+  float* scratch;        // workspace [units][mlp_bwd_unit_floats]
+  float* partial;        // workspace [units][2 d m + 1]
+};
+// Floats of one unit's scratch: chunk-start weights, the gradient accumulators and
+// one chunk's matrices.
+__host__ __device__ inline size_t mlp_bwd_unit_floats(int T, int d, int b) {
+  const size_t m = static_cast<size_t>(4) * d, dm = static_cast<size_t>(d) * m;
+  const size_t nch = (static_cast<size_t>(T) + b - 1) / b;
+  const size_t cap = static_cast<size_t>(T < b ? T : b);
+  return nch * 2 * dm + 4 * dm + 8 * cap * d + 11 * cap * m + 3 * cap * cap;
+}
+size_t mlp_bwd_scratch_bytes(int units, int T, int d, int b);  // scratch + partials
+cudaError_t launch_mlp_bwd(const MlpBwdParams& p, cudaStream_t stream);  // both kernels
+
 // Inner-model variants of TTT-Linear (linear_variants.cu), fp32 arithmetic.
 enum : int { kVarBias = TTT_INNER_BIAS, kVarTokenEta = TTT_INNER_TOKEN_ETA, kVarLn = TTT_INNER_LN,
               kVarMomentum = TTT_INNER_MOMENTUM };

@@ -834,6 +834,54 @@ ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype
   return err == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
+size_t ttt_mlp_bwd_workspace_bytes(int B, int H, int T, int d, int b) {
+  if (!sizes_ok(B, H, T, d, b)) return 0;
+  return kStatusBytes + round_up(ttt::mlp_bwd_scratch_bytes(B * H, T, d, b), 16);
+}
+
+ttt_status ttt_mlp_bwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                       const float* W1_0, const float* W2_0, int B, int H, int T, int d, int b, const void* dZ,
+                       const float* dW1_out, const float* dW2_out, void* dQ, void* dK, void* dV, float* deta,
+                       float* dW1, float* dW2, void* workspace, size_t ws_bytes, void* stream) {
+  if (dt != TTT_F32 && dt != TTT_BF16) return TTT_ERR_ARG;
+  if (!sizes_ok(B, H, T, d, b)) return TTT_ERR_ARG;
+  if (d > kMaxD) return TTT_ERR_UNSUPPORTED;
+  if (!eta || !W1_0 || !W2_0 || !dW1_out || !dW2_out || !deta || !dW1 || !dW2 || !workspace) return TTT_ERR_ARG;
+  if (T > 0 && (!Q || !K || !V || !dZ || !dQ || !dK || !dV)) return TTT_ERR_ARG;
+  for (const void* p : {Q, K, V, dZ, static_cast<const void*>(dQ), static_cast<const void*>(dK),
+                        static_cast<const void*>(dV), static_cast<const void*>(eta), static_cast<const void*>(W1_0),
+                        static_cast<const void*>(W2_0), static_cast<const void*>(dW1_out),
+                        static_cast<const void*>(dW2_out), static_cast<const void*>(deta),
+                        static_cast<const void*>(dW1), static_cast<const void*>(dW2),
+                        static_cast<const void*>(workspace)})
+    if (p && !aligned16(p)) return TTT_ERR_ARG;
+  if (ws_bytes < ttt_mlp_bwd_workspace_bytes(B, H, T, d, b)) return TTT_ERR_ARG;
+  const int m = static_cast<int>(mlp_hidden(d));
+  {
+    const size_t seq = bytes4(B, H, T, d, dt == TTT_BF16 ? 2 : 4), hw = bytes4(H, d, m, 1, 4);
+    const size_t bw = bytes4(B, H, d, m, 4);
+    if (!outputs_disjoint({{dQ, seq}, {dK, seq}, {dV, seq}, {deta, bytes4(H, 1, 1, 1, 4)}, {dW1, hw}, {dW2, hw},
+                           {workspace, ws_bytes}},
+                          {{Q, seq}, {K, seq}, {V, seq}, {dZ, seq}, {eta, bytes4(H, 1, 1, 1, 4)}, {W1_0, hw},
+                           {W2_0, hw}, {dW1_out, bw}, {dW2_out, bw}}))
+      return TTT_ERR_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ttt::MlpBwdParams p;
+  p.Q = Q; p.K = K; p.V = V; p.dZ = dZ;
+  p.eta = eta; p.W1_0 = W1_0; p.W2_0 = W2_0; p.dW1_out = dW1_out; p.dW2_out = dW2_out;
+  p.dQ = dQ; p.dK = dK; p.dV = dV;
+  p.deta = deta; p.dW1 = dW1; p.dW2 = dW2;
+  p.B = B; p.H = H; p.T = T; p.d = d; p.m = m; p.b = b;
+  p.units = B * H;
+  p.bf16 = dt == TTT_BF16;
+  p.scratch = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+  p.partial = p.scratch + static_cast<size_t>(p.units) * ttt::mlp_bwd_unit_floats(T, d, b);
+  const ttt_status st = reset_status(workspace, s);
+  if (st != TTT_OK) return st;
+  return ttt::launch_mlp_bwd(p, s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
 ttt_status ttt_last_device_status(void* workspace, void* stream) {
   if (!workspace || !aligned16(workspace)) return TTT_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 22
+    assert len(names) == 24
     assert set(names) == set(ttt.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -280,3 +280,42 @@ def test_variant_fast_calls_reject_bad_arguments(lib, name, kw, want):
     """No workspace, a misaligned or too small one, a null input, the workspace over an input or an
     output inside the workspace, d > 64, a bad dtype or chunk size: refused before anything runs."""
     assert _var_ex(lib, name, **kw) == want
+
+
+def test_mlp_backward_workspace_bytes(lib):
+    """A status block, then per unit: every chunk-start (W1, W2), four d x 4d gradient buffers,
+    one chunk's matrices (8 of b x d, 11 of b x 4d, 3 of b x b, b capped at T); then per-unit
+    partials of dW1, dW2, d eta."""
+    d, m, T, b, units = 16, 64, 40, 16, 6
+    per = 3 * 2 * d * m + 4 * d * m + 8 * b * d + 11 * b * m + 3 * b * b
+    raw = 4 * (units * per + units * (2 * d * m + 1))
+    assert ttt.ttt_mlp_bwd_workspace_bytes(2, 3, T, d, b) == 256 + -(-raw // 16) * 16
+    per = 1 * 2 * d * m + 4 * d * m + 8 * 10 * d + 11 * 10 * m + 3 * 100
+    raw = 4 * (units * per + units * (2 * d * m + 1))
+    assert ttt.ttt_mlp_bwd_workspace_bytes(2, 3, 10, d, 64) == 256 + -(-raw // 16) * 16
+    assert ttt.ttt_mlp_bwd_workspace_bytes(0, 3, 10, d, 64) == 0
+
+
+def _mlp_bwd(lib, **kw):
+    a = dict(Q=1 * MB, K=2 * MB, V=3 * MB, dt=0, eta=4 * MB, W1=5 * MB, W2=6 * MB, B=2, H=3, T=40, d=16, b=8,
+             dZ=7 * MB, dW1o=8 * MB, dW2o=9 * MB, dQ=10 * MB, dK=11 * MB, dV=12 * MB, deta=13 * MB, dW1=14 * MB,
+             dW2=15 * MB, ws=32 * MB, wsb=1 << 24, s=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.ttt_mlp_bwd(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W1"]), vp(a["W2"]),
+                           a["B"], a["H"], a["T"], a["d"], a["b"], vp(a["dZ"]), vp(a["dW1o"]), vp(a["dW2o"]),
+                           vp(a["dQ"]), vp(a["dK"]), vp(a["dV"]), vp(a["deta"]), vp(a["dW1"]), vp(a["dW2"]),
+                           vp(a["ws"]), a["wsb"], vp(a["s"]))
+
+
+@pytest.mark.parametrize("kw,want", [(dict(Q=0), ttt.TTT_ERR_ARG), (dict(dW2o=0), ttt.TTT_ERR_ARG),
+                                     (dict(ws=0), ttt.TTT_ERR_ARG), (dict(wsb=4096), ttt.TTT_ERR_ARG),
+                                     (dict(b=0), ttt.TTT_ERR_ARG), (dict(dt=3), ttt.TTT_ERR_ARG),
+                                     (dict(d=65), ttt.TTT_ERR_UNSUPPORTED), (dict(dQ=1 * MB), ttt.TTT_ERR_ARG),
+                                     (dict(dW1=5 * MB), ttt.TTT_ERR_ARG), (dict(ws=9 * MB), ttt.TTT_ERR_ARG),
+                                     (dict(dW2=14 * MB + 1024), ttt.TTT_ERR_ARG), (dict(dK=2 * MB + 8), ttt.TTT_ERR_ARG)])
+def test_mlp_backward_rejects_bad_arguments(lib, kw, want):
+    """Null pointers, no or a short workspace, bad sizes or dtype, d > 64, an output on an input
+    (dQ on Q, dW1 on W1_0, the workspace over dW2_out), outputs that overlap (dW2 inside dW1), a
+    misaligned output: refused before anything runs."""
+    assert _mlp_bwd(lib, **kw) == want

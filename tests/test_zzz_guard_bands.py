@@ -141,6 +141,49 @@ def test_backward_writes_inside_its_outputs():
         assert rel_l2(to64(got), r) <= 1e-4
 
 
+def test_long_chunk_backward_and_mlp_backward_write_inside_their_outputs():
+    """The backward for chunks longer than 64 tokens (b = 100) and the TTT-MLP backward, each with
+    every output and its workspace inside guard bands."""
+    vp = lambda x: ctypes.c_void_p(x.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    lib = ttt.load_library()
+    g = np.random.default_rng(6)
+    # TTT-Linear, b = 100 over T = 230 (two full chunks and a ragged one)
+    w = synth.WORKLOADS["linear_tiny_f32"].with_(B=2, H=2, T=230, d=16, b=100, eta=("const", 0.05), w_std=0.02)
+    t = torch_inputs(synth.make_inputs(w))
+    dZ = torch.from_numpy(g.standard_normal((w.B, w.H, w.T, w.d)).astype(np.float32)).cuda()
+    dWo = torch.from_numpy(g.standard_normal((w.B, w.H, w.d, w.d)).astype(np.float32)).cuda()
+    outs = [Guarded((w.B, w.H, w.T, w.d), torch.float32, -3.0) for _ in range(3)]
+    deta, dW0 = Guarded((w.H,), torch.float32, -5.0), Guarded((w.H, w.d, w.d), torch.float32, -7.0)
+    need = ttt.ttt_linear_bwd_workspace_bytes(w.B, w.H, w.T, w.d, w.b)
+    ws = guarded_workspace(need)
+    st = lib.ttt_linear_bwd(vp(t["Q"]), vp(t["K"]), vp(t["V"]), ttt.TTT_F32, vp(t["eta"]), vp(t["W0"]), w.B, w.H,
+                            w.T, w.d, w.b, vp(dZ), vp(dWo), vp(outs[0].t), vp(outs[1].t), vp(outs[2].t), vp(deta.t),
+                            vp(dW0.t), vp(ws.t), need, stream)
+    assert st == ttt.TTT_OK
+    torch.cuda.synchronize()
+    assert all(o.margins_intact() for o in outs) and deta.margins_intact() and dW0.margins_intact()
+    assert ws.margins_intact()
+    # TTT-MLP, d = 16 (hidden 64), b = 5 over T = 23
+    w = synth.WORKLOADS["mlp_125m"].with_(B=2, H=2, T=23, d=16, b=5, hidden=64, dtype="f32", w_std=0.3)
+    t = torch_inputs(synth.make_inputs(w))
+    dZ = torch.from_numpy(g.standard_normal((w.B, w.H, w.T, w.d)).astype(np.float32)).cuda()
+    dW1o = torch.from_numpy(g.standard_normal((w.B, w.H, w.d, 64)).astype(np.float32)).cuda()
+    dW2o = torch.from_numpy(g.standard_normal((w.B, w.H, 64, w.d)).astype(np.float32)).cuda()
+    outs = [Guarded((w.B, w.H, w.T, w.d), torch.float32, -3.0) for _ in range(3)]
+    deta = Guarded((w.H,), torch.float32, -5.0)
+    dW1, dW2 = Guarded((w.H, w.d, 64), torch.float32, -7.0), Guarded((w.H, 64, w.d), torch.float32, -9.0)
+    need = ttt.ttt_mlp_bwd_workspace_bytes(w.B, w.H, w.T, w.d, w.b)
+    ws = guarded_workspace(need)
+    st = lib.ttt_mlp_bwd(vp(t["Q"]), vp(t["K"]), vp(t["V"]), ttt.TTT_F32, vp(t["eta"]), vp(t["W1"]), vp(t["W2"]),
+                         w.B, w.H, w.T, w.d, w.b, vp(dZ), vp(dW1o), vp(dW2o), vp(outs[0].t), vp(outs[1].t),
+                         vp(outs[2].t), vp(deta.t), vp(dW1.t), vp(dW2.t), vp(ws.t), need, stream)
+    assert st == ttt.TTT_OK
+    torch.cuda.synchronize()
+    assert all(o.margins_intact() for o in outs) and deta.margins_intact()
+    assert dW1.margins_intact() and dW2.margins_intact() and ws.margins_intact()
+
+
 @pytest.mark.parametrize("opts", [{"force_path": ttt.PATH_SEGMENTED, "seg_len": 256},
                                   {"force_path": ttt.PATH_TENSOR}, {"force_path": ttt.PATH_SIMT}])
 def test_nan_stays_in_its_unit(opts):
