@@ -688,6 +688,23 @@ def bench_extras(ttt, dev, stream):
         del Q, K, V, dZ
     except Exception as exc:  # reported in the line, never silently dropped
         out["linear_bwd_small_f32_b16"] = {"error": f"{type(exc).__name__}: {exc}"}
+    # backward of TTT-MLP (fp32 parity kernel), B2 H4 T512 d64 hidden 256
+    try:
+        w = synth.WORKLOADS["mlp_125m"].with_(B=2, H=4, T=512, dtype="f32")
+        inp = synth.make_inputs(w, want_exact=False)
+        Q, K, V = (torch.from_numpy(a).to(dev) for a in (inp.q, inp.k, inp.v))
+        eta, W1, W2 = (torch.from_numpy(a).to(dev) for a in (inp.eta, inp.W1, inp.W2))
+        dZ = torch.randn_like(Q)
+        dW1 = torch.randn(w.B, w.H, w.d, 4 * w.d, device=dev)
+        dW2 = torch.randn(w.B, w.H, 4 * w.d, w.d, device=dev)
+        ws = torch.empty(ttt.ttt_mlp_bwd_workspace_bytes(w.B, w.H, w.T, w.d, 16), dtype=torch.uint8, device=dev)
+        ms = t_ms(lambda: ttt.ttt_mlp_bwd(Q, K, V, eta, W1, W2, 16, dZ, dW1, dW2, workspace=ws, stream=stream), 2)
+        out["mlp_bwd_small_f32_b16"] = {"ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                                        "note": "B2 H4 T512 d64 hidden 256 fp32; dQ, dK, dV, d eta, dW1, dW2; "
+                                                "fp32 parity kernel, one CTA per (batch row, head)"}
+        del Q, K, V, dZ
+    except Exception as exc:  # reported in the line, never silently dropped
+        out["mlp_bwd_small_f32_b16"] = {"error": f"{type(exc).__name__}: {exc}"}
     # decode: one token for B1 H32 from a state
     try:
         q = torch.randn(1, 32, 64, device=dev).to(torch.bfloat16)

@@ -16,7 +16,8 @@
 // variant_prep_kernel writes the changed inputs (bf16, 64 features per row) and
 // W0' (fp32); variant_post_kernel copies Z, W_out and beta_out back out of the
 // padded results and merges the status words. Both are elementwise passes with
-// one warp per token row.
+// one warp per token row (16-byte accesses, 8 features per thread, where the rows
+// are already 64 wide: the per-token rate at d = 64).
 #include <algorithm>
 
 #include "ttt_device.cuh"
@@ -57,6 +58,36 @@ __global__ void __launch_bounds__(kPrepThreads) variant_prep_kernel(VariantPrepP
   }
   const int lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(p.units) * p.T;
+  if (d == kP && !p.bias && p.Qp == nullptr) {
+    // Rows of 64 features, 16-byte aligned: a thread scales 8 features of K and of V.
+    const long long items = rows * (kP / 8);
+    const long long stride = static_cast<long long>(gridDim.x - p.H) * kPrepThreads;
+    for (long long x = static_cast<long long>(blockIdx.x - p.H) * kPrepThreads + threadIdx.x; x < items; x += stride) {
+      const long long r = x / (kP / 8);
+      float s = 1.f;
+      if (p.tok_rate) {
+        const float et = p.tok_rate[r];
+        if (et < 0.f) {
+          if ((x % (kP / 8)) == 0) report_error(p.status, TTT_ERR_DEVICE_CHECK, kWhereNegativeRate, static_cast<int>(r / p.T));
+          s = 0.f;
+        } else {
+          s = sqrtf(et);
+        }
+      }
+      const uint4 kv = reinterpret_cast<const uint4*>(p.K)[x];
+      const uint4 vv = reinterpret_cast<const uint4*>(p.V)[x];
+      const uint32_t ki[4] = {kv.x, kv.y, kv.z, kv.w}, vi[4] = {vv.x, vv.y, vv.z, vv.w};
+      uint32_t ko[4], vo[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        ko[q] = pack_bf16(s * bf16_lo(ki[q]), s * bf16_hi(ki[q]));
+        vo[q] = pack_bf16(s * bf16_lo(vi[q]), s * bf16_hi(vi[q]));
+      }
+      reinterpret_cast<uint4*>(p.Kp)[x] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+      reinterpret_cast<uint4*>(p.Vp)[x] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+    }
+    return;
+  }
   const long long warps = static_cast<long long>(gridDim.x - p.H) * (kPrepThreads / 32);
   for (long long r = static_cast<long long>(blockIdx.x - p.H) * (kPrepThreads / 32) + (threadIdx.x >> 5); r < rows;
        r += warps) {
@@ -117,7 +148,7 @@ __global__ void __launch_bounds__(kPrepThreads) variant_post_kernel(VariantPostP
 
 int row_blocks(long long rows) {
   const long long want = (rows + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
-  return static_cast<int>(std::min<long long>(want, 148LL * 16));
+  return static_cast<int>(std::min<long long>(want, 148LL * 32));
 }
 
 }  // namespace
