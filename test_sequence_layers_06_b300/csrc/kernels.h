@@ -83,6 +83,13 @@ struct LinearBwdParams {
                    // the state at the start of every 64-token block)
   float* partial;  // workspace [units][d*d + 1]: per-unit dW0, then d eta
   float* chunk_buf;  // workspace [units][2][min(b, T)][d]: E, dE of one chunk (chunks longer than 64)
+  // Segments (tensor-core kernel): a unit's sequence in bseg_count ranges of bseg_len tokens (a
+  // multiple of 64), one CTA each; partial is then [units][bseg_count][d*d + 1].
+  int bseg_len;
+  int bseg_count;
+  const float* w_starts;  // [units][S-1][d][d]: W at the start of segments 1..S-1
+  float* hA;              // [units][S-1][2][d][d]: H_s, then A_s, of segments 1..S-1
+  float* g_ends;          // [units][S-1][d][d]: gradient of the end state of segments 0..S-2
   StatusBlock* status;
   uint64_t timeout_ns;
 };
@@ -248,6 +255,12 @@ size_t linear_bwd_scratch_bytes(int units, int T, int d, int b);  // states + pa
 float* linear_bwd_chunk_buf(float* partial, int units, int d);       // where chunk_buf starts
 cudaError_t launch_linear_bwd(const LinearBwdParams& p, cudaStream_t stream);
 cudaError_t launch_linear_bwd_reduce(const LinearBwdParams& p, cudaStream_t stream);
+// Segment-parallel backward (linear_bwd_seg.cu): H_s and A_s of segments 1..S-1, and the
+// gradients at the segments' ends.
+int linear_bwd_hmap_rows();
+cudaError_t launch_linear_bwd_hmap(const LinearBwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                   const CUtensorMap& mdz, cudaStream_t stream);
+cudaError_t launch_linear_bwd_rcombine(const LinearBwdParams& p, cudaStream_t stream);
 
 // Backward of TTT-Linear on the tensor cores (linear_bwd_mma.cu): bf16, d = 64, b = 16.
 // Tensor maps over Q, K, V, dZ with linear_bwd_mma_rows()-row boxes.

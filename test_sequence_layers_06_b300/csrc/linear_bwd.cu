@@ -420,13 +420,16 @@ __global__ void __launch_bounds__(kBwdThreads) linear_bwd_wide_kernel(LinearBwdP
   if (tid == 0) part[d * d] = red[0];
 }
 
-// dW0[h] and d eta[h]: sums over the batch rows of the per-unit partials.
+// dW0[h] and d eta[h]: sums over the batch rows (and segments) of the per-unit partials.
 __global__ void __launch_bounds__(kBwdThreads) linear_bwd_reduce_kernel(LinearBwdParams p) {
   const int h = blockIdx.x;
   const int d = p.d;
+  const int S = p.bseg_count > 1 ? p.bseg_count : 1;
   for (int i = threadIdx.x; i <= d * d; i += kBwdThreads) {
     float acc = 0.f;
-    for (int n = 0; n < p.B; ++n) acc += p.partial[static_cast<size_t>(n * p.H + h) * (d * d + 1) + i];
+    for (int n = 0; n < p.B; ++n)
+      for (int s = 0; s < S; ++s)
+        acc += p.partial[(static_cast<size_t>(n * p.H + h) * S + s) * (d * d + 1) + i];
     if (i < d * d)
       p.dW0[static_cast<size_t>(h) * d * d + i] = acc;
     else

@@ -106,13 +106,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc);
   const uint32_t s0 = smem_u32(sm);
 
-  const int unit = blockIdx.x;
+  // One CTA per (unit, segment): blocks [blk0, blk1) of 64 tokens (all of them without segments).
+  const int S = p.bseg_count;
+  const int unit = blockIdx.x / S;
+  const int seg = blockIdx.x % S;
   const int h = unit % p.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tg = lane & 3, mi = lane >> 3, mr = lane & 7;
   const int T = p.T;
   const int ntiles = (T + kTile - 1) / kTile;
-  const int nblk = (T + kBlk - 1) / kBlk;
+  const int nblk_all = (T + kBlk - 1) / kBlk;
+  const int blk0 = seg * (p.bseg_len / kBlk);
+  const int blk1 = min(nblk_all, blk0 + p.bseg_len / kBlk);
+  const int nblk = blk1 - blk0;  // this CTA's blocks
   const float eta = p.eta[h];
 
   if (threadIdx.x == 0) {
@@ -138,19 +144,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&mv);
       prefetch_tmap(&mq);
       prefetch_tmap(&mdz);
-      for (int bk = 0; bk < nblk && ok; ++bk) {
-        const int s = bk & 1;
-        if (bk >= 2) ok = mbar_wait_or_abort(&empty1[s], ((bk >> 1) - 1) & 1, p.timeout_ns, abort_flag);
+      for (int lb = 0; lb < nblk && ok; ++lb) {
+        const int s = lb & 1, bk = blk0 + lb;
+        if (lb >= 2) ok = mbar_wait_or_abort(&empty1[s], ((lb >> 1) - 1) & 1, p.timeout_ns, abort_flag);
         if (!ok) break;
         mbar_arrive_expect_tx(&full1[s], 2 * kBlkBytes);
         tma_load_3d(sm + kP1 + s * 2 * kBlkBytes, &mk, &full1[s], 0, bk * kBlk, unit);
         tma_load_3d(sm + kP1 + s * 2 * kBlkBytes + kBlkBytes, &mv, &full1[s], 0, bk * kBlk, unit);
-        issued1 = bk + 1;
+        issued1 = lb + 1;
       }
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     for (int r = 0; r < nblk && ok; ++r) {
-      const int bk = nblk - 1 - r, s = r & 1;
+      const int bk = blk1 - 1 - r, s = r & 1;
       if (lane == 0) {
         if (r >= 2) ok = mbar_wait_or_abort(&empty2[s], ((r >> 1) - 1) & 1, p.timeout_ns, abort_flag);
         if (ok) {
@@ -228,17 +234,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
   float Wt[8][4];  // W^T rows j = jw + g (+8), columns i = 8q + 2tg (+1)
   {
-    const float* W0 = p.W0 + static_cast<size_t>(h) * kD * kD;
+    const float* W0 = seg == 0 ? p.W0 + static_cast<size_t>(h) * kD * kD
+                               : p.w_starts + (static_cast<size_t>(unit) * (S - 1) + seg - 1) * kD * kD;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int i = 8 * q + 2 * tg;
-      Wt[q][0] = W0[i * kD + jw + g];
-      Wt[q][1] = W0[(i + 1) * kD + jw + g];
-      Wt[q][2] = W0[i * kD + jw + g + 8];
-      Wt[q][3] = W0[(i + 1) * kD + jw + g + 8];
+      Wt[q][0] = __ldcg(W0 + i * kD + jw + g);
+      Wt[q][1] = __ldcg(W0 + (i + 1) * kD + jw + g);
+      Wt[q][2] = __ldcg(W0 + i * kD + jw + g + 8);
+      Wt[q][3] = __ldcg(W0 + (i + 1) * kD + jw + g + 8);
     }
   }
-  float* ckpt = p.states + static_cast<size_t>(unit) * nblk * kD * kD;
+  float* ckpt = p.states + static_cast<size_t>(unit) * nblk_all * kD * kD;  // by absolute block
   auto save_w = [&](float* dst) {
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -306,9 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // ---------------------------------------------------------------- pass 1: checkpoints
-  for (int bk = 0; bk < nblk; ++bk) {
-    const int s = bk & 1;
-    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&full1[s], (bk >> 1) & 1, p.timeout_ns, abort_flag))) {
+  for (int lb = 0; lb < nblk; ++lb) {
+    const int s = lb & 1, bk = blk0 + lb;
+    if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&full1[s], (lb >> 1) & 1, p.timeout_ns, abort_flag))) {
       if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdPass1, unit);
       *abort_flag = 1;
       ok = false;
@@ -330,14 +337,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- pass 2: the backward
   float Gt[8][4];  // G^T rows j = jw + g (+8), columns i = 8q + 2tg (+1)
   {
-    const float* G0 = p.dW_out + static_cast<size_t>(unit) * kD * kD;
+    const float* G0 = seg == S - 1 ? p.dW_out + static_cast<size_t>(unit) * kD * kD
+                                   : p.g_ends + (static_cast<size_t>(unit) * (S - 1) + seg) * kD * kD;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int i = 8 * q + 2 * tg;
-      Gt[q][0] = G0[i * kD + jw + g];
-      Gt[q][1] = G0[(i + 1) * kD + jw + g];
-      Gt[q][2] = G0[i * kD + jw + g + 8];
-      Gt[q][3] = G0[(i + 1) * kD + jw + g + 8];
+      Gt[q][0] = __ldcg(G0 + i * kD + jw + g);
+      Gt[q][1] = __ldcg(G0 + (i + 1) * kD + jw + g);
+      Gt[q][2] = __ldcg(G0 + i * kD + jw + g + 8);
+      Gt[q][3] = __ldcg(G0 + (i + 1) * kD + jw + g + 8);
     }
   }
   float deta = 0.f;
@@ -356,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int ktile = 0;  // chunks done in pass 2 (which G and dE copy)
 
   for (int r = 0; ok && r < nblk; ++r) {
-    const int bk = nblk - 1 - r, s = r & 1;
+    const int bk = blk1 - 1 - r, s = r & 1;
     if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&ready2[s], (r >> 1) & 1, p.timeout_ns, abort_flag))) {
       if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdPass2, unit);
       *abort_flag = 1;
@@ -551,15 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ok && !*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereBwdSync, unit);
   if (!ok) *abort_flag = 1;
 
-  // dW0 share of this unit (G after the first chunk) and d eta.
-  float* part = p.partial + static_cast<size_t>(unit) * (kD * kD + 1);
+  // dW0 share of this unit (G after the first chunk: the first segment's CTA only) and d eta.
+  float* part = p.partial + (static_cast<size_t>(unit) * S + seg) * (kD * kD + 1);
+  const float keep = seg == 0 ? 1.f : 0.f;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int i = 8 * q + 2 * tg;
-    part[i * kD + jw + g] = Gt[q][0];
-    part[(i + 1) * kD + jw + g] = Gt[q][1];
-    part[i * kD + jw + g + 8] = Gt[q][2];
-    part[(i + 1) * kD + jw + g + 8] = Gt[q][3];
+    part[i * kD + jw + g] = keep * Gt[q][0];
+    part[(i + 1) * kD + jw + g] = keep * Gt[q][1];
+    part[i * kD + jw + g + 8] = keep * Gt[q][2];
+    part[(i + 1) * kD + jw + g + 8] = keep * Gt[q][3];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) deta += __shfl_xor_sync(0xffffffffu, deta, o);
@@ -580,7 +589,7 @@ cudaError_t launch_linear_bwd_mma(const LinearBwdParams& p, const CUtensorMap& m
   if (p.units == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(linear_bwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  linear_bwd_mma_kernel<<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdz, p);
+  linear_bwd_mma_kernel<<<p.units * p.bseg_count, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdz, p);
   return cudaGetLastError();
 }
 

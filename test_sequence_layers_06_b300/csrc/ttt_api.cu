@@ -767,9 +767,37 @@ ttt_status ttt_linear_momentum_fwd(const void* Q, const void* K, const void* V, 
                      W_out, M_out, stream);
 }
 
+// Segments of the tensor-core backward (bf16, d = 64, b = 16): as many as fill the SMs with one
+// CTA per (unit, segment), each a whole number of 64-token blocks.
+struct BwdPlan {
+  int seg_len, seg_count;
+};
+
+BwdPlan plan_linear_bwd(int B, int H, int T, int d, int b, bool mma) {
+  BwdPlan pl{static_cast<int>(round_up(static_cast<size_t>(T > 0 ? T : 1), 64)), 1};
+  if (!mma || T <= 64 || d != 64 || b != 16) return pl;
+  const long long units = static_cast<long long>(B) * H;
+  const long long want = std::min<long long>((T + 63) / 64, std::max<long long>(1, sm_count() / units));
+  if (want < 2) return pl;
+  const long long len = round_up(static_cast<size_t>((T + want - 1) / want), 64);
+  pl.seg_len = static_cast<int>(len);
+  pl.seg_count = static_cast<int>((T + len - 1) / len);
+  return pl;
+}
+
+// Bytes after the backward's states and partials: per-segment partials, the forward's segment
+// maps and start states, H_s and A_s, the segments' end gradients (fp32).
+size_t bwd_seg_bytes(const BwdPlan& pl, int units) {
+  if (pl.seg_count < 2) return 0;
+  const size_t dd = 64 * 64, u = static_cast<size_t>(units), S = pl.seg_count;
+  return round_up(u * S * (dd + 1) * 4, 256) + u * (S - 1) * dd * 4 * (2 + 1 + 2 + 1);
+}
+
 size_t ttt_linear_bwd_workspace_bytes(int B, int H, int T, int d, int b) {
   if (!sizes_ok(B, H, T, d, b)) return 0;
-  return kStatusBytes + round_up(ttt::linear_bwd_scratch_bytes(B * H, T, d, b), 16);
+  // Sized for bf16 operands, the only dtype whose backward may use segments.
+  const BwdPlan pl = plan_linear_bwd(B, H, T, d, b, ttt::linear_bwd_mma_supported(d, b, true) && T > 0);
+  return kStatusBytes + round_up(ttt::linear_bwd_scratch_bytes(B * H, T, d, b), 16) + bwd_seg_bytes(pl, B * H);
 }
 
 ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
@@ -814,6 +842,25 @@ ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype
   p.partial = p.states + static_cast<size_t>(p.units) * nch * d * d;
   p.chunk_buf = ttt::linear_bwd_chunk_buf(p.partial, p.units, d);
   p.status = static_cast<ttt::StatusBlock*>(workspace);
+  const BwdPlan bpl = plan_linear_bwd(B, H, T, d, b, mma);
+  p.bseg_len = bpl.seg_len;
+  p.bseg_count = bpl.seg_count;
+  p.w_starts = nullptr;
+  p.hA = nullptr;
+  p.g_ends = nullptr;
+  float* seg_maps = nullptr;
+  float* seg_starts = nullptr;
+  if (bpl.seg_count > 1) {
+    const size_t dd = static_cast<size_t>(d) * d, S = bpl.seg_count, u = p.units;
+    uint8_t* seg = static_cast<uint8_t*>(workspace) + kStatusBytes +
+                   round_up(ttt::linear_bwd_scratch_bytes(B * H, T, d, b), 16);
+    p.partial = reinterpret_cast<float*>(seg);
+    seg_maps = reinterpret_cast<float*>(seg + round_up(u * S * (dd + 1) * 4, 256));
+    seg_starts = seg_maps + u * (S - 1) * 2 * dd;
+    p.hA = seg_starts + u * (S - 1) * dd;
+    p.g_ends = p.hA + u * (S - 1) * 2 * dd;
+    p.w_starts = seg_starts;
+  }
   p.timeout_ns = kDefaultTimeoutNs;
   const ttt_status st = reset_status(workspace, s);
   if (st != TTT_OK) return st;
@@ -826,7 +873,40 @@ ttt_status ttt_linear_bwd(const void* Q, const void* K, const void* V, ttt_dtype
         !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_3d(&mdz, dZ, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
       return TTT_ERR_CUDA;
-    err = ttt::launch_linear_bwd_mma(p, mq, mk, mv, mdz, s);
+    err = cudaSuccess;
+    if (bpl.seg_count > 1) {
+      // Start states of segments 1..S-1: the forward's segment maps and their combine.
+      ttt::LinearParams fp{};
+      fp.Q = Q; fp.K = K; fp.V = V; fp.Z = nullptr;
+      fp.eta = eta; fp.W0 = W0; fp.W_out = nullptr;
+      fp.B = B; fp.H = H; fp.T = T; fp.d = d; fp.b = b;
+      fp.units = p.units;
+      fp.bf16 = true;
+      fp.status = p.status;
+      fp.timeout_ns = p.timeout_ns;
+      fp.inject_stall = 0;
+      fp.seg_len = bpl.seg_len;
+      fp.seg_count = bpl.seg_count;
+      fp.seg_maps = seg_maps;
+      fp.seg_starts = seg_starts;
+      fp.affine_wy = 1;
+      fp.seg_first = 0;
+      fp.seg_num = bpl.seg_count - 1;
+      CUtensorMap mk64, mv64, mq16, mk16, mdz16;
+      const int rows64 = ttt::linear_seg_wy_rows(), rows16 = ttt::linear_bwd_hmap_rows();
+      if (!encode_3d(&mk64, K, p.units, T, d, rows64, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_3d(&mv64, V, p.units, T, d, rows64, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_3d(&mq16, Q, p.units, T, d, rows16, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_3d(&mk16, K, p.units, T, d, rows16, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_3d(&mdz16, dZ, p.units, T, d, rows16, d, CU_TENSOR_MAP_SWIZZLE_128B))
+        return TTT_ERR_CUDA;
+      err = ttt::launch_linear_seg_affine_wy(fp, mk64, mv64, s);
+      if (err == cudaSuccess) err = ttt::launch_linear_seg_combine(fp, s);
+      // H_s, A_s of segments 1..S-1 and the gradients at the segments' ends.
+      if (err == cudaSuccess) err = ttt::launch_linear_bwd_hmap(p, mq16, mk16, mdz16, s);
+      if (err == cudaSuccess) err = ttt::launch_linear_bwd_rcombine(p, s);
+    }
+    if (err == cudaSuccess) err = ttt::launch_linear_bwd_mma(p, mq, mk, mv, mdz, s);
   } else {
     err = ttt::launch_linear_bwd(p, s);
   }

@@ -167,6 +167,20 @@ def _bwd(lib, **kw):
                               vp(a["dV"]), vp(a["deta"]), vp(a["dW0"]), vp(a["ws"]), a["wsb"], vp(a["s"]))
 
 
+def test_backward_workspace_bytes_with_segments(lib):
+    """bf16-sized at d = 64, b = 16 with few units: the sequence is cut into segments that fill the
+    SMs (148 without a GPU), which adds per-segment partials and six d x d matrices per segment
+    boundary (forward maps and start states, H_s and A_s, end gradients)."""
+    B, H, T = 1, 2, 8192
+    S = 64                                   # min(8192 / 64, 148 // 2) = 74 -> 128-token segments -> 64
+    base = 2 * (T // 16) * 64 * 64 * 4 + 2 * (64 * 64 + 1) * 4
+    seg = -(-2 * S * (64 * 64 + 1) * 4 // 256) * 256 + 2 * (S - 1) * 64 * 64 * 4 * 6
+    assert ttt.ttt_linear_bwd_workspace_bytes(B, H, T, 64, 16) == 256 + -(-base // 16) * 16 + seg
+    # 84 units: one segment each, no extra
+    base = 84 * (200 // 16 + 1) * 64 * 64 * 4 + 84 * (64 * 64 + 1) * 4
+    assert ttt.ttt_linear_bwd_workspace_bytes(7, 12, 200, 64, 16) == 256 + -(-base // 16) * 16
+
+
 def test_backward_workspace_bytes(lib):
     """A status block, every chunk-start state and a per-unit partial of dW0 and d eta."""
     assert ttt.ttt_linear_bwd_workspace_bytes(2, 3, 40, 16, 8) == 256 + 6 * 5 * 16 * 16 * 4 + 6 * (16 * 16 + 1) * 4 + 8

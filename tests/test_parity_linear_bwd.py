@@ -114,3 +114,38 @@ def test_backward_bf16_125m_shape_sampled_heads():
     want = linear_backward(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, 16, dZ, dW)
     for name, gg, r in zip(("dQ", "dK", "dV", "deta", "dW0"), got, want):
         assert rel_err(f"bf16 125m {name}", to64(gg), r, 2e-2) <= 2e-2, name
+
+
+def _bf16_case(B, H, T, seed, eta=("uniform", 0.05, 0.5)):
+    w = W["linear_small"].with_(B=B, H=H, T=T, d=64, b=16, eta=eta, seed=seed)
+    inp = synth.make_inputs(w)
+    g = np.random.default_rng(seed)
+    dZ = bf16_round(g.standard_normal((B, H, T, 64)).astype(np.float32))
+    dW = g.standard_normal((B, H, 64, 64)).astype(np.float32)
+    t = torch_inputs(inp)
+    dev = t["Q"].device
+    got = ttt.ttt_linear_bwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], 16,
+                             torch.from_numpy(dZ).to(dev).to(torch.bfloat16), torch.from_numpy(dW).to(dev))
+    torch.cuda.synchronize()
+    want = linear_backward(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, 16, dZ, dW)
+    return got, want
+
+
+def test_backward_bf16_one_cta_per_unit_when_units_fill_the_gpu():
+    """B7 H12 (84 units >= half the SMs): one segment per unit, the whole sequence in one CTA."""
+    got, want = _bf16_case(7, 12, 200, 66)
+    for name, g, r in zip(("dQ", "dK", "dV", "deta", "dW0"), got, want):
+        assert rel_err(f"bf16 unsegmented {name}", to64(g), r, 2e-2) <= 2e-2, name
+
+
+def test_backward_bf16_segment_parallel_long_sequence():
+    """B1 H2 T8192: 64 segments of 128 tokens per unit (start states from the forward's segment
+    maps, end gradients from the H pass and the reverse combine), against the oracle, at the
+    long-context workload's eta = 0.1. (d eta is one sum over ~10^6 products with cancellation:
+    with eta up to 0.5 over 8192 tokens its bf16 error reaches 2-5 % on both the segmented and the
+    one-CTA path, so that setting is no test of the segmentation.)"""
+    got, want = _bf16_case(1, 2, 8192, 67, eta=("const", 0.1))
+    for name, g, r in zip(("dQ", "dK", "dV", "deta", "dW0"), got, want):
+        g = to64(g)
+        assert np.all(np.isfinite(g)), name
+        assert rel_err(f"bf16 segmented {name}", g, r, 2e-2) <= 2e-2, name
