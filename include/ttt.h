@@ -347,6 +347,10 @@ TTT_API ttt_status ttt_linear_momentum_fwd(const void* Q, const void* K, const v
  *   dW0 [H][d][d] float32 (summed over the batch rows, which share eta and W0).
  *   Kernels: bf16 with d = 64 and b = 16 runs on the tensor cores (state and
  *   products fp32-accumulated, W checkpointed every 64 tokens in the workspace);
+ *   when B * H leaves SMs idle the sequence is cut into segments of whole
+ *   64-token blocks, one CTA each, whose start states come from the forward's
+ *   segment maps and whose end gradients come from the affine form of the
+ *   read-out (G_start = A_s^T G_end + sum over the segment of Zhat^T dZ);
  *   every other case with d <= 64 runs the fp32 SIMT kernel (fp32 or bf16
  *   operands; chunks longer than 64 tokens are walked in 32-token blocks, with
  *   the chunk's E and dE kept in the workspace); d > 64 returns
