@@ -688,6 +688,27 @@ def bench_extras(ttt, dev, stream):
         del Q, K, V, dZ
     except Exception as exc:  # reported in the line, never silently dropped
         out["linear_bwd_small_f32_b16"] = {"error": f"{type(exc).__name__}: {exc}"}
+    # backward of TTT-Linear with few units: the segment-parallel form (B2 H4 T8192, B1 H32 T131072)
+    for tag, w in (("linear_bwd_seg_small_bf16_b16", synth.WORKLOADS["linear_small"].with_(T=8192)),
+                   ("linear_bwd_seg_long_bf16_b16", synth.WORKLOADS["linear_long"])):
+        try:
+            inp, Q, K, V, eta = dev_inputs(w)
+            W0 = torch.from_numpy(inp.W0).to(dev)
+            dZ = torch.randn_like(Q, dtype=torch.float32).to(torch.bfloat16)
+            dW = torch.randn(w.B, w.H, w.d, w.d, device=dev)
+            ws = torch.empty(ttt.ttt_linear_bwd_workspace_bytes(w.B, w.H, w.T, w.d, 16), dtype=torch.uint8,
+                             device=dev)
+            ms = t_ms(lambda: ttt.ttt_linear_bwd(Q, K, V, eta, W0, 16, dZ, dW, workspace=ws, stream=stream), 3)
+            if ttt.ttt_last_device_status(ws, stream) != 0:
+                raise RuntimeError("device status not OK")
+            bwd_bytes = w.token_heads * 7 * w.d * 2
+            out[tag] = {"ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                        "hbm_frac": round(bwd_bytes / (ms * 1e-3) / 1e9 / hbm_gbs, 4),
+                        "note": f"B{w.B} H{w.H} T{w.T} d64 bf16: segments of whole 64-token blocks, one "
+                                "tensor-core backward CTA each"}
+            del Q, K, V, dZ, ws
+        except Exception as exc:  # reported in the line, never silently dropped
+            out[tag] = {"error": f"{type(exc).__name__}: {exc}"}
     # backward of TTT-MLP (fp32 parity kernel), B2 H4 T512 d64 hidden 256
     try:
         w = synth.WORKLOADS["mlp_125m"].with_(B=2, H=4, T=512, dtype="f32")

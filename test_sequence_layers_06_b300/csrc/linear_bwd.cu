@@ -421,20 +421,22 @@ __global__ void __launch_bounds__(kBwdThreads) linear_bwd_wide_kernel(LinearBwdP
 }
 
 // dW0[h] and d eta[h]: sums over the batch rows (and segments) of the per-unit partials.
+// Blocks: (head, slice of 256 of the d*d + 1 entries); one thread per entry.
 __global__ void __launch_bounds__(kBwdThreads) linear_bwd_reduce_kernel(LinearBwdParams p) {
-  const int h = blockIdx.x;
   const int d = p.d;
+  const int n_ent = d * d + 1;
+  const int slices = (n_ent + kBwdThreads - 1) / kBwdThreads;
+  const int h = blockIdx.x / slices;
+  const int i = (blockIdx.x % slices) * kBwdThreads + threadIdx.x;
+  if (i >= n_ent) return;
   const int S = p.bseg_count > 1 ? p.bseg_count : 1;
-  for (int i = threadIdx.x; i <= d * d; i += kBwdThreads) {
-    float acc = 0.f;
-    for (int n = 0; n < p.B; ++n)
-      for (int s = 0; s < S; ++s)
-        acc += p.partial[(static_cast<size_t>(n * p.H + h) * S + s) * (d * d + 1) + i];
-    if (i < d * d)
-      p.dW0[static_cast<size_t>(h) * d * d + i] = acc;
-    else
-      p.deta[h] = acc;
-  }
+  float acc = 0.f;
+  for (int n = 0; n < p.B; ++n)
+    for (int s = 0; s < S; ++s) acc += p.partial[(static_cast<size_t>(n * p.H + h) * S + s) * n_ent + i];
+  if (i < d * d)
+    p.dW0[static_cast<size_t>(h) * d * d + i] = acc;
+  else
+    p.deta[h] = acc;
 }
 
 }  // namespace
@@ -481,7 +483,8 @@ cudaError_t launch_linear_bwd(const LinearBwdParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_linear_bwd_reduce(const LinearBwdParams& p, cudaStream_t stream) {
-  linear_bwd_reduce_kernel<<<p.H, kBwdThreads, 0, stream>>>(p);
+  const int slices = (p.d * p.d + 1 + kBwdThreads - 1) / kBwdThreads;
+  linear_bwd_reduce_kernel<<<p.H * slices, kBwdThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -91,6 +91,9 @@ __device__ __forceinline__ void store_t(uint32_t base, const uint32_t (&a)[4][4]
   for (int s = 0; s < 4; ++s) stsm_x4_t(base + swz128(16 * s + ((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)), a[s]);
 }
 
+// kSeg: the unit's sequence is cut into p.bseg_count segments (one CTA each);
+// without it every CTA takes a whole unit.
+template <bool kSeg>
 __global__ void __launch_bounds__(kThreads, 1)
     linear_bwd_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                           const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdz,
@@ -107,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s0 = smem_u32(sm);
 
   // One CTA per (unit, segment): blocks [blk0, blk1) of 64 tokens (all of them without segments).
-  const int S = p.bseg_count;
+  const int S = kSeg ? p.bseg_count : 1;
   const int unit = blockIdx.x / S;
   const int seg = blockIdx.x % S;
   const int h = unit % p.H;
@@ -116,8 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = p.T;
   const int ntiles = (T + kTile - 1) / kTile;
   const int nblk_all = (T + kBlk - 1) / kBlk;
-  const int blk0 = seg * (p.bseg_len / kBlk);
-  const int blk1 = min(nblk_all, blk0 + p.bseg_len / kBlk);
+  const int blk0 = kSeg ? seg * (p.bseg_len / kBlk) : 0;
+  const int blk1 = kSeg ? min(nblk_all, blk0 + p.bseg_len / kBlk) : nblk_all;
   const int nblk = blk1 - blk0;  // this CTA's blocks
   const float eta = p.eta[h];
 
@@ -587,9 +590,10 @@ int linear_bwd_mma_rows() { return kBlk; }
 cudaError_t launch_linear_bwd_mma(const LinearBwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                   const CUtensorMap& mv, const CUtensorMap& mdz, cudaStream_t stream) {
   if (p.units == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(linear_bwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  auto kern = p.bseg_count > 1 ? linear_bwd_mma_kernel<true> : linear_bwd_mma_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  linear_bwd_mma_kernel<<<p.units * p.bseg_count, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdz, p);
+  kern<<<p.units * p.bseg_count, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdz, p);
   return cudaGetLastError();
 }
 

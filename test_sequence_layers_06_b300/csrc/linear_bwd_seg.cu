@@ -295,14 +295,24 @@ __global__ void __launch_bounds__(kRcThreads) linear_bwd_rcombine_kernel(LinearB
   const int c = (tid & 1) * 4;
   *reinterpret_cast<float4*>(&sG[i * kRcCols + c]) =
       *reinterpret_cast<const float4*>(p.dW_out + static_cast<size_t>(unit) * kD * kD + i * kD + j0 + c);
-  for (int s = nseg; s >= 1; --s) {
+  // A_s (8 float4 per thread) and this thread's four entries of H_s, fetched one step ahead.
+  float4 ra[kD * kD / 4 / kRcThreads];
+  float4 hv;
+  auto fetch = [&](int s) {
     const float* Hs = p.hA + (static_cast<size_t>(unit) * nseg + s - 1) * 2 * kD * kD;
-    const float* As = Hs + kD * kD;
-    for (int x = tid; x < kD * kD / 4; x += kRcThreads)
-      reinterpret_cast<float4*>(sA)[x] = __ldcg(reinterpret_cast<const float4*>(As) + x);
-    const float4 hv = __ldcg(reinterpret_cast<const float4*>(Hs + i * kD + j0 + c));
+#pragma unroll
+    for (int r = 0; r < kD * kD / 4 / kRcThreads; ++r)
+      ra[r] = __ldcg(reinterpret_cast<const float4*>(Hs + kD * kD) + tid + kRcThreads * r);
+    hv = __ldcg(reinterpret_cast<const float4*>(Hs + i * kD + j0 + c));
+  };
+  if (nseg >= 1) fetch(nseg);
+  for (int s = nseg; s >= 1; --s) {
+#pragma unroll
+    for (int r = 0; r < kD * kD / 4 / kRcThreads; ++r) reinterpret_cast<float4*>(sA)[tid + kRcThreads * r] = ra[r];
+    const float4 h4 = hv;
     __syncthreads();  // sA holds A_s; sG holds G_end(s)
-    float acc[4] = {hv.x, hv.y, hv.z, hv.w};
+    if (s > 1) fetch(s - 1);
+    float acc[4] = {h4.x, h4.y, h4.z, h4.w};
     for (int k = 0; k < kD; ++k) {
       const float a = sA[k * kD + i];  // (A_s^T)[i][k]
       const float4 gv = *reinterpret_cast<const float4*>(&sG[k * kRcCols + c]);
