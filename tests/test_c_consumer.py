@@ -56,6 +56,14 @@ int main(void) {
   printf("bwd.d65=%d\n", (int)ttt_linear_bwd(dummy, dummy, dummy, TTT_BF16, dummy, dummy, 1, 1, 16, 65, 16,
                                               dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, 1u << 20,
                                               NULL));
+  printf("ws.var_bias=%zu\n", ttt_linear_variant_workspace_bytes(TTT_INNER_BIAS, TTT_BF16, 2, 3, 40, 16, 16));
+  printf("ws.var_ln=%zu\n", ttt_linear_variant_workspace_bytes(TTT_INNER_LN, TTT_BF16, 2, 3, 40, 16, 16));
+  printf("ws.mlp_bwd=%zu\n", ttt_mlp_bwd_workspace_bytes(2, 3, 40, 16, 8));
+  printf("mlp_bwd.d65=%d\n", (int)ttt_mlp_bwd(dummy, dummy, dummy, TTT_F32, dummy, dummy, dummy, 1, 1, 16, 65, 16,
+                                              dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy, dummy,
+                                              dummy, 1u << 20, NULL));
+  printf("bias_ex.nows=%d\n", (int)ttt_linear_bias_fwd_ex(dummy, dummy, dummy, TTT_BF16, dummy, dummy, dummy, 1, 1,
+                                                          16, 16, 16, dummy, dummy, dummy, NULL, 0, NULL));
   return 0;
 }
 """
@@ -93,6 +101,15 @@ def test_calls_from_c_agree_with_the_binding(c_output):
     assert int(c_output["ws.mlp"]) == ttt.ttt_workspace_bytes(2, 3, 100, 64, 16, variant=ttt.TTT_VARIANT_MLP) >= 256
     assert int(c_output["ws.bad"]) == 0
     assert int(c_output["ws.bwd"]) == ttt.ttt_linear_bwd_workspace_bytes(2, 3, 100, 64, 16) > 256
+
+
+def test_variant_and_mlp_backward_calls_from_c(c_output):
+    assert int(c_output["ws.var_bias"]) == ttt.ttt_linear_variant_workspace_bytes(
+        ttt.TTT_INNER_BIAS, ttt.TTT_BF16, 2, 3, 40, 16, 16) > 256
+    assert int(c_output["ws.var_ln"]) == 0
+    assert int(c_output["ws.mlp_bwd"]) == ttt.ttt_mlp_bwd_workspace_bytes(2, 3, 40, 16, 8) > 256
+    assert int(c_output["mlp_bwd.d65"]) == -2   # d > 64
+    assert int(c_output["bias_ex.nows"]) == -1  # no workspace
 
 
 def test_argument_errors_from_c(c_output):
