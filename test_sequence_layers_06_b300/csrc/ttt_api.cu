@@ -92,7 +92,6 @@ struct LinearPlan {
 };
 
 constexpr int kSegMinTokens = 256;  // shortest segment the automatic plan makes
-constexpr int kSegWavesTarget = 2;  // read-out work items per resident CTA slot (at most)
 constexpr int kMmaCtasPerSm = 3;    // linear_mma_kernel's occupancy (its launch bounds)
 constexpr int kAutoPieces = 1;      // pieces of the automatic plan
 
@@ -117,15 +116,31 @@ ttt_status plan_linear(int B, int H, int T, int d, int b, bool bf16, const ttt_o
   if (seg) {
     long long len = o.seg_len;
     if (len == 0) {
-      // Whole waves of read-out CTAs: units * S <= kSegWavesTarget * slots.
-      const long long S = std::max(1LL, static_cast<long long>(kSegWavesTarget) * slots / units);
-      len = (T + S - 1) / S;
       // Segments hold whole chunks; where the 64-token tensor-core affine kernel
       // applies (b = 16, 32 or a multiple of 64) they also hold whole 64-token steps.
       const long long align = (b % 64 == 0 || 64 % b == 0) ? std::max(b, 64) : b;
       const long long min_len = ((kSegMinTokens + align - 1) / align) * align;
-      len = ((len + align - 1) / align) * align;
-      if (len < min_len) len = min_len;
+      // The segment count that minimises an estimate of the step: waves of affine-map CTAs
+      // (two per SM) and of read-out CTAs (three per SM), each wave as long as one segment
+      // at the per-token time one CTA of that kernel measured at full occupancy, plus the
+      // combine's chain over the segment boundaries. Partial waves count as whole ones.
+      const double aff_ns = b <= 32 ? 25.0 : (b < 256 ? 19.0 : 12.5), out_ns = 47.0, step_ns = 1400.0;
+      const long long slots_a = 2LL * sm_count(), slots_r = slots;
+      double best = -1.0;
+      for (long long S = 2; S <= T / min_len; ++S) {
+        long long L = ((T + S - 1) / S + align - 1) / align * align;
+        if (L < min_len) L = min_len;
+        const long long cnt = (T + L - 1) / L;
+        if (cnt < 2) continue;
+        const double waves_a = static_cast<double>((units * (cnt - 1) + slots_a - 1) / slots_a);
+        const double waves_r = static_cast<double>((units * cnt + slots_r - 1) / slots_r);
+        const double cost = waves_a * L * aff_ns + (cnt - 1) * step_ns + waves_r * L * out_ns;
+        if (best < 0.0 || cost < best) {
+          best = cost;
+          len = L;
+        }
+      }
+      if (len == 0) len = min_len;
     }
     const long long count = (T + len - 1) / len;
     // Grids of one read-out CTA per (unit, segment) and 8 combine CTAs per unit
