@@ -222,11 +222,21 @@ __global__ void __launch_bounds__(kAffThreads, 2)
 // columns 4c .. 4c+3 of its CTA's slice.
 constexpr int kCmbCols = 8;
 constexpr int kCmbThreads = 128;
-constexpr int kCmbPad = 68;  // row stride of A in shared memory (floats): conflict-free 16-byte reads
+constexpr int kCmbPad = 68;   // row stride of A in shared memory (floats): conflict-free 16-byte reads
+constexpr int kCmbRing = 4;   // maps in flight: the chain's loads run this many steps ahead
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __global__ void __launch_bounds__(kCmbThreads) linear_seg_combine_kernel(LinearParams p) {
-  __shared__ __align__(16) float sA[kD * kCmbPad];
-  __shared__ __align__(16) float sW[kD * kCmbCols];
+  extern __shared__ __align__(16) float cmb_smem[];
+  float* sA = cmb_smem;                            // [kCmbRing][kD][kCmbPad]
+  float* sB = sA + kCmbRing * kD * kCmbPad;        // [kCmbRing][kCmbThreads][4]: this thread's entries of B
+  float* sW = sB + kCmbRing * kCmbThreads * 4;     // [kD][kCmbCols]
   const int groups = kD / kCmbCols;
   const int unit = blockIdx.x / groups;
   const int j0 = (blockIdx.x % groups) * kCmbCols;
@@ -243,31 +253,34 @@ __global__ void __launch_bounds__(kCmbThreads) linear_seg_combine_kernel(LinearP
                         : p.seg_starts + (static_cast<size_t>(unit) * maps + p.seg_first - 1) * kD * kD;
   *reinterpret_cast<float4*>(&sW[i * kCmbCols + c]) = __ldcg(reinterpret_cast<const float4*>(Ws + i * kD + j0 + c));
 
-  // Registers that carry map s into shared memory: A (4096 floats, 8 float4 per
-  // thread) and this thread's four entries of B.
-  float4 ra[8];
-  float4 rb;
-  auto fetch = [&](int s) {
-    const float* A = p.seg_maps + (static_cast<size_t>(unit) * maps + s) * 2 * kD * kD;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) ra[r] = __ldcg(reinterpret_cast<const float4*>(A) + tid + kCmbThreads * r);
-    rb = __ldcg(reinterpret_cast<const float4*>(A + kD * kD + i * kD + j0 + c));
-  };
+  // Map s into ring slot (s - seg_first) % kCmbRing: A (4096 floats, 8 x 16 bytes per thread)
+  // and this thread's four entries of B, as one cp.async group.
   const int s_end = p.seg_first + p.seg_num;
-  if (p.seg_num > 0) fetch(p.seg_first);
-  for (int s = p.seg_first; s < s_end; ++s) {
+  auto fetch = [&](int s) {
+    const int slot = (s - p.seg_first) % kCmbRing;
+    const float* A = p.seg_maps + (static_cast<size_t>(unit) * maps + s) * 2 * kD * kD;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const int f = (tid + kCmbThreads * r) * 4;
-      *reinterpret_cast<float4*>(&sA[(f / kD) * kCmbPad + (f % kD)]) = ra[r];
+      cp_async16(&sA[(slot * kD + f / kD) * kCmbPad + f % kD], A + f);
     }
-    const float4 b = rb;
-    __syncthreads();  // sA complete; sW holds W_start(s)
-    if (s + 1 < s_end) fetch(s + 1);
+    cp_async16(&sB[(slot * kCmbThreads + tid) * 4], A + kD * kD + i * kD + j0 + c);
+  };
+#pragma unroll
+  for (int r = 0; r < kCmbRing; ++r) {
+    if (p.seg_first + r < s_end) fetch(p.seg_first + r);
+    cp_async_commit();  // one group per map (empty past the end), so the count below holds
+  }
+  for (int s = p.seg_first; s < s_end; ++s) {
+    const int slot = (s - p.seg_first) % kCmbRing;
+    cp_async_wait<kCmbRing - 1>();  // this thread's copies of map s have landed
+    __syncthreads();                // everyone's have; sW holds W_start(s)
+    const float* a_s = sA + slot * kD * kCmbPad;
+    const float4 b = *reinterpret_cast<const float4*>(&sB[(slot * kCmbThreads + tid) * 4]);
     float acc[2][4] = {{b.x, b.y, b.z, b.w}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int k = 0; k < kD; k += 4) {
-      const float4 a = *reinterpret_cast<const float4*>(&sA[i * kCmbPad + k]);
+      const float4 a = *reinterpret_cast<const float4*>(&a_s[i * kCmbPad + k]);
       const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
@@ -281,11 +294,14 @@ __global__ void __launch_bounds__(kCmbThreads) linear_seg_combine_kernel(LinearP
     }
     const float4 nw = make_float4(acc[0][0] + acc[1][0], acc[0][1] + acc[1][1], acc[0][2] + acc[1][2],
                                   acc[0][3] + acc[1][3]);
-    __syncthreads();  // every thread is done reading sW and sA
+    __syncthreads();  // every thread is done reading sW and this slot
     *reinterpret_cast<float4*>(&sW[i * kCmbCols + c]) = nw;
     *reinterpret_cast<float4*>(p.seg_starts + (static_cast<size_t>(unit) * maps + s) * kD * kD + i * kD + j0 + c) =
         nw;
+    if (s + kCmbRing < s_end) fetch(s + kCmbRing);  // refill the slot just read
+    cp_async_commit();
   }
+  cp_async_wait<0>();
 }
 
 }  // namespace
@@ -302,7 +318,11 @@ cudaError_t launch_linear_seg_affine(const LinearParams& p, const CUtensorMap& m
 
 cudaError_t launch_linear_seg_combine(const LinearParams& p, cudaStream_t stream) {
   if (p.seg_count < 2 || p.units == 0 || p.seg_num == 0) return cudaSuccess;
-  linear_seg_combine_kernel<<<p.units * (kD / kCmbCols), kCmbThreads, 0, stream>>>(p);
+  constexpr int smem = (kCmbRing * kD * kCmbPad + kCmbRing * kCmbThreads * 4 + kD * kCmbCols) * 4;
+  const cudaError_t e =
+      cudaFuncSetAttribute(linear_seg_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  linear_seg_combine_kernel<<<p.units * (kD / kCmbCols), kCmbThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
