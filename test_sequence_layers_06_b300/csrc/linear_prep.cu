@@ -15,9 +15,10 @@
 //
 // variant_prep_kernel writes the changed inputs (bf16, 64 features per row) and
 // W0' (fp32); variant_post_kernel copies Z, W_out and beta_out back out of the
-// padded results and merges the status words. Both are elementwise passes with
-// one warp per token row (16-byte accesses, 8 features per thread, where the rows
-// are already 64 wide: the per-token rate at d = 64).
+// padded results and merges the status words. Both are elementwise passes in which
+// a thread handles 8 features of a padded row (16-byte loads of K and V where the
+// rows are already 64 wide, element loads otherwise; 16-byte stores of the padded
+// rows).
 #include <algorithm>
 
 #include "ttt_device.cuh"
@@ -33,9 +34,6 @@ enum : int { kWhereNegativeRate = 20 };
 
 __device__ __forceinline__ float ldbf(const void* p, size_t i) {
   return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
-}
-__device__ __forceinline__ void stbf(void* p, size_t i, float v) {
-  static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
 }
 
 // Blocks [0, H): W0' and eta' of head h. Blocks from H on: token rows, one warp
@@ -56,7 +54,6 @@ __global__ void __launch_bounds__(kPrepThreads) variant_prep_kernel(VariantPrepP
     if (threadIdx.x == 0) p.etap[h] = p.eta ? p.eta[h] : 1.f;
     return;
   }
-  const int lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(p.units) * p.T;
   if (d == kP && !p.bias && p.Qp == nullptr) {
     // Rows of 64 features, 16-byte aligned: a thread scales 8 features of K and of V.
@@ -88,28 +85,43 @@ __global__ void __launch_bounds__(kPrepThreads) variant_prep_kernel(VariantPrepP
     }
     return;
   }
-  const long long warps = static_cast<long long>(gridDim.x - p.H) * (kPrepThreads / 32);
-  for (long long r = static_cast<long long>(blockIdx.x - p.H) * (kPrepThreads / 32) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
-    float s = 1.f;
-    if (p.tok_rate) {
-      const float et = p.tok_rate[r];
-      if (et < 0.f) {
-        if (lane == 0) report_error(p.status, TTT_ERR_DEVICE_CHECK, kWhereNegativeRate, static_cast<int>(r / p.T));
-        s = 0.f;
-      } else {
-        s = sqrtf(et);
+  // Other widths (rows of d < 64 features, not 16-byte aligned): a thread forms 8 padded
+  // features of a row from element loads and writes them as one 16-byte store.
+  {
+    const long long items = rows * (kP / 8);
+    const long long stride = static_cast<long long>(gridDim.x - p.H) * kPrepThreads;
+    for (long long x = static_cast<long long>(blockIdx.x - p.H) * kPrepThreads + threadIdx.x; x < items; x += stride) {
+      const long long r = x / (kP / 8);
+      const int f0 = static_cast<int>(x % (kP / 8)) * 8;
+      float s = 1.f;
+      if (p.tok_rate) {
+        const float et = p.tok_rate[r];
+        if (et < 0.f) {
+          if (f0 == 0) report_error(p.status, TTT_ERR_DEVICE_CHECK, kWhereNegativeRate, static_cast<int>(r / p.T));
+          s = 0.f;
+        } else {
+          s = sqrtf(et);
+        }
       }
-    }
-    const size_t in = static_cast<size_t>(r) * d, out = static_cast<size_t>(r) * kP;
+      const size_t in = static_cast<size_t>(r) * d;
+      float q[8], k[8], v[8];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int f = lane + 32 * half;
-      const float one = (p.bias && f == d) ? 1.f : 0.f;
-      if (p.Qp) stbf(p.Qp, out + f, f < d ? ldbf(p.Q, in + f) : one);
-      stbf(p.Kp, out + f, f < d ? s * ldbf(p.K, in + f) : one);
-      stbf(p.Vp, out + f, f < d ? s * ldbf(p.V, in + f) : 0.f);
+      for (int e = 0; e < 8; ++e) {
+        const int f = f0 + e;
+        const float one = (p.bias && f == d) ? 1.f : 0.f;
+        q[e] = f < d ? ldbf(p.Q, in + f) : one;
+        k[e] = f < d ? s * ldbf(p.K, in + f) : one;
+        v[e] = f < d ? s * ldbf(p.V, in + f) : 0.f;
+      }
+      if (p.Qp)
+        reinterpret_cast<uint4*>(p.Qp)[x] = make_uint4(pack_bf16(q[0], q[1]), pack_bf16(q[2], q[3]),
+                                                       pack_bf16(q[4], q[5]), pack_bf16(q[6], q[7]));
+      reinterpret_cast<uint4*>(p.Kp)[x] = make_uint4(pack_bf16(k[0], k[1]), pack_bf16(k[2], k[3]),
+                                                     pack_bf16(k[4], k[5]), pack_bf16(k[6], k[7]));
+      reinterpret_cast<uint4*>(p.Vp)[x] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]),
+                                                     pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
     }
+    return;
   }
 }
 
@@ -132,16 +144,22 @@ __global__ void __launch_bounds__(kPrepThreads) variant_post_kernel(VariantPostP
     return;
   }
   if (p.Zp == nullptr) return;
-  const int lane = threadIdx.x & 31;
+  // A thread reads 8 padded features of a row as one 16-byte load and writes those below d.
   const long long rows = static_cast<long long>(p.units) * p.T;
-  const long long warps = static_cast<long long>(gridDim.x - p.units) * (kPrepThreads / 32);
-  for (long long r = static_cast<long long>(blockIdx.x - p.units) * (kPrepThreads / 32) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
-    const size_t in = static_cast<size_t>(r) * kP, out = static_cast<size_t>(r) * d;
+  const long long items = rows * (kP / 8);
+  const long long stride = static_cast<long long>(gridDim.x - p.units) * kPrepThreads;
+  for (long long x = static_cast<long long>(blockIdx.x - p.units) * kPrepThreads + threadIdx.x; x < items; x += stride) {
+    const long long r = x / (kP / 8);
+    const int f0 = static_cast<int>(x % (kP / 8)) * 8;
+    const uint4 zv = reinterpret_cast<const uint4*>(p.Zp)[x];
+    const uint32_t zz[4] = {zv.x, zv.y, zv.z, zv.w};
+    const size_t out = static_cast<size_t>(r) * d;
+    __nv_bfloat16* Z = static_cast<__nv_bfloat16*>(p.Z);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int f = lane + 32 * half;
-      if (f < d) static_cast<__nv_bfloat16*>(p.Z)[out + f] = static_cast<const __nv_bfloat16*>(p.Zp)[in + f];
+    for (int e = 0; e < 8; ++e) {
+      const int f = f0 + e;
+      const uint16_t bits = static_cast<uint16_t>((e & 1) ? (zz[e >> 1] >> 16) : (zz[e >> 1] & 0xFFFFu));
+      if (f < d) Z[out + f] = __ushort_as_bfloat16(bits);
     }
   }
 }
