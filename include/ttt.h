@@ -173,7 +173,11 @@ TTT_API ttt_status ttt_linear_fwd_ex(const void* Q, const void* K, const void* V
  * TTT-MLP forward: f(x) = gelu(x W1) W2 with tanh-GELU (Hendrycks and Gimpel
  * 2016), hidden width m = 4 d ("Test-Time Training (TTT) guide", section 3).
  * With bf16 operands, d = 64 and b % 16 == 0 a tensor-core kernel serves the
- * call (ttt_options.force_path = 2 requires it, 1 forces the fp32 SIMT kernel).
+ * call: for b = 16 a cluster of two CTAs per (batch row, head), each holding half
+ * of the hidden units and exchanging its partial sums of G and Z with the other
+ * through distributed shared memory; otherwise one CTA per (batch row, head).
+ * ttt_options.force_path: 1 forces the fp32 SIMT kernel, 2 the one-CTA tensor
+ * kernel, 3 the two-CTA kernel (b = 16 only; TTT_ERR_UNSUPPORTED elsewhere).
  *   W1_0 [H][d][4d], W2_0 [H][4d][d] float32, shared by the batch.
  *   W1_out [B][H][d][4d], W2_out [B][H][4d][d] float32.
  *   Other arguments as ttt_linear_fwd.

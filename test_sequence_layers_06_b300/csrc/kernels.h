@@ -222,6 +222,9 @@ cudaError_t launch_linear_simt(const LinearParams& p, cudaStream_t stream);
 
 // Tensor-core TTT-MLP (bf16, d = 64, hidden 256, b % 16 == 0), one CTA per unit.
 bool mlp_mma_supported(const MlpParams& p);
+bool mlp_cluster_supported(const MlpParams& p);  // b = 16: two CTAs per unit (mlp_cluster.cu)
+cudaError_t launch_mlp_cluster(const MlpParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                               const CUtensorMap& mv, cudaStream_t stream);
 int mlp_mma_tile_rows();
 cudaError_t launch_mlp_mma(const MlpParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            cudaStream_t stream);

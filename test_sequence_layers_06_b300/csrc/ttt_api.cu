@@ -318,7 +318,7 @@ ttt_status mlp_forward(const void* Q, const void* K, const void* V, ttt_dtype dt
                         static_cast<const void*>(W2_out), static_cast<const void*>(workspace)})
     if (p && !aligned16(p)) return TTT_ERR_ARG;
   const ttt_options o = defaults(opt);
-  if (o.force_path < 0 || o.force_path > 2) return TTT_ERR_ARG;
+  if (o.force_path < 0 || o.force_path > 3) return TTT_ERR_ARG;
   const size_t need = ws_by_path ? mlp_workspace_bytes_for_path(B, H, T, d, b, dt, opt)
                                  : workspace_bytes_impl(B, H, T, d, b, TTT_VARIANT_MLP, nullptr);
   if (need == 0 || ws_bytes < need) return TTT_ERR_ARG;
@@ -343,8 +343,12 @@ ttt_status mlp_forward(const void* Q, const void* K, const void* V, ttt_dtype dt
   p.inject_stall = o.inject_stall;
 
   const bool mma_ok = ttt::mlp_mma_supported(p);
+  const bool cluster_ok = ttt::mlp_cluster_supported(p);
   if (o.force_path == 2 && !mma_ok) return TTT_ERR_UNSUPPORTED;
+  if (o.force_path == 3 && !cluster_ok) return TTT_ERR_UNSUPPORTED;
   const bool use_mma = mma_ok && o.force_path != 1 && T > 0;
+  // b = 16: two CTAs per unit (a cluster sharing the hidden units) unless one CTA is forced.
+  const bool use_cluster = use_mma && cluster_ok && o.force_path != 2;
 
   ttt_status st = reset_status(workspace, s);
   if (st != TTT_OK) return st;
@@ -356,7 +360,7 @@ ttt_status mlp_forward(const void* Q, const void* K, const void* V, ttt_dtype dt
         !encode_3d(&mk, K, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
       return TTT_ERR_CUDA;
-    err = ttt::launch_mlp_mma(p, mq, mk, mv, s);
+    err = use_cluster ? ttt::launch_mlp_cluster(p, mq, mk, mv, s) : ttt::launch_mlp_mma(p, mq, mk, mv, s);
   } else {
     err = ttt::launch_mlp_simt(p, s);
   }

@@ -76,3 +76,29 @@ def test_mlp_full_size_sampled():
         assert rel_err(f"W1 unit {n},{h}", to64(W1[n, h]), W1r[0, k], tolerance(w)) <= tolerance(w)
         assert rel_err(f"W2 unit {n},{h}", to64(W2[n, h]), W2r[0, k], tolerance(w)) <= tolerance(w)
     assert bool(torch.isfinite(Z.float()).all())
+
+
+@pytest.mark.parametrize("T", [0, 1, 16, 37, 64, 200])
+def test_mlp_b16_one_and_two_ctas_per_unit(T):
+    """b = 16: the two-CTA kernel (each CTA of a cluster holds half of the hidden units; the partial
+    sums of G and Z cross through distributed shared memory; the automatic choice) and the one-CTA
+    kernel, against the oracle: empty, shorter than a tile, ragged and several tiles."""
+    w = W["mlp_125m"].with_(B=2, H=3, T=T, seed=500 + T)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    Zr, W1r, W2r = oracle_mlp(inp, 16)
+    for fp in (0, ttt.PATH_TENSOR, 3):
+        Z, W1, W2 = ttt.ttt_mlp_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W1"], t["W2"], 16,
+                                    options={"force_path": fp})
+        torch.cuda.synchronize()
+        for name, x, r in (("Z", Z, Zr), ("W1", W1, W1r), ("W2", W2, W2r)):
+            if x.numel() == 0:
+                continue
+            assert rel_err(f"path {fp} {name}", to64(x), r, tolerance(w)) <= tolerance(w), (fp, name)
+
+
+def test_mlp_two_ctas_refused_where_they_do_not_apply():
+    w = W["mlp_125m"].with_(B=1, H=1, T=64, seed=510)
+    t = torch_inputs(synth.make_inputs(w))
+    with pytest.raises(ttt.TTTError):
+        ttt.ttt_mlp_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W1"], t["W2"], 32, options={"force_path": 3})
