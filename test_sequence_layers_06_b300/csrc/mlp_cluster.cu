@@ -13,16 +13,21 @@
 // Everything but the two sums is local to the hidden units, so only G and Z cross
 // between the CTAs. Each CTA splits its 128 hidden units into two quarters of 64;
 // a warp forms the 16 x 16 block of a quarter's partial G (or Z) for 16 value
-// columns and writes it to both CTAs' shared memory: locally with plain stores,
-// to the peer with st.async, whose bytes complete a transaction count on the
-// peer's mbarrier. So both CTAs hold all four quarters of G; Z's blocks go to the
-// CTA that writes those 32 columns of Z. The exchange buffers are double-buffered
-// by tile parity and every mbarrier wait is bounded. Each mbarrier phase is armed
-// (expect_tx) two tiles ahead, after the buffer's last read, which always precedes
-// the peer's next send into it (the peer's send of tile u + 2 needs this CTA's
-// partial of tile u + 2). A cluster barrier at the start (the peer's barriers are
-// initialised and armed) and at the end (no st.async still targets an exited CTA)
-// are the only unbounded waits; both CTAs always reach both.
+// columns in its own shared memory and hands it to the peer's with one 1 KB bulk
+// copy, whose bytes complete a transaction count on the peer's mbarrier. So both
+// CTAs hold all four quarters of G; Z's blocks go to the CTA that writes those 32
+// columns of Z (staged, then copied, when that is the peer).
+//
+// Neighbouring tiles overlap: tile u + 1's U/A/P/S (and Q W1 of its Hq) need only
+// tile u's W1 update, so they run in the phase of tile u's Z partials, and tile u's
+// Z sum runs in the phase of tile u + 1's G partials; a tile takes four CTA
+// barriers. A, the bf16 W2 copy and the exchange buffers are double-buffered by
+// tile parity and every mbarrier wait is bounded. Each exchange barrier's phase is
+// armed (expect_tx) after its buffer's last read, and that read precedes, through
+// the chain of exchanges, the peer's next send into it. A cluster barrier at the
+// start (the peer's barriers are initialised and armed) and at the end (no copy
+// still targets an exited CTA) are the only unbounded waits; both CTAs always
+// reach both.
 #include "kernels.h"
 #include "mlp_frag.cuh"
 #include "ttt_device.cuh"
@@ -40,21 +45,24 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileBytes = kTile * kD * 2;
 constexpr int kRowH = kMh * 2;          // 256-byte rows of [.][128] bf16
-constexpr int kPad = 68;                // fp32 row stride of the G partials
-constexpr int kPadZ = 36;               // ... of the Z partials (32 columns)
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int kQKV = 0;                                  // [2 stages][Q, K, V]
 constexpr int kW1b = kQKV + 2 * 3 * kTileBytes;          // W1[:, own], bf16 [64][128]
-constexpr int kW2b = kW1b + kD * kRowH;                  // W2[own, :], bf16 [128][64]
-constexpr int kAb = kW2b + kMh * 128;                    // A, bf16 [16][128]
-constexpr int kAqb = kAb + kTile * kRowH;                // Aq, bf16 [16][128]
+constexpr int kW2b = kW1b + kD * kRowH;                  // [2 parity] W2[own, :], bf16 [128][64]
+constexpr int kW2bBytes = kMh * 128;
+constexpr int kAb = kW2b + 2 * kW2bBytes;                // [2 parity] A, bf16 [16][128]
+constexpr int kAbBytes = kTile * kRowH;
+constexpr int kAqb = kAb + 2 * kAbBytes;                 // Aq, bf16 [16][128]
 constexpr int kGb = kAqb + kTile * kRowH;                // G, bf16 [16][64]
 constexpr int kSb = kGb + kTile * 128;                   // tril(Q K^T), bf16 [16][16] in 128-byte rows
-constexpr int kPartG = kSb + kTile * 128;                // [2 parity][4 quarters][16][kPad] fp32
-constexpr int kPartGBytes = 4 * kTile * kPad * 4;
-constexpr int kPartZ = kPartG + 2 * kPartGBytes;         // [2 parity][4 quarters][16][kPadZ] fp32
-constexpr int kPartZBytes = 4 * kTile * kPadZ * 4;
-constexpr int kBar = kPartZ + 2 * kPartZBytes;           // full[2], gfull[2], zfull[2]
+constexpr int kBlk = kTile * 16;                         // floats of a 16 x 16 fp32 block (1 KB)
+constexpr int kPartG = kSb + kTile * 128;                // [2 parity][4 quarters][4 column blocks] blocks
+constexpr int kPartGBytes = 16 * kBlk * 4;
+constexpr int kPartZ = kPartG + 2 * kPartGBytes;         // [2 parity][4 quarters][2 column blocks] blocks
+constexpr int kPartZBytes = 8 * kBlk * 4;
+constexpr int kZStage = kPartZ + 2 * kPartZBytes;        // [2 parity][2 quarters][2 column blocks]: Z for the peer
+constexpr int kZStageBytes = 4 * kBlk * 4;
+constexpr int kBar = kZStage + 2 * kZStageBytes;         // full[2], gfull[2], zfull[2]
 constexpr int kSmemBytes = kBar + 64 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "fits one CTA per SM");
 constexpr uint32_t kGRecv = 8 * kTile * 16 * 4;          // the peer's 8 warps: a 16 x 16 fp32 block each
@@ -72,13 +80,16 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
   return d;
 }
-// Eight bytes into the peer's shared memory; their arrival completes 8 bytes of the
+// A shared-memory block of this CTA to the peer's; its arrival completes `bytes` of the
 // transaction count of the peer's mbarrier.
-__device__ __forceinline__ void st_async_f2(uint32_t remote, float a, float b, uint32_t remote_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(remote),
-               "f"(a), "f"(b), "r"(remote_bar)
+__device__ __forceinline__ void bulk_to_peer(uint32_t remote, uint32_t local, uint32_t bytes, uint32_t remote_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   remote),
+               "r"(local), "r"(bytes), "r"(remote_bar)
                : "memory");
 }
+// Float offset of (row r, column c) in a 16 x 16 fp32 block: 16-byte chunks XOR-swizzled by row pair.
+__device__ __forceinline__ int blk_off(int r, int c) { return r * 16 + ((((c >> 2) ^ (r >> 1)) & 3) << 2) + (c & 3); }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -143,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       w2[nt][3] = W20[(r + 8) * kD + c + 1];
     }
   }
-  // bf16 copies of this warp's slices (local hidden index 16 * warp).
+  // bf16 copies of this warp's slices (local hidden index 16 * warp); W2's by tile parity.
   auto store_w1 = [&]() {
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
@@ -156,16 +167,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             pack_bf16(w1[mt][nt][2], w1[mt][nt][3]);
       }
   };
-  auto store_w2 = [&]() {
+  auto store_w2 = [&](int par) {
+    uint8_t* base = sm + kW2b + par * kW2bBytes;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
-      *reinterpret_cast<uint32_t*>(sm + kW2b + swz(16 * warp + g, nt, 128) + 4 * tg) = pack_bf16(w2[nt][0], w2[nt][1]);
-      *reinterpret_cast<uint32_t*>(sm + kW2b + swz(16 * warp + g + 8, nt, 128) + 4 * tg) =
+      *reinterpret_cast<uint32_t*>(base + swz(16 * warp + g, nt, 128) + 4 * tg) = pack_bf16(w2[nt][0], w2[nt][1]);
+      *reinterpret_cast<uint32_t*>(base + swz(16 * warp + g + 8, nt, 128) + 4 * tg) =
           pack_bf16(w2[nt][2], w2[nt][3]);
     }
   };
   store_w1();
-  store_w2();
+  store_w2(0);
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised and armed before anything is sent to it
 
@@ -184,77 +196,117 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&mk);
     prefetch_tmap(&mv);
     load_tile(0);
+    if (n_tiles > 1) load_tile(1);
   }
 
-  const uint32_t W1b = s0 + kW1b, W2b = s0 + kW2b, Ab = s0 + kAb, Aqb = s0 + kAqb, Gb = s0 + kGb, Sb = s0 + kSb;
-  const uint32_t gbar_peer[2] = {map_peer(smem_u32(&gfull[0]), peer), map_peer(smem_u32(&gfull[1]), peer)};
-  const uint32_t zbar_peer[2] = {map_peer(smem_u32(&zfull[0]), peer), map_peer(smem_u32(&zfull[1]), peer)};
-  bool ok = true;
-  bool late_fail = false;        // a wait of the previous tile's Z phase gave up
+  const uint32_t W1b = s0 + kW1b, Aqb = s0 + kAqb, Gb = s0 + kGb, Sb = s0 + kSb;
+  // The peer's exchange barriers (parity s at + 8 s bytes: the window maps offsets linearly).
+  const uint32_t gbar_peer = map_peer(smem_u32(&gfull[0]), peer), zbar_peer = map_peer(smem_u32(&zfull[0]), peer);
+
+  // Tile v's U = K W1, A = gelu(U) (into the A copy of its parity) and P = gelu'(U) (registers)
+  // for this warp's hidden units; warps 0 and 1 form one n-tile each of tril(Q K^T).
+  float cp[2][4], cq[2][4];
+  auto phase_u = [&](int v) {
+    const uint32_t sQ = s0 + kQKV + (v & 1) * 3 * kTileBytes, sK = sQ + kTileBytes;
+    float cu[2][4] = {};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) cq[nt][r] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t a[4], b[4], aq[4];
+      ldA(a, sK, 128, 0, 2 * ks, lane);
+      ldA(aq, sQ, 128, 0, 2 * ks, lane);
+      ldBT(b, W1b, kRowH, 16 * ks, 2 * warp, lane);
+      mma2(cu, a, b);
+      mma2(cq, aq, b);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) gelu2(cu[nt][r], cu[nt][r], cp[nt][r]);
+    st_tile(sm + kAb + (v & 1) * kAbBytes, kRowH, 0, warp, cu, lane);
+    if (warp < 2) {
+      const int nt = warp;
+      float cs[4] = {};
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[4], b[4];
+        ldA(a, sQ, 128, 0, 2 * ks, lane);
+        ldB(b, sK, 128, 0, 2 * ks, lane);
+        const uint32_t bn[2] = {nt ? b[2] : b[0], nt ? b[3] : b[1]};  // selects: no local copy of b
+        mma_bf16_16816(cs, a, bn);
+      }
+      const int c = 8 * nt + 2 * tg;  // keep column <= row (update, then read)
+      if (c > g) cs[0] = 0.f;
+      if (c + 1 > g) cs[1] = 0.f;
+      if (c > g + 8) cs[2] = 0.f;
+      if (c + 1 > g + 8) cs[3] = 0.f;
+      *reinterpret_cast<uint32_t*>(sm + kSb + swz(g, nt, 128) + 4 * tg) = pack_bf16(cs[0], cs[1]);
+      *reinterpret_cast<uint32_t*>(sm + kSb + swz(g + 8, nt, 128) + 4 * tg) = pack_bf16(cs[2], cs[3]);
+    }
+  };
+  // Tile v's stage has landed (bounded wait).
+  auto wait_stage = [&](int v) {
+    const bool got = mbar_wait_bounded(&full[v & 1], static_cast<uint32_t>(v >> 1) & 1u, p.timeout_ns);
+    if (!got) report_error(p.status, TTT_ERR_TIMEOUT, kWhereClLoad, unit);
+    fence_proxy_async_smem();
+    return got;
+  };
+  // Z of tile v for this CTA's 32 columns: the peer's blocks (bounded wait) and ours.
+  auto z_sum = [&](int v) {
+    const bool got = mbar_wait_bounded(&zfull[v & 1], static_cast<uint32_t>(v >> 1) & 1u, p.timeout_ns);
+    if (!got) {
+      report_error(p.status, TTT_ERR_TIMEOUT, kWhereClZ, unit);
+      return false;
+    }
+    const float* pz = partZ + (v & 1) * (kPartZBytes / 4);
+    const int t = tid >> 4, j = (tid & 15) * 2;
+    float2 z = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 w = *reinterpret_cast<const float2*>(pz + (q * 2 + (j >> 4)) * kBlk + blk_off(t, j & 15));
+      z.x += w.x;
+      z.y += w.y;
+    }
+    const int tt = v * kTile + t;
+    if (tt < p.T) {
+      __nv_bfloat16* Z = static_cast<__nv_bfloat16*>(p.Z) + (static_cast<size_t>(unit) * p.T + tt) * kD +
+                         32 * static_cast<int>(rank) + j;
+      *reinterpret_cast<uint32_t*>(Z) = pack_bf16(z.x, z.y);
+    }
+    return true;
+  };
+
+  // Neighbouring tiles overlap: tile u + 1's U/A/P/S (which needs only the W1 update of tile u)
+  // runs in the phase of tile u's Z partials, and tile u's Z sum in the phase of tile u + 1's
+  // G partials, so a tile takes four CTA barriers and neither exchange waits on its own phase.
+  bool ok = n_tiles > 0;
+  if (ok) {
+    const bool got = wait_stage(0);
+    if (__syncthreads_or(!got)) ok = false;
+    else phase_u(0);
+  }
+  bool stage_ok = true;
   for (int u = 0; ok && u < n_tiles; ++u) {
     const int s = u & 1;
     const uint32_t ph = static_cast<uint32_t>(u >> 1) & 1u;
     const uint32_t sQ = s0 + kQKV + s * 3 * kTileBytes, sK = sQ + kTileBytes;
     const uint8_t* sVp = sm + kQKV + s * 3 * kTileBytes + 2 * kTileBytes;
+    const uint32_t Ab = s0 + kAb + s * kAbBytes, W2b = s0 + kW2b + s * kW2bBytes;
     float* pg = partG + s * (kPartGBytes / 4);
     float* pz = partZ + s * (kPartZBytes / 4);
 
-    // Tile start: its data has landed; the stage of tile u - 1 and every buffer of the
-    // previous tile are free.
-    bool mine = mbar_wait_bounded(&full[s], ph, p.timeout_ns);
-    if (!mine) report_error(p.status, TTT_ERR_TIMEOUT, kWhereClLoad, unit);
-    fence_proxy_async_smem();
-    if (__syncthreads_or(!mine || late_fail)) {
+    // A, P and S of tile u are complete, the W2 copy of parity s holds tile u's start weights,
+    // and this CTA's Z blocks of tile u - 1 are written.
+    if (__syncthreads_or(!stage_ok)) {
       ok = false;
       break;
     }
-    if (tid == 0) {
-      if (u + 1 < n_tiles) load_tile(u + 1);
-      // Z blocks of tile u - 1 are read (all threads passed the barrier above): arm for tile u + 1.
-      if (u >= 1 && u + 1 < n_tiles) mbar_arrive_expect_tx(&zfull[s ^ 1], kZRecv);
-    }
 
-    // (1) U = K W1, A = gelu(U), P = gelu'(U) for this warp's hidden units; warps 0 and 1
-    //     form one n-tile each of tril(Q K^T).
-    float cp[2][4];
-    {
-      float cu[2][4] = {};
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t a[4], b[4];
-        ldA(a, sK, 128, 0, 2 * ks, lane);
-        ldBT(b, W1b, kRowH, 16 * ks, 2 * warp, lane);
-        mma2(cu, a, b);
-      }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) gelu2(cu[nt][r], cu[nt][r], cp[nt][r]);
-      st_tile(sm + kAb, kRowH, 0, warp, cu, lane);
-      if (warp < 2) {
-        const int nt = warp;
-        float cs[4] = {};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          uint32_t a[4], b[4];
-          ldA(a, sQ, 128, 0, 2 * ks, lane);
-          ldB(b, sK, 128, 0, 2 * ks, lane);
-          const uint32_t bn[2] = {b[2 * nt], b[2 * nt + 1]};
-          mma_bf16_16816(cs, a, bn);
-        }
-        const int c = 8 * nt + 2 * tg;  // keep column <= row (update, then read)
-        if (c > g) cs[0] = 0.f;
-        if (c + 1 > g) cs[1] = 0.f;
-        if (c > g + 8) cs[2] = 0.f;
-        if (c + 1 > g + 8) cs[3] = 0.f;
-        *reinterpret_cast<uint32_t*>(sm + kSb + swz(g, nt, 128) + 4 * tg) = pack_bf16(cs[0], cs[1]);
-        *reinterpret_cast<uint32_t*>(sm + kSb + swz(g + 8, nt, 128) + 4 * tg) = pack_bf16(cs[2], cs[3]);
-      }
-    }
-    __syncthreads();
-
-    // (2) This CTA's quarter kq = w >> 2 of G for value columns [16 np, +16), np = w & 3,
-    //     into quarter slot 2 rank + kq of both CTAs.
+    // (1) This CTA's quarter kq = w >> 2 of G for value columns [16 np, +16), np = w & 3,
+    //     into quarter slot 2 rank + kq of both CTAs; then tile u - 1's Z.
     {
       const int np = warp & 3, kq = warp >> 2;
       float cg[2][4] = {};
@@ -265,32 +317,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         ldBT(b, W2b, 128, 64 * kq + 16 * ks, 2 * np, lane);
         mma2(cg, a, b);
       }
-      float* dst = pg + (2 * static_cast<int>(rank) + kq) * kTile * kPad;
-      const uint32_t rdst = map_peer(smem_u32(dst), peer);
+      float* blk = pg + ((2 * static_cast<int>(rank) + kq) * 4 + np) * kBlk;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const int c = 16 * np + 8 * nt + 2 * tg;
-        *reinterpret_cast<float2*>(dst + g * kPad + c) = make_float2(cg[nt][0], cg[nt][1]);
-        *reinterpret_cast<float2*>(dst + (g + 8) * kPad + c) = make_float2(cg[nt][2], cg[nt][3]);
-        st_async_f2(rdst + (g * kPad + c) * 4, cg[nt][0], cg[nt][1], gbar_peer[s]);
-        st_async_f2(rdst + ((g + 8) * kPad + c) * 4, cg[nt][2], cg[nt][3], gbar_peer[s]);
+        const int c = 8 * nt + 2 * tg;
+        *reinterpret_cast<float2*>(blk + blk_off(g, c)) = make_float2(cg[nt][0], cg[nt][1]);
+        *reinterpret_cast<float2*>(blk + blk_off(g + 8, c)) = make_float2(cg[nt][2], cg[nt][3]);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) bulk_to_peer(map_peer(smem_u32(blk), peer), smem_u32(blk), kBlk * 4, gbar_peer + 8u * s);
     }
-    // The peer's two quarters (bounded wait on their bytes) and this CTA's (the barrier).
-    mine = mbar_wait_bounded(&gfull[s], ph, p.timeout_ns);
-    if (!mine) report_error(p.status, TTT_ERR_TIMEOUT, kWhereClG, unit);
-    if (__syncthreads_or(!mine)) {
+    const bool zok = u == 0 || z_sum(u - 1);
+    // The peer's two quarters of G (bounded wait) and this CTA's (the barrier).
+    const bool gok = mbar_wait_bounded(&gfull[s], ph, p.timeout_ns);
+    if (!gok) report_error(p.status, TTT_ERR_TIMEOUT, kWhereClG, unit);
+    if (__syncthreads_or(!gok || !zok)) {
       ok = false;
       break;
     }
+    // The Z blocks of tile u - 1 are read: arm their slots for tile u + 1.
+    if (tid == 0 && u >= 1 && u + 1 < n_tiles) mbar_arrive_expect_tx(&zfull[s ^ 1], kZRecv);
 
-    // (3) G = the sum of the four quarters - V, bf16 (four columns per thread).
+    // (2) G = the sum of the four quarters - V, bf16 (four columns per thread).
     {
       const int t = tid >> 4, j = (tid & 15) * 4;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(pg + q * kTile * kPad + t * kPad + j);
+        const float4 v = *reinterpret_cast<const float4*>(pg + (q * 4 + (j >> 4)) * kBlk + blk_off(t, j & 15));
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -305,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The G slots of this parity are read: arm them for tile u + 2.
     if (tid == 0 && u + 2 < n_tiles) mbar_arrive_expect_tx(&gfull[s], kGRecv);
 
-    // (4) D = (G W2^T) .* P and the W2 update; Hq, Aq and the W1 update (this warp's hidden units).
+    // (3) D = (G W2^T) .* P and the W2 update; Hq, Aq and the W1 update (this warp's hidden units).
     uint32_t bd[4];
     {
       float cd[2][4] = {};
@@ -340,14 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     {
-      float ch[2][4] = {}, cs[2][4] = {};
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t a[4], b[4];
-        ldA(a, sQ, 128, 0, 2 * ks, lane);
-        ldBT(b, W1b, kRowH, 16 * ks, 2 * warp, lane);
-        mma2(ch, a, b);
-      }
+      float cs[2][4] = {};
       {
         uint32_t a[4];
         ldA(a, Sb, 128, 0, 0, lane);
@@ -356,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) ch[nt][r] = gelu1(fmaf(-eta, cs[nt][r], ch[nt][r]));
-      st_tile(sm + kAqb, kRowH, 0, warp, ch, lane);
+        for (int r = 0; r < 4; ++r) cq[nt][r] = gelu1(fmaf(-eta, cs[nt][r], cq[nt][r]));
+      st_tile(sm + kAqb, kRowH, 0, warp, cq, lane);
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         uint32_t a[4];
@@ -373,9 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // This warp's columns of the W1 copy are read by this warp alone: rewrite them now.
     __syncwarp();
     store_w1();
-    __syncthreads();  // Aq complete
+    __syncthreads();  // Aq complete; the stage of tile u is read
+    if (tid == 0 && u + 2 < n_tiles) load_tile(u + 2);
 
-    // (5) Quarter kq's block of Z for value columns [16 np, +16) (with its block of
+    // (4) Quarter kq's block of Z for value columns [16 np, +16) (with its block of
     //     tril(Aq A^T) applied to G), to the CTA that writes those columns: np < 2 rank 0.
     {
       const int np = warp & 3, kq = warp >> 2;
@@ -402,47 +451,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t bg[4];
       ldBT(bg, Gb, 128, 0, 2 * np, lane);
       mma2(cz, sa, bg);
-      float* dst = pz + (2 * static_cast<int>(rank) + kq) * kTile * kPadZ;
+      // Its slot in the owner's Z blocks; a block for the peer is staged here first.
+      float* slot = pz + ((2 * static_cast<int>(rank) + kq) * 2 + (np & 1)) * kBlk;
       const bool local = static_cast<uint32_t>(np >> 1) == rank;
-      const uint32_t rdst = map_peer(smem_u32(dst), peer);
+      float* blk = local ? slot : reinterpret_cast<float*>(sm + kZStage + s * kZStageBytes) + (kq * 2 + (np & 1)) * kBlk;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const int c = 16 * (np & 1) + 8 * nt + 2 * tg;
-        if (local) {
-          *reinterpret_cast<float2*>(dst + g * kPadZ + c) = make_float2(cz[nt][0], cz[nt][1]);
-          *reinterpret_cast<float2*>(dst + (g + 8) * kPadZ + c) = make_float2(cz[nt][2], cz[nt][3]);
-        } else {
-          st_async_f2(rdst + (g * kPadZ + c) * 4, cz[nt][0], cz[nt][1], zbar_peer[s]);
-          st_async_f2(rdst + ((g + 8) * kPadZ + c) * 4, cz[nt][2], cz[nt][3], zbar_peer[s]);
-        }
+        const int c = 8 * nt + 2 * tg;
+        *reinterpret_cast<float2*>(blk + blk_off(g, c)) = make_float2(cz[nt][0], cz[nt][1]);
+        *reinterpret_cast<float2*>(blk + blk_off(g + 8, c)) = make_float2(cz[nt][2], cz[nt][3]);
+      }
+      if (!local) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) bulk_to_peer(map_peer(smem_u32(slot), peer), smem_u32(blk), kBlk * 4, zbar_peer + 8u * s);
       }
     }
-    __syncthreads();  // every read of this tile's W2, A, Aq and G copies is done; our Z blocks are written
-    store_w2();       // this warp's rows of the updated W2
-
-    // Z of this CTA's 32 columns: the peer's blocks (bounded wait) and ours.
-    mine = mbar_wait_bounded(&zfull[s], ph, p.timeout_ns);
-    if (!mine) {
-      report_error(p.status, TTT_ERR_TIMEOUT, kWhereClZ, unit);
-      late_fail = true;
-    } else {
-      const int t = tid >> 4, j = (tid & 15) * 2;
-      float2 z = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 v = *reinterpret_cast<const float2*>(pz + q * kTile * kPadZ + t * kPadZ + j);
-        z.x += v.x;
-        z.y += v.y;
-      }
-      const int tt = u * kTile + t;
-      if (tt < p.T) {
-        __nv_bfloat16* Z = static_cast<__nv_bfloat16*>(p.Z) + (static_cast<size_t>(unit) * p.T + tt) * kD +
-                           32 * static_cast<int>(rank) + j;
-        *reinterpret_cast<uint32_t*>(Z) = pack_bf16(z.x, z.y);
-      }
+    // Tile u + 1's U/A/P/S, and this warp's rows of the updated W2 into the copy of parity s ^ 1
+    // (its last reads, tile u - 1's, preceded this tile's first barrier).
+    if (u + 1 < n_tiles) {
+      stage_ok = wait_stage(u + 1);
+      if (stage_ok) phase_u(u + 1);
     }
+    store_w2(s ^ 1);
   }
-  if (late_fail) ok = false;
+  // The last tile's Z: this CTA's blocks are written (the barrier), the peer's are awaited.
+  __syncthreads();
+  if (ok && !z_sum(n_tiles - 1)) ok = false;
   // TMA loads still in flight when a wait gave up must land before the CTA exits.
   if (!ok && tid == 0)
     for (int v = issued > 2 ? issued - 2 : 0; v < issued; ++v)

@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a[4], b[4];
         ldA(a, sQ, 128, 0, 2 * ks, lane);
         ldB(b, sK, 128, 0, 2 * ks, lane);
-        const uint32_t bn[2] = {b[2 * nt], b[2 * nt + 1]};
+        const uint32_t bn[2] = {nt ? b[2] : b[0], nt ? b[3] : b[1]};  // selects: no local copy of b
         mma_bf16_16816(cs, a, bn);
       }
       const int c = 8 * nt + 2 * tg;  // keep column <= row (update, then read)
@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a[4], b[4];
         ldA(a, sQ, 128, 0, 2 * ks, lane);
         ldB(b, sK, 128, 0, 2 * ks, lane);
-        const uint32_t bn[2] = {b[2 * nt], b[2 * nt + 1]};
+        const uint32_t bn[2] = {nt ? b[2] : b[0], nt ? b[3] : b[1]};  // selects: no local copy of b
         mma_bf16_16816(cs, a, bn);
       }
       const int c = 8 * nt + 2 * tg;  // keep column <= row (update, then read)
