@@ -56,12 +56,13 @@ constexpr int kAqb = kAb + 2 * kAbBytes;                 // Aq, bf16 [16][128]
 constexpr int kGb = kAqb + kTile * kRowH;                // G, bf16 [16][64]
 constexpr int kSb = kGb + kTile * 128;                   // tril(Q K^T), bf16 [16][16] in 128-byte rows
 constexpr int kBlk = kTile * 16;                         // floats of a 16 x 16 fp32 block (1 KB)
+constexpr int kBlkS = kBlk + 16;                         // block stride: neighbouring blocks 64 B apart in banks
 constexpr int kPartG = kSb + kTile * 128;                // [2 parity][4 quarters][4 column blocks] blocks
-constexpr int kPartGBytes = 16 * kBlk * 4;
+constexpr int kPartGBytes = 16 * kBlkS * 4;
 constexpr int kPartZ = kPartG + 2 * kPartGBytes;         // [2 parity][4 quarters][2 column blocks] blocks
-constexpr int kPartZBytes = 8 * kBlk * 4;
+constexpr int kPartZBytes = 8 * kBlkS * 4;
 constexpr int kZStage = kPartZ + 2 * kPartZBytes;        // [2 parity][2 quarters][2 column blocks]: Z for the peer
-constexpr int kZStageBytes = 4 * kBlk * 4;
+constexpr int kZStageBytes = 4 * kBlkS * 4;
 constexpr int kBar = kZStage + 2 * kZStageBytes;         // full[2], gfull[2], zfull[2]
 constexpr int kSmemBytes = kBar + 64 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "fits one CTA per SM");
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2 z = make_float2(0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float2 w = *reinterpret_cast<const float2*>(pz + (q * 2 + (j >> 4)) * kBlk + blk_off(t, j & 15));
+      const float2 w = *reinterpret_cast<const float2*>(pz + (q * 2 + (j >> 4)) * kBlkS + blk_off(t, j & 15));
       z.x += w.x;
       z.y += w.y;
     }
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ldBT(b, W2b, 128, 64 * kq + 16 * ks, 2 * np, lane);
         mma2(cg, a, b);
       }
-      float* blk = pg + ((2 * static_cast<int>(rank) + kq) * 4 + np) * kBlk;
+      float* blk = pg + ((2 * static_cast<int>(rank) + kq) * 4 + np) * kBlkS;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         const int c = 8 * nt + 2 * tg;
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float4 v = *reinterpret_cast<const float4*>(pg + (q * 4 + (j >> 4)) * kBlk + blk_off(t, j & 15));
+        const float4 v = *reinterpret_cast<const float4*>(pg + (q * 4 + (j >> 4)) * kBlkS + blk_off(t, j & 15));
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -452,9 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ldBT(bg, Gb, 128, 0, 2 * np, lane);
       mma2(cz, sa, bg);
       // Its slot in the owner's Z blocks; a block for the peer is staged here first.
-      float* slot = pz + ((2 * static_cast<int>(rank) + kq) * 2 + (np & 1)) * kBlk;
+      float* slot = pz + ((2 * static_cast<int>(rank) + kq) * 2 + (np & 1)) * kBlkS;
       const bool local = static_cast<uint32_t>(np >> 1) == rank;
-      float* blk = local ? slot : reinterpret_cast<float*>(sm + kZStage + s * kZStageBytes) + (kq * 2 + (np & 1)) * kBlk;
+      float* blk = local ? slot : reinterpret_cast<float*>(sm + kZStage + s * kZStageBytes) + (kq * 2 + (np & 1)) * kBlkS;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         const int c = 8 * nt + 2 * tg;
