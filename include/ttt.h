@@ -83,7 +83,10 @@ typedef enum {
 typedef struct {
   uint64_t wait_timeout_ns; /* limit for every wait inside a kernel; 0 = 2 s */
   int32_t inject_stall;     /* test hook: 1 = the load pipeline never fills, so the
-                               consumers' bounded wait must run out (TTT_ERR_TIMEOUT) */
+                               consumers' bounded wait must run out (TTT_ERR_TIMEOUT);
+                               2 = TTT-MLP on two CTAs per unit: the second CTA never
+                               sends its G partials, so the first CTA's exchange wait
+                               must run out (TTT_ERR_TIMEOUT) */
   int32_t force_path;       /* 0 = automatic; 1 = general fp32 SIMT kernel;
                                2 = tensor-core kernel, one pass per sequence;
                                3 = tensor-core kernels, segment-parallel form.

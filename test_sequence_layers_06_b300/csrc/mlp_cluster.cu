@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, u * kTile, unit);
     issued = u + 1;
   };
-  if (tid == 0 && n_tiles > 0) {
+  if (tid == 0 && n_tiles > 0 && p.inject_stall != 1) {  // test hook: the loads never start
     prefetch_tmap(&mq);
     prefetch_tmap(&mk);
     prefetch_tmap(&mv);
@@ -327,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) bulk_to_peer(map_peer(smem_u32(blk), peer), smem_u32(blk), kBlk * 4, gbar_peer + 8u * s);
+      // (Test hook 2: the second CTA withholds its G blocks, so the first CTA's exchange wait runs out.)
+      if (lane == 0 && !(p.inject_stall == 2 && rank == 1))
+        bulk_to_peer(map_peer(smem_u32(blk), peer), smem_u32(blk), kBlk * 4, gbar_peer + 8u * s);
     }
     const bool zok = u == 0 || z_sum(u - 1);
     // The peer's two quarters of G (bounded wait) and this CTA's (the barrier).

@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_3d(st + kTileBytes, &mk, &full[s], 0, u * kTile, unit);
     tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, u * kTile, unit);
   };
-  if (tid == 0 && n_tiles > 0) {
+  if (tid == 0 && n_tiles > 0 && p.inject_stall != 1) {  // test hook: the loads never start
     prefetch_tmap(&mq);
     prefetch_tmap(&mk);
     prefetch_tmap(&mv);
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, u * kTile, unit);
     issued = u + 1;
   };
-  if (tid == 0 && n_tiles > 0) {
+  if (tid == 0 && n_tiles > 0 && p.inject_stall != 1) {  // test hook: the loads never start
     prefetch_tmap(&mq);
     prefetch_tmap(&mk);
     prefetch_tmap(&mv);

@@ -102,3 +102,25 @@ def test_mlp_two_ctas_refused_where_they_do_not_apply():
     t = torch_inputs(synth.make_inputs(w))
     with pytest.raises(ttt.TTTError):
         ttt.ttt_mlp_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W1"], t["W2"], 32, options={"force_path": 3})
+
+
+@pytest.mark.parametrize("stall,path,b", [(1, 3, 16), (2, 3, 16), (1, ttt.PATH_TENSOR, 16), (1, ttt.PATH_TENSOR, 32)])
+def test_mlp_bounded_waits_report_timeout_and_context_survives(stall, path, b):
+    """A wait that nothing will end runs out after 1 ms: the loads never start (1), or the second
+    CTA of each cluster withholds its G partials (2). The kernel returns, the status says
+    TTT_ERR_TIMEOUT, reading clears it, and the next call on the same context matches the oracle."""
+    w = W["mlp_125m"].with_(B=1, H=2, T=64, seed=520 + stall)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    args = (t["Q"], t["K"], t["V"], t["eta"], t["W1"], t["W2"], b)
+    ws = torch.zeros(max(ttt.ttt_workspace_bytes(w.B, w.H, w.T, w.d, b, ttt.TTT_VARIANT_MLP), 256),
+                     dtype=torch.uint8, device="cuda")
+    ttt.ttt_mlp_fwd(*args, workspace=ws,
+                    options={"inject_stall": stall, "wait_timeout_ns": 1_000_000, "force_path": path})
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_ERR_TIMEOUT
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    Z, W1, W2 = ttt.ttt_mlp_fwd(*args, workspace=ws, options={"force_path": path})
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    Zr, W1r, W2r = oracle_mlp(inp, b)
+    for name, x, r in (("Z", Z, Zr), ("W1", W1, W1r), ("W2", W2, W2r)):
+        assert rel_err(f"after timeout {name}", to64(x), r, tolerance(w)) <= tolerance(w), name
