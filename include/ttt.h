@@ -306,7 +306,8 @@ TTT_API ttt_status ttt_linear_token_eta_fwd(const void* Q, const void* K, const 
  * waits and, for the per-token rate, TTT_ERR_DEVICE_CHECK when some eta_t < 0
  * (that unit's results are then undefined).
  * ttt_linear_variant_workspace_bytes returns 0 for bad sizes or a variant
- * without an *_ex call (TTT_INNER_LN, TTT_INNER_MOMENTUM).
+ * without an *_ex call (TTT_INNER_LN); for TTT_INNER_MOMENTUM it is the status
+ * word alone.
  */
 TTT_API size_t ttt_linear_variant_workspace_bytes(int variant, ttt_dtype dt, int B, int H, int T, int d, int b);
 
@@ -341,6 +342,28 @@ TTT_API ttt_status ttt_linear_momentum_fwd(const void* Q, const void* K, const v
                                            const float* alpha, const float* beta, const float* W0, int B,
                                            int H, int T, int d, int b, void* Z, float* W_out, float* M_out,
                                            void* stream);
+
+/* ttt_linear_momentum_fwd_ex: the same layer; with bf16 operands, d = 64 and
+ * b = 16 it runs on the tensor cores (one CTA per (batch row, head), W and M
+ * resident as fp32 accumulator fragments; bf16 operands of every product), in
+ * the closed form of a chunk: E = K W_a - V,
+ *   Z = Q W_a - alpha c .* (Q M_a) - alpha (tril(Q K^T) .* D) E,
+ *   c_s = beta + ... + beta^s,  D[s][i] = 1 - beta^(s-i+1),
+ * and at the chunk end (n tokens) W = W_a - alpha (c_n M_a + K^T (d .* E)),
+ * M = beta^n M_a + (1 - beta) K^T (w .* E), d_i = 1 - beta^(n-i+1),
+ * w_i = beta^(n-i). Otherwise it runs the fp32 variant kernel like the plain
+ * call. workspace: ttt_linear_variant_workspace_bytes(TTT_INNER_MOMENTUM, ...)
+ * bytes (the status word; 16-byte aligned, disjoint from every input and
+ * output); ttt_last_device_status(workspace, stream) reports the tensor
+ * kernel's bounded waits. opt may be NULL: wait_timeout_ns and inject_stall
+ * as for ttt_linear_fwd_ex; force_path 1 = the fp32 kernel, 2 = the tensor
+ * kernel (TTT_ERR_UNSUPPORTED where it cannot serve, and for T = 0), 3 =
+ * TTT_ERR_UNSUPPORTED (no segment-parallel form). */
+TTT_API ttt_status ttt_linear_momentum_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                              const float* alpha, const float* beta, const float* W0, int B,
+                                              int H, int T, int d, int b, void* Z, float* W_out, float* M_out,
+                                              void* workspace, size_t ws_bytes, void* stream,
+                                              const ttt_options* opt);
 
 /*
  * Backward of ttt_linear_fwd: the vector-Jacobian product of (Z, W_out) with

@@ -189,3 +189,52 @@ def test_fast_token_eta_reports_a_negative_rate():
                                        workspace=ws)
     assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
     check("Z,W_out", got, token_eta_primal(inp.q64, inp.k64, inp.v64, et, inp.W0_64, 16), w)
+
+
+FAST_MOM = [(1, 2, 1, 0.6), (1, 2, 3, 0.6), (2, 3, 16, 0.9), (2, 3, 37, 0.5), (1, 2, 100, 0.0), (1, 2, 1024, 0.8),
+            (1, 2, 2048, 0.95)]
+
+
+@pytest.mark.parametrize("B,H,T,beta", FAST_MOM)
+def test_momentum_fast_path_matches_oracle(B, H, T, beta):
+    """bf16, d = 64, b = 16 on the tensor-core momentum kernel (forced, so that no other kernel can
+    serve): a single short chunk, ragged last chunks, beta = 0 (plain TTT-Linear with the last
+    token's gradient as M), strong momentum, and sequences of 64 and 128 chunks."""
+    w, inp, t = inputs(64, T, "bf16", 800 + T, B=B, H=H)
+    alpha = np.linspace(0.05, 0.15, H).astype(np.float32)
+    betas = (beta * (1.0 - 0.05 * np.arange(H))).astype(np.float32)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    got = ttt.ttt_linear_momentum_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(alpha).cuda(),
+                                      torch.from_numpy(betas).cuda(), t["W0"], 16, fast=True, workspace=ws,
+                                      options={"force_path": ttt.PATH_TENSOR})
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    want = momentum_primal(inp.q64, inp.k64, inp.v64, alpha, betas, inp.W0_64, 16)
+    check("Z,W_out,M_out", got, want, w)
+
+
+def test_momentum_fast_call_takes_the_variant_kernel_elsewhere():
+    """fp32 operands (or d != 64, b != 16): ttt_linear_momentum_fwd_ex runs the fp32 variant kernel
+    and matches the oracle at the fp32 bar."""
+    w, inp, t = inputs(32, 45, "f32", 820)
+    alpha = np.full(w.H, 0.1, np.float32)
+    betas = np.full(w.H, 0.7, np.float32)
+    got = ttt.ttt_linear_momentum_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(alpha).cuda(),
+                                      torch.from_numpy(betas).cuda(), t["W0"], 16, fast=True)
+    torch.cuda.synchronize()
+    check("Z,W_out,M_out", got, momentum_primal(inp.q64, inp.k64, inp.v64, alpha, betas, inp.W0_64, 16), w)
+
+
+def test_momentum_fast_path_bounded_wait_reports_timeout():
+    """The load pipeline never fills: the tensor kernel's waits run out after 1 ms, the status says
+    TTT_ERR_TIMEOUT, reading clears it, and the next call on the same context matches the oracle."""
+    w, inp, t = inputs(64, 64, "bf16", 830, B=1, H=2)
+    alpha, betas = np.full(w.H, 0.1, np.float32), np.full(w.H, 0.8, np.float32)
+    args = (t["Q"], t["K"], t["V"], torch.from_numpy(alpha).cuda(), torch.from_numpy(betas).cuda(), t["W0"], 16)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ttt.ttt_linear_momentum_fwd(*args, fast=True, workspace=ws,
+                                options={"inject_stall": 1, "wait_timeout_ns": 1_000_000, "force_path": ttt.PATH_TENSOR})
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_ERR_TIMEOUT
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    got = ttt.ttt_linear_momentum_fwd(*args, fast=True, workspace=ws)
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    check("Z,W_out,M_out", got, momentum_primal(inp.q64, inp.k64, inp.v64, alpha, betas, inp.W0_64, 16), w)
