@@ -610,11 +610,17 @@ def bench_extras(ttt, dev, stream):
     hbm_gbs, tflops, _ = measured_peaks()
     out = {}
 
-    def t_ms(fn, n):
+    def t_ms(fn, n, ahead=True):
+        """Device time per call. With `ahead`, a bounded sleep kernel (torch's, a fixed cycle count)
+        holds the stream while the n calls are enqueued, so the host cost of the binding does not
+        show in the device time of short calls."""
         for _ in range(2):
             fn()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if ahead:
+            with torch.cuda.stream(stream):
+                torch.cuda._sleep(int(4e6) * (n + 1))  # about 2 ms per call at 2 GHz
         a.record(stream)
         for _ in range(n):
             fn()
@@ -796,7 +802,8 @@ def bench_extras(ttt, dev, stream):
         Wa = torch.zeros(1, 32, 64, 64, device=dev)
         Wr = torch.zeros(1, 32, 64, 64, device=dev)
         e32 = torch.full((32,), 0.1, device=dev)
-        ms = t_ms(lambda: ttt.ttt_linear_decode_step(q, q, q, e32, Wa, Wr, 5, 16, stream=stream), 200)
+        ms = t_ms(lambda: ttt.ttt_linear_decode_step(q, q, q, e32, Wa, Wr, 5, 16, stream=stream), 200,
+                  ahead=False)
         # The same 100 tokens replayed from a CUDA graph: the GPU-side cost per token
         # without the Python call overhead of the loop above.
         z = torch.empty_like(q)
