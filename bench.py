@@ -701,23 +701,30 @@ def bench_extras(ttt, dev, stream):
                 "note": f"B1 H32 T131072 d{d} bf16: changed inputs (padded to 64 features) through the "
                         "tensor-core segment-parallel path; bytes counted at d"}
             del Q, K, V, vws
-        # Momentum on its tensor-core kernel (bf16, d = 64, b = 16, one CTA per unit).
+        # Momentum and LN + residual on their tensor-core kernels (bf16, d = 64, b = 16, one CTA per unit).
         for wname, tag in (("linear_small", "small"), ("linear_125m", "125m")):
             w = synth.WORKLOADS[wname]
             inp, Q, K, V, eta = dev_inputs(w)
             W0 = torch.from_numpy(inp.W0).to(dev)
             mbeta = torch.full((w.H,), 0.9, dtype=torch.float32, device=dev)
+            gam, lnb = torch.ones((w.H, w.d), device=dev), torch.zeros((w.H, w.d), device=dev)
             mws = torch.zeros(256, dtype=torch.uint8, device=dev)
-            fn = lambda: ttt.ttt_linear_momentum_fwd(Q, K, V, eta, mbeta, W0, 16, stream=stream, fast=True,
-                                                     workspace=mws, options={"force_path": ttt.PATH_TENSOR})
-            ms = t_ms(fn, 5)
-            if ttt.ttt_last_device_status(mws, stream) != 0:
-                raise RuntimeError("momentum: device status not OK")
-            out[f"variant_momentum_fast_{tag}_b16"] = {
-                "ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
-                "hbm_frac": round(algorithmic_bytes(w) / (ms * 1e-3) / 1e9 / hbm_gbs, 4),
-                "note": f"B{w.B} H{w.H} T{w.T} d64 bf16, beta 0.9: tensor-core momentum kernel, one CTA per "
-                        "(batch row, head)"}
+            fns = {"momentum": (lambda: ttt.ttt_linear_momentum_fwd(Q, K, V, eta, mbeta, W0, 16, stream=stream,
+                                                                    fast=True, workspace=mws,
+                                                                    options={"force_path": ttt.PATH_TENSOR}),
+                                "beta 0.9: tensor-core momentum kernel"),
+                   "ln_residual": (lambda: ttt.ttt_linear_ln_fwd(Q, K, V, eta, W0, gam, lnb, 16, stream=stream,
+                                                                 fast=True, workspace=mws,
+                                                                 options={"force_path": ttt.PATH_TENSOR}),
+                                   "tensor-core LN + residual kernel")}
+            for vname, (fn, what) in fns.items():
+                ms = t_ms(fn, 5)
+                if ttt.ttt_last_device_status(mws, stream) != 0:
+                    raise RuntimeError(f"{vname}: device status not OK")
+                out[f"variant_{vname}_fast_{tag}_b16"] = {
+                    "ms": round(ms, 3), "token_heads_per_s": w.token_heads / (ms * 1e-3),
+                    "hbm_frac": round(algorithmic_bytes(w) / (ms * 1e-3) / 1e9 / hbm_gbs, 4),
+                    "note": f"B{w.B} H{w.H} T{w.T} d64 bf16, {what}, one CTA per (batch row, head)"}
             del Q, K, V
     except Exception as exc:  # reported in the line, never silently dropped
         out["variants"] = {"error": f"{type(exc).__name__}: {exc}"}

@@ -305,9 +305,8 @@ TTT_API ttt_status ttt_linear_token_eta_fwd(const void* Q, const void* K, const 
  * ttt_last_device_status(workspace, stream) reports the inner forward's bounded
  * waits and, for the per-token rate, TTT_ERR_DEVICE_CHECK when some eta_t < 0
  * (that unit's results are then undefined).
- * ttt_linear_variant_workspace_bytes returns 0 for bad sizes or a variant
- * without an *_ex call (TTT_INNER_LN); for TTT_INNER_MOMENTUM it is the status
- * word alone.
+ * ttt_linear_variant_workspace_bytes returns 0 for bad sizes or an unknown
+ * variant; for TTT_INNER_LN and TTT_INNER_MOMENTUM it is the status word alone.
  */
 TTT_API size_t ttt_linear_variant_workspace_bytes(int variant, ttt_dtype dt, int B, int H, int T, int d, int b);
 
@@ -330,6 +329,23 @@ TTT_API ttt_status ttt_linear_ln_fwd(const void* Q, const void* K, const void* V
                                      const float* eta, const float* W0, const float* gamma,
                                      const float* beta, int B, int H, int T, int d, int b, void* Z,
                                      float* W_out, void* stream);
+
+/* ttt_linear_ln_fwd_ex: the same layer; with bf16 operands, d = 64 and b = 16 it
+ * runs on the tensor cores (one CTA per (batch row, head), W resident as fp32
+ * accumulator fragments, bf16 operands of every product; each token's layer-norm
+ * statistics summed over the 64 features across the CTA's warps), in the chunk's
+ * form: Y = K W_a, x = (Y - mean) / s, g = gamma (K + gamma x + beta - V),
+ * E = (g - mean(g) - x mean(g x)) / s, X = Q W_a - eta tril(Q K^T) E,
+ * Z = Q + LN(X), W = W_a - eta K^T E. Otherwise it runs the fp32 variant kernel
+ * like the plain call. workspace: ttt_linear_variant_workspace_bytes(
+ * TTT_INNER_LN, ...) bytes (the status word; 16-byte aligned, disjoint from every
+ * input and output); ttt_last_device_status reports the tensor kernel's bounded
+ * waits. opt may be NULL; its fields as for ttt_linear_momentum_fwd_ex. */
+TTT_API ttt_status ttt_linear_ln_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt,
+                                        const float* eta, const float* W0, const float* gamma,
+                                        const float* beta, int B, int H, int T, int d, int b, void* Z,
+                                        float* W_out, void* workspace, size_t ws_bytes, void* stream,
+                                        const ttt_options* opt);
 
 /* ttt_linear_momentum_fwd: momentum gradient descent with chunk-start
  * gradients ("推理时的“临阵磨枪”：Test-Time Training如何教会AI“边做边学”",

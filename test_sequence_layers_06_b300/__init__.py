@@ -8,7 +8,7 @@ library is missing or no GPU is present the calls fail loudly.
 
 Names match the C entry points: ttt_workspace_bytes(_ex), ttt_linear_plan, ttt_linear_fwd,
 ttt_linear_bias_fwd, ttt_linear_token_eta_fwd, ttt_linear_ln_fwd, ttt_linear_momentum_fwd,
-ttt_linear_variant_workspace_bytes (the bias, per-token-rate and momentum *_ex calls are reached through fast=True),
+ttt_linear_variant_workspace_bytes (the variants' *_ex calls are reached through fast=True),
 ttt_mlp_fwd, ttt_mlp_fwd_noalloc, ttt_mlp_noalloc_last_device_status, ttt_linear_decode_step, ttt_linear_bwd_workspace_bytes,
 ttt_linear_bwd, ttt_mlp_bwd_workspace_bytes, ttt_mlp_bwd, ttt_last_device_status, ttt_status_str. The *_fwd_ex forms are reached
 through the options argument.
@@ -33,7 +33,8 @@ EXPORTS = ("ttt_workspace_bytes", "ttt_workspace_bytes_ex", "ttt_linear_plan", "
            "ttt_last_device_status", "ttt_status_str", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
            "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode",
            "ttt_linear_variant_workspace_bytes", "ttt_linear_bias_fwd_ex", "ttt_linear_token_eta_fwd_ex",
-           "ttt_mlp_bwd_workspace_bytes", "ttt_mlp_bwd", "ttt_linear_momentum_fwd_ex")
+           "ttt_mlp_bwd_workspace_bytes", "ttt_mlp_bwd", "ttt_linear_momentum_fwd_ex",
+           "ttt_linear_ln_fwd_ex")
 
 
 class TTTError(RuntimeError):
@@ -99,12 +100,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ttt_linear_bias_fwd_ex.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
     lib.ttt_linear_token_eta_fwd_ex.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, vp, vp, sz, vp]
     lib.ttt_linear_momentum_fwd_ex.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp, vp]
+    lib.ttt_linear_ln_fwd_ex.argtypes = [vp, vp, vp, i, vp, vp, vp, vp, i, i, i, i, i, vp, vp, vp, sz, vp, vp]
     lib.ttt_status_str.argtypes = [i]
     lib.ttt_status_str.restype = ctypes.c_char_p
     for f in ("ttt_linear_fwd", "ttt_linear_fwd_ex", "ttt_mlp_fwd", "ttt_mlp_fwd_ex", "ttt_mlp_fwd_noalloc",
               "ttt_mlp_noalloc_last_device_status", "ttt_linear_bias_fwd", "ttt_linear_token_eta_fwd",
               "ttt_linear_ln_fwd", "ttt_linear_momentum_fwd", "ttt_linear_decode", "ttt_linear_bias_fwd_ex",
-              "ttt_linear_token_eta_fwd_ex", "ttt_linear_momentum_fwd_ex", "ttt_mlp_bwd",
+              "ttt_linear_token_eta_fwd_ex", "ttt_linear_momentum_fwd_ex", "ttt_linear_ln_fwd_ex", "ttt_mlp_bwd",
               "ttt_linear_decode_step", "ttt_linear_bwd", "ttt_last_device_status"):
         getattr(lib, f).restype = i
     _lib = lib
@@ -371,15 +373,24 @@ def ttt_linear_token_eta_fwd(Q, K, V, eta_tok, W0, b: int, stream=None, fast=Fal
     return Z, W_out
 
 
-def ttt_linear_ln_fwd(Q, K, V, eta, W0, gamma, beta, b: int, stream=None):
-    """TTT-Linear with f(k) = k + LN(k W) (gamma, beta [H, d]); returns (Z, W_out)."""
+def ttt_linear_ln_fwd(Q, K, V, eta, W0, gamma, beta, b: int, stream=None, fast=False, workspace=None,
+                      options=None):
+    """TTT-Linear with f(k) = k + LN(k W) (gamma, beta [H, d]); returns (Z, W_out). fast=True calls
+    ttt_linear_ln_fwd_ex (the tensor-core kernel for bf16, d = 64, b = 16), with `options` passed
+    through."""
     import torch
     B, H, T, d, dev, Z, W_out = _variant_prologue(Q, K, V, W0)
     _check(eta, "eta", torch.float32, (H,), dev)
     _check(gamma, "gamma", torch.float32, (H, d), dev)
     _check(beta, "beta", torch.float32, (H, d), dev)
-    _variant_call("ttt_linear_ln_fwd", _p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), _p(gamma), _p(beta), B,
-                  H, T, d, int(b), _p(Z), _p(W_out), _stream_ptr(stream, dev), dev=dev)
+    args = (_p(Q), _p(K), _p(V), _dtype_code(Q), _p(eta), _p(W0), _p(gamma), _p(beta), B, H, T, d, int(b), _p(Z),
+            _p(W_out))
+    if fast:
+        ws = _variant_workspace(TTT_INNER_LN, Q, B, H, T, d, b, dev, workspace)
+        _variant_call("ttt_linear_ln_fwd_ex", *args, _p(ws), ws.numel(), _stream_ptr(stream, dev), _opts(options),
+                      dev=dev)
+    else:
+        _variant_call("ttt_linear_ln_fwd", *args, _stream_ptr(stream, dev), dev=dev)
     return Z, W_out
 
 

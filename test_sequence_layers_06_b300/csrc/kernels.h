@@ -173,6 +173,28 @@ int linear_mom_mma_tile_rows();
 cudaError_t launch_linear_mom_mma(const MomParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                   const CUtensorMap& mv, cudaStream_t stream);
 
+// The layer-norm + residual variant on the tensor cores (linear_ln_mma.cu): bf16, d = 64,
+// b = 16, one CTA per (batch row, head).
+struct LnParams {
+  const void* Q;          // [units][T][64] bf16
+  const void* K;
+  const void* V;
+  void* Z;
+  const float* eta;       // [H]
+  const float* gamma;     // [H][64]
+  const float* beta;      // [H][64]
+  const float* W0;        // [H][64][64]
+  float* W_out;           // [units][64][64]
+  int H, T, units;
+  StatusBlock* status;
+  uint64_t timeout_ns;
+  int inject_stall;
+};
+bool linear_ln_mma_supported(int d, int b, bool bf16);
+int linear_ln_mma_tile_rows();
+cudaError_t launch_linear_ln_mma(const LnParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                 const CUtensorMap& mv, cudaStream_t stream);
+
 // The bias and per-token-rate variants as the plain rule on changed inputs
 // (linear_prep.cu): padded to 64 features, bf16.
 struct VariantPrepParams {

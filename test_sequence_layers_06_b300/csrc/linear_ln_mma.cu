@@ -1,0 +1,423 @@
+// TTT-Linear with a layer norm and a residual inside the inner model, bf16 inputs,
+// d = 64, b = 16, on the tensor cores: one CTA per (batch row, head), W resident in
+// registers across the sequence.
+//
+// Method ("5 · TestingTime 训练与长上下文", section 3.1 lists the layer norm and the
+// residual inside f in its ablation ladder; the oracle's reading): f(k; W) =
+// k + LN(k W), LN(y) = gamma (y - mean y) / sqrt(var y + 1e-6) + beta over the 64
+// features of a token (biased variance), trained on 1/2 ||f(k) - v||^2 by the
+// chunk rule (every gradient at the chunk-start W_a), read out as z_t = f(q_t; W_t).
+// For a chunk: Y = K W_a, x = (Y - mu) / s, r = K + gamma x + beta - V, g = gamma r,
+//   E = (g - mean(g) - x mean(g x)) / s            (the chain rule through LN, per row)
+//   X = Q W_a - eta tril(Q K^T) E,   Z = Q + LN(X),   W = W_a - eta K^T E.
+//
+// Layout as the TTT-Linear read-out (linear_mma.cu): each of 4 consumer warps owns 16
+// output features j and keeps W^T (16 x 64) as fp32 mma.sync accumulator fragments;
+// Y^T, E^T and X^T are C fragments with rows j and columns t. The per-token means run
+// over all 64 features, so each needs every consumer warp: a warp sums its 16 rows
+// (two per lane, then across the 8 lanes of a column by shuffles), writes the partial
+// to shared memory and arrives on that reduction's mbarrier; all wait (bounded) and
+// add the four partials. Three such reductions per tile (Y's mean and mean square,
+// g's two means, X's mean and mean square), each with its own buffer and barrier.
+// A producer warp streams the Q, K, V tiles by TMA into a 6-stage ring and forms
+// S^T once per tile. Every wait is bounded in wall-clock time.
+#include "ttt_device.cuh"
+#include "kernels.h"
+
+namespace ttt {
+namespace {
+
+constexpr int kD = 64;
+constexpr int kTile = 16;
+constexpr int kStages = 6;
+constexpr int kWarps = 4;                     // consumer warps; one more produces
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kTileBytes = kTile * kD * 2;    // 2048
+constexpr int kStageBytes = 3 * kTileBytes;   // Q, K, V
+constexpr int kZOff = kStages * kStageBytes;
+constexpr int kZBytes = kTile * 16 * 2;       // 512 per warp and buffer
+constexpr int kSOff = kZOff + kWarps * 2 * kZBytes;  // per stage: (S .* D)^T B fragments, 16 bytes per lane
+constexpr int kSBytes = 32 * 16;
+constexpr int kRedOff = kSOff + kStages * kSBytes;   // [3 reductions][4 warps][16 tokens][2] fp32 partial sums
+constexpr int kRedBytes = 3 * kWarps * kTile * 2 * 4;
+constexpr int kBarOff = kRedOff + kRedBytes;
+constexpr int kAbortOff = kBarOff + 3 * kStages * 8 + 3 * 8;  // + the consumers' three reduction barriers
+constexpr int kSmemBytes = kAbortOff + 16 + 1024;    // + slack to align the base to 1024
+static_assert(kSmemBytes <= 48 * 1024, "no opt-in to more dynamic shared memory");
+
+enum : int { kWhereLnProducer = 52, kWhereLnConsumer = 53 };
+
+__global__ void __launch_bounds__(kThreads, 2)
+    linear_ln_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                         const __grid_constant__ CUtensorMap mv, LnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* empty = full + kStages;
+  uint64_t* sready = empty + kStages;  // the tile's S^T fragments are written
+  uint64_t* rbar = sready + kStages;   // [3] every consumer warp's partial sums of a reduction are written
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+  float* red = reinterpret_cast<float*>(smem + kRedOff);
+
+  const int unit = blockIdx.x;
+  const int h = unit % p.H;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = (p.T + kTile - 1) / kTile;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+      mbar_init(&sready[s], 1);
+    }
+    for (int r = 0; r < 3; ++r) mbar_init(&rbar[r], kWarps);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ------------------------------------------------------------ producer
+    const int g = lane >> 2, tg = lane & 3, mi = lane >> 3, mr = lane & 7;
+    int issued = 0;  // lane 0
+    auto load = [&](int u) {
+      const int s = u % kStages;
+      mbar_arrive_expect_tx(&full[s], kStageBytes);
+      uint8_t* st = smem + s * kStageBytes;
+      tma_load_3d(st, &mq, &full[s], 0, u * kTile, unit);
+      tma_load_3d(st + kTileBytes, &mk, &full[s], 0, u * kTile, unit);
+      tma_load_3d(st + 2 * kTileBytes, &mv, &full[s], 0, u * kTile, unit);
+      ++issued;
+    };
+    if (lane == 0) {
+      prefetch_tmap(&mq);
+      prefetch_tmap(&mk);
+      prefetch_tmap(&mv);
+      if (!p.inject_stall)
+        for (int u = 0; u < min(kStages, num_tiles); ++u) load(u);
+    }
+    bool ok = true;
+    for (int u = 0; u < num_tiles; ++u) {
+      const int s = u % kStages;
+      if (!mbar_wait_or_abort(&full[s], (u / kStages) & 1, p.timeout_ns, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sQ = smem_u32(smem + s * kStageBytes);
+      const uint32_t sK = sQ + kTileBytes;
+      float sacc[2][4] = {};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t qa[4], r[4];
+        ldsm_x4(qa, sQ + swz128(((mi & 1) << 3) + mr, 2 * k + (mi >> 1)));  // Q: A (m = t, k = i)
+        ldsm_x4(r, sK + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));   // K: B (k = i, n = t')
+        const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
+        mma_bf16_16816(sacc[0], qa, b0);
+        mma_bf16_16816(sacc[1], qa, b1);
+      }
+      // Element (t, t') with t = g (+8), t' = 8nt + 2tg (+1); keep t' <= t.
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = 8 * nt + 2 * tg;
+        if (c > g) sacc[nt][0] = 0.f;
+        if (c + 1 > g) sacc[nt][1] = 0.f;
+        if (c > g + 8) sacc[nt][2] = 0.f;
+        if (c + 1 > g + 8) sacc[nt][3] = 0.f;
+      }
+      // S's C fragment (rows t, columns t') is the B fragment (k = t', n = t) of S^T.
+      *reinterpret_cast<uint4*>(smem + kSOff + s * kSBytes + lane * 16) =
+          make_uint4(pack_bf16(sacc[0][0], sacc[0][1]), pack_bf16(sacc[1][0], sacc[1][1]),
+                     pack_bf16(sacc[0][2], sacc[0][3]), pack_bf16(sacc[1][2], sacc[1][3]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sready[s]);
+      // Refill the stage of tile u - 1 once the consumers have released it.
+      const int v = u - 1 + kStages;
+      if (u >= 1 && v < num_tiles && !p.inject_stall) {
+        if (lane == 0) {
+          ok = mbar_wait_or_abort(&empty[(u - 1) % kStages], ((u - 1) / kStages) & 1, p.timeout_ns, abort_flag);
+          if (ok) load(v);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+    }
+    if (lane == 0) {
+      if (!ok) {
+        if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereLnProducer, unit);
+        *abort_flag = 1;
+      }
+      // Loads still in flight must land before the CTA may exit.
+      for (int u = (issued > kStages ? issued - kStages : 0); u < issued; ++u)
+        (void)mbar_wait_bounded(&full[u % kStages], (u / kStages) & 1, p.timeout_ns);
+    }
+    return;
+  }
+
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2;   // fragment row group
+  const int tg = lane & 3;   // thread in group
+  const int jw = 16 * warp;  // first output feature of this warp
+  const int mi = lane >> 3;
+  const int mr = lane & 7;
+  const float neta = -p.eta[h];
+  __nv_bfloat16* Zg = static_cast<__nv_bfloat16*>(p.Z);
+  // gamma and beta of this lane's two rows j = jw + g, jw + g + 8.
+  const float gm[2] = {p.gamma[h * kD + jw + g], p.gamma[h * kD + jw + g + 8]};
+  const float bt[2] = {p.beta[h * kD + jw + g], p.beta[h * kD + jw + g + 8]};
+  constexpr float kInvD = 1.f / kD, kEps = 1e-6f;
+
+  // Per-token sums over all 64 features of two quantities held as C fragments (rows j,
+  // columns t): reduction r of tile u. Returns, for this lane's token columns
+  // (nt, c) = 8 nt + 2 tg + c, the sums of a and of b. False if a wait gave up.
+  auto reduce2 = [&](int r, int u, const float (*a)[4], const float (*b)[4], float (*sa)[2],
+                     float (*sb)[2]) -> bool {
+    float pa[2][2], pb[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        pa[nt][c] = a[nt][c] + a[nt][c + 2];
+        pb[nt][c] = b[nt][c] + b[nt][c + 2];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          pa[nt][c] += __shfl_xor_sync(0xffffffffu, pa[nt][c], off);
+          pb[nt][c] += __shfl_xor_sync(0xffffffffu, pb[nt][c], off);
+        }
+      }
+    float* slot = red + r * (kWarps * kTile * 2);
+    if (lane < 4) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+        *reinterpret_cast<float4*>(slot + (warp * kTile + 8 * nt + 2 * tg) * 2) =
+            make_float4(pa[nt][0], pb[nt][0], pa[nt][1], pb[nt][1]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rbar[r]);
+    if (!mbar_wait_or_abort(&rbar[r], u & 1, p.timeout_ns, abort_flag)) return false;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sa[nt][0] = sa[nt][1] = sb[nt][0] = sb[nt][1] = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float4 v = *reinterpret_cast<const float4*>(slot + (w * kTile + 8 * nt + 2 * tg) * 2);
+        sa[nt][0] += v.x;
+        sb[nt][0] += v.y;
+        sa[nt][1] += v.z;
+        sb[nt][1] += v.w;
+      }
+    }
+    return true;
+  };
+  // C-fragment pairs (rows j = jw + g (+8), columns t) of a tile's transpose, for this warp's
+  // 16 features, by ldmatrix.trans of the tile's 8x8 blocks.
+  auto ld_t = [&](uint32_t base, float (*o)[4]) {
+    uint32_t vt[4];
+    ldsm_x4_t(vt, base + swz128(((mi >> 1) << 3) + mr, 2 * warp + (mi & 1)));
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      o[nt][0] = bf16_lo(vt[2 * nt]);
+      o[nt][1] = bf16_hi(vt[2 * nt]);
+      o[nt][2] = bf16_lo(vt[2 * nt + 1]);
+      o[nt][3] = bf16_hi(vt[2 * nt + 1]);
+    }
+  };
+
+  // W^T fragments: Wt[q] covers input columns i in [8q, 8q+8) of rows j = jw+g, jw+g+8.
+  float Wt[8][4];
+  {
+    const float* W0 = p.W0 + static_cast<size_t>(h) * kD * kD;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = 8 * q + 2 * tg;
+      Wt[q][0] = W0[i * kD + jw + g];
+      Wt[q][1] = W0[(i + 1) * kD + jw + g];
+      Wt[q][2] = W0[i * kD + jw + g + 8];
+      Wt[q][3] = W0[(i + 1) * kD + jw + g + 8];
+    }
+  }
+
+  bool ok = true;
+  for (int u = 0; ok && u < num_tiles; ++u) {
+    const int s = u % kStages;
+    if (!mbar_wait_or_abort(&sready[s], (u / kStages) & 1, p.timeout_ns, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const uint4 sv = *reinterpret_cast<const uint4*>(smem + kSOff + s * kSBytes + lane * 16);
+    const uint32_t sQ = smem_u32(smem + s * kStageBytes);
+    const uint32_t sK = sQ + kTileBytes;
+    const uint32_t sV = sQ + 2 * kTileBytes;
+
+    uint32_t wr[4][4];  // bf16 A fragments of the chunk-start W^T (k-step k: i in [16k, 16k+16))
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      wr[k][0] = pack_bf16(Wt[2 * k][0], Wt[2 * k][1]);
+      wr[k][1] = pack_bf16(Wt[2 * k][2], Wt[2 * k][3]);
+      wr[k][2] = pack_bf16(Wt[2 * k + 1][0], Wt[2 * k + 1][1]);
+      wr[k][3] = pack_bf16(Wt[2 * k + 1][2], Wt[2 * k + 1][3]);
+    }
+    float kt[2][4], vt[2][4];
+    ld_t(sK, kt);
+    ld_t(sV, vt);
+
+    // Y^T = W_a^T K^T, in two partial sums to shorten the chain.
+    float y[2][4] = {}, y2[2][4] = {};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t r[4];
+      ldsm_x4(r, sK + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
+      const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
+      mma_bf16_16816(k < 2 ? y[0] : y2[0], wr[k], b0);
+      mma_bf16_16816(k < 2 ? y[1] : y2[1], wr[k], b1);
+    }
+    // K as the B operand of the update (k = t, n = i): kbt[q] for i in [8q, 8q+8).
+    uint32_t kbt[8][2];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      uint32_t r[4];
+      ldsm_x4_t(r, sK + swz128(((mi & 1) << 3) + mr, 2 * qq + (mi >> 1)));
+      kbt[2 * qq][0] = r[0];
+      kbt[2 * qq][1] = r[1];
+      kbt[2 * qq + 1][0] = r[2];
+      kbt[2 * qq + 1][1] = r[3];
+    }
+    float ysq[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        y[nt][r] += y2[nt][r];
+        ysq[nt][r] = y[nt][r] * y[nt][r];
+      }
+
+    // (1) mean and scale of each token's y; x, r = k + LN(y) - v, g = gamma r.
+    float s1[2][2], s2[2][2];
+    if (!(ok = reduce2(0, u, y, ysq, s1, s2))) break;
+    float mu[2][2], rs[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        mu[nt][c] = s1[nt][c] * kInvD;
+        rs[nt][c] = rsqrtf(fmaxf(s2[nt][c] * kInvD - mu[nt][c] * mu[nt][c], 0.f) + kEps);
+      }
+    float xx[2][4], gg[2][4], ggx[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int c = r & 1, row = r >> 1;
+        xx[nt][r] = (y[nt][r] - mu[nt][c]) * rs[nt][c];
+        gg[nt][r] = gm[row] * (kt[nt][r] + fmaf(gm[row], xx[nt][r], bt[row]) - vt[nt][r]);
+        ggx[nt][r] = gg[nt][r] * xx[nt][r];
+      }
+    // (2) the two means of the chain rule through LN: E^T = (g - mean g - x mean(g x)) / s.
+    if (!(ok = reduce2(1, u, gg, ggx, s1, s2))) break;
+    uint32_t ea[4];  // -eta E^T as the A operand (m = j, k = t)
+    {
+      float e[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int c = r & 1;
+          e[nt][r] = neta * (gg[nt][r] - s1[nt][c] * kInvD - xx[nt][r] * (s2[nt][c] * kInvD)) * rs[nt][c];
+        }
+      ea[0] = pack_bf16(e[0][0], e[0][1]);
+      ea[1] = pack_bf16(e[0][2], e[0][3]);
+      ea[2] = pack_bf16(e[1][0], e[1][1]);
+      ea[3] = pack_bf16(e[1][2], e[1][3]);
+    }
+
+    // W^T += (-eta E^T) K: the state update (the chain to the next tile) first.
+#pragma unroll
+    for (int q = 0; q < 8; ++q) mma_bf16_16816(Wt[q], ea, kbt[q]);
+
+    // X^T = W_a^T Q^T + (-eta E^T) S^T.
+    float xo[2][4] = {};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t r[4];
+      ldsm_x4(r, sQ + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
+      const uint32_t qb0[2] = {r[0], r[1]}, qb1[2] = {r[2], r[3]};
+      mma_bf16_16816(xo[0], wr[k], qb0);
+      mma_bf16_16816(xo[1], wr[k], qb1);
+    }
+    const uint32_t sb0[2] = {sv.x, sv.y}, sb1[2] = {sv.z, sv.w};
+    mma_bf16_16816(xo[0], ea, sb0);
+    mma_bf16_16816(xo[1], ea, sb1);
+    float qt[2][4];
+    ld_t(sQ, qt);
+
+    // Every register loaded from the stage has been consumed: hand it back to the producer
+    // (the proxy fence orders these reads before its next TMA write).
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    // (3) Z = Q + LN(X).
+    float xsq[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) xsq[nt][r] = xo[nt][r] * xo[nt][r];
+    if (!(ok = reduce2(2, u, xo, xsq, s1, s2))) break;
+    float z[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int c = r & 1, row = r >> 1;
+        const float m = s1[nt][c] * kInvD;
+        const float sc = rsqrtf(fmaxf(s2[nt][c] * kInvD - m * m, 0.f) + kEps);
+        z[nt][r] = qt[nt][r] + fmaf(gm[row], (xo[nt][r] - m) * sc, bt[row]);
+      }
+
+    // Z^T (rows j, columns t) -> Z[t][j] through the warp's staging tile (transposing stmatrix).
+    uint8_t* zbuf = smem + kZOff + (warp * 2 + (u & 1)) * kZBytes;
+    {
+      uint32_t zr[4] = {pack_bf16(z[0][0], z[0][1]), pack_bf16(z[0][2], z[0][3]),
+                        pack_bf16(z[1][0], z[1][1]), pack_bf16(z[1][2], z[1][3])};
+      stsm_x4_t(smem_u32(zbuf) + (((mi >> 1) << 3) + mr) * 32 + (mi & 1) * 16, zr);
+    }
+    __syncwarp();
+    {
+      const int tok = u * kTile + (lane >> 1);
+      const uint4 zv = *reinterpret_cast<const uint4*>(zbuf + (lane >> 1) * 32 + (lane & 1) * 16);
+      if (tok < p.T)
+        *reinterpret_cast<uint4*>(Zg + (static_cast<size_t>(unit) * p.T + tok) * kD + jw + 8 * (lane & 1)) = zv;
+    }
+  }
+  if (!ok) {
+    if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereLnConsumer, unit);
+    *abort_flag = 1;
+  }
+
+  // Final state, W_out[unit][i][j].
+  float* Wo = p.W_out + static_cast<size_t>(unit) * kD * kD;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int i = 8 * q + 2 * tg;
+    Wo[i * kD + jw + g] = Wt[q][0];
+    Wo[(i + 1) * kD + jw + g] = Wt[q][1];
+    Wo[i * kD + jw + g + 8] = Wt[q][2];
+    Wo[(i + 1) * kD + jw + g + 8] = Wt[q][3];
+  }
+}
+
+}  // namespace
+
+bool linear_ln_mma_supported(int d, int b, bool bf16) { return bf16 && d == kD && b == kTile; }
+
+int linear_ln_mma_tile_rows() { return kTile; }
+
+cudaError_t launch_linear_ln_mma(const LnParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                                 const CUtensorMap& mv, cudaStream_t stream) {
+  if (p.units == 0) return cudaSuccess;
+  linear_ln_mma_kernel<<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ttt

@@ -677,7 +677,7 @@ VariantLayout variant_layout(int variant, int B, int H, int T, int d, int b) {
 
 size_t ttt_linear_variant_workspace_bytes(int variant, ttt_dtype dt, int B, int H, int T, int d, int b) {
   if (!sizes_ok(B, H, T, d, b) || !sizes_ok(B, H, T, kPadD, b)) return 0;
-  if (variant == ttt::kVarMomentum) return kStatusBytes;  // the status word alone (both kernels)
+  if (variant == ttt::kVarMomentum || variant == ttt::kVarLn) return kStatusBytes;  // the status word alone
   if (variant != ttt::kVarBias && variant != ttt::kVarTokenEta) return 0;
   if (!variant_fast_ok(variant, dt, d, b)) return kStatusBytes;
   return variant_layout(variant, B, H, T, d, b).total;
@@ -828,6 +828,49 @@ ttt_status ttt_linear_momentum_fwd_ex(const void* Q, const void* K, const void* 
       !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
     return TTT_ERR_CUDA;
   return ttt::launch_linear_mom_mma(p, mq, mk, mv, s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_linear_ln_fwd_ex(const void* Q, const void* K, const void* V, ttt_dtype dt, const float* eta,
+                                const float* W0, const float* gamma, const float* beta, int B, int H, int T, int d,
+                                int b, void* Z, float* W_out, void* workspace, size_t ws_bytes, void* stream,
+                                const ttt_options* opt) {
+  ttt_status st = variant_check(ttt::kVarLn, Q, K, V, dt, eta, nullptr, nullptr, W0, gamma, beta, B, H, T, d, b, Z,
+                                W_out, nullptr);
+  if (st != TTT_OK) return st;
+  const size_t need = ttt_linear_variant_workspace_bytes(ttt::kVarLn, dt, B, H, T, d, b);
+  if (need == 0) return TTT_ERR_ARG;
+  if (!workspace || !aligned16(workspace) || ws_bytes < need) return TTT_ERR_ARG;
+  const ttt_options o = defaults(opt);
+  {
+    const size_t seq = bytes4(B, H, T, d, dt == TTT_BF16 ? 2 : 4), hd = bytes4(H, d, 1, 1, 4);
+    if (!outputs_disjoint({{Z, seq}, {W_out, bytes4(B, H, d, d, 4)}, {workspace, ws_bytes}},
+                          {{Q, seq}, {K, seq}, {V, seq}, {eta, bytes4(H, 1, 1, 1, 4)}, {W0, bytes4(H, d, d, 1, 4)},
+                           {gamma, hd}, {beta, hd}}))
+      return TTT_ERR_ARG;
+  }
+  if (o.force_path < 0 || o.force_path > 3) return TTT_ERR_ARG;
+  const bool mma = ttt::linear_ln_mma_supported(d, b, dt == TTT_BF16) && T > 0;
+  if (o.force_path == 3 || (o.force_path == 2 && !mma)) return TTT_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = reset_status(workspace, s);
+  if (st != TTT_OK) return st;
+  if (!mma || o.force_path == 1)
+    return variant_simt(ttt::kVarLn, Q, K, V, dt, eta, nullptr, nullptr, W0, gamma, beta, B, H, T, d, b, Z, W_out,
+                        nullptr, stream);
+  ttt::LnParams p;
+  p.Q = Q; p.K = K; p.V = V; p.Z = Z;
+  p.eta = eta; p.gamma = gamma; p.beta = beta; p.W0 = W0; p.W_out = W_out;
+  p.H = H; p.T = T; p.units = B * H;
+  p.status = static_cast<ttt::StatusBlock*>(workspace);
+  p.timeout_ns = o.wait_timeout_ns;
+  p.inject_stall = o.inject_stall;
+  CUtensorMap mq, mk, mv;
+  const int rows = ttt::linear_ln_mma_tile_rows();
+  if (!encode_3d(&mq, Q, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_3d(&mk, K, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_3d(&mv, V, p.units, T, d, rows, d, CU_TENSOR_MAP_SWIZZLE_128B))
+    return TTT_ERR_CUDA;
+  return ttt::launch_linear_ln_mma(p, mq, mk, mv, s) == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
 // Segments of the tensor-core backward (bf16, d = 64, b = 16): as many as fill the SMs with one

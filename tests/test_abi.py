@@ -25,7 +25,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 25
+    assert len(names) == 26
     assert set(names) == set(ttt.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -261,7 +261,8 @@ def test_variant_workspace_bytes(lib):
     assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_BIAS, bf, 2, 3, 40, 64, 16) == 256   # no room for 1
     assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_BIAS, f32, 2, 3, 40, 16, 16) == 256
     assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_TOKEN_ETA, bf, 2, 3, 40, 64, 5) == 256
-    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_LN, bf, 2, 3, 40, 64, 16) == 0
+    assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_LN, bf, 2, 3, 40, 64, 16) == 256
+    assert ttt.ttt_linear_variant_workspace_bytes(7, bf, 2, 3, 40, 64, 16) == 0
     assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_MOMENTUM, bf, 2, 3, 40, 64, 16) == 256
     assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_MOMENTUM, f32, 2, 3, 40, 16, 5) == 256
     assert ttt.ttt_linear_variant_workspace_bytes(ttt.TTT_INNER_MOMENTUM, bf, 2, 3, 40, 64, 0) == 0
@@ -273,7 +274,8 @@ def test_variant_workspace_bytes(lib):
 
 
 def _var_ex(lib, name, **kw):
-    a = dict(Q=1 * MB, K=2 * MB, V=3 * MB, dt=1, eta=4 * MB, W0=5 * MB, beta0=6 * MB, B=2, H=3, T=40, d=16, b=16,
+    a = dict(Q=1 * MB, K=2 * MB, V=3 * MB, dt=1, eta=4 * MB, W0=5 * MB, beta0=6 * MB, gb=7 * MB, B=2, H=3, T=40,
+             d=16, b=16,
              Z=8 * MB, W=9 * MB, beta=10 * MB, ws=16 * MB, wsb=1 << 24, s=0)
     a.update(kw)
     vp = ctypes.c_void_p
@@ -281,6 +283,12 @@ def _var_ex(lib, name, **kw):
         return lib.ttt_linear_bias_fwd_ex(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W0"]),
                                           vp(a["beta0"]), a["B"], a["H"], a["T"], a["d"], a["b"], vp(a["Z"]),
                                           vp(a["W"]), vp(a["beta"]), vp(a["ws"]), a["wsb"], vp(a["s"]))
+    if name == "ln":
+        o = ttt.ttt_options()
+        o.force_path = a.get("fp", 0)
+        return lib.ttt_linear_ln_fwd_ex(vp(a["Q"]), vp(a["K"]), vp(a["V"]), a["dt"], vp(a["eta"]), vp(a["W0"]),
+                                        vp(a["beta0"]), vp(a["gb"]), a["B"], a["H"], a["T"], a["d"], a["b"], vp(a["Z"]),
+                                        vp(a["W"]), vp(a["ws"]), a["wsb"], vp(a["s"]), ctypes.byref(o))
     if name == "momentum":
         o = ttt.ttt_options()
         o.force_path = a.get("fp", 0)
@@ -307,7 +315,20 @@ def test_momentum_fast_call_paths_and_arguments(lib, kw, want):
     assert _var_ex(lib, "momentum", **base) == want
 
 
-@pytest.mark.parametrize("name", ["bias", "token_eta", "momentum"])
+@pytest.mark.parametrize("kw,want", [(dict(fp=3), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=2, d=32), ttt.TTT_ERR_UNSUPPORTED),
+                                     (dict(fp=2, b=32), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=2, dt=0), ttt.TTT_ERR_UNSUPPORTED),
+                                     (dict(fp=2, T=0), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=-1), ttt.TTT_ERR_ARG),
+                                     (dict(gb=0), ttt.TTT_ERR_ARG), (dict(W=7 * MB + 256), ttt.TTT_ERR_ARG)])
+def test_ln_fast_call_paths_and_arguments(lib, kw, want):
+    """ttt_linear_ln_fwd_ex: no segment-parallel form; the tensor kernel, when forced, only for bf16,
+    d = 64, b = 16 and T > 0; a bad path, a null beta, W_out over beta: refused before anything runs
+    (gamma is the `beta0` slot of the shared argument set, beta the `gb` slot)."""
+    base = dict(d=64, W=9 * MB)
+    base.update(kw)
+    assert _var_ex(lib, "ln", **base) == want
+
+
+@pytest.mark.parametrize("name", ["bias", "token_eta", "momentum", "ln"])
 @pytest.mark.parametrize("kw,want", [(dict(ws=0), ttt.TTT_ERR_ARG), (dict(ws=16 * MB + 8), ttt.TTT_ERR_ARG),
                                      (dict(wsb=4096), ttt.TTT_ERR_ARG), (dict(Q=0), ttt.TTT_ERR_ARG),
                                      (dict(ws=2 * MB), ttt.TTT_ERR_ARG), (dict(Z=16 * MB + 4096), ttt.TTT_ERR_ARG),
@@ -316,7 +337,7 @@ def test_momentum_fast_call_paths_and_arguments(lib, kw, want):
 def test_variant_fast_calls_reject_bad_arguments(lib, name, kw, want):
     """No workspace, a misaligned or too small one, a null input, the workspace over an input or an
     output inside the workspace, d > 64, a bad dtype or chunk size: refused before anything runs."""
-    if name == "momentum" and kw == dict(wsb=4096):
+    if name in ("momentum", "ln") and kw == dict(wsb=4096):
         kw = dict(wsb=128)  # its workspace is the 256-byte status word alone
     assert _var_ex(lib, name, **kw) == want
 

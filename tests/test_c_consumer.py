@@ -65,6 +65,8 @@ int main(void) {
   printf("bias_ex.nows=%d\n", (int)ttt_linear_bias_fwd_ex(dummy, dummy, dummy, TTT_BF16, dummy, dummy, dummy, 1, 1,
                                                           16, 16, 16, dummy, dummy, dummy, NULL, 0, NULL));
   printf("ws.var_mom=%zu\n", ttt_linear_variant_workspace_bytes(TTT_INNER_MOMENTUM, TTT_BF16, 2, 3, 40, 64, 16));
+  printf("ln_ex.nows=%d\n", (int)ttt_linear_ln_fwd_ex(dummy, dummy, dummy, TTT_BF16, dummy, dummy, dummy, dummy, 1,
+                                                       1, 16, 64, 16, dummy, dummy, NULL, 0, NULL, &opt));
   printf("mom_ex.nows=%d\n", (int)ttt_linear_momentum_fwd_ex(dummy, dummy, dummy, TTT_BF16, dummy, dummy, dummy, 1,
                                                              1, 16, 64, 16, dummy, dummy, dummy, NULL, 0, NULL,
                                                              &opt));
@@ -110,9 +112,10 @@ def test_calls_from_c_agree_with_the_binding(c_output):
 def test_variant_and_mlp_backward_calls_from_c(c_output):
     assert int(c_output["ws.var_bias"]) == ttt.ttt_linear_variant_workspace_bytes(
         ttt.TTT_INNER_BIAS, ttt.TTT_BF16, 2, 3, 40, 16, 16) > 256
-    assert int(c_output["ws.var_ln"]) == 0
+    assert int(c_output["ws.var_ln"]) == 256
     assert int(c_output["ws.var_mom"]) == 256
     assert int(c_output["mom_ex.nows"]) == ttt.TTT_ERR_ARG
+    assert int(c_output["ln_ex.nows"]) == ttt.TTT_ERR_ARG
     assert int(c_output["ws.mlp_bwd"]) == ttt.ttt_mlp_bwd_workspace_bytes(2, 3, 40, 16, 8) > 256
     assert int(c_output["mlp_bwd.d65"]) == -2   # d > 64
     assert int(c_output["bias_ex.nows"]) == -1  # no workspace

@@ -238,3 +238,57 @@ def test_momentum_fast_path_bounded_wait_reports_timeout():
     got = ttt.ttt_linear_momentum_fwd(*args, fast=True, workspace=ws)
     assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
     check("Z,W_out,M_out", got, momentum_primal(inp.q64, inp.k64, inp.v64, alpha, betas, inp.W0_64, 16), w)
+
+
+FAST_LN = [(1, 2, 1), (1, 2, 3), (2, 3, 16), (2, 3, 37), (1, 2, 100), (1, 2, 1024), (1, 2, 2048)]
+
+
+def ln_params(H, seed):
+    g = np.random.default_rng(seed)
+    return ((1.0 + 0.2 * g.standard_normal((H, 64))).astype(np.float32),
+            (0.1 * g.standard_normal((H, 64))).astype(np.float32))
+
+
+@pytest.mark.parametrize("B,H,T", FAST_LN)
+def test_ln_fast_path_matches_oracle(B, H, T):
+    """bf16, d = 64, b = 16 on the tensor-core LN + residual kernel (forced, so that no other kernel
+    can serve): a single short chunk, ragged last chunks, and sequences of 64 and 128 chunks."""
+    w, inp, t = inputs(64, T, "bf16", 840 + T, B=B, H=H)
+    gamma, beta = ln_params(w.H, T)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    got = ttt.ttt_linear_ln_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(gamma).cuda(),
+                                torch.from_numpy(beta).cuda(), 16, fast=True, workspace=ws,
+                                options={"force_path": ttt.PATH_TENSOR})
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    want = ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma, beta, 16)
+    check("Z,W_out", got, want, w)
+
+
+def test_ln_fast_call_takes_the_variant_kernel_elsewhere():
+    """fp32 operands (or d != 64, b != 16): ttt_linear_ln_fwd_ex runs the fp32 variant kernel and
+    matches the oracle at the fp32 bar."""
+    w, inp, t = inputs(32, 45, "f32", 850)
+    g = np.random.default_rng(3)
+    gamma = (1.0 + 0.2 * g.standard_normal((w.H, 32))).astype(np.float32)
+    beta = (0.1 * g.standard_normal((w.H, 32))).astype(np.float32)
+    got = ttt.ttt_linear_ln_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(gamma).cuda(),
+                                torch.from_numpy(beta).cuda(), 16, fast=True)
+    torch.cuda.synchronize()
+    check("Z,W_out", got, ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma, beta, 16), w)
+
+
+def test_ln_fast_path_bounded_wait_reports_timeout():
+    """The load pipeline never fills: the tensor kernel's waits run out after 1 ms, the status says
+    TTT_ERR_TIMEOUT, reading clears it, and the next call on the same context matches the oracle."""
+    w, inp, t = inputs(64, 64, "bf16", 860, B=1, H=2)
+    gamma, beta = ln_params(w.H, 5)
+    args = (t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(gamma).cuda(), torch.from_numpy(beta).cuda(),
+            16)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ttt.ttt_linear_ln_fwd(*args, fast=True, workspace=ws,
+                          options={"inject_stall": 1, "wait_timeout_ns": 1_000_000, "force_path": ttt.PATH_TENSOR})
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_ERR_TIMEOUT
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    got = ttt.ttt_linear_ln_fwd(*args, fast=True, workspace=ws)
+    assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
+    check("Z,W_out", got, ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma, beta, 16), w)

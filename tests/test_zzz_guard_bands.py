@@ -127,6 +127,33 @@ def test_momentum_tensor_kernel_writes_inside_its_outputs():
         assert rel_l2(to64(x), r) <= tolerance(w)
 
 
+def test_ln_tensor_kernel_writes_inside_its_outputs():
+    """The tensor-core LN + residual kernel (bf16, d = 64, b = 16), a ragged last chunk: Z, W_out and
+    the workspace keep their margins, and the results match the oracle."""
+    from oracle.variants import ln_residual_primal
+    w = synth.WORKLOADS["linear_small"].with_(B=1, H=3, T=45, seed=916)
+    inp = synth.make_inputs(w)
+    t = torch_inputs(inp)
+    g = np.random.default_rng(9)
+    gamma = torch.from_numpy((1.0 + 0.2 * g.standard_normal((w.H, 64))).astype(np.float32)).cuda()
+    beta = torch.from_numpy((0.1 * g.standard_normal((w.H, 64))).astype(np.float32)).cuda()
+    Z = Guarded((w.B, w.H, w.T, w.d), torch.bfloat16, -3.0)
+    Wo = Guarded((w.B, w.H, w.d, w.d), torch.float32, -5.0)
+    ws = guarded_workspace(256)
+    o = ttt.ttt_options()
+    o.force_path = ttt.PATH_TENSOR
+    p = lambda x: ctypes.c_void_p(x.data_ptr())
+    st = ttt.load_library().ttt_linear_ln_fwd_ex(
+        p(t["Q"]), p(t["K"]), p(t["V"]), ttt.TTT_BF16, p(t["eta"]), p(t["W0"]), p(gamma), p(beta), w.B, w.H, w.T, w.d,
+        16, p(Z.t), p(Wo.t), p(ws.t), 256, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), ctypes.byref(o))
+    assert st == ttt.TTT_OK
+    assert ttt.ttt_last_device_status(ws.t) == ttt.TTT_OK
+    assert Z.margins_intact() and Wo.margins_intact() and ws.margins_intact()
+    Zr, Wr = ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma.cpu().numpy(),
+                                beta.cpu().numpy(), 16)
+    assert rel_l2(to64(Z.t), Zr) <= tolerance(w) and rel_l2(to64(Wo.t), Wr) <= tolerance(w)
+
+
 def test_decode_writes_inside_its_outputs():
     g = np.random.default_rng(7)
     B, H, d = 2, 3, 64
