@@ -707,16 +707,17 @@ def bench_extras(ttt, dev, stream):
             inp, Q, K, V, eta = dev_inputs(w)
             W0 = torch.from_numpy(inp.W0).to(dev)
             mbeta = torch.full((w.H,), 0.9, dtype=torch.float32, device=dev)
+            malpha = torch.full((w.H,), 0.05, dtype=torch.float32, device=dev)  # a stable momentum step
             gam, lnb = torch.ones((w.H, w.d), device=dev), torch.zeros((w.H, w.d), device=dev)
             mws = torch.zeros(256, dtype=torch.uint8, device=dev)
-            fns = {"momentum": (lambda: ttt.ttt_linear_momentum_fwd(Q, K, V, eta, mbeta, W0, 16, stream=stream,
+            fns = {"momentum": (lambda: ttt.ttt_linear_momentum_fwd(Q, K, V, malpha, mbeta, W0, 16, stream=stream,
                                                                     fast=True, workspace=mws,
                                                                     options={"force_path": ttt.PATH_TENSOR}),
-                                "beta 0.9: tensor-core momentum kernel"),
-                   "ln_residual": (lambda: ttt.ttt_linear_ln_fwd(Q, K, V, eta, W0, gam, lnb, 16, stream=stream,
+                                "alpha 0.05, beta 0.9: tensor-core momentum kernel"),
+                   "ln_residual": (lambda: ttt.ttt_linear_ln_fwd(Q, K, V, malpha, W0, gam, lnb, 16, stream=stream,
                                                                  fast=True, workspace=mws,
                                                                  options={"force_path": ttt.PATH_TENSOR}),
-                                   "tensor-core LN + residual kernel")}
+                                   "eta 0.05: tensor-core LN + residual kernel")}
             for vname, (fn, what) in fns.items():
                 ms = t_ms(fn, 5)
                 if ttt.ttt_last_device_status(mws, stream) != 0:

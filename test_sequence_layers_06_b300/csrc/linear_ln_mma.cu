@@ -18,7 +18,10 @@
 // (two per lane, then across the 8 lanes of a column by shuffles), writes the partial
 // to shared memory and arrives on that reduction's mbarrier; all wait (bounded) and
 // add the four partials. Three such reductions per tile (Y's mean and mean square,
-// g's two means, X's mean and mean square), each with its own buffer and barrier.
+// g's two means, X's mean and mean square), each with its own buffer and barrier. The
+// third is finished one tile late: a warp hands in its partials of tile u's X, then those
+// of tile u + 1's Y, and only then waits for the others' X sums and writes tile u's Z,
+// so that its wait overlaps the next tile's work.
 // A producer warp streams the Q, K, V tiles by TMA into a 6-stage ring and forms
 // S^T once per tile. Every wait is bounded in wall-clock time.
 #include "ttt_device.cuh"
@@ -171,8 +174,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // Per-token sums over all 64 features of two quantities held as C fragments (rows j,
   // columns t): reduction r of tile u. Returns, for this lane's token columns
   // (nt, c) = 8 nt + 2 tg + c, the sums of a and of b. False if a wait gave up.
-  auto reduce2 = [&](int r, int u, const float (*a)[4], const float (*b)[4], float (*sa)[2],
-                     float (*sb)[2]) -> bool {
+  auto red_put = [&](int r, const float (*a)[4], const float (*b)[4]) -> bool {
     float pa[2][2], pb[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -195,6 +197,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&rbar[r]);
+    return true;
+  };
+  // The four warps' sums of reduction r of tile u (bounded wait). False if the wait gave up.
+  auto red_get = [&](int r, int u, float (*sa)[2], float (*sb)[2]) -> bool {
+    const float* slot = red + r * (kWarps * kTile * 2);
     if (!mbar_wait_or_abort(&rbar[r], u & 1, p.timeout_ns, abort_flag)) return false;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -210,6 +217,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     return true;
   };
+  auto reduce2 = [&](int r, int u, const float (*a)[4], const float (*b)[4], float (*sa)[2],
+                     float (*sb)[2]) -> bool { return red_put(r, a, b) && red_get(r, u, sa, sb); };
   // C-fragment pairs (rows j = jw + g (+8), columns t) of a tile's transpose, for this warp's
   // 16 features, by ldmatrix.trans of the tile's 8x8 blocks.
   auto ld_t = [&](uint32_t base, float (*o)[4]) {
@@ -237,6 +246,37 @@ __global__ void __launch_bounds__(kThreads, 2)
       Wt[q][3] = W0[(i + 1) * kD + jw + g + 8];
     }
   }
+
+  // Z of tile v = Q + LN(X) from its X^T and Q^T fragments (xprev, qprev) and reduction 2.
+  float xprev[2][4], qprev[2][4], xsq[2][4];
+  bool pending = false;
+  auto finish_z = [&](int v) -> bool {
+    float s1[2][2], s2[2][2];
+    if (!red_get(2, v, s1, s2)) return false;
+    float z[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int c = r & 1, row = r >> 1;
+        const float m = s1[nt][c] * kInvD;
+        const float sc = rsqrtf(fmaxf(s2[nt][c] * kInvD - m * m, 0.f) + kEps);
+        z[nt][r] = qprev[nt][r] + fmaf(gm[row], (xprev[nt][r] - m) * sc, bt[row]);
+      }
+    // Z^T (rows j, columns t) -> Z[t][j] through the warp's staging tile (transposing stmatrix).
+    uint8_t* zbuf = smem + kZOff + (warp * 2 + (v & 1)) * kZBytes;
+    {
+      uint32_t zr[4] = {pack_bf16(z[0][0], z[0][1]), pack_bf16(z[0][2], z[0][3]),
+                        pack_bf16(z[1][0], z[1][1]), pack_bf16(z[1][2], z[1][3])};
+      stsm_x4_t(smem_u32(zbuf) + (((mi >> 1) << 3) + mr) * 32 + (mi & 1) * 16, zr);
+    }
+    __syncwarp();
+    const int tok = v * kTile + (lane >> 1);
+    const uint4 zv = *reinterpret_cast<const uint4*>(zbuf + (lane >> 1) * 32 + (lane & 1) * 16);
+    if (tok < p.T)
+      *reinterpret_cast<uint4*>(Zg + (static_cast<size_t>(unit) * p.T + tok) * kD + jw + 8 * (lane & 1)) = zv;
+    return true;
+  };
 
   bool ok = true;
   for (int u = 0; ok && u < num_tiles; ++u) {
@@ -294,7 +334,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // (1) mean and scale of each token's y; x, r = k + LN(y) - v, g = gamma r.
     float s1[2][2], s2[2][2];
-    if (!(ok = reduce2(0, u, y, ysq, s1, s2))) break;
+    red_put(0, y, ysq);
+    if (pending) {
+      pending = false;
+      if (!(ok = finish_z(u - 1))) break;
+    }
+    if (!(ok = red_get(0, u, s1, s2))) break;
     float mu[2][2], rs[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -357,39 +402,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
 
-    // (3) Z = Q + LN(X).
-    float xsq[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) xsq[nt][r] = xo[nt][r] * xo[nt][r];
-    if (!(ok = reduce2(2, u, xo, xsq, s1, s2))) break;
-    float z[2][4];
+    // (3) Z = Q + LN(X): this warp's partial sums now, the rest once the next tile's first
+    // partials are out (the wait then overlaps work of that tile).
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int c = r & 1, row = r >> 1;
-        const float m = s1[nt][c] * kInvD;
-        const float sc = rsqrtf(fmaxf(s2[nt][c] * kInvD - m * m, 0.f) + kEps);
-        z[nt][r] = qt[nt][r] + fmaf(gm[row], (xo[nt][r] - m) * sc, bt[row]);
+        xprev[nt][r] = xo[nt][r];
+        qprev[nt][r] = qt[nt][r];
+        xsq[nt][r] = xo[nt][r] * xo[nt][r];
       }
-
-    // Z^T (rows j, columns t) -> Z[t][j] through the warp's staging tile (transposing stmatrix).
-    uint8_t* zbuf = smem + kZOff + (warp * 2 + (u & 1)) * kZBytes;
-    {
-      uint32_t zr[4] = {pack_bf16(z[0][0], z[0][1]), pack_bf16(z[0][2], z[0][3]),
-                        pack_bf16(z[1][0], z[1][1]), pack_bf16(z[1][2], z[1][3])};
-      stsm_x4_t(smem_u32(zbuf) + (((mi >> 1) << 3) + mr) * 32 + (mi & 1) * 16, zr);
-    }
-    __syncwarp();
-    {
-      const int tok = u * kTile + (lane >> 1);
-      const uint4 zv = *reinterpret_cast<const uint4*>(zbuf + (lane >> 1) * 32 + (lane & 1) * 16);
-      if (tok < p.T)
-        *reinterpret_cast<uint4*>(Zg + (static_cast<size_t>(unit) * p.T + tok) * kD + jw + 8 * (lane & 1)) = zv;
-    }
+    red_put(2, xo, xsq);
+    pending = true;
   }
+  if (ok && pending) ok = finish_z(num_tiles - 1);
   if (!ok) {
     if (!*abort_flag) report_error(p.status, TTT_ERR_TIMEOUT, kWhereLnConsumer, unit);
     *abort_flag = 1;

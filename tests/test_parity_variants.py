@@ -292,3 +292,37 @@ def test_ln_fast_path_bounded_wait_reports_timeout():
     got = ttt.ttt_linear_ln_fwd(*args, fast=True, workspace=ws)
     assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
     check("Z,W_out", got, ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma, beta, 16), w)
+
+
+@pytest.mark.parametrize("variant", ["momentum", "ln"])
+def test_variant_tensor_kernels_full_size_sampled(variant):
+    """B8 H12 T8192 d64 bf16 (the 125M-shaped workload the benchmark times): the momentum and
+    LN + residual tensor kernels over all 96 units, the oracle on two sampled ones."""
+    w = synth.WORKLOADS["linear_125m"]
+    full = synth.make_inputs(w, want_exact=False)
+    t = torch_inputs(full)
+    units = [(0, 0), (7, 11)]
+    sub = synth.make_inputs(w, units=units)
+    heads = [h for _, h in units]
+    if variant == "momentum":
+        alpha = np.full(w.H, 0.1, np.float32)  # alpha / (1 - beta) <= 1: a stable step at unit-norm keys
+        beta = np.linspace(0.5, 0.9, w.H).astype(np.float32)
+        got = ttt.ttt_linear_momentum_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(alpha).cuda(),
+                                          torch.from_numpy(beta).cuda(), t["W0"], 16, fast=True,
+                                          options={"force_path": ttt.PATH_TENSOR})
+        want = momentum_primal(sub.q64, sub.k64, sub.v64, alpha[heads], beta[heads], sub.W0_64, 16)
+        names = ("Z", "W_out", "M_out")
+    else:
+        gamma, beta = ln_params(w.H, 11)
+        eta = np.full(w.H, 0.05, np.float32)
+        got = ttt.ttt_linear_ln_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(eta).cuda(), t["W0"],
+                                    torch.from_numpy(gamma).cuda(), torch.from_numpy(beta).cuda(), 16, fast=True,
+                                    options={"force_path": ttt.PATH_TENSOR})
+        want = ln_residual_primal(sub.q64, sub.k64, sub.v64, eta[heads], sub.W0_64, gamma[heads], beta[heads], 16)
+        names = ("Z", "W_out")
+    torch.cuda.synchronize()
+    bar = tolerance(w)
+    for k, (n, h) in enumerate(units):
+        for name, g, r in zip(names, got, want):
+            assert rel_err(f"{variant} {name} unit {n},{h}", to64(g[n, h]), r[0, k], bar) <= bar, (name, n, h)
+    assert bool(torch.isfinite(got[0].float()).all())
