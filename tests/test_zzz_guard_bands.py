@@ -1,7 +1,7 @@
 """Guard bands around every output, and non-finite inputs (GPU).
 
-No memory checker runs on this GPU pool, so out-of-bounds writes are looked for
-directly: every output and workspace of a call is a view into a larger buffer
+Out-of-bounds writes are looked for directly, without a memory checker: every
+output and workspace of a call is a view into a larger buffer
 whose margins hold a known pattern, and the margins must be bit-identical after
 the call. A write past either end of an output lands in memory the test owns,
 so a bad kernel shows up here as a failed comparison rather than a fault.
