@@ -72,8 +72,9 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--mode", choices=["fwd", "bwd"], default="fwd",
-                    help="bwd: time the TTT-Linear backward (ttt_linear_bwd) on the workload instead")
+    ap.add_argument("--mode", choices=["fwd", "bwd", "momentum", "ln"], default="fwd",
+                    help="bwd: time the TTT-Linear backward (ttt_linear_bwd) on the workload instead; "
+                         "momentum / ln: the inner-model variant's tensor-core kernel (bf16, d = 64, b = 16)")
     return ap.parse_args()
 
 
@@ -922,6 +923,57 @@ def bench_mlp(args, world, rank, local):
                                        "peak_kind": f"{kind} bf16 burst"}}), flush=True)
 
 
+def bench_variant(args, world, rank, local):
+    """The momentum or LN + residual variant through its *_ex call on the workload's shape (secondary;
+    used for profiling those tensor-core kernels). Reports against the HBM roofline of the plain
+    read-out's bytes."""
+    import torch
+    import test_sequence_layers_06_b300 as ttt
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload].with_(b=16)
+    if args.T:
+        w = w.with_(T=args.T)
+    inp = synth.make_inputs(w, want_exact=False)
+    cv = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev))
+    Q, K, V = cv(inp.q), cv(inp.k), cv(inp.v)
+    W0 = torch.from_numpy(inp.W0).to(dev)
+    rate = torch.full((w.H,), 0.05, dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    opts = {"force_path": ttt.PATH_TENSOR}
+    if args.mode == "momentum":
+        mbeta = torch.full((w.H,), 0.9, dtype=torch.float32, device=dev)
+        step = lambda: ttt.ttt_linear_momentum_fwd(Q, K, V, rate, mbeta, W0, 16, stream=stream, fast=True,
+                                                   workspace=ws, options=opts)
+    else:
+        gam, lnb = torch.ones((w.H, w.d), device=dev), torch.zeros((w.H, w.d), device=dev)
+        step = lambda: ttt.ttt_linear_ln_fwd(Q, K, V, rate, W0, gam, lnb, 16, stream=stream, fast=True,
+                                             workspace=ws, options=opts)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    if ttt.ttt_last_device_status(ws, stream) != 0:
+        raise RuntimeError("device status not OK")
+    ms = a.elapsed_time(e) / args.steps
+    hbm_gbs, _, kind = measured_peaks()
+    gbs = algorithmic_bytes(w) / (ms * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({"metric": f"TTT-Linear {args.mode} variant tokens·heads/sec", "value": w.token_heads / (ms * 1e-3),
+                          "unit": UNIT, "n_gpus": world, "steps": args.steps, "ms_per_step": round(ms, 4),
+                          "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                          "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "d": w.d, "b": 16,
+                                     "variant": args.mode},
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_gbs, "unit": "GB/s",
+                                       "frac": round(gbs / hbm_gbs, 4), "peak_kind": kind}}), flush=True)
+
+
 def bench_bwd(args, world, rank, local):
     """The TTT-Linear backward through ttt_linear_bwd on a workload (secondary; used for the
     backward's profiles). Reports against the HBM roofline of its algorithmic bytes: Q, K, V, dZ
@@ -975,6 +1027,8 @@ def main():
         bench_reference(args, world, rank)
     elif args.mode == "bwd":
         bench_bwd(args, world, rank, local)
+    elif args.mode in ("momentum", "ln"):
+        bench_variant(args, world, rank, local)
     elif synth.WORKLOADS[args.workload].variant == "mlp":
         bench_mlp(args, world, rank, local)
     else:
