@@ -17,7 +17,10 @@ chunk by chunk, on random inputs:
     group maps composed in pairs (exact, and with the kernel's bf16 rounding);
   - two inner-model variants that reduce to plain TTT-Linear on changed inputs:
     a bias in f (a constant extra input) and a per-token learning rate
-    (keys and values scaled by its square root).
+    (keys and values scaled by its square root);
+  - the momentum kernel's transposed per-tile form ("推理时的“临阵磨枪”：Test-Time
+    Training如何教会AI“边做边学”", sections 2.3 and 5.1, read as token-level
+    momentum with chunk-start gradients).
 """
 import numpy as np
 import pytest
@@ -366,3 +369,43 @@ def test_pairwise_composition_keeps_the_rounding_error_of_the_chain():
         assert err(X, B) < 1.15 * err(chain, B)
         # A's part of a start state, |dA| |W| with |W| ~ |B|, stays below B's own error
         assert np.linalg.norm(X[:, A] - ref[:, A]) * np.linalg.norm(ref[:, B]) < np.linalg.norm(X[:, B] - ref[:, B])
+
+
+@pytest.mark.parametrize("T,beta", [(16, 0.5), (37, 0.9), (100, 0.0), (5, 0.7)])
+def test_momentum_in_transposed_16_token_tiles(T, beta):
+    """The momentum kernel's per-tile form (W^T and M^T per output-column block, token-column
+    scalings of E^T, a ragged last tile with its own n) equals token-level momentum with
+    chunk-start gradients: g_t = k_t^T (k_t W_a - v_t), M = beta M + (1 - beta) g_t,
+    W = W - alpha M, z_t = q_t W."""
+    g = np.random.default_rng(T)
+    d, alpha = 16, 0.1
+    Q, K, V = g.standard_normal((T, d)) / 4, g.standard_normal((T, d)) / 4, g.standard_normal((T, d))
+    W0 = 0.05 * g.standard_normal((d, d))
+    # token by token
+    W, M, Wa, Z = W0.copy(), np.zeros((d, d)), W0.copy(), np.zeros((T, d))
+    for t in range(T):
+        if t % 16 == 0:
+            Wa = W.copy()
+        M = beta * M + (1 - beta) * np.outer(K[t], K[t] @ Wa - V[t])
+        W = W - alpha * M
+        Z[t] = Q[t] @ W
+    # the kernel's tiles: transposed states, beta powers as a table
+    pw = beta ** np.arange(18)
+    c = np.cumsum(pw[1:17])                                   # c[t] = beta + ... + beta^(t+1)
+    t16 = np.arange(16)
+    D = np.tril(1.0 - pw[np.clip(t16[:, None] - t16[None, :] + 1, 0, 17)])
+    Wt, Mt, Zk = W0.T.copy(), np.zeros((d, d)), np.zeros((T, d))
+    for c0 in range(0, T, 16):
+        n = min(16, T - c0)
+        Qc, Kc, Vc = (np.zeros((16, d)) for _ in range(3))
+        Qc[:n], Kc[:n], Vc[:n] = Q[c0:c0 + n], K[c0:c0 + n], V[c0:c0 + n]
+        Et = Wt @ Kc.T - Vc.T                                 # rows j, columns t
+        S = np.tril(Qc @ Kc.T)
+        Zt = Wt @ Qc.T - alpha * (Mt @ Qc.T) * c[None, :] - alpha * Et @ (S * D).T
+        Zk[c0:c0 + n] = Zt.T[:n]
+        dvec = np.where(t16 < n, 1.0 - pw[np.clip(n - t16, 0, 17)], 0.0)
+        wvec = np.where(t16 < n, pw[np.clip(n - 1 - t16, 0, 17)], 0.0)
+        Wt = Wt - alpha * c[n - 1] * Mt - alpha * (Et * dvec[None, :]) @ Kc
+        Mt = pw[n] * Mt + (1 - beta) * (Et * wvec[None, :]) @ Kc
+    assert np.allclose(Zk, Z, rtol=0, atol=1e-12)
+    assert np.allclose(Wt.T, W, rtol=0, atol=1e-12) and np.allclose(Mt.T, M, rtol=0, atol=1e-12)
