@@ -82,7 +82,7 @@ def test_linear_fp32_forward_writes_inside_its_outputs():
     assert rel_l2(to64(Z.t), Zr) <= 1e-4 and rel_l2(to64(Wo.t), Wr) <= 1e-4
 
 
-@pytest.mark.parametrize("T,opts", [(40, None), (37, {"force_path": ttt.PATH_SIMT})])
+@pytest.mark.parametrize("T,opts", [(40, None), (37, {"force_path": ttt.PATH_SIMT}), (37, {"force_path": ttt.PATH_TENSOR})])
 def test_mlp_forward_writes_inside_its_outputs(T, opts):
     w = synth.WORKLOADS["mlp_125m"].with_(B=1, H=2, T=T, seed=910 + T)
     inp = synth.make_inputs(w)
