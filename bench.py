@@ -72,9 +72,10 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--mode", choices=["fwd", "bwd", "momentum", "ln"], default="fwd",
+    ap.add_argument("--mode", choices=["fwd", "bwd", "momentum", "ln", "decode"], default="fwd",
                     help="bwd: time the TTT-Linear backward (ttt_linear_bwd) on the workload instead; "
-                         "momentum / ln: the inner-model variant's tensor-core kernel (bf16, d = 64, b = 16)")
+                         "momentum / ln: the inner-model variant's tensor-core kernel (bf16, d = 64, b = 16); "
+                         "decode: ttt_linear_decode on the workload's heads, --T tokens per launch (default 1)")
     return ap.parse_args()
 
 
@@ -923,6 +924,45 @@ def bench_mlp(args, world, rank, local):
                                        "peak_kind": f"{kind} bf16 burst"}}), flush=True)
 
 
+def bench_decode(args, world, rank, local):
+    """Decode after a prefill: N = --T tokens (default 1) per ttt_linear_decode launch for every (batch
+    row, head) of the workload, from a state (secondary; used for profiling the decode kernel)."""
+    import torch
+    import test_sequence_layers_06_b300 as ttt
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    n = args.T or 1
+    g = torch.Generator(device=dev).manual_seed(5)
+    q = torch.randn(w.B, w.H, n, w.d, device=dev, generator=g).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(torch.randn(w.B, w.H, n, w.d, device=dev, generator=g), dim=-1).to(torch.bfloat16)
+    v = torch.randn(w.B, w.H, n, w.d, device=dev, generator=g).to(torch.bfloat16)
+    eta = torch.full((w.H,), 0.1, device=dev)
+    Wa = 0.02 * torch.randn(w.B, w.H, w.d, w.d, device=dev, generator=g)
+    Wr = Wa.clone()
+    z = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: ttt.ttt_linear_decode(q, k, v, eta, Wa, Wr, 5, args.b, z=z, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(4e6) * (args.steps + 1))  # hold the stream while the launches are enqueued
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / args.steps
+    if rank == 0:
+        print(json.dumps({"metric": "TTT-Linear decode tokens·heads/sec", "value": w.units * n / (ms * 1e-3),
+                          "unit": UNIT, "n_gpus": world, "steps": args.steps, "us_per_launch": round(ms * 1e3, 3),
+                          "us_per_token": round(ms * 1e3 / n, 3), "higher_is_better": True, "dtype": "bf16",
+                          "data": "synthetic", "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d,
+                                                          "b": args.b, "tokens_per_launch": n}}), flush=True)
+
+
 def bench_variant(args, world, rank, local):
     """The momentum or LN + residual variant through its *_ex call on the workload's shape (secondary;
     used for profiling those tensor-core kernels). Reports against the HBM roofline of the plain
@@ -1029,6 +1069,8 @@ def main():
         bench_bwd(args, world, rank, local)
     elif args.mode in ("momentum", "ln"):
         bench_variant(args, world, rank, local)
+    elif args.mode == "decode":
+        bench_decode(args, world, rank, local)
     elif synth.WORKLOADS[args.workload].variant == "mlp":
         bench_mlp(args, world, rank, local)
     else:
