@@ -14,7 +14,9 @@
 // d = 64). A CTA holds its columns of W_anchor and W_run in registers for all
 // N tokens: thread (i, c) keeps row i, columns 4c .. 4c + 3 of the slice of each
 // state. Per token the column sums over i are a shuffle reduction within each
-// warp plus a sum of the warps' partials in shared memory.
+// warp plus a sum of the warps' partials in shared memory. The tokens' q, k and
+// v are staged in shared memory 32 at a time; a launch of more than 32 tokens
+// loads the next 32 into registers while the current ones are processed.
 #include "kernels.h"
 #include "ttt_device.cuh"
 
@@ -34,7 +36,7 @@ __device__ __forceinline__ float ld<float>(const float* p) { return *p; }
 template <>
 __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
-template <typename T>
+template <typename T, bool kPrefetch>
 __global__ void __launch_bounds__(kThreads) linear_decode_kernel(DecodeParams p) {
   __shared__ float qs[kTokBuf][kMaxD], ks[kTokBuf][kMaxD], vs[kTokBuf][kCols];
   __shared__ float part[2][kWarpsD][kCols];  // per-warp column sums of k W_anchor and q W_run
@@ -64,17 +66,63 @@ __global__ void __launch_bounds__(kThreads) linear_decode_kernel(DecodeParams p)
       wr[q] = Wr[i * d + j0 + c + q];
     }
 
+  // With more than one batch of tokens (kPrefetch), a batch's q, k and v go through registers: the
+  // next batch's loads are issued before the current batch's tokens are processed. A launch of one
+  // batch stages directly (its code stays small: a one-token step is bound by its launch).
+  constexpr int kPerQK = kPrefetch ? kTokBuf * kMaxD / kThreads : 1;
+  constexpr int kPerV = kPrefetch ? kTokBuf * kCols / kThreads : 1;
+  float rq[kPerQK], rk[kPerQK], rv[kPerV];
+  auto fetch = [&](int n0) {
+    const int nb = min(kTokBuf, p.N - n0);
+#pragma unroll
+    for (int y = 0; y < kPerQK; ++y) {
+      const int x = tid + y * kThreads, t = x / kMaxD, f = x % kMaxD;
+      rq[y] = rk[y] = 0.f;
+      if (t < nb && f < d) {
+        const size_t g = (static_cast<size_t>(unit) * p.N + n0 + t) * d + f;
+        rq[y] = ld<T>(static_cast<const T*>(p.q) + g);
+        rk[y] = ld<T>(static_cast<const T*>(p.k) + g);
+      }
+    }
+#pragma unroll
+    for (int y = 0; y < kPerV; ++y) {
+      const int x = tid + y * kThreads, t = x / kCols, f = x % kCols;
+      rv[y] = 0.f;
+      if (t < nb && j0 + f < d)
+        rv[y] = ld<T>(static_cast<const T*>(p.v) + (static_cast<size_t>(unit) * p.N + n0 + t) * d + j0 + f);
+    }
+  };
+  if constexpr (kPrefetch) {
+    if (p.N > 0) fetch(0);
+  }
   for (int n0 = 0; n0 < p.N; n0 += kTokBuf) {
     const int nb = min(kTokBuf, p.N - n0);
-    // Stage the q, k (all d) and v (this slice) of the next nb tokens.
-    for (int x = tid; x < nb * d; x += kThreads) {
-      const int t = x / d, f = x % d;
-      const size_t g = (static_cast<size_t>(unit) * p.N + n0 + t) * d + f;
-      qs[t][f] = ld<T>(static_cast<const T*>(p.q) + g);
-      ks[t][f] = ld<T>(static_cast<const T*>(p.k) + g);
-      if (f >= j0 && f < j0 + kCols) vs[t][f - j0] = ld<T>(static_cast<const T*>(p.v) + g);
+    if constexpr (kPrefetch) {
+      // Stage this batch (zeros past d and past the last token), then fetch the next one.
+#pragma unroll
+      for (int y = 0; y < kPerQK; ++y) {
+        const int x = tid + y * kThreads;
+        qs[x / kMaxD][x % kMaxD] = rq[y];
+        ks[x / kMaxD][x % kMaxD] = rk[y];
+      }
+#pragma unroll
+      for (int y = 0; y < kPerV; ++y) {
+        const int x = tid + y * kThreads;
+        vs[x / kCols][x % kCols] = rv[y];
+      }
+      __syncthreads();
+      if (n0 + kTokBuf < p.N) fetch(n0 + kTokBuf);
+    } else {
+      // Stage the q, k (all d) and v (this slice) of the next nb tokens.
+      for (int x = tid; x < nb * d; x += kThreads) {
+        const int t = x / d, f = x % d;
+        const size_t g = (static_cast<size_t>(unit) * p.N + n0 + t) * d + f;
+        qs[t][f] = ld<T>(static_cast<const T*>(p.q) + g);
+        ks[t][f] = ld<T>(static_cast<const T*>(p.k) + g);
+        if (f >= j0 && f < j0 + kCols) vs[t][f - j0] = ld<T>(static_cast<const T*>(p.v) + g);
+      }
+      __syncthreads();
     }
-    __syncthreads();
     for (int t = warp; t < nb; t += kWarpsD) {  // q . k per token, a warp each
       float s = 0.f;
       for (int f = lane; f < d; f += 32) s = fmaf(qs[t][f], ks[t][f], s);
@@ -146,10 +194,18 @@ __global__ void __launch_bounds__(kThreads) linear_decode_kernel(DecodeParams p)
 cudaError_t launch_linear_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.units == 0 || p.N == 0) return cudaSuccess;
   const int grid = p.units * ((p.d + kCols - 1) / kCols);
-  if (p.bf16)
-    linear_decode_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(p);
-  else
-    linear_decode_kernel<float><<<grid, kThreads, 0, stream>>>(p);
+  const bool many = p.N > kTokBuf;
+  if (p.bf16) {
+    if (many)
+      linear_decode_kernel<__nv_bfloat16, true><<<grid, kThreads, 0, stream>>>(p);
+    else
+      linear_decode_kernel<__nv_bfloat16, false><<<grid, kThreads, 0, stream>>>(p);
+  } else {
+    if (many)
+      linear_decode_kernel<float, true><<<grid, kThreads, 0, stream>>>(p);
+    else
+      linear_decode_kernel<float, false><<<grid, kThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
