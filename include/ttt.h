@@ -330,8 +330,8 @@ TTT_API ttt_status ttt_linear_ln_fwd(const void* Q, const void* K, const void* V
                                      const float* beta, int B, int H, int T, int d, int b, void* Z,
                                      float* W_out, void* stream);
 
-/* ttt_linear_ln_fwd_ex: the same layer; with bf16 operands, d = 64 and b = 16 it
- * runs on the tensor cores (one CTA per (batch row, head), W resident as fp32
+/* ttt_linear_ln_fwd_ex: the same layer; with bf16 operands, d = 64 and b a
+ * multiple of 16 it runs on the tensor cores (one CTA per (batch row, head), W resident as fp32
  * accumulator fragments, bf16 operands of every product; each token's layer-norm
  * statistics summed over the 64 features across the CTA's warps), in the chunk's
  * form: Y = K W_a, x = (Y - mean) / s, g = gamma (K + gamma x + beta - V),
@@ -360,9 +360,10 @@ TTT_API ttt_status ttt_linear_momentum_fwd(const void* Q, const void* K, const v
                                            void* stream);
 
 /* ttt_linear_momentum_fwd_ex: the same layer; with bf16 operands, d = 64 and
- * b = 16 it runs on the tensor cores (one CTA per (batch row, head), W and M
- * resident as fp32 accumulator fragments; bf16 operands of every product), in
- * the closed form of a chunk: E = K W_a - V,
+ * b a multiple of 16 it runs on the tensor cores (one CTA per (batch row, head),
+ * W and M resident as fp32 accumulator fragments; bf16 operands of every
+ * product; a chunk walked in 16-token tiles, each tile's E from the chunk-start
+ * W), in the closed form of a run of tokens: E = K W_a - V,
  *   Z = Q W_a - alpha c .* (Q M_a) - alpha (tril(Q K^T) .* D) E,
  *   c_s = beta + ... + beta^s,  D[s][i] = 1 - beta^(s-i+1),
  * and at the chunk end (n tokens) W = W_a - alpha (c_n M_a + K^T (d .* E)),

@@ -151,7 +151,7 @@ struct VariantParams {
 };
 cudaError_t launch_linear_variant(const VariantParams& p, cudaStream_t stream);
 
-// The momentum variant on the tensor cores (linear_mom_mma.cu): bf16, d = 64, b = 16,
+// The momentum variant on the tensor cores (linear_mom_mma.cu): bf16, d = 64, b % 16 = 0,
 // one CTA per (batch row, head).
 struct MomParams {
   const void* Q;          // [units][T][64] bf16
@@ -163,7 +163,7 @@ struct MomParams {
   const float* W0;        // [H][64][64]
   float* W_out;           // [units][64][64]
   float* M_out;           // [units][64][64]
-  int H, T, units;
+  int H, T, b, units;
   StatusBlock* status;
   uint64_t timeout_ns;
   int inject_stall;
@@ -174,7 +174,7 @@ cudaError_t launch_linear_mom_mma(const MomParams& p, const CUtensorMap& mq, con
                                   const CUtensorMap& mv, cudaStream_t stream);
 
 // The layer-norm + residual variant on the tensor cores (linear_ln_mma.cu): bf16, d = 64,
-// b = 16, one CTA per (batch row, head).
+// b % 16 = 0, one CTA per (batch row, head).
 struct LnParams {
   const void* Q;          // [units][T][64] bf16
   const void* K;
@@ -185,7 +185,7 @@ struct LnParams {
   const float* beta;      // [H][64]
   const float* W0;        // [H][64][64]
   float* W_out;           // [units][64][64]
-  int H, T, units;
+  int H, T, b, units;
   StatusBlock* status;
   uint64_t timeout_ns;
   int inject_stall;

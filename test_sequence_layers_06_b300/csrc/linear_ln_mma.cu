@@ -1,6 +1,6 @@
 // TTT-Linear with a layer norm and a residual inside the inner model, bf16 inputs,
-// d = 64, b = 16, on the tensor cores: one CTA per (batch row, head), W resident in
-// registers across the sequence.
+// d = 64, b a multiple of 16, on the tensor cores: one CTA per (batch row, head), W
+// resident in registers across the sequence.
 //
 // Method ("5 · TestingTime 训练与长上下文", section 3.1 lists the layer norm and the
 // residual inside f in its ablation ladder; the oracle's reading): f(k; W) =
@@ -10,6 +10,11 @@
 // For a chunk: Y = K W_a, x = (Y - mu) / s, r = K + gamma x + beta - V, g = gamma r,
 //   E = (g - mean(g) - x mean(g x)) / s            (the chain rule through LN, per row)
 //   X = Q W_a - eta tril(Q K^T) E,   Z = Q + LN(X),   W = W_a - eta K^T E.
+//
+// A chunk larger than 16 tokens is walked in 16-token tiles as in the TTT-Linear
+// read-out: Y (and so E) of every tile from the chunk-start W, X from the running W,
+// which already holds the chunk's earlier tiles' gradients (Q_u W_a - eta sum over
+// the earlier tiles of (Q_u K_u'^T) E_u' = Q_u W_run).
 //
 // Layout as the TTT-Linear read-out (linear_mma.cu): each of 4 consumer warps owns 16
 // output features j and keeps W^T (16 x 64) as fp32 mma.sync accumulator fragments;
@@ -50,6 +55,9 @@ static_assert(kSmemBytes <= 48 * 1024, "no opt-in to more dynamic shared memory"
 
 enum : int { kWhereLnProducer = 52, kWhereLnConsumer = 53 };
 
+// kTileChunk: every 16-token tile is a whole chunk (b = 16), so the chunk-start copy of W^T is the
+// running one and no second copy is kept; otherwise a tile's Y uses the chunk-start copy.
+template <bool kTileChunk>
 __global__ void __launch_bounds__(kThreads, 2)
     linear_ln_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, LnParams p) {
@@ -279,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
 
   bool ok = true;
+  uint32_t wa[4][4];  // bf16 A fragments of the chunk-start W^T (not kept when every tile is a chunk)
   for (int u = 0; ok && u < num_tiles; ++u) {
     const int s = u % kStages;
     if (!mbar_wait_or_abort(&sready[s], (u / kStages) & 1, p.timeout_ns, abort_flag)) {
@@ -290,13 +299,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t sK = sQ + kTileBytes;
     const uint32_t sV = sQ + 2 * kTileBytes;
 
-    uint32_t wr[4][4];  // bf16 A fragments of the chunk-start W^T (k-step k: i in [16k, 16k+16))
+    uint32_t wr[4][4];  // bf16 A fragments of the tile-start (running) W^T (k-step k: i in [16k, 16k+16))
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       wr[k][0] = pack_bf16(Wt[2 * k][0], Wt[2 * k][1]);
       wr[k][1] = pack_bf16(Wt[2 * k][2], Wt[2 * k][3]);
       wr[k][2] = pack_bf16(Wt[2 * k + 1][0], Wt[2 * k + 1][1]);
       wr[k][3] = pack_bf16(Wt[2 * k + 1][2], Wt[2 * k + 1][3]);
+    }
+    if constexpr (!kTileChunk) {
+      if ((u * kTile) % p.b == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) wa[k][r] = wr[k][r];
+      }
     }
     float kt[2][4], vt[2][4];
     ld_t(sK, kt);
@@ -309,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       uint32_t r[4];
       ldsm_x4(r, sK + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
       const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
-      mma_bf16_16816(k < 2 ? y[0] : y2[0], wr[k], b0);
-      mma_bf16_16816(k < 2 ? y[1] : y2[1], wr[k], b1);
+      mma_bf16_16816(k < 2 ? y[0] : y2[0], kTileChunk ? wr[k] : wa[k], b0);
+      mma_bf16_16816(k < 2 ? y[1] : y2[1], kTileChunk ? wr[k] : wa[k], b1);
     }
     // K as the B operand of the update (k = t, n = i): kbt[q] for i in [8q, 8q+8).
     uint32_t kbt[8][2];
@@ -435,14 +452,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace
 
-bool linear_ln_mma_supported(int d, int b, bool bf16) { return bf16 && d == kD && b == kTile; }
+bool linear_ln_mma_supported(int d, int b, bool bf16) { return bf16 && d == kD && b > 0 && b % kTile == 0; }
 
 int linear_ln_mma_tile_rows() { return kTile; }
 
 cudaError_t launch_linear_ln_mma(const LnParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                  const CUtensorMap& mv, cudaStream_t stream) {
   if (p.units == 0) return cudaSuccess;
-  linear_ln_mma_kernel<<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (p.b == kTile)
+    linear_ln_mma_kernel<true><<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    linear_ln_mma_kernel<false><<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

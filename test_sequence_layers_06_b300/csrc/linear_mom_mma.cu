@@ -1,6 +1,6 @@
-// TTT-Linear with momentum gradient descent, bf16 inputs, d = 64, b = 16, on the
-// tensor cores: one CTA per (batch row, head), W and the momentum M resident in
-// registers across the sequence.
+// TTT-Linear with momentum gradient descent, bf16 inputs, d = 64, b a multiple of
+// 16, on the tensor cores: one CTA per (batch row, head), W and the momentum M
+// resident in registers across the sequence.
 //
 // Method (the E²-TTT write-up, "推理时的“临阵磨枪”：Test-Time Training如何教会AI“边做边学”",
 // sections 2.3 and 5.1, as the oracle reads it: token-level momentum with the
@@ -20,7 +20,11 @@
 //   W^T += (-alpha c_n) M_a^T + (-alpha E^T .* d) K,     d_i = 1 - beta^(n-i+1)
 //   M^T  = beta^n M_a^T + ((1 - beta) E^T .* w) K,      w_i = beta^(n-i)
 // (the column scalings act on the token index of E^T's C fragment before it is
-// packed as the A operand). A producer warp streams the Q, K, V tiles by TMA into
+// packed as the A operand). These are the token recurrence solved over any run of
+// tokens that share one W_a, so a chunk larger than 16 tokens is walked in 16-token
+// tiles: E of every tile from the chunk-start W (a kept bf16 copy), the rest from
+// the running (W, M) with the tile's own c, D, d and w (b = 16: every tile is a
+// chunk). A producer warp streams the Q, K, V tiles by TMA into
 // a 6-stage ring and forms (S .* D)^T once per tile for the consumers. Every wait
 // is bounded in wall-clock time. Powers of beta are products in fp32, as a table.
 #include "ttt_device.cuh"
@@ -48,6 +52,9 @@ static_assert(kSmemBytes <= 48 * 1024, "no opt-in to more dynamic shared memory"
 
 enum : int { kWhereMomProducer = 50, kWhereMomConsumer = 51 };
 
+// kTileChunk: every 16-token tile is a whole chunk (b = 16), so the chunk-start copy of W^T is the
+// running one and no second copy is kept; otherwise a tile's error uses the chunk-start copy.
+template <bool kTileChunk>
 __global__ void __launch_bounds__(kThreads, 2)
     linear_mom_mma_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                           const __grid_constant__ CUtensorMap mv, MomParams p) {
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
 
+  uint32_t wa[4][4];  // bf16 A fragments of the chunk-start W^T (not kept when every tile is a chunk)
   for (int u = 0; u < num_tiles; ++u) {
     const int s = u % kStages;
     if (!mbar_wait_or_abort(&sready[s], (u / kStages) & 1, p.timeout_ns, abort_flag)) {
@@ -231,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t sV = sQ + 2 * kTileBytes;
     if (u == num_tiles - 1 && p.T - u * kTile < kTile) set_chunk(p.T - u * kTile);  // a ragged last chunk
 
-    // bf16 A fragments of the chunk-start W^T and M^T (k-step k: i in [16k, 16k+16)).
+    // bf16 A fragments of the tile-start (running) W^T and M^T (k-step k: i in [16k, 16k+16)).
     uint32_t wr[4][4], mra[4][4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -243,6 +251,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       mra[k][1] = pack_bf16(Mt[2 * k][2], Mt[2 * k][3]);
       mra[k][2] = pack_bf16(Mt[2 * k + 1][0], Mt[2 * k + 1][1]);
       mra[k][3] = pack_bf16(Mt[2 * k + 1][2], Mt[2 * k + 1][3]);
+    }
+    if constexpr (!kTileChunk) {
+      if ((u * kTile) % p.b == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) wa[k][r] = wr[k][r];
+      }
     }
 
     // -V^T as the accumulator of E^T (ldmatrix.trans of V's 8x8 blocks gives the C-fragment pairs).
@@ -265,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       uint32_t r[4];
       ldsm_x4(r, sK + swz128(((mi >> 1) << 3) + mr, 2 * k + (mi & 1)));
       const uint32_t b0[2] = {r[0], r[1]}, b1[2] = {r[2], r[3]};
-      mma_bf16_16816(k < 2 ? e[0] : e2[0], wr[k], b0);
-      mma_bf16_16816(k < 2 ? e[1] : e2[1], wr[k], b1);
+      mma_bf16_16816(k < 2 ? e[0] : e2[0], kTileChunk ? wr[k] : wa[k], b0);
+      mma_bf16_16816(k < 2 ? e[1] : e2[1], kTileChunk ? wr[k] : wa[k], b1);
     }
     // K as the B operand of the updates (k = t, n = i): kbt[q] for i in [8q, 8q+8).
     uint32_t kbt[8][2];
@@ -372,14 +388,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 }  // namespace
 
-bool linear_mom_mma_supported(int d, int b, bool bf16) { return bf16 && d == kD && b == kTile; }
+bool linear_mom_mma_supported(int d, int b, bool bf16) { return bf16 && d == kD && b > 0 && b % kTile == 0; }
 
 int linear_mom_mma_tile_rows() { return kTile; }
 
 cudaError_t launch_linear_mom_mma(const MomParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                                   const CUtensorMap& mv, cudaStream_t stream) {
   if (p.units == 0) return cudaSuccess;
-  linear_mom_mma_kernel<<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  if (p.b == kTile)
+    linear_mom_mma_kernel<true><<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
+  else
+    linear_mom_mma_kernel<false><<<p.units, kThreads, kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

@@ -817,7 +817,7 @@ ttt_status ttt_linear_momentum_fwd_ex(const void* Q, const void* K, const void* 
   ttt::MomParams p;
   p.Q = Q; p.K = K; p.V = V; p.Z = Z;
   p.alpha = alpha; p.beta = beta; p.W0 = W0; p.W_out = W_out; p.M_out = M_out;
-  p.H = H; p.T = T; p.units = B * H;
+  p.H = H; p.T = T; p.b = b; p.units = B * H;
   p.status = static_cast<ttt::StatusBlock*>(workspace);
   p.timeout_ns = o.wait_timeout_ns;
   p.inject_stall = o.inject_stall;
@@ -860,7 +860,7 @@ ttt_status ttt_linear_ln_fwd_ex(const void* Q, const void* K, const void* V, ttt
   ttt::LnParams p;
   p.Q = Q; p.K = K; p.V = V; p.Z = Z;
   p.eta = eta; p.gamma = gamma; p.beta = beta; p.W0 = W0; p.W_out = W_out;
-  p.H = H; p.T = T; p.units = B * H;
+  p.H = H; p.T = T; p.b = b; p.units = B * H;
   p.status = static_cast<ttt::StatusBlock*>(workspace);
   p.timeout_ns = o.wait_timeout_ns;
   p.inject_stall = o.inject_stall;

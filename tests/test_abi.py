@@ -302,13 +302,13 @@ def _var_ex(lib, name, **kw):
 
 
 @pytest.mark.parametrize("kw,want", [(dict(fp=3), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=2, d=32), ttt.TTT_ERR_UNSUPPORTED),
-                                     (dict(fp=2, b=32), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=2, dt=0), ttt.TTT_ERR_UNSUPPORTED),
+                                     (dict(fp=2, b=24), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=2, dt=0), ttt.TTT_ERR_UNSUPPORTED),
                                      (dict(fp=2, T=0), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=5), ttt.TTT_ERR_ARG),
                                      (dict(beta0=0), ttt.TTT_ERR_ARG), (dict(beta=9 * MB + 4096), ttt.TTT_ERR_ARG),
                                      (dict(beta=4 * MB), ttt.TTT_ERR_ARG)])
 def test_momentum_fast_call_paths_and_arguments(lib, kw, want):
     """ttt_linear_momentum_fwd_ex: no segment-parallel form; the tensor kernel, when forced, only for
-    bf16, d = 64, b = 16 and T > 0; a bad path, a null beta, M_out over W_out or over an input:
+    bf16, d = 64, b a multiple of 16 and T > 0; a bad path, a null beta, M_out over W_out or over an input:
     refused before anything runs (M_out is the `beta` slot of the shared argument set)."""
     base = dict(d=64, W=9 * MB, beta=9 * MB + 64 * 64 * 4 * 6)
     base.update(kw)
@@ -316,12 +316,12 @@ def test_momentum_fast_call_paths_and_arguments(lib, kw, want):
 
 
 @pytest.mark.parametrize("kw,want", [(dict(fp=3), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=2, d=32), ttt.TTT_ERR_UNSUPPORTED),
-                                     (dict(fp=2, b=32), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=2, dt=0), ttt.TTT_ERR_UNSUPPORTED),
+                                     (dict(fp=2, b=24), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=2, dt=0), ttt.TTT_ERR_UNSUPPORTED),
                                      (dict(fp=2, T=0), ttt.TTT_ERR_UNSUPPORTED), (dict(fp=-1), ttt.TTT_ERR_ARG),
                                      (dict(gb=0), ttt.TTT_ERR_ARG), (dict(W=7 * MB + 256), ttt.TTT_ERR_ARG)])
 def test_ln_fast_call_paths_and_arguments(lib, kw, want):
     """ttt_linear_ln_fwd_ex: no segment-parallel form; the tensor kernel, when forced, only for bf16,
-    d = 64, b = 16 and T > 0; a bad path, a null beta, W_out over beta: refused before anything runs
+    d = 64, b a multiple of 16 and T > 0; a bad path, a null beta, W_out over beta: refused before anything runs
     (gamma is the `beta0` slot of the shared argument set, beta the `gb` slot)."""
     base = dict(d=64, W=9 * MB)
     base.update(kw)

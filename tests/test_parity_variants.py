@@ -191,24 +191,26 @@ def test_fast_token_eta_reports_a_negative_rate():
     check("Z,W_out", got, token_eta_primal(inp.q64, inp.k64, inp.v64, et, inp.W0_64, 16), w)
 
 
-FAST_MOM = [(1, 2, 1, 0.6), (1, 2, 3, 0.6), (2, 3, 16, 0.9), (2, 3, 37, 0.5), (1, 2, 100, 0.0), (1, 2, 1024, 0.8),
-            (1, 2, 2048, 0.95)]
+FAST_MOM = [(1, 2, 1, 0.6, 16), (1, 2, 3, 0.6, 16), (2, 3, 16, 0.9, 16), (2, 3, 37, 0.5, 16),
+            (1, 2, 100, 0.0, 16), (1, 2, 1024, 0.8, 16), (1, 2, 2048, 0.95, 16), (2, 3, 100, 0.7, 32),
+            (1, 2, 1000, 0.5, 64), (1, 2, 600, 0.5, 256)]
 
 
-@pytest.mark.parametrize("B,H,T,beta", FAST_MOM)
-def test_momentum_fast_path_matches_oracle(B, H, T, beta):
-    """bf16, d = 64, b = 16 on the tensor-core momentum kernel (forced, so that no other kernel can
-    serve): a single short chunk, ragged last chunks, beta = 0 (plain TTT-Linear with the last
-    token's gradient as M), strong momentum, and sequences of 64 and 128 chunks."""
-    w, inp, t = inputs(64, T, "bf16", 800 + T, B=B, H=H)
+@pytest.mark.parametrize("B,H,T,beta,b", FAST_MOM)
+def test_momentum_fast_path_matches_oracle(B, H, T, beta, b):
+    """bf16, d = 64, b a multiple of 16 on the tensor-core momentum kernel (forced, so that no other
+    kernel can serve): a single short chunk, ragged last chunks, beta = 0 (plain TTT-Linear with the
+    last token's gradient as M), strong momentum, sequences of 64 and 128 chunks, and chunks of 2,
+    4 and 16 tiles (each tile's E from the chunk-start W)."""
+    w, inp, t = inputs(64, T, "bf16", 800 + T + b, B=B, H=H)
     alpha = np.linspace(0.05, 0.15, H).astype(np.float32)
     betas = (beta * (1.0 - 0.05 * np.arange(H))).astype(np.float32)
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     got = ttt.ttt_linear_momentum_fwd(t["Q"], t["K"], t["V"], torch.from_numpy(alpha).cuda(),
-                                      torch.from_numpy(betas).cuda(), t["W0"], 16, fast=True, workspace=ws,
+                                      torch.from_numpy(betas).cuda(), t["W0"], b, fast=True, workspace=ws,
                                       options={"force_path": ttt.PATH_TENSOR})
     assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
-    want = momentum_primal(inp.q64, inp.k64, inp.v64, alpha, betas, inp.W0_64, 16)
+    want = momentum_primal(inp.q64, inp.k64, inp.v64, alpha, betas, inp.W0_64, b)
     check("Z,W_out,M_out", got, want, w)
 
 
@@ -240,7 +242,8 @@ def test_momentum_fast_path_bounded_wait_reports_timeout():
     check("Z,W_out,M_out", got, momentum_primal(inp.q64, inp.k64, inp.v64, alpha, betas, inp.W0_64, 16), w)
 
 
-FAST_LN = [(1, 2, 1), (1, 2, 3), (2, 3, 16), (2, 3, 37), (1, 2, 100), (1, 2, 1024), (1, 2, 2048)]
+FAST_LN = [(1, 2, 1, 16), (1, 2, 3, 16), (2, 3, 16, 16), (2, 3, 37, 16), (1, 2, 100, 16), (1, 2, 1024, 16),
+           (1, 2, 2048, 16), (2, 3, 100, 32), (1, 2, 512, 64), (1, 2, 600, 256)]
 
 
 def ln_params(H, seed):
@@ -249,18 +252,19 @@ def ln_params(H, seed):
             (0.1 * g.standard_normal((H, 64))).astype(np.float32))
 
 
-@pytest.mark.parametrize("B,H,T", FAST_LN)
-def test_ln_fast_path_matches_oracle(B, H, T):
-    """bf16, d = 64, b = 16 on the tensor-core LN + residual kernel (forced, so that no other kernel
-    can serve): a single short chunk, ragged last chunks, and sequences of 64 and 128 chunks."""
-    w, inp, t = inputs(64, T, "bf16", 840 + T, B=B, H=H)
+@pytest.mark.parametrize("B,H,T,b", FAST_LN)
+def test_ln_fast_path_matches_oracle(B, H, T, b):
+    """bf16, d = 64, b a multiple of 16 on the tensor-core LN + residual kernel (forced, so that no
+    other kernel can serve): a single short chunk, ragged last chunks, sequences of 64 and 128 chunks,
+    and chunks of 2, 4 and 16 tiles (each tile's Y and E from the chunk-start W)."""
+    w, inp, t = inputs(64, T, "bf16", 840 + T + b, B=B, H=H)
     gamma, beta = ln_params(w.H, T)
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     got = ttt.ttt_linear_ln_fwd(t["Q"], t["K"], t["V"], t["eta"], t["W0"], torch.from_numpy(gamma).cuda(),
-                                torch.from_numpy(beta).cuda(), 16, fast=True, workspace=ws,
+                                torch.from_numpy(beta).cuda(), b, fast=True, workspace=ws,
                                 options={"force_path": ttt.PATH_TENSOR})
     assert ttt.ttt_last_device_status(ws) == ttt.TTT_OK
-    want = ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma, beta, 16)
+    want = ln_residual_primal(inp.q64, inp.k64, inp.v64, inp.eta64, inp.W0_64, gamma, beta, b)
     check("Z,W_out", got, want, w)
 
 
